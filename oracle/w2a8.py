@@ -1,0 +1,238 @@
+"""Plain CPU oracle for the W2A8 ternary linear.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+module.  The product path (the CUDA library and its Python binding) never
+imports, links or calls it, and this module shares no code, table or constant
+generator with that path.
+
+What is computed, and where it comes from
+-----------------------------------------
+The pages ("BitMTP: When Multi-Token Prediction Meets Low-Bit Large Language
+Models", AI summary) describe the backbone as BitNet b1.58-style ternary
+("What This Paper Is About"; "Overview": ultra-low-bit ternary / 1.58-bit
+backbones), run in the "W2A8 setting (2-bit weights, 8-bit activations)"
+("Main Findings", first bullet) through "packed W2A8 execution" and
+width-specialised packed low-bit operators ("Methodology in Plain English",
+third and last paragraphs).  The pages print no formula.  This library's
+specification fills that in with the BitNet b1.58 definitions, which this
+oracle writes out directly:
+
+* weights: T in {-1, 0, +1} with one fp32 per-tensor absmean scale,
+  W ~= w_scale * T  (``ternarize_absmean``);
+* activations: per row, amax = max|x|, s = 127 / amax, q = round-half-even(x*s)
+  in fp32, a_scale = amax / 127  (``quant_act``);
+* integer accumulation acc[m, n] = sum_k T[n, k] * q[m, k]  (``gemm_acc``);
+* dequant epilogue y = acc * a_scale[m] * w_scale  (``dequant``).
+
+Readings taken where the pages are silent are listed in the design doc (zero row ->
+all-zero codes and a_scale 0; clamp to +-127; s multiplied, not divided; the
+weight epsilon 1e-5; exact bf16 widening; dequant evaluated in fp64 and rounded
+once to fp32, then to bf16 for bf16 output).
+
+The packed-weight format (``pack_tiles`` / ``unpack_tiles``) is this library's
+own internal layout, not the pages'; it is restated here from its written
+definition so that the device pack kernel can be checked byte for byte.
+
+Precision: the quantiser is fp32 (the specification fixes it); accumulation is
+exact int64; dequant is fp64 then rounded to fp32.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F32 = np.float32
+F64 = np.float64
+
+QMAX = 127
+WEIGHT_EPS = F32(1e-5)
+
+
+# ---------------------------------------------------------------------------
+# bf16 helpers (bf16 values are carried as their uint16 bit patterns)
+# ---------------------------------------------------------------------------
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to fp32."""
+    b = np.asarray(bits).astype(np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(F32)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 to bf16, round-to-nearest-even, returning uint16 bits.
+
+    Finite inputs only (the oracle never produces non-finite values)."""
+    u = np.ascontiguousarray(np.asarray(x, dtype=F32)).view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    r = (u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
+    return r.astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# A2: absmean ternarisation (BitNet b1.58 weight quantiser)
+# ---------------------------------------------------------------------------
+def ternarize_absmean(W: np.ndarray) -> tuple[np.ndarray, np.float32]:
+    """T = clamp(round_half_even(W / gamma), -1, 1), gamma = max(mean|W|, 1e-5).
+
+    mean|W| is summed in fp64 and rounded once to fp32; the division and the
+    rounding are fp32 IEEE operations.  Returns (T int8 [N, K], w_scale fp32)
+    with W ~= w_scale * T."""
+    W = np.asarray(W, dtype=F32)
+    if W.size == 0:
+        raise ValueError("empty weight matrix")
+    if not np.all(np.isfinite(W)):
+        raise ValueError("non-finite weight")
+    gamma = F32(np.sum(np.abs(W.astype(F64))) / W.size)
+    gamma = max(gamma, WEIGHT_EPS)
+    ratio = (W / gamma).astype(F32)
+    T = np.clip(np.rint(ratio), -1, 1).astype(np.int8)
+    return T, F32(gamma)
+
+
+# ---------------------------------------------------------------------------
+# A3: per-row absmax int8 activation quantiser
+# ---------------------------------------------------------------------------
+def quant_act(x: np.ndarray):
+    """Quantise each row of x (fp32 [M, K]) to int8 codes by absmax.
+
+    Per row m, all in fp32 round-to-nearest-even:
+      amax = max_k |x[m, k]|
+      amax == 0  ->  q = 0, a_scale = 0, rowsum = 0
+      otherwise  ->  s = 127 / amax;  q = clamp(rint(x * s), -127, 127);
+                     a_scale = amax / 127;  rowsum = sum_k q  (int32)
+    Returns (q int8 [M, K], a_scale fp32 [M], rowsum int32 [M])."""
+    x = np.asarray(x, dtype=F32)
+    if x.ndim != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    if not np.all(np.isfinite(x)):
+        raise ValueError("non-finite activation")
+    M, K = x.shape
+    q = np.zeros((M, K), dtype=np.int8)
+    a_scale = np.zeros(M, dtype=F32)
+    rowsum = np.zeros(M, dtype=np.int32)
+    for m in range(M):
+        row = x[m]
+        amax = F32(np.max(np.abs(row))) if K else F32(0)
+        if amax == 0:
+            continue
+        s = F32(F32(QMAX) / amax)
+        v = (row * s).astype(F32)
+        qm = np.clip(np.rint(v), -QMAX, QMAX).astype(np.int8)
+        q[m] = qm
+        a_scale[m] = F32(amax / F32(QMAX))
+        rowsum[m] = np.int32(np.sum(qm.astype(np.int64)))
+    return q, a_scale, rowsum
+
+
+def quant_act_bf16(x_bits: np.ndarray):
+    """``quant_act`` on bf16 activations given as uint16 bit patterns."""
+    return quant_act(bf16_bits_to_f32(x_bits))
+
+
+# ---------------------------------------------------------------------------
+# A4: integer accumulation and the dequant epilogue
+# ---------------------------------------------------------------------------
+def gemm_acc(T: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """acc[m, n] = sum_k T[n, k] * q[m, k], exact in int64.
+
+    Raises if a result does not fit int32 (the device accumulator type)."""
+    T = np.asarray(T)
+    q = np.asarray(q)
+    if T.ndim != 2 or q.ndim != 2 or T.shape[1] != q.shape[1]:
+        raise ValueError("shape mismatch: T [N, K], q [M, K]")
+    acc = q.astype(np.int64) @ T.astype(np.int64).T
+    if acc.size and (acc.max() > np.iinfo(np.int32).max or acc.min() < np.iinfo(np.int32).min):
+        raise OverflowError("accumulator exceeds int32")
+    return acc
+
+
+def dequant(acc: np.ndarray, a_scale: np.ndarray, w_scale, out: str = "f32") -> np.ndarray:
+    """y[m, n] = acc[m, n] * a_scale[m] * w_scale, evaluated in fp64 and
+    rounded once to fp32; ``out="bf16"`` then rounds that fp32 value to bf16
+    (round-to-nearest-even) and returns uint16 bit patterns."""
+    y64 = (np.asarray(acc, dtype=F64)
+           * np.asarray(a_scale, dtype=F64)[:, None]
+           * F64(F32(w_scale)))
+    y32 = y64.astype(F32)
+    if out == "f32":
+        return y32
+    if out == "bf16":
+        return f32_to_bf16_bits(y32)
+    raise ValueError(f"unknown output dtype {out!r}")
+
+
+def w2a8_linear(T, w_scale, x, out: str = "f32", x_is_bf16: bool = False):
+    """quant_act -> gemm_acc -> dequant.  Returns (y, acc, q, a_scale, rowsum)."""
+    q, a_scale, rowsum = quant_act_bf16(x) if x_is_bf16 else quant_act(x)
+    acc = gemm_acc(T, q)
+    return dequant(acc, a_scale, w_scale, out), acc, q, a_scale, rowsum
+
+
+# ---------------------------------------------------------------------------
+# Packed-weight format (this library's own layout; restated from its definition)
+#
+#   * rows are grouped in row tiles of 128, k in k tiles of 128; both padded
+#     with T = 0;
+#   * tile (rt, kt) is 4096 contiguous bytes at byte offset (rt*KT + kt)*4096;
+#   * inside a tile, row r has eight 32-bit words j = 0..7; word j of row r is
+#     stored at word index (j // 4)*512 + r*4 + (j % 4);
+#   * word j holds k = kt*128 + 16*j + 2*p + e (p = 0..7, e = 0..1) as the
+#     2-bit code u = T + 1 in bits 16*e + 2*p .. 16*e + 2*p + 1 (u = 3 never
+#     occurs);
+#   * a 16-byte trailer follows the tiles: uint32 {0x38413242, N, K, invalid},
+#     invalid = number of entries of the source that were not in {-1, 0, 1}.
+# ---------------------------------------------------------------------------
+TILE_N = 128
+TILE_K = 128
+TILE_BYTES = 4096
+TRAILER_MAGIC = 0x38413242
+
+
+def packed_bytes(N: int, K: int) -> int:
+    nt = -(-N // TILE_N)
+    kt = -(-K // TILE_K)
+    return nt * kt * TILE_BYTES + 16
+
+
+def pack_tiles(T: np.ndarray) -> np.ndarray:
+    """Pack ternary int8 T [N, K] into the tiled 2-bit format (uint8 bytes)."""
+    T = np.asarray(T)
+    N, K = T.shape
+    nt, kt = -(-N // TILE_N), -(-K // TILE_K)
+    invalid = int(np.count_nonzero((T < -1) | (T > 1)))
+    Tp = np.zeros((nt * TILE_N, kt * TILE_K), dtype=np.int64)
+    Tp[:N, :K] = T
+    u = np.where((Tp >= -1) & (Tp <= 1), Tp + 1, 1).astype(np.uint64)
+    # axes: [rt, r, kt, j, p, e]
+    u = u.reshape(nt, TILE_N, kt, 8, 8, 2)
+    shifts = (np.uint64(16) * np.arange(2, dtype=np.uint64)[None, :]
+              + np.uint64(2) * np.arange(8, dtype=np.uint64)[:, None])  # [p, e]
+    words = np.sum(u << shifts, axis=(4, 5)).astype(np.uint32)          # [rt, r, kt, j]
+    words = words.reshape(nt, TILE_N, kt, 2, 4)                         # j = 4*half + jj
+    tiles = np.transpose(words, (0, 2, 3, 1, 4))                        # [rt, kt, half, r, jj]
+    body = np.ascontiguousarray(tiles).reshape(-1).view(np.uint8)
+    trailer = np.array([TRAILER_MAGIC, N, K, invalid], dtype=np.uint32).view(np.uint8)
+    return np.concatenate([body, trailer])
+
+
+def unpack_tiles(pk: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Inverse of ``pack_tiles``: tiled bytes -> T int8 [N, K].
+
+    Raises on a 2-bit code of 3 anywhere (including padding)."""
+    pk = np.asarray(pk, dtype=np.uint8)
+    nt, kt = -(-N // TILE_N), -(-K // TILE_K)
+    body = pk[: nt * kt * TILE_BYTES].view(np.uint32).reshape(nt, kt, 2, TILE_N, 4)
+    words = np.transpose(body, (0, 3, 1, 2, 4)).reshape(nt, TILE_N, kt, 8).astype(np.uint64)
+    shifts = (np.uint64(16) * np.arange(2, dtype=np.uint64)[None, :]
+              + np.uint64(2) * np.arange(8, dtype=np.uint64)[:, None])
+    u = (words[..., None, None] >> shifts) & np.uint64(3)                # [rt, r, kt, j, p, e]
+    if np.any(u == 3):
+        raise ValueError("invalid 2-bit code 3 in packed weights")
+    T = u.astype(np.int64).reshape(nt * TILE_N, kt * TILE_K) - 1
+    return T[:N, :K].astype(np.int8)
+
+
+def read_trailer(pk: np.ndarray, N: int, K: int) -> tuple[int, int, int, int]:
+    nt, kt = -(-N // TILE_N), -(-K // TILE_K)
+    off = nt * kt * TILE_BYTES
+    t = np.asarray(pk, dtype=np.uint8)[off: off + 16].view(np.uint32)
+    return int(t[0]), int(t[1]), int(t[2]), int(t[3])

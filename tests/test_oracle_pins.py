@@ -1,0 +1,298 @@
+"""Pins for the CPU oracle against facts fixed outside the oracle itself:
+hand-derived closed forms (tests/golden), brute force on tiny inputs with
+plain Python integers, exact rational arithmetic, invariants of the
+definitions, and library routines for the special cases they cover.
+
+Runs on CPU only (no GPU marker)."""
+import itertools
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from ternary_w2a8_linear_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield [c.strip() for c in line.split(";")]
+
+
+# ---------------------------------------------------------------------------
+# Activation quantiser
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", list(_rows("quant_act_closed_forms.txt")))
+def test_quant_act_golden(case):
+    xs, qs, rs, amax = case
+    x = np.array([[float(v) for v in xs.split()]], dtype=np.float32)
+    q, a_scale, rowsum = oracle.quant_act(x)
+    assert q[0].tolist() == [int(v) for v in qs.split()]
+    assert int(rowsum[0]) == int(rs)
+    expect_scale = np.float32(float(amax)) / np.float32(127) if float(amax) else np.float32(0)
+    assert a_scale[0] == expect_scale
+
+
+def test_quant_act_one_hot():
+    for v in (1e-3, 0.7, -3.25, 1e4, -1e-20):
+        x = np.zeros((1, 37), dtype=np.float32)
+        x[0, 11] = v
+        q, a_scale, rowsum = oracle.quant_act(x)
+        expect = np.zeros(37, dtype=np.int8)
+        expect[11] = 127 if v > 0 else -127
+        assert np.array_equal(q[0], expect)
+        assert rowsum[0] == expect[11]
+
+
+def test_quant_act_rational_bound():
+    """Each code is within 1/2 (+ the fp32 rounding of s and of x*s) of the
+    exact rational x*127/amax; the largest-magnitude entry maps to +-127."""
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((5, 300)).astype(np.float32)
+    x[2] *= np.float32(1e-3)
+    x[3, 17] = np.float32(55.0)
+    q, a_scale, rowsum = oracle.quant_act(x)
+    for m in range(x.shape[0]):
+        amax = Fraction(float(np.max(np.abs(x[m]))))
+        for k in range(x.shape[1]):
+            exact = Fraction(float(x[m, k])) * 127 / amax
+            assert abs(Fraction(int(q[m, k])) - exact) <= Fraction(1, 2) + Fraction(1, 2**14)
+            if x[m, k] == 0:
+                assert q[m, k] == 0
+            else:
+                assert q[m, k] == 0 or np.sign(q[m, k]) == np.sign(x[m, k])
+        k_max = int(np.argmax(np.abs(x[m])))
+        assert abs(int(q[m, k_max])) == 127
+        assert int(rowsum[m]) == sum(int(v) for v in q[m])
+        assert a_scale[m] == np.float32(np.max(np.abs(x[m]))) / np.float32(127)
+
+
+def test_quant_act_monotone_and_odd():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((3, 513)).astype(np.float32)
+    q, _, _ = oracle.quant_act(x)
+    qn, _, rn = oracle.quant_act(-x)
+    assert np.array_equal(qn, -q)
+    for m in range(3):
+        order = np.argsort(x[m], kind="stable")
+        assert np.all(np.diff(q[m][order].astype(int)) >= 0)
+
+
+def test_quant_act_power_of_two_scaling():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((4, 200)).astype(np.float32)
+    q, a, r = oracle.quant_act(x)
+    for j in (-7, -1, 3, 10):
+        q2, a2, r2 = oracle.quant_act((x * np.float32(2.0 ** j)).astype(np.float32))
+        assert np.array_equal(q2, q) and np.array_equal(r2, r)
+        assert np.array_equal(a2, (a * np.float32(2.0 ** j)).astype(np.float32))
+
+
+def test_quant_act_bf16_widening():
+    vals = np.array([[1.0, -2.5, 0.0078125, 3.0e38, -1.0e-30]], dtype=np.float32)
+    bits = inputs.to_bf16_bits(vals)
+    widened = oracle.bf16_bits_to_f32(bits)
+    import torch
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    assert np.array_equal(widened, ref)
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding helper against torch's conversion (a library routine)
+# ---------------------------------------------------------------------------
+def test_f32_to_bf16_matches_torch():
+    import torch
+    rng = np.random.default_rng(10)
+    x = np.concatenate([
+        rng.standard_normal(10000).astype(np.float32) * np.float32(1e3),
+        np.array([1 + 2**-8, 1 + 3 * 2**-8, -(1 + 2**-8), 0.0, -0.0, 2**-130, 65504.0], dtype=np.float32),
+    ])
+    ours = oracle.f32_to_bf16_bits(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ---------------------------------------------------------------------------
+# Absmean ternarisation
+# ---------------------------------------------------------------------------
+def test_ternarize_constant_magnitude():
+    rng = np.random.default_rng(11)
+    sgn = np.where(rng.random((9, 33)) < 0.5, -1.0, 1.0).astype(np.float32)
+    for c in (0.125, 0.7, 3.0):
+        T, g = oracle.ternarize_absmean(sgn * np.float32(c))
+        assert g == np.float32(c)
+        assert np.array_equal(T, sgn.astype(np.int8))
+
+
+def test_ternarize_ties_and_clamp():
+    W = np.array([[1.0, 3.0, -1.0, -3.0]], dtype=np.float32)  # mean|W| = 2 -> ratios +-0.5, +-1.5
+    T, g = oracle.ternarize_absmean(W)
+    assert g == np.float32(2.0)
+    assert T.tolist() == [[0, 1, 0, -1]]
+    W = np.array([[2.0, -2.0, 1.0, 3.0, -1.0, 0.0]], dtype=np.float32)  # mean 1.5
+    T, g = oracle.ternarize_absmean(W)
+    assert g == np.float32(1.5)
+    assert T.tolist() == [[1, -1, 1, 1, -1, 0]]
+
+
+def test_ternarize_epsilon():
+    T, g = oracle.ternarize_absmean(np.zeros((3, 4), dtype=np.float32))
+    assert g == np.float32(1e-5) and not T.any()
+    T, g = oracle.ternarize_absmean(np.full((2, 2), 1e-7, dtype=np.float32))
+    assert g == np.float32(1e-5) and not T.any()
+
+
+# ---------------------------------------------------------------------------
+# Integer accumulation: brute force with plain Python integers
+# ---------------------------------------------------------------------------
+def _brute_acc(T, q):
+    N, K = len(T), len(T[0])
+    M = len(q)
+    return [[sum(int(T[n][k]) * int(q[m][k]) for k in range(K)) for n in range(N)] for m in range(M)]
+
+
+def test_gemm_exhaustive_tiny():
+    rng = np.random.default_rng(12)
+    q = rng.integers(-127, 128, size=(2, 3)).astype(np.int8)
+    for vals in itertools.product((-1, 0, 1), repeat=6):
+        T = np.array(vals, dtype=np.int8).reshape(2, 3)
+        assert oracle.gemm_acc(T, q).tolist() == _brute_acc(T.tolist(), q.tolist())
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 7), (4, 2, 9), (16, 3, 4), (2, 8, 1)])
+def test_gemm_brute_force_shapes(M, N, K):
+    rng = np.random.default_rng(M * 100 + N * 10 + K)
+    T = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    q = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    assert oracle.gemm_acc(T, q).tolist() == _brute_acc(T.tolist(), q.tolist())
+
+
+def test_gemm_invariants():
+    rng = np.random.default_rng(13)
+    K = 48
+    q = rng.integers(-127, 128, size=(5, K)).astype(np.int8)
+    assert not oracle.gemm_acc(np.zeros((7, K), np.int8), q).any()
+    eye = np.eye(K, dtype=np.int8)
+    assert np.array_equal(oracle.gemm_acc(eye, q), q.astype(np.int64))
+    assert np.array_equal(oracle.gemm_acc(-eye, q), -q.astype(np.int64))
+    perm = rng.permutation(K)
+    P = eye[perm]
+    assert np.array_equal(oracle.gemm_acc(P, q), q[:, perm].astype(np.int64))
+    ones = np.ones((3, 11008), dtype=np.int8)
+    q127 = np.full((2, 11008), 127, dtype=np.int8)
+    assert np.all(oracle.gemm_acc(ones, q127) == 127 * 11008)
+
+
+def test_gemm_rejects_int32_overflow():
+    # int32 overflow needs > 16.9 M terms of 127; fake it with a wide int input
+    with pytest.raises(OverflowError):
+        oracle.gemm_acc(np.ones((1, 2), np.int64) * 2**30, np.ones((1, 2), np.int64) * 2)
+
+
+# ---------------------------------------------------------------------------
+# Dequant epilogue: exact rationals
+# ---------------------------------------------------------------------------
+def test_dequant_exact_rational():
+    rng = np.random.default_rng(14)
+    acc = rng.integers(-400000, 400000, size=(4, 50))
+    acc[0, :3] = 0
+    a_scale = (rng.random(4).astype(np.float32) * np.float32(0.1)).astype(np.float32)
+    w_scale = np.float32(0.0312)
+    y = oracle.dequant(acc, a_scale, w_scale)
+    assert y.dtype == np.float32
+    assert np.all(y[0, :3] == 0)
+    for m in range(4):
+        for n in range(50):
+            exact = Fraction(int(acc[m, n])) * Fraction(float(a_scale[m])) * Fraction(float(w_scale))
+            got = Fraction(float(y[m, n]))
+            ulp = Fraction(float(np.spacing(np.float32(abs(float(exact)))))) if exact else Fraction(0)
+            assert abs(got - exact) <= ulp
+
+
+def test_dequant_power_of_two_scaling():
+    rng = np.random.default_rng(15)
+    acc = rng.integers(-10**6, 10**6, size=(3, 40))
+    a = rng.random(3).astype(np.float32)
+    y = oracle.dequant(acc, a, np.float32(0.02))
+    y2 = oracle.dequant(acc, a, np.float32(0.02) * np.float32(8))
+    assert np.array_equal(y2, (y * np.float32(8)).astype(np.float32))
+
+
+def test_dequant_bf16_is_rounded_f32():
+    import torch
+    rng = np.random.default_rng(16)
+    acc = rng.integers(-10**5, 10**5, size=(2, 300))
+    a = rng.random(2).astype(np.float32)
+    y32 = oracle.dequant(acc, a, np.float32(0.03))
+    yb = oracle.dequant(acc, a, np.float32(0.03), out="bf16")
+    ref = torch.from_numpy(y32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(yb, ref)
+
+
+def test_linear_activation_sign_and_scale():
+    T, w, x = inputs.random_problem(17, 3, 40, 70)
+    y, acc, q, a, r = oracle.w2a8_linear(T, w, x)
+    yn, accn, qn, _, _ = oracle.w2a8_linear(T, w, -x)
+    assert np.array_equal(accn, -acc) and np.array_equal(qn, -q)
+    assert np.array_equal(yn, -y)
+    y4, acc4, _, _, _ = oracle.w2a8_linear(T, w, (x * np.float32(4)).astype(np.float32))
+    assert np.array_equal(acc4, acc) and np.array_equal(y4, (y * np.float32(4)).astype(np.float32))
+
+
+def test_linear_row_independence():
+    T, w, x = inputs.random_problem(18, 6, 33, 90)
+    y, acc, *_ = oracle.w2a8_linear(T, w, x)
+    for m in range(6):
+        y1, acc1, *_ = oracle.w2a8_linear(T, w, x[m:m + 1])
+        assert np.array_equal(acc1[0], acc[m]) and np.array_equal(y1[0], y[m])
+
+
+# ---------------------------------------------------------------------------
+# Packed format: hand-derived words, round trip, trailer
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", list(_rows("pack_words.txt")))
+def test_pack_golden_words(case):
+    shape, entries, words = case
+    N, K = (int(v) for v in shape.split())
+    T = np.zeros((N, K), dtype=np.int8)
+    if entries != "-":
+        for e in entries.split():
+            n, k, t = (int(v) for v in e.split(":"))
+            T[n, k] = t
+    pk = oracle.pack_tiles(T)
+    assert pk.size == oracle.packed_bytes(N, K)
+    body = pk[:-16].view(np.uint32)
+    for w in words.split():
+        idx, val = w.split(":")
+        assert body[int(idx)] == int(val, 16), (idx, hex(int(body[int(idx)])))
+    assert oracle.read_trailer(pk, N, K) == (oracle.TRAILER_MAGIC, N, K, 0)
+
+
+@pytest.mark.parametrize("N,K", [(1, 1), (5, 17), (128, 128), (129, 300), (640, 2560), (300, 1000)])
+def test_pack_round_trip(N, K):
+    T = inputs.ternary(np.random.default_rng(N + K), (N, K), None)
+    pk = oracle.pack_tiles(T)
+    assert np.array_equal(oracle.unpack_tiles(pk, N, K), T)
+    nt, kt = -(-N // 128), -(-K // 128)
+    assert pk.size == nt * kt * 4096 + 16
+
+
+def test_pack_counts_invalid():
+    T = np.zeros((3, 40), dtype=np.int8)
+    T[0, 0] = 2
+    T[2, 39] = -128
+    pk = oracle.pack_tiles(T)
+    assert oracle.read_trailer(pk, 3, 40)[3] == 2
+
+
+def test_unpack_rejects_code_three():
+    pk = oracle.pack_tiles(np.zeros((1, 16), np.int8))
+    pk[0] = 0xFF
+    with pytest.raises(ValueError):
+        oracle.unpack_tiles(pk, 1, 16)
