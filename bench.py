@@ -1,0 +1,444 @@
+"""Benchmark of the W2A8 ternary linear on GB300.
+
+Default workload (one "step"): the BitNet-2B-shaped layer set -- projections
+q 2560->2560, k/v 2560->640, o 2560->2560, gate/up 2560->6912, down 6912->2560,
+ternary weights with P(0)=0.5, bf16 activations with 1% outliers x20 -- at
+block widths M = 1, 2, 4, 8.  One step runs, for each width, the seven
+projections back to back, each a single fused launch (absmax quantisation of
+the raw bf16 rows, 2-bit weight stream, exact integer product, dequant to
+bf16).  Weights rotate over enough distinct copies that no step finds its
+weights in L2.  Steps are replayed from CUDA graphs with programmatic
+dependent launch between consecutive linears.
+
+Metric: achieved HBM GB/s on algorithmic bytes (packed weights + activations),
+also as a fraction of the measured copy bandwidth, plus rows/s per width.
+
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload (its only use of the oracle besides the cpu_baseline field).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from ternary_w2a8_linear_gb300 import inputs  # noqa: E402
+
+WIDTHS = (1, 2, 4, 8)
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "W2A8 linear achieved HBM GB/s (% of roofline) and rows/s at widths 1-16"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--copies", type=int, default=16, help="distinct weight copies rotated per step")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--e2e-steps", type=int, default=200)
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------
+def algorithmic_bytes(K, N, M, x_bytes=2):
+    """Packed weight bytes (tiles) + activation bytes of one linear."""
+    pk = -(-N // 128) * -(-K // 128) * 4096
+    return pk + M * K * x_bytes
+
+
+def step_bytes():
+    tot = 0
+    for M in WIDTHS:
+        for _, K, N in inputs.BITNET2B_PROJ:
+            tot += algorithmic_bytes(K, N, M)
+    return tot
+
+
+def out_bytes_per_step():
+    return sum(M * N * 2 for M in WIDTHS for _, _, N in inputs.BITNET2B_PROJ)
+
+
+def in_bytes_per_step():
+    return sum(M * K * 2 for M in WIDTHS for _, K, _ in inputs.BITNET2B_PROJ)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+def run_ours(args, rank, world):
+    import torch
+    import ternary_w2a8_linear_gb300.linear as L
+    from ternary_w2a8_linear_gb300 import build as B
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    B.build()
+    L.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    R = max(4, args.copies)
+
+    # weights: R distinct copies of the layer set (different layer seeds)
+    weights = []   # weights[c][p] = (pk, w_scale, K, N)
+    with torch.cuda.stream(stream):
+        for c in range(R):
+            row = []
+            for p, (_, K, N) in enumerate(inputs.BITNET2B_PROJ):
+                T, w = inputs.bitnet2b_weights(p, layer=c)
+                pk = L.pack(torch.from_numpy(T).to(dev), stream=stream)
+                row.append((pk, float(w), K, N))
+            weights.append(row)
+        xs = [torch.from_numpy(inputs.bitnet2b_act(p, 16).view(np.int16)).to(dev).view(torch.bfloat16)
+              for p in range(len(inputs.BITNET2B_PROJ))]
+        ys = [torch.empty((16, N), dtype=torch.bfloat16, device=dev) for _, _, N in inputs.BITNET2B_PROJ]
+    torch.cuda.synchronize()
+
+    def enqueue_step(s, widths=WIDTHS, flags=L.FLAG_PDL):
+        n = 0
+        for wi, M in enumerate(widths):
+            c = (s * len(WIDTHS) + WIDTHS.index(M)) % R
+            for p, (pk, w, K, N) in enumerate(weights[c]):
+                act = L.Act(L.BF16, xs[p].data_ptr(), K, None)
+                out = L.Out(L.BF16, ys[p].data_ptr(), N, None, 0)
+                st = L.bitmtp_linear_gemm(pk.data_ptr(), w, N, K, M, act, out, flags,
+                                          L.ctypes.c_void_p(stream.cuda_stream))
+                if st != L.OK:
+                    raise L.BitmtpError(st, "gemm")
+                n += 1
+        return n
+
+    def capture(nsteps, start, widths=WIDTHS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            enqueue_step(start, widths)          # untimed warm call outside capture
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for s in range(nsteps):
+                    enqueue_step(start + s, widths)
+        return g
+
+    G = 16  # steps per graph; weights cycle every R/len(WIDTHS) steps
+    g_full = capture(G, 0)
+    K = args.steps
+    reps, rem = divmod(K, G)
+    g_rem = capture(rem, 0) if rem else None
+    launches_per_step = len(WIDTHS) * len(inputs.BITNET2B_PROJ)
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, -(-args.warmup // G))):
+            g_full.replay()
+    stream.synchronize()
+
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    clocks = sampler.stop() if sampler else None
+    ms = e0.elapsed_time(e1)
+    ms = dist_max(ms, world)
+    sec = ms / 1e3
+    bytes_step = step_bytes()
+    value = bytes_step * K * world / sec / 1e9
+    ms_per_step = ms / K
+
+    # per-width breakdown (same rotation, widths timed on their own)
+    per_width = {}
+    for M in WIDTHS:
+        g = capture(G, 0, (M,))
+        with torch.cuda.stream(stream):
+            g.replay()
+            stream.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            n_rep = 20
+            a.record(stream)
+            for _ in range(n_rep):
+                g.replay()
+            b.record(stream)
+        b.synchronize()
+        t = a.elapsed_time(b) / 1e3 / (n_rep * G)  # seconds per width-pass (7 linears)
+        byt = sum(algorithmic_bytes(Kp, Np, M) for _, Kp, Np in inputs.BITNET2B_PROJ)
+        per_width[str(M)] = {"gbs": round(byt / t / 1e9, 1), "us_per_layer_set": round(t * 1e6, 2),
+                             "rows_per_s": round(M / t, 1),
+                             "us_per_linear": round(t * 1e6 / len(inputs.BITNET2B_PROJ), 2)}
+        del g
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, L, torch, dev, stream, weights, rank, world)
+
+    return dict(value=value, ms_per_step=ms_per_step, clocks=clocks, per_width=per_width, e2e=e2e,
+                gpu_launches=K * launches_per_step, copies=R, graph_steps=G)
+
+
+def run_e2e(args, L, torch, dev, stream, weights, rank, world):
+    """Same workload through the binding with host buffers: every step copies
+    its activations host->device from pinned memory and reads the outputs back."""
+    R = len(weights)
+    hx = [torch.from_numpy(inputs.bitnet2b_act(p, 16).view(np.int16)).view(torch.bfloat16).pin_memory()
+          for p in range(len(inputs.BITNET2B_PROJ))]
+    dx = [torch.empty_like(h, device=dev) for h in hx]
+    dy = [torch.empty((16, N), dtype=torch.bfloat16, device=dev) for _, _, N in inputs.BITNET2B_PROJ]
+    hy = [torch.empty((16, N), dtype=torch.bfloat16).pin_memory() for _, _, N in inputs.BITNET2B_PROJ]
+    steps = args.e2e_steps
+
+    def one(s):
+        for M in WIDTHS:
+            c = (s * len(WIDTHS) + WIDTHS.index(M)) % R
+            for p, (pk, w, K, N) in enumerate(weights[c]):
+                dx[p][:M].copy_(hx[p][:M], non_blocking=True)
+                L.gemm(pk, w, N, K, dx[p][:M], y=dy[p][:M], stream=stream)
+                hy[p][:M].copy_(dy[p][:M], non_blocking=True)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for s in range(3):
+            one(s)
+        dist_barrier(world)
+        t0 = time.perf_counter()
+        for s in range(steps):
+            one(s)
+        t1 = time.perf_counter()
+    sec = dist_max(t1 - t0, world)
+    return {"value": round(step_bytes() * steps * world / sec / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": in_bytes_per_step(), "d2h_bytes_per_step": out_bytes_per_step(),
+            "steps": steps, "ms_per_step": round(sec * 1e3 / steps, 4)}
+
+
+# --------------------------------------------------------------------------
+def oracle_sample(seconds):
+    """Time the CPU oracle on the workload's linears, cycling (width, projection)
+    pairs until about `seconds` of work.  Returns (GB/s, description)."""
+    import oracle
+    pairs = [(M, p) for M in WIDTHS for p in range(len(inputs.BITNET2B_PROJ))]
+    data = {}
+    done_bytes, done_sec, n = 0, 0.0, 0
+    while done_sec < seconds:
+        M, p = pairs[n % len(pairs)]
+        if p not in data:
+            T, w = inputs.bitnet2b_weights(p, layer=0)
+            data[p] = (T, w, inputs.bitnet2b_act(p, 16))
+        T, w, x = data[p]
+        _, K, N = inputs.BITNET2B_PROJ[p]
+        t0 = time.perf_counter()
+        oracle.w2a8_linear(T, w, x[:M], "bf16", x_is_bf16=True)
+        done_sec += time.perf_counter() - t0
+        done_bytes += algorithmic_bytes(K, N, M)
+        n += 1
+    return done_bytes / done_sec / 1e9, f"{n} linears of the layer set cycling widths {list(WIDTHS)}", n
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    per = []
+    tot_b, tot_s = 0, 0.0
+    import oracle
+    pairs = [(M, p) for M in WIDTHS for p in range(len(inputs.BITNET2B_PROJ))]
+    cache = {}
+
+    def step(i):
+        M, p = pairs[i % len(pairs)]
+        if p not in cache:
+            T, w = inputs.bitnet2b_weights(p, layer=0)
+            cache[p] = (T, w, inputs.bitnet2b_act(p, 16))
+        T, w, x = cache[p]
+        _, K, N = inputs.BITNET2B_PROJ[p]
+        t0 = time.perf_counter()
+        oracle.w2a8_linear(T, w, x[:M], "bf16", x_is_bf16=True)
+        return algorithmic_bytes(K, N, M), time.perf_counter() - t0
+
+    for i in range(args.warmup):
+        step(i)
+    for i in range(args.steps):
+        b, s = step(args.warmup + i)
+        tot_b += b
+        tot_s += s
+        per.append(s)
+    v = tot_b / tot_s / 1e9
+    line = {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "w2a8-int32",
+            "data": "synthetic", "impl": "reference",
+            "config": workload_config(args),
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "each step is one (width, projection) linear of the layer set, "
+                                       "cycling widths 1,2,4,8 and the 7 projections"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def workload_config(args, extra=None):
+    cfg = {"workload": "bitnet2b_layer_set", "projections": "q,k,v,o 2560->2560/640/640/2560; gate,up 2560->6912; "
+                                                       "down 6912->2560",
+           "widths": list(WIDTHS), "weights": "ternary P(0)=0.5, per-tensor scale U[0.01,0.05]",
+           "activations": "bf16 N(0,1), 1% x20 outliers, quantised per row in-kernel",
+           "output": "bf16", "parallelism": f"replicas{args.gpus}"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# --------------------------------------------------------------------------
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("BITMTP_DIST_BACKEND", "nccl")
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(v, world):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse()
+    rank, world = dist_init()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    res = run_ours(args, rank, world)
+    if rank != 0:
+        return
+    peak, peak_kind = load_peaks()
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, desc, n = oracle_sample(args.cpu_seconds)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
+    value = res["value"]
+    per_gpu = value / world
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "w2a8-int32",
+        "data": "synthetic (seeded ternary weights, bf16 activations)",
+        "config": workload_config(args, {"weight_copies": res["copies"],
+                                         "l2": f"weights rotate over {res['copies']} distinct copies "
+                                               f"({res['copies']} x 17.4 MB > L2)",
+                                         "graph_steps": res["graph_steps"], "launch": "CUDA graph + PDL"}),
+        "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(per_gpu / peak, 4), "peak_kind": peak_kind, "traffic": None,
+                     "kernel": "w2a8_gemm_kernel (all launches of the step)"},
+        "per_width": res["per_width"],
+        "e2e": res["e2e"],
+        "gpu_launches": res["gpu_launches"],
+        "clocks": res["clocks"],
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

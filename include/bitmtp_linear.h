@@ -1,0 +1,186 @@
+/*
+ * bitmtp_linear.h -- C ABI of the GB300 (sm_103a) W2A8 ternary linear.
+ *
+ * The operation is the "packed W2A8" linear of "BitMTP: When Multi-Token
+ * Prediction Meets Low-Bit Large Language Models" (AI summary): ternary
+ * BitNet b1.58-style weights ("What This Paper Is About"), 2-bit weights and
+ * 8-bit activations ("Main Findings", first bullet), run through packed
+ * low-bit operators that are picked by block width and by input/output
+ * dimensions, including role-dependent output projections ("Methodology in
+ * Plain English", third and last paragraphs).  The pages print no formula;
+ * the library implements the BitNet b1.58 definitions:
+ *
+ *   weights      T[n][k] in {-1, 0, +1}, one fp32 per-tensor scale w_scale,
+ *                W ~= w_scale * T;
+ *   activations  per row m: amax = max_k |x[m][k]|, s = RN(127 / amax),
+ *                q[m][k] = clamp(rint(RN(x * s)), -127, 127) (fp32, round
+ *                half to even), a_scale[m] = RN(amax / 127); a zero row gives
+ *                q = 0 and a_scale = 0;
+ *   product      acc[m][n] = sum_k T[n][k] * q[m][k]   (exact int32);
+ *   epilogue     y[m][n] = acc[m][n] * a_scale[m] * w_scale  (fp32, or that
+ *                value rounded to bf16).
+ *
+ * Conventions for every call:
+ *   - Matrices are row-major; ld* arguments count elements between rows.
+ *   - Pointers are DEVICE pointers owned by the caller unless stated
+ *     otherwise.  The library never allocates device memory and keeps no
+ *     per-call state.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously on it; only
+ *     bitmtp_linear_pack and bitmtp_linear_device_error synchronise it.
+ *   - Arguments are validated on the host before any CUDA call; an invalid
+ *     call returns a negative status and enqueues nothing.  Nothing is thrown
+ *     across the ABI.
+ *   - The current CUDA device must be compute capability 10.3 (sm_103a);
+ *     otherwise calls return BITMTP_ERR_UNSUPPORTED.
+ */
+#ifndef BITMTP_LINEAR_H
+#define BITMTP_LINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define BITMTP_OK               0
+#define BITMTP_ERR_INVALID     (-1) /* NULL pointer, unknown enum, ld too small   */
+#define BITMTP_ERR_ALIGN       (-2) /* packed-weight pointer not 16-byte aligned  */
+#define BITMTP_ERR_SHAPE       (-3) /* dimension out of the supported range, or
+                                       pk_bytes smaller than packed_bytes(N, K)   */
+#define BITMTP_ERR_NOT_TERNARY (-4) /* pack: an entry of T outside {-1, 0, +1}    */
+#define BITMTP_ERR_UNSUPPORTED (-5) /* no device, or device is not sm_103        */
+#define BITMTP_ERR_CUDA        (-6) /* a CUDA runtime call failed                 */
+#define BITMTP_ERR_DEVICE      (-7) /* a kernel gave up a bounded wait (see
+                                       bitmtp_linear_device_error)               */
+
+/* ---- element kinds --------------------------------------------------------- */
+#define BITMTP_F32  0   /* IEEE fp32                                   */
+#define BITMTP_BF16 1   /* bfloat16 (raw 16-bit patterns)              */
+#define BITMTP_Q8   2   /* int8 codes plus a per-row fp32 a_scale      */
+
+/* ---- limits --------------------------------------------------------------- */
+#define BITMTP_MAX_M      16       /* block width: rows per call (draft + verify rows) */
+#define BITMTP_MAX_K      32768    /* in-features                                     */
+#define BITMTP_MAX_N      16777216 /* out-features                                    */
+#define BITMTP_MAX_GROUP  8        /* problems in one grouped launch                  */
+
+/* ---- gemm flags ------------------------------------------------------------ */
+/* Programmatic dependent launch: the GEMM may be scheduled while the kernel
+ * launched before it on the same stream is still running, and it starts
+ * streaming the packed weights before that kernel has finished.  It waits for
+ * that kernel's completion before reading activations or writing outputs.
+ * Only valid when the packed weights are not written by the preceding kernel. */
+#define BITMTP_FLAG_PDL        0x1u
+/* Force one of the two compute paths instead of the width/shape table
+ * (testing and measurement): the tensor-core path (tcgen05, all widths) or the
+ * integer dot-product path (dp4a, widths 1..4). */
+#define BITMTP_FLAG_FORCE_TC   0x2u
+#define BITMTP_FLAG_FORCE_DP   0x4u
+
+/*
+ * Packed ternary weights (this library's own layout; the pages only say the
+ * weights are executed "packed"): rows in tiles of 128, k in tiles of 128,
+ * both padded with T = 0.  Tile (rt, kt) is 4096 contiguous bytes at offset
+ * (rt * ceil(K/128) + kt) * 4096.  Inside a tile row r owns eight 32-bit
+ * words; word j of row r sits at word index (j/4)*512 + r*4 + j%4 and holds
+ * k = kt*128 + 16*j + 2*p + e (p = 0..7, e = 0..1) as u = T + 1 in bits
+ * 16*e + 2*p.  A 16-byte trailer {0x38413242, N, K, invalid-count} follows.
+ * 2 bits per weight; the trailer is 16 bytes.
+ */
+
+/* Bytes needed for the packed form of an N x K ternary matrix:
+ * ceil(N/128) * ceil(K/128) * 4096 + 16.  Returns 0 if N < 1 or K < 1. */
+size_t bitmtp_linear_packed_bytes(int64_t N, int64_t K);
+
+/* Pack ternary weights (offline step before the linear).
+ *   T        device int8 [N][ldt], entries in {-1, 0, +1}
+ *   N, K     out- and in-features (1 <= N <= BITMTP_MAX_N, 1 <= K <= BITMTP_MAX_K)
+ *   ldt      >= K
+ *   pk       device buffer of pk_bytes >= bitmtp_linear_packed_bytes(N, K),
+ *            16-byte aligned; fully overwritten (tiles and trailer)
+ * Synchronises `stream` to read the invalid-entry count; returns
+ * BITMTP_ERR_NOT_TERNARY (pk then holds a clamped, unusable packing) if any
+ * entry was outside {-1, 0, +1}. */
+int bitmtp_linear_pack(const int8_t* T, int64_t N, int64_t K, int64_t ldt,
+                       void* pk, size_t pk_bytes, void* stream);
+
+/* Quantise a block of activation rows to int8 codes with per-row scales
+ * (the quantiser defined at the top of this file).
+ *   x        device [M][ldx], element kind x_kind = BITMTP_F32 or BITMTP_BF16,
+ *            finite values
+ *   M, K     rows (0 <= M <= 2^20) and in-features (1 <= K <= BITMTP_MAX_K)
+ *   q        device int8 [M][ldq], ldq >= K
+ *   a_scale  device fp32 [M]   = amax/127 (0 for an all-zero row)
+ *   rowsum   device int32 [M]  = sum_k q[m][k]; may be NULL
+ * M == 0 is a no-op. */
+int bitmtp_linear_quant_act(const void* x, int x_kind, int64_t M, int64_t K, int64_t ldx,
+                            int8_t* q, int64_t ldq, float* a_scale, int32_t* rowsum,
+                            void* stream);
+
+/* Activation operand of a GEMM. */
+typedef struct bitmtp_act {
+    int kind;              /* BITMTP_F32 / BITMTP_BF16: raw rows, quantised inside the
+                              GEMM with the quantiser above (bit-identical to
+                              bitmtp_linear_quant_act);  BITMTP_Q8: int8 codes        */
+    const void* x;         /* [M][ldx] elements of `kind` (int8 for BITMTP_Q8)        */
+    int64_t ldx;           /* >= K                                                   */
+    const float* a_scale;  /* BITMTP_Q8 only: [M] per-row scales; ignored otherwise   */
+} bitmtp_act;
+
+/* Output of a GEMM. */
+typedef struct bitmtp_out {
+    int dtype;             /* BITMTP_F32 or BITMTP_BF16 (round-to-nearest-even)     */
+    void* y;               /* [M][ldy]                                              */
+    int64_t ldy;           /* >= N                                                  */
+    int32_t* acc;          /* optional int32 [M][lda] accumulators, may be NULL     */
+    int64_t lda;           /* >= N when acc != NULL                                  */
+} bitmtp_out;
+
+/* y = dequant(T * q): the W2A8 linear at block width M.
+ *   pk       packed weights from bitmtp_linear_pack (16-byte aligned)
+ *   w_scale  per-tensor weight scale
+ *   N, K     out-/in-features the weights were packed with
+ *   M        block width, 0 <= M <= BITMTP_MAX_M (0: no-op)
+ *   flags    BITMTP_FLAG_* bits
+ * The compute path and launch shape are chosen from (M, N, K) (width
+ * specialisation); results do not depend on the choice. */
+int bitmtp_linear_gemm(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M,
+                       const bitmtp_act* act, const bitmtp_out* out,
+                       unsigned flags, void* stream);
+
+/* One problem of a grouped launch (same meaning as bitmtp_linear_gemm). */
+typedef struct bitmtp_gemm_desc {
+    const void* pk;
+    float w_scale;
+    int64_t N, K, M;
+    bitmtp_act act;
+    bitmtp_out out;
+} bitmtp_gemm_desc;
+
+/* Run up to BITMTP_MAX_GROUP independent problems in ONE kernel launch --
+ * the role-dependent output projections of one block step (e.g. verify rows
+ * through one projection and draft rows through another).  `d` is a HOST
+ * array of n_desc descriptors (copied by value into the launch).  Problems
+ * must not write overlapping outputs. */
+int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc,
+                               unsigned flags, void* stream);
+
+/* Synchronise `stream`, then return and clear the device error word that a
+ * kernel sets when one of its bounded waits expires (0 = none; otherwise a
+ * code naming the wait).  Never set by correct launches. */
+int bitmtp_linear_device_error(void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* bitmtp_linear_status_string(int status);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int bitmtp_linear_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITMTP_LINEAR_H */

@@ -1,0 +1,358 @@
+// api.cu -- the C ABI (include/bitmtp_linear.h): argument validation, device
+// checks, the width/shape dispatch table and the pack / activation-quantisation
+// kernels.  The GEMM kernels live in gemm.cu.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "internal.h"
+#include "quant.cuh"
+
+namespace bitmtp {
+
+// Device error word: set by a kernel whose bounded wait expired.
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr uint32_t kTrailerMagic = 0x38413242u;
+
+// ----------------------------------------------------------------- pack --
+// Grid (KT, NT); each block writes one 4 KiB tile, each thread four words.
+__global__ void __launch_bounds__(256)
+pack_kernel(const int8_t* __restrict__ T, long long ldt, int N, int K, int KT,
+            uint32_t* __restrict__ pk, uint32_t* __restrict__ invalid) {
+    const int kt = blockIdx.x;
+    const int rt = blockIdx.y;
+    uint32_t* tile = pk + (static_cast<size_t>(rt) * KT + kt) * (kTileBytes / 4);
+    int bad = 0;
+    for (int widx = threadIdx.x; widx < kTileBytes / 4; widx += blockDim.x) {
+        const int half = widx >> 9;
+        const int r = (widx & 511) >> 2;
+        const int j = half * 4 + (widx & 3);
+        const int n = rt * kTileN + r;
+        const int k0 = kt * kTileK + 16 * j;
+        uint32_t word = 0;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            const int k = k0 + kk;
+            int t = 0;
+            if (n < N && k < K) t = T[static_cast<long long>(n) * ldt + k];
+            if (t < -1 || t > 1) {
+                ++bad;
+                t = t < 0 ? -1 : 1;
+            }
+            word |= static_cast<uint32_t>(t + 1) << (16 * (kk & 1) + 2 * (kk >> 1));
+        }
+        tile[widx] = word;
+    }
+    // block-reduce the invalid count
+    for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if ((threadIdx.x & 31) == 0 && bad) atomicAdd(invalid, static_cast<uint32_t>(bad));
+}
+
+// ------------------------------------------------------------ quant_act --
+// One block per activation row.
+__global__ void __launch_bounds__(256)
+quant_act_kernel(const void* __restrict__ x, int kind, int K, long long ldx, int8_t* __restrict__ q,
+                 long long ldq, float* __restrict__ a_scale, int32_t* __restrict__ rowsum) {
+    __shared__ float red_f[8];
+    __shared__ int red_i[8];
+    const int m = blockIdx.x;
+    const int tid = threadIdx.x;
+    const long long xo = static_cast<long long>(m) * ldx;
+    float a = 0.f;
+    for (int k = tid; k < K; k += blockDim.x) a = fmaxf(a, fabsf(load_act(x, kind, xo + k)));
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if ((tid & 31) == 0) red_f[tid >> 5] = a;
+    __syncthreads();
+    float amax = red_f[0];
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) amax = fmaxf(amax, red_f[w]);
+    const float s = quant_scale(amax);
+    int sum = 0;
+    const long long qo = static_cast<long long>(m) * ldq;
+    for (int k = tid; k < K; k += blockDim.x) {
+        const int v = (amax > 0.f) ? quantize(load_act(x, kind, xo + k), s) : 0;
+        q[qo + k] = static_cast<int8_t>(v);
+        sum += v;
+    }
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if ((tid & 31) == 0) red_i[tid >> 5] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        int tot = 0;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += red_i[w];
+        a_scale[m] = dequant_scale(amax);
+        if (rowsum) rowsum[m] = tot;
+    }
+}
+
+// ------------------------------------------------------------- device --
+struct DevInfo {
+    int checked = 0;   // 0 unknown, 1 ok, -1 unsupported
+    int sms = 0;
+    int* err = nullptr;
+};
+DevInfo g_dev[64];
+
+int current_device(DevInfo** info) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return BITMTP_ERR_UNSUPPORTED;
+    }
+    if (dev >= 64) return BITMTP_ERR_UNSUPPORTED;
+    DevInfo& d = g_dev[dev];
+    if (d.checked == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return BITMTP_ERR_UNSUPPORTED;
+        }
+        if (major != 10 || minor != 3) {
+            d.checked = -1;
+        } else {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+                cudaGetLastError();
+                return BITMTP_ERR_CUDA;
+            }
+            d.err = static_cast<int*>(p);
+            d.sms = sms;
+            d.checked = 1;
+        }
+    }
+    if (d.checked != 1) return BITMTP_ERR_UNSUPPORTED;
+    *info = &d;
+    return BITMTP_OK;
+}
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return BITMTP_OK;
+    cudaGetLastError();
+    return BITMTP_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Validate one GEMM problem and fill its kernel descriptor (no CUDA calls).
+int check_problem(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M,
+                  const bitmtp_act* act, const bitmtp_out* out, GemmProblem* g) {
+    if (!act || !out) return BITMTP_ERR_INVALID;
+    if (M < 0 || M > BITMTP_MAX_M || N < 0 || N > BITMTP_MAX_N || K < 1 || K > BITMTP_MAX_K)
+        return BITMTP_ERR_SHAPE;
+    if (M == 0 || N == 0) {
+        g->M = 0;
+        g->N = 0;
+        return BITMTP_OK;
+    }
+    if (!pk) return BITMTP_ERR_INVALID;
+    if (!aligned16(pk)) return BITMTP_ERR_ALIGN;
+    if (act->kind != BITMTP_F32 && act->kind != BITMTP_BF16 && act->kind != BITMTP_Q8)
+        return BITMTP_ERR_INVALID;
+    if (!act->x || act->ldx < K) return BITMTP_ERR_INVALID;
+    if (act->kind == BITMTP_Q8 && !act->a_scale) return BITMTP_ERR_INVALID;
+    if (out->dtype != BITMTP_F32 && out->dtype != BITMTP_BF16) return BITMTP_ERR_INVALID;
+    if (!out->y || out->ldy < N) return BITMTP_ERR_INVALID;
+    if (out->acc && out->lda < N) return BITMTP_ERR_INVALID;
+    if (!(w_scale == w_scale)) return BITMTP_ERR_INVALID;  // NaN scale
+    g->pk = static_cast<const uint8_t*>(pk);
+    g->x = act->x;
+    g->a_scale = act->a_scale;
+    g->y = out->y;
+    g->acc = out->acc;
+    g->ldx = act->ldx;
+    g->ldy = out->ldy;
+    g->lda = out->acc ? out->lda : 0;
+    g->w_scale = w_scale;
+    g->N = static_cast<int>(N);
+    g->K = static_cast<int>(K);
+    g->M = static_cast<int>(M);
+    g->nt = static_cast<int>(ceil_div(N, kTileN));
+    g->kt = static_cast<int>(ceil_div(K, kTileK));
+    g->act_kind = act->kind;
+    g->out_dtype = out->dtype;
+    g->cluster_begin = 0;
+    return BITMTP_OK;
+}
+
+// Width-specialised operator choice (the analogue of picking packed low-bit
+// operators by replay width and input/output dimensions).
+int choose_path(int max_m, unsigned flags, int* dp_rows) {
+    if (flags & BITMTP_FLAG_FORCE_TC) return kPathTC;
+    int r = max_m <= 1 ? 1 : (max_m <= 2 ? 2 : 4);
+    if (flags & BITMTP_FLAG_FORCE_DP) {
+        if (max_m > 4) return -1;
+        *dp_rows = r;
+        return kPathDP;
+    }
+    if (max_m <= 2) {
+        *dp_rows = r;
+        return kPathDP;
+    }
+    return kPathTC;
+}
+
+// Split-K factor: enough CTAs to cover every SM about twice, at most 16 per
+// cluster, at most kMaxKtPerCta resident k tiles per CTA.
+int choose_csize(int total_row_tiles, int max_kt, int sms) {
+    const int target = 2 * sms;
+    int c = static_cast<int>(ceil_div(target, total_row_tiles));
+    c = std::min(c, kMaxCluster);
+    c = std::min(c, max_kt);
+    const int need = static_cast<int>(ceil_div(max_kt, kMaxKtPerCta));
+    c = std::max(c, need);
+    return std::max(c, 1);
+}
+
+int run_gemms(const GemmProblem* probs, int n, unsigned flags, cudaStream_t stream) {
+    bool any = false;
+    for (int i = 0; i < n; ++i) any = any || (probs[i].M > 0 && probs[i].N > 0);
+    if (!any) return BITMTP_OK;  // empty problems never touch the device
+    DevInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != BITMTP_OK) return st;
+    GemmParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    int total_rt = 0, max_kt = 1, max_m = 1, np = 0;
+    for (int i = 0; i < n; ++i) {
+        if (probs[i].M == 0 || probs[i].N == 0) continue;
+        prm.p[np] = probs[i];
+        prm.p[np].cluster_begin = total_rt;
+        total_rt += probs[i].nt;
+        max_kt = std::max(max_kt, probs[i].kt);
+        max_m = std::max(max_m, probs[i].M);
+        ++np;
+    }
+    if (np == 0) return BITMTP_OK;
+    int dp_rows = 1;
+    const int path = choose_path(max_m, flags, &dp_rows);
+    if (path < 0) return BITMTP_ERR_SHAPE;
+    prm.n_problems = np;
+    prm.csize = choose_csize(total_rt, max_kt, dev->sms);
+    prm.nkt_max = static_cast<int>(ceil_div(max_kt, prm.csize));
+    if (prm.nkt_max > kMaxKtPerCta) return BITMTP_ERR_SHAPE;
+    prm.err = dev->err;
+    return cuda_status(launch_gemm(prm, path, dp_rows, total_rt, (flags & BITMTP_FLAG_PDL) != 0, stream));
+}
+
+}  // namespace
+}  // namespace bitmtp
+
+using namespace bitmtp;
+
+extern "C" {
+
+size_t bitmtp_linear_packed_bytes(int64_t N, int64_t K) {
+    if (N < 1 || K < 1 || N > BITMTP_MAX_N || K > BITMTP_MAX_K) return 0;
+    return static_cast<size_t>(ceil_div(N, kTileN)) * static_cast<size_t>(ceil_div(K, kTileK)) * kTileBytes + 16;
+}
+
+int bitmtp_linear_pack(const int8_t* T, int64_t N, int64_t K, int64_t ldt, void* pk, size_t pk_bytes,
+                       void* stream) {
+    if (N < 1 || K < 1 || N > BITMTP_MAX_N || K > BITMTP_MAX_K) return BITMTP_ERR_SHAPE;
+    if (!T || !pk || ldt < K) return BITMTP_ERR_INVALID;
+    if (!aligned16(pk)) return BITMTP_ERR_ALIGN;
+    const size_t need = bitmtp_linear_packed_bytes(N, K);
+    if (pk_bytes < need) return BITMTP_ERR_SHAPE;
+    DevInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != BITMTP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int NT = static_cast<int>(ceil_div(N, kTileN));
+    const int KT = static_cast<int>(ceil_div(K, kTileK));
+    uint8_t* base = static_cast<uint8_t*>(pk);
+    uint32_t* trailer = reinterpret_cast<uint32_t*>(base + need - 16);
+    const uint32_t head[4] = {kTrailerMagic, static_cast<uint32_t>(N), static_cast<uint32_t>(K), 0u};
+    st = cuda_status(cudaMemcpyAsync(trailer, head, sizeof(head), cudaMemcpyHostToDevice, s));
+    if (st != BITMTP_OK) return st;
+    pack_kernel<<<dim3(KT, NT), 256, 0, s>>>(T, ldt, static_cast<int>(N), static_cast<int>(K), KT,
+                                             reinterpret_cast<uint32_t*>(base), trailer + 3);
+    st = cuda_status(cudaGetLastError());
+    if (st != BITMTP_OK) return st;
+    uint32_t invalid = 0;
+    st = cuda_status(cudaMemcpyAsync(&invalid, trailer + 3, 4, cudaMemcpyDeviceToHost, s));
+    if (st != BITMTP_OK) return st;
+    st = cuda_status(cudaStreamSynchronize(s));
+    if (st != BITMTP_OK) return st;
+    return invalid ? BITMTP_ERR_NOT_TERNARY : BITMTP_OK;
+}
+
+int bitmtp_linear_quant_act(const void* x, int x_kind, int64_t M, int64_t K, int64_t ldx, int8_t* q,
+                            int64_t ldq, float* a_scale, int32_t* rowsum, void* stream) {
+    if (M < 0 || M > (1 << 20) || K < 1 || K > BITMTP_MAX_K) return BITMTP_ERR_SHAPE;
+    if (x_kind != BITMTP_F32 && x_kind != BITMTP_BF16) return BITMTP_ERR_INVALID;
+    if (M == 0) return BITMTP_OK;
+    if (!x || !q || !a_scale || ldx < K || ldq < K) return BITMTP_ERR_INVALID;
+    DevInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != BITMTP_OK) return st;
+    quant_act_kernel<<<static_cast<unsigned>(M), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        x, x_kind, static_cast<int>(K), ldx, q, ldq, a_scale, rowsum);
+    return cuda_status(cudaGetLastError());
+}
+
+int bitmtp_linear_gemm(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M, const bitmtp_act* act,
+                       const bitmtp_out* out, unsigned flags, void* stream) {
+    GemmProblem g;
+    std::memset(&g, 0, sizeof(g));
+    int st = check_problem(pk, w_scale, N, K, M, act, out, &g);
+    if (st != BITMTP_OK) return st;
+    if ((flags & BITMTP_FLAG_FORCE_TC) && (flags & BITMTP_FLAG_FORCE_DP)) return BITMTP_ERR_INVALID;
+    if (g.M == 0) return BITMTP_OK;
+    return run_gemms(&g, 1, flags, static_cast<cudaStream_t>(stream));
+}
+
+int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc, unsigned flags, void* stream) {
+    if (n_desc < 0 || n_desc > BITMTP_MAX_GROUP) return BITMTP_ERR_SHAPE;
+    if (n_desc > 0 && !d) return BITMTP_ERR_INVALID;
+    if ((flags & BITMTP_FLAG_FORCE_TC) && (flags & BITMTP_FLAG_FORCE_DP)) return BITMTP_ERR_INVALID;
+    GemmProblem g[BITMTP_MAX_GROUP];
+    std::memset(g, 0, sizeof(g));
+    for (int i = 0; i < n_desc; ++i) {
+        int st = check_problem(d[i].pk, d[i].w_scale, d[i].N, d[i].K, d[i].M, &d[i].act, &d[i].out, &g[i]);
+        if (st != BITMTP_OK) return st;
+    }
+    if (n_desc == 0) return BITMTP_OK;
+    return run_gemms(g, n_desc, flags, static_cast<cudaStream_t>(stream));
+}
+
+int bitmtp_linear_device_error(void* stream) {
+    DevInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != BITMTP_OK) return st;
+    st = cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    if (st != BITMTP_OK) return st;
+    int v = 0;
+    st = cuda_status(cudaMemcpy(&v, dev->err, sizeof(int), cudaMemcpyDeviceToHost));
+    if (st != BITMTP_OK) return st;
+    if (v != 0) {
+        const int zero = 0;
+        st = cuda_status(cudaMemcpy(dev->err, &zero, sizeof(int), cudaMemcpyHostToDevice));
+        if (st != BITMTP_OK) return st;
+    }
+    return v;
+}
+
+const char* bitmtp_linear_status_string(int status) {
+    switch (status) {
+        case BITMTP_OK: return "BITMTP_OK";
+        case BITMTP_ERR_INVALID: return "BITMTP_ERR_INVALID: invalid argument";
+        case BITMTP_ERR_ALIGN: return "BITMTP_ERR_ALIGN: packed weights must be 16-byte aligned";
+        case BITMTP_ERR_SHAPE: return "BITMTP_ERR_SHAPE: dimension out of the supported range";
+        case BITMTP_ERR_NOT_TERNARY: return "BITMTP_ERR_NOT_TERNARY: weight entry outside {-1,0,+1}";
+        case BITMTP_ERR_UNSUPPORTED: return "BITMTP_ERR_UNSUPPORTED: no sm_103 device is current";
+        case BITMTP_ERR_CUDA: return "BITMTP_ERR_CUDA: a CUDA runtime call failed";
+        case BITMTP_ERR_DEVICE: return "BITMTP_ERR_DEVICE: a kernel gave up a bounded wait";
+        default: return "BITMTP: unknown status";
+    }
+}
+
+int bitmtp_linear_version(void) { return 0x000100; }
+
+}  // extern "C"

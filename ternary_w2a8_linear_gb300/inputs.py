@@ -34,12 +34,13 @@ def ternary(rng: np.random.Generator, shape, p_zero: float | None) -> np.ndarray
     otherwise P(0) = p_zero and P(+1) = P(-1) = (1 - p_zero) / 2."""
     if p_zero is None:
         return rng.integers(-1, 2, size=shape, dtype=np.int8)
-    r = rng.random(shape, dtype=np.float32)
-    half = (1.0 - p_zero) / 2.0
-    T = np.zeros(shape, dtype=np.int8)
-    T[(r >= p_zero) & (r < p_zero + half)] = 1
-    T[r >= p_zero + half] = -1
-    return T
+    # 16-bit uniform draw through a lookup table: P(0) = round(p_zero * 2^16) / 2^16
+    z = int(round(p_zero * 65536))
+    h = z + (65536 - z) // 2
+    lut = np.full(65536, -1, dtype=np.int8)
+    lut[:z] = 0
+    lut[z:h] = 1
+    return lut[rng.integers(0, 65536, size=shape, dtype=np.uint16)]
 
 
 def normal_f32(rng: np.random.Generator, shape) -> np.ndarray:

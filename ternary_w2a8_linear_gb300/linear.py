@@ -1,0 +1,238 @@
+"""Thin ctypes binding over libbitmtp_linear.so (include/bitmtp_linear.h).
+
+Argument marshalling only: every step of the linear runs in the library's CUDA
+kernels.  PyTorch provides device memory and the current stream.  The raw
+entry points keep the C names (``bitmtp_linear_*``); ``pack``, ``quant_act``,
+``gemm`` and ``gemm_grouped`` are tensor conveniences over them.
+
+The library must have been built (``ternary_w2a8_linear_gb300.build``); if it
+is missing this module raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libbitmtp_linear.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "bitmtp_linear.h")
+
+OK = 0
+ERR_INVALID, ERR_ALIGN, ERR_SHAPE, ERR_NOT_TERNARY, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE = range(-1, -8, -1)
+F32, BF16, Q8 = 0, 1, 2
+FLAG_PDL, FLAG_FORCE_TC, FLAG_FORCE_DP = 0x1, 0x2, 0x4
+MAX_M, MAX_K, MAX_N, MAX_GROUP = 16, 32768, 16777216, 8
+
+
+class BitmtpError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})" if what else status_string(status))
+
+
+class Act(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("x", ctypes.c_void_p), ("ldx", ctypes.c_int64),
+                ("a_scale", ctypes.c_void_p)]
+
+
+class Out(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("y", ctypes.c_void_p), ("ldy", ctypes.c_int64),
+                ("acc", ctypes.c_void_p), ("lda", ctypes.c_int64)]
+
+
+class GemmDesc(ctypes.Structure):
+    _fields_ = [("pk", ctypes.c_void_p), ("w_scale", ctypes.c_float), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("M", ctypes.c_int64), ("act", Act), ("out", Out)]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m ternary_w2a8_linear_gb300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    c = ctypes
+    sig = {
+        "bitmtp_linear_packed_bytes": (c.c_size_t, [c.c_int64, c.c_int64]),
+        "bitmtp_linear_pack": (c.c_int, [c.c_void_p, c.c_int64, c.c_int64, c.c_int64, c.c_void_p,
+                                         c.c_size_t, c.c_void_p]),
+        "bitmtp_linear_quant_act": (c.c_int, [c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_int64,
+                                              c.c_void_p, c.c_int64, c.c_void_p, c.c_void_p, c.c_void_p]),
+        "bitmtp_linear_gemm": (c.c_int, [c.c_void_p, c.c_float, c.c_int64, c.c_int64, c.c_int64,
+                                         c.POINTER(Act), c.POINTER(Out), c.c_uint, c.c_void_p]),
+        "bitmtp_linear_gemm_grouped": (c.c_int, [c.POINTER(GemmDesc), c.c_int, c.c_uint, c.c_void_p]),
+        "bitmtp_linear_device_error": (c.c_int, [c.c_void_p]),
+        "bitmtp_linear_status_string": (c.c_char_p, [c.c_int]),
+        "bitmtp_linear_version": (c.c_int, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def header_symbols() -> list[str]:
+    """Every function the public header declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(bitmtp_linear_\w+)\s*\(", text, re.M)))
+
+
+# ---------------------------------------------------------------- raw ABI --
+def bitmtp_linear_packed_bytes(N: int, K: int) -> int:
+    return int(load().bitmtp_linear_packed_bytes(N, K))
+
+
+def bitmtp_linear_pack(T_ptr, N, K, ldt, pk_ptr, pk_bytes, stream) -> int:
+    return load().bitmtp_linear_pack(T_ptr, N, K, ldt, pk_ptr, pk_bytes, stream)
+
+
+def bitmtp_linear_quant_act(x_ptr, x_kind, M, K, ldx, q_ptr, ldq, a_scale_ptr, rowsum_ptr, stream) -> int:
+    return load().bitmtp_linear_quant_act(x_ptr, x_kind, M, K, ldx, q_ptr, ldq, a_scale_ptr, rowsum_ptr, stream)
+
+
+def bitmtp_linear_gemm(pk_ptr, w_scale, N, K, M, act: Act, out: Out, flags, stream) -> int:
+    return load().bitmtp_linear_gemm(pk_ptr, w_scale, N, K, M, ctypes.byref(act), ctypes.byref(out), flags, stream)
+
+
+def bitmtp_linear_gemm_grouped(descs, flags, stream) -> int:
+    arr = (GemmDesc * max(1, len(descs)))(*descs)
+    return load().bitmtp_linear_gemm_grouped(arr, len(descs), flags, stream)
+
+
+def bitmtp_linear_device_error(stream=None) -> int:
+    return load().bitmtp_linear_device_error(_stream(stream))
+
+
+def bitmtp_linear_status_string(status: int) -> str:
+    return load().bitmtp_linear_status_string(status).decode()
+
+
+def bitmtp_linear_version() -> int:
+    return load().bitmtp_linear_version()
+
+
+status_string = bitmtp_linear_status_string
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise BitmtpError(status, what)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _act_kind(x: torch.Tensor) -> int:
+    if x.dtype == torch.float32:
+        return F32
+    if x.dtype == torch.bfloat16:
+        return BF16
+    if x.dtype == torch.int8:
+        return Q8
+    raise TypeError(f"unsupported activation dtype {x.dtype}")
+
+
+def _rowmajor(t: torch.Tensor, name: str) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with unit stride along columns")
+    return t.stride(0)
+
+
+# ------------------------------------------------------- tensor wrappers --
+def packed_bytes(N: int, K: int) -> int:
+    return bitmtp_linear_packed_bytes(N, K)
+
+
+def pack(T: torch.Tensor, stream=None) -> torch.Tensor:
+    """Pack ternary int8 weights [N, K] (device) -> uint8 packed buffer."""
+    if T.dtype != torch.int8 or not T.is_cuda:
+        raise TypeError("T must be a CUDA int8 tensor")
+    N, K = T.shape
+    ldt = _rowmajor(T, "T")
+    nb = packed_bytes(N, K)
+    if nb == 0:
+        raise BitmtpError(ERR_SHAPE, "pack")
+    pk = torch.empty(nb, dtype=torch.uint8, device=T.device)
+    _check(bitmtp_linear_pack(_ptr(T), N, K, ldt, _ptr(pk), nb, _stream(stream)), "pack")
+    return pk
+
+
+def quant_act(x: torch.Tensor, stream=None):
+    """Per-row absmax int8 quantisation -> (q int8 [M,K], a_scale fp32 [M], rowsum int32 [M])."""
+    kind = _act_kind(x)
+    if kind == Q8:
+        raise TypeError("x must be float32 or bfloat16")
+    M, K = x.shape
+    ldx = _rowmajor(x, "x")
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    a_scale = torch.empty(M, dtype=torch.float32, device=x.device)
+    rowsum = torch.empty(M, dtype=torch.int32, device=x.device)
+    _check(bitmtp_linear_quant_act(_ptr(x), kind, M, K, ldx, _ptr(q), K, _ptr(a_scale), _ptr(rowsum),
+                                   _stream(stream)), "quant_act")
+    return q, a_scale, rowsum
+
+
+def make_act(x: torch.Tensor, a_scale: torch.Tensor | None = None) -> Act:
+    kind = _act_kind(x)
+    if kind == Q8 and a_scale is None:
+        raise ValueError("int8 activations need a_scale")
+    return Act(kind, x.data_ptr(), _rowmajor(x, "x"), a_scale.data_ptr() if kind == Q8 else None)
+
+
+def make_out(y: torch.Tensor, acc: torch.Tensor | None = None) -> Out:
+    dt = F32 if y.dtype == torch.float32 else BF16 if y.dtype == torch.bfloat16 else None
+    if dt is None:
+        raise TypeError("y must be float32 or bfloat16")
+    return Out(dt, y.data_ptr(), _rowmajor(y, "y"),
+               acc.data_ptr() if acc is not None else None,
+               _rowmajor(acc, "acc") if acc is not None else 0)
+
+
+def gemm(pk: torch.Tensor, w_scale: float, N: int, K: int, x: torch.Tensor,
+         a_scale: torch.Tensor | None = None, out_dtype=torch.float32, y: torch.Tensor | None = None,
+         acc: torch.Tensor | bool | None = None, flags: int = 0, stream=None):
+    """y = W2A8 linear of x ([M, K] fp32 / bf16 raw, or int8 codes with a_scale).
+
+    Returns y, or (y, acc) when ``acc`` is True or a tensor."""
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    want_acc = acc is not None and acc is not False
+    if acc is True:
+        acc = torch.empty((M, N), dtype=torch.int32, device=x.device)
+    act = make_act(x, a_scale)
+    out = make_out(y, acc if want_acc else None)
+    _check(bitmtp_linear_gemm(_ptr(pk), float(w_scale), N, K, M, act, out, flags, _stream(stream)), "gemm")
+    return (y, acc) if want_acc else y
+
+
+def gemm_grouped(problems, flags: int = 0, stream=None):
+    """One launch over several problems.  Each problem is a dict with keys
+    pk, w_scale, N, K, x, (a_scale), y, (acc)."""
+    descs = []
+    for p in problems:
+        x = p["x"]
+        descs.append(GemmDesc(p["pk"].data_ptr(), float(p["w_scale"]), p["N"], p["K"], x.shape[0],
+                              make_act(x, p.get("a_scale")), make_out(p["y"], p.get("acc"))))
+    _check(bitmtp_linear_gemm_grouped(descs, flags, _stream(stream)), "gemm_grouped")

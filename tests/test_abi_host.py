@@ -1,0 +1,123 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every
+function include/bitmtp_linear.h declares, and rejects invalid arguments on
+the host before any CUDA call.  No kernel is launched: calls that pass
+validation are only made where no GPU is present (they must then report
+BITMTP_ERR_UNSUPPORTED)."""
+import ctypes
+
+import pytest
+import torch
+
+import oracle
+from ternary_w2a8_linear_gb300 import build, linear as L
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return L.load()
+
+
+def test_exports_every_header_symbol(lib):
+    syms = L.header_symbols()
+    assert set(syms) == {
+        "bitmtp_linear_packed_bytes", "bitmtp_linear_pack", "bitmtp_linear_quant_act",
+        "bitmtp_linear_gemm", "bitmtp_linear_gemm_grouped", "bitmtp_linear_device_error",
+        "bitmtp_linear_status_string", "bitmtp_linear_version",
+    }
+    for s in syms:
+        assert hasattr(lib, s), s
+        assert hasattr(L, s), s  # binding keeps the C names
+
+
+def test_version_and_status_strings(lib):
+    assert L.bitmtp_linear_version() == 0x000100
+    for st in (L.OK, L.ERR_INVALID, L.ERR_ALIGN, L.ERR_SHAPE, L.ERR_NOT_TERNARY,
+               L.ERR_UNSUPPORTED, L.ERR_CUDA, L.ERR_DEVICE):
+        assert L.status_string(st).startswith("BITMTP")
+    assert "unknown" in L.status_string(12345)
+
+
+@pytest.mark.parametrize("N,K", [(1, 1), (2560, 2560), (640, 2560), (32000, 2560), (4096, 11008),
+                                 (129, 130), (7, 300)])
+def test_packed_bytes_matches_oracle_definition(lib, N, K):
+    assert L.packed_bytes(N, K) == oracle.packed_bytes(N, K)
+
+
+def test_packed_bytes_rejects(lib):
+    assert L.packed_bytes(0, 5) == 0
+    assert L.packed_bytes(5, 0) == 0
+    assert L.packed_bytes(5, L.MAX_K + 1) == 0
+
+
+def _act(kind=L.F32, x=FAKE, ldx=64, a_scale=None):
+    return L.Act(kind, x, ldx, a_scale)
+
+
+def _out(dtype=L.F32, y=FAKE, ldy=64, acc=None, lda=0):
+    return L.Out(dtype, y, ldy, acc, lda)
+
+
+def gemm(pk=FAKE, w=0.02, N=64, K=64, M=4, act=None, out=None, flags=0):
+    act = act or _act()
+    out = out or _out()
+    return L.bitmtp_linear_gemm(pk, w, N, K, M, act, out, flags, None)
+
+
+def test_gemm_validation(lib):
+    assert gemm(M=17) == L.ERR_SHAPE
+    assert gemm(M=-1) == L.ERR_SHAPE
+    assert gemm(K=0) == L.ERR_SHAPE
+    assert gemm(K=L.MAX_K + 1) == L.ERR_SHAPE
+    assert gemm(N=-3) == L.ERR_SHAPE
+    assert gemm(pk=None) == L.ERR_INVALID
+    assert gemm(pk=FAKE + 8) == L.ERR_ALIGN
+    assert gemm(act=_act(kind=7)) == L.ERR_INVALID
+    assert gemm(act=_act(x=None)) == L.ERR_INVALID
+    assert gemm(act=_act(ldx=63)) == L.ERR_INVALID
+    assert gemm(act=_act(kind=L.Q8)) == L.ERR_INVALID          # Q8 without a_scale
+    assert gemm(out=_out(dtype=5)) == L.ERR_INVALID
+    assert gemm(out=_out(y=None)) == L.ERR_INVALID
+    assert gemm(out=_out(ldy=10)) == L.ERR_INVALID
+    assert gemm(out=_out(acc=FAKE, lda=3)) == L.ERR_INVALID
+    assert gemm(w=float("nan")) == L.ERR_INVALID
+    assert gemm(flags=L.FLAG_FORCE_TC | L.FLAG_FORCE_DP) == L.ERR_INVALID
+    assert L.load().bitmtp_linear_gemm(FAKE, 0.02, 64, 64, 4, None, ctypes.byref(_out()), 0, None) == L.ERR_INVALID
+    # empty problems are valid no-ops and never touch the device
+    assert gemm(M=0) == L.OK
+    assert gemm(N=0) == L.OK
+
+
+def test_grouped_validation(lib):
+    good = L.GemmDesc(FAKE, 0.02, 64, 64, 4, _act(), _out())
+    bad = L.GemmDesc(FAKE, 0.02, 64, 64, 20, _act(), _out())
+    assert L.bitmtp_linear_gemm_grouped([good, bad], 0, None) == L.ERR_SHAPE
+    assert L.bitmtp_linear_gemm_grouped([good] * (L.MAX_GROUP + 1), 0, None) == L.ERR_SHAPE
+    assert L.bitmtp_linear_gemm_grouped([], 0, None) == L.OK
+    empty = L.GemmDesc(FAKE, 0.02, 64, 64, 0, _act(), _out())
+    assert L.bitmtp_linear_gemm_grouped([empty], 0, None) == L.OK
+
+
+def test_pack_and_quant_validation(lib):
+    pk = L.bitmtp_linear_pack
+    assert pk(FAKE, 0, 16, 16, FAKE, 4096 + 16, None) == L.ERR_SHAPE
+    assert pk(None, 4, 16, 16, FAKE, 4096 + 16, None) == L.ERR_INVALID
+    assert pk(FAKE, 4, 16, 8, FAKE, 4096 + 16, None) == L.ERR_INVALID
+    assert pk(FAKE, 4, 16, 16, FAKE + 4, 4096 + 16, None) == L.ERR_ALIGN
+    assert pk(FAKE, 4, 16, 16, FAKE, 4096, None) == L.ERR_SHAPE   # trailer does not fit
+    qa = L.bitmtp_linear_quant_act
+    assert qa(FAKE, L.Q8, 2, 16, 16, FAKE, 16, FAKE, None, None) == L.ERR_INVALID
+    assert qa(FAKE, L.F32, 2, 0, 16, FAKE, 16, FAKE, None, None) == L.ERR_SHAPE
+    assert qa(FAKE, L.F32, 2, 16, 8, FAKE, 16, FAKE, None, None) == L.ERR_INVALID
+    assert qa(FAKE, L.F32, 2, 16, 16, None, 16, FAKE, None, None) == L.ERR_INVALID
+    assert qa(FAKE, L.F32, 0, 16, 16, None, 16, None, None, None) == L.OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")
+def test_valid_calls_without_device_report_unsupported(lib):
+    assert gemm() == L.ERR_UNSUPPORTED
+    assert L.bitmtp_linear_quant_act(FAKE, L.F32, 2, 16, 16, FAKE, 16, FAKE, None, None) == L.ERR_UNSUPPORTED
+    assert L.bitmtp_linear_pack(FAKE, 4, 16, 16, FAKE, 4096 + 16, None) == L.ERR_UNSUPPORTED
+    assert L.bitmtp_linear_device_error(0) == L.ERR_UNSUPPORTED
