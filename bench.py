@@ -49,8 +49,11 @@ def parse():
     p.add_argument("--copies", type=int, default=16, help="distinct weight copies rotated per step")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-width", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--mode", choices=["grouped", "chained"], default="grouped",
+                   help="grouped: each width's seven projections in one launch; chained: one launch each")
     return p.parse_args()
 
 
@@ -171,28 +174,47 @@ def run_ours(args, rank, world):
         ys = [torch.empty((16, N), dtype=torch.bfloat16, device=dev) for _, _, N in inputs.BITNET2B_PROJ]
     torch.cuda.synchronize()
 
-    def enqueue_step(s, widths=WIDTHS, flags=L.FLAG_PDL):
+    cstream = L.ctypes.c_void_p(stream.cuda_stream)
+    # per (copy, width): the seven problems as one grouped-launch descriptor array
+    group_desc = {}
+    for c in range(R):
+        for M in WIDTHS:
+            descs = []
+            for p, (pk, w, K, N) in enumerate(weights[c]):
+                descs.append(L.GemmDesc(pk.data_ptr(), w, N, K, M,
+                                        L.Act(L.BF16, xs[p].data_ptr(), K, None),
+                                        L.Out(L.BF16, ys[p].data_ptr(), N, None, 0)))
+            group_desc[(c, M)] = ((L.GemmDesc * len(descs))(*descs), len(descs))
+
+    def enqueue_step(s, widths=WIDTHS, mode=None, flags=L.FLAG_PDL):
+        mode = mode or args.mode
         n = 0
-        for wi, M in enumerate(widths):
+        for M in widths:
             c = (s * len(WIDTHS) + WIDTHS.index(M)) % R
+            if mode == "grouped":
+                arr, nd = group_desc[(c, M)]
+                st = L.load().bitmtp_linear_gemm_grouped(arr, nd, flags, cstream)
+                if st != L.OK:
+                    raise L.BitmtpError(st, "gemm_grouped")
+                n += 1
+                continue
             for p, (pk, w, K, N) in enumerate(weights[c]):
                 act = L.Act(L.BF16, xs[p].data_ptr(), K, None)
                 out = L.Out(L.BF16, ys[p].data_ptr(), N, None, 0)
-                st = L.bitmtp_linear_gemm(pk.data_ptr(), w, N, K, M, act, out, flags,
-                                          L.ctypes.c_void_p(stream.cuda_stream))
+                st = L.bitmtp_linear_gemm(pk.data_ptr(), w, N, K, M, act, out, flags, cstream)
                 if st != L.OK:
                     raise L.BitmtpError(st, "gemm")
                 n += 1
         return n
 
-    def capture(nsteps, start, widths=WIDTHS):
+    def capture(nsteps, start, widths=WIDTHS, mode=None):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            enqueue_step(start, widths)          # untimed warm call outside capture
+            enqueue_step(start, widths, mode)    # untimed warm call outside capture
             stream.synchronize()
             with torch.cuda.graph(g, stream=stream):
                 for s in range(nsteps):
-                    enqueue_step(start + s, widths)
+                    enqueue_step(start + s, widths, mode)
         return g
 
     G = 16  # steps per graph; weights cycle every R/len(WIDTHS) steps
@@ -200,7 +222,7 @@ def run_ours(args, rank, world):
     K = args.steps
     reps, rem = divmod(K, G)
     g_rem = capture(rem, 0) if rem else None
-    launches_per_step = len(WIDTHS) * len(inputs.BITNET2B_PROJ)
+    launches_per_step = len(WIDTHS) * (1 if args.mode == "grouped" else len(inputs.BITNET2B_PROJ))
 
     # warm-up
     with torch.cuda.stream(stream):
@@ -233,27 +255,28 @@ def run_ours(args, rank, world):
     value = bytes_step * K * world / sec / 1e9
     ms_per_step = ms / K
 
-    # per-width breakdown (same rotation, widths timed on their own)
+    # per-width breakdown, both execution modes (same weight rotation)
     per_width = {}
-    for M in WIDTHS:
-        g = capture(G, 0, (M,))
-        with torch.cuda.stream(stream):
-            g.replay()
-            stream.synchronize()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            n_rep = 20
-            a.record(stream)
-            for _ in range(n_rep):
+    for mode in (() if args.no_per_width else ("grouped", "chained")):
+        per_width[mode] = {}
+        for M in WIDTHS:
+            g = capture(G, 0, (M,), mode)
+            with torch.cuda.stream(stream):
                 g.replay()
-            b.record(stream)
-        b.synchronize()
-        t = a.elapsed_time(b) / 1e3 / (n_rep * G)  # seconds per width-pass (7 linears)
-        byt = sum(algorithmic_bytes(Kp, Np, M) for _, Kp, Np in inputs.BITNET2B_PROJ)
-        per_width[str(M)] = {"gbs": round(byt / t / 1e9, 1), "us_per_layer_set": round(t * 1e6, 2),
-                             "rows_per_s": round(M / t, 1),
-                             "us_per_linear": round(t * 1e6 / len(inputs.BITNET2B_PROJ), 2)}
-        del g
+                stream.synchronize()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                n_rep = 20
+                a.record(stream)
+                for _ in range(n_rep):
+                    g.replay()
+                b.record(stream)
+            b.synchronize()
+            t = a.elapsed_time(b) / 1e3 / (n_rep * G)  # seconds per width-pass (7 linears)
+            byt = sum(algorithmic_bytes(Kp, Np, M) for _, Kp, Np in inputs.BITNET2B_PROJ)
+            per_width[mode][str(M)] = {"gbs": round(byt / t / 1e9, 1), "us_per_layer_set": round(t * 1e6, 2),
+                                       "rows_per_s": round(M / t, 1)}
+            del g
 
     e2e = None
     if not args.no_e2e:
@@ -277,9 +300,15 @@ def run_e2e(args, L, torch, dev, stream, weights, rank, world):
     def one(s):
         for M in WIDTHS:
             c = (s * len(WIDTHS) + WIDTHS.index(M)) % R
-            for p, (pk, w, K, N) in enumerate(weights[c]):
+            for p in range(len(weights[c])):
                 dx[p][:M].copy_(hx[p][:M], non_blocking=True)
-                L.gemm(pk, w, N, K, dx[p][:M], y=dy[p][:M], stream=stream)
+            if args.mode == "grouped":
+                L.gemm_grouped([dict(pk=pk, w_scale=w, N=N, K=K, x=dx[p][:M], y=dy[p][:M])
+                                for p, (pk, w, K, N) in enumerate(weights[c])], stream=stream)
+            else:
+                for p, (pk, w, K, N) in enumerate(weights[c]):
+                    L.gemm(pk, w, N, K, dx[p][:M], y=dy[p][:M], stream=stream)
+            for p in range(len(weights[c])):
                 hy[p][:M].copy_(dy[p][:M], non_blocking=True)
         stream.synchronize()
 
@@ -427,7 +456,8 @@ def main():
         "config": workload_config(args, {"weight_copies": res["copies"],
                                          "l2": f"weights rotate over {res['copies']} distinct copies "
                                                f"({res['copies']} x 17.4 MB > L2)",
-                                         "graph_steps": res["graph_steps"], "launch": "CUDA graph + PDL"}),
+                                         "graph_steps": res["graph_steps"],
+                                         "launch": f"{args.mode}; CUDA graph + PDL"}),
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(per_gpu / peak, 4), "peak_kind": peak_kind, "traffic": None,
                      "kernel": "w2a8_gemm_kernel (all launches of the step)"},
