@@ -175,6 +175,17 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
 
     cstream = L.ctypes.c_void_p(stream.cuda_stream)
+    # one caller-owned workspace, zero-filled once, shared by every launch on the stream
+    ws_need = 0
+    for M in WIDTHS:
+        for _, K, N in inputs.BITNET2B_PROJ:
+            ws_need = max(ws_need, L.bitmtp_linear_workspace_bytes(N, K, M))
+    probe = [L.GemmDesc(0, 0.0, N, K, max(WIDTHS), L.Act(L.BF16, 0, K, None), L.Out(L.BF16, 0, N, None, 0))
+             for _, K, N in inputs.BITNET2B_PROJ]
+    ws_need = max(ws_need, L.bitmtp_linear_workspace_bytes_grouped(probe))
+    ws = torch.zeros(ws_need, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    ws_ptr, ws_n = L.ctypes.c_void_p(ws.data_ptr()), ws.numel()
     # per (copy, width): the seven problems as one grouped-launch descriptor array
     group_desc = {}
     for c in range(R):
@@ -193,7 +204,7 @@ def run_ours(args, rank, world):
             c = (s * len(WIDTHS) + WIDTHS.index(M)) % R
             if mode == "grouped":
                 arr, nd = group_desc[(c, M)]
-                st = L.load().bitmtp_linear_gemm_grouped(arr, nd, flags, cstream)
+                st = L.load().bitmtp_linear_gemm_grouped(arr, nd, ws_ptr, ws_n, flags, cstream)
                 if st != L.OK:
                     raise L.BitmtpError(st, "gemm_grouped")
                 n += 1
@@ -201,7 +212,7 @@ def run_ours(args, rank, world):
             for p, (pk, w, K, N) in enumerate(weights[c]):
                 act = L.Act(L.BF16, xs[p].data_ptr(), K, None)
                 out = L.Out(L.BF16, ys[p].data_ptr(), N, None, 0)
-                st = L.bitmtp_linear_gemm(pk.data_ptr(), w, N, K, M, act, out, flags, cstream)
+                st = L.bitmtp_linear_gemm(pk.data_ptr(), w, N, K, M, act, out, ws_ptr, ws_n, flags, cstream)
                 if st != L.OK:
                     raise L.BitmtpError(st, "gemm")
                 n += 1

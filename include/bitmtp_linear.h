@@ -23,8 +23,8 @@
  * Conventions for every call:
  *   - Matrices are row-major; ld* arguments count elements between rows.
  *   - Pointers are DEVICE pointers owned by the caller unless stated
- *     otherwise.  The library never allocates device memory and keeps no
- *     per-call state.
+ *     otherwise.  The library never allocates device memory; GEMM calls take
+ *     a caller-owned workspace (see bitmtp_linear_workspace_bytes).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is enqueued asynchronously on it; only
  *     bitmtp_linear_pack and bitmtp_linear_device_error synchronise it.
@@ -47,9 +47,9 @@ extern "C" {
 /* ---- status codes -------------------------------------------------------- */
 #define BITMTP_OK               0
 #define BITMTP_ERR_INVALID     (-1) /* NULL pointer, unknown enum, ld too small   */
-#define BITMTP_ERR_ALIGN       (-2) /* packed-weight pointer not 16-byte aligned  */
-#define BITMTP_ERR_SHAPE       (-3) /* dimension out of the supported range, or
-                                       pk_bytes smaller than packed_bytes(N, K)   */
+#define BITMTP_ERR_ALIGN       (-2) /* packed weights or workspace not 16-byte aligned */
+#define BITMTP_ERR_SHAPE       (-3) /* dimension out of the supported range, or a
+                                       buffer smaller than its size query         */
 #define BITMTP_ERR_NOT_TERNARY (-4) /* pack: an entry of T outside {-1, 0, +1}    */
 #define BITMTP_ERR_UNSUPPORTED (-5) /* no device, or device is not sm_103        */
 #define BITMTP_ERR_CUDA        (-6) /* a CUDA runtime call failed                 */
@@ -79,6 +79,8 @@ extern "C" {
  * integer dot-product path (dp4a, widths 1..4). */
 #define BITMTP_FLAG_FORCE_TC   0x2u
 #define BITMTP_FLAG_FORCE_DP   0x4u
+/* (Forcing the tensor path at widths 1..2 uses its 8-row activation tile;
+ * forcing dp4a is valid for widths 1..4.) */
 
 /*
  * Packed ternary weights (this library's own layout; the pages only say the
@@ -139,16 +141,30 @@ typedef struct bitmtp_out {
     int64_t lda;           /* >= N when acc != NULL                                  */
 } bitmtp_out;
 
+/* Workspace of a GEMM call: a device buffer the caller allocates once,
+ * 16-byte aligned, zero-filled before its first use (e.g. cudaMemset); every
+ * call leaves it ready for the next call.  It holds the quantised activation
+ * tiles, the split-row-tile partial sums and self-resetting arrival counters.
+ * Calls that may execute concurrently on the GPU need distinct workspaces.
+ * If a call reports BITMTP_ERR_DEVICE the workspace must be zero-filled again.
+ * These return the bytes needed (0 for out-of-range arguments); the size
+ * depends on the shapes only, not on the device. */
+size_t bitmtp_linear_workspace_bytes(int64_t N, int64_t K, int64_t M);
+
 /* y = dequant(T * q): the W2A8 linear at block width M.
- *   pk       packed weights from bitmtp_linear_pack (16-byte aligned)
- *   w_scale  per-tensor weight scale
- *   N, K     out-/in-features the weights were packed with
- *   M        block width, 0 <= M <= BITMTP_MAX_M (0: no-op)
- *   flags    BITMTP_FLAG_* bits
- * The compute path and launch shape are chosen from (M, N, K) (width
- * specialisation); results do not depend on the choice. */
+ *   pk        packed weights from bitmtp_linear_pack (16-byte aligned)
+ *   w_scale   per-tensor weight scale
+ *   N, K      out-/in-features the weights were packed with
+ *   M         block width, 0 <= M <= BITMTP_MAX_M (0: no-op)
+ *   workspace >= bitmtp_linear_workspace_bytes(N, K, M) bytes, see above
+ *   flags     BITMTP_FLAG_* bits
+ * One kernel launch: it quantises raw activation rows (BITMTP_F32/BF16) with
+ * the quantiser above, streams the packed weights and writes y (and acc).
+ * The compute path is chosen from M (width specialisation); results do not
+ * depend on the choice. */
 int bitmtp_linear_gemm(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M,
                        const bitmtp_act* act, const bitmtp_out* out,
+                       void* workspace, size_t workspace_bytes,
                        unsigned flags, void* stream);
 
 /* One problem of a grouped launch (same meaning as bitmtp_linear_gemm). */
@@ -160,12 +176,17 @@ typedef struct bitmtp_gemm_desc {
     bitmtp_out out;
 } bitmtp_gemm_desc;
 
+/* Workspace bytes for a grouped launch of these descriptors (0 if invalid). */
+size_t bitmtp_linear_workspace_bytes_grouped(const bitmtp_gemm_desc* d, int n_desc);
+
 /* Run up to BITMTP_MAX_GROUP independent problems in ONE kernel launch --
- * the role-dependent output projections of one block step (e.g. verify rows
- * through one projection and draft rows through another).  `d` is a HOST
- * array of n_desc descriptors (copied by value into the launch).  Problems
- * must not write overlapping outputs. */
+ * e.g. the role-dependent output projections of one block step (verify rows
+ * through one projection and draft rows through another), or the independent
+ * projections of a layer.  `d` is a HOST array of n_desc descriptors (copied
+ * by value into the launch).  The compute path follows the widest problem.
+ * Problems must not write overlapping outputs. */
 int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc,
+                               void* workspace, size_t workspace_bytes,
                                unsigned flags, void* stream);
 
 /* Synchronise `stream`, then return and clear the device error word that a

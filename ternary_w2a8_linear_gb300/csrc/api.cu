@@ -163,7 +163,7 @@ int check_problem(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M
     if (!(w_scale == w_scale)) return BITMTP_ERR_INVALID;  // NaN scale
     g->pk = static_cast<const uint8_t*>(pk);
     g->x = act->x;
-    g->a_scale = act->a_scale;
+    g->a_scale_in = act->a_scale;
     g->y = out->y;
     g->acc = out->acc;
     g->ldx = act->ldx;
@@ -177,68 +177,107 @@ int check_problem(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M
     g->kt = static_cast<int>(ceil_div(K, kTileK));
     g->act_kind = act->kind;
     g->out_dtype = out->dtype;
-    g->cluster_begin = 0;
     return BITMTP_OK;
 }
 
 // Width-specialised operator choice (the analogue of picking packed low-bit
-// operators by replay width and input/output dimensions).
+// operators by replay width and input/output dimensions): dp4a for one or two
+// rows, tensor cores with an 8-row activation tile up to 8 rows, 16 rows above.
 int choose_path(int max_m, unsigned flags, int* dp_rows) {
-    if (flags & BITMTP_FLAG_FORCE_TC) return kPathTC;
-    int r = max_m <= 1 ? 1 : (max_m <= 2 ? 2 : 4);
+    const int r = max_m <= 1 ? 1 : (max_m <= 2 ? 2 : 4);
     if (flags & BITMTP_FLAG_FORCE_DP) {
         if (max_m > 4) return -1;
         *dp_rows = r;
         return kPathDP;
     }
-    if (max_m <= 2) {
+    if (!(flags & BITMTP_FLAG_FORCE_TC) && max_m <= 2) {
         *dp_rows = r;
         return kPathDP;
     }
-    return kPathTC;
+    return max_m <= 8 ? kPathTC8 : kPathTC16;
 }
 
-// Split-K factor: enough CTAs to cover every SM about twice, at most 16 per
-// cluster, at most kMaxKtPerCta resident k tiles per CTA.
-int choose_csize(int total_row_tiles, int max_kt, int sms) {
-    const int target = 2 * sms;
-    int c = static_cast<int>(ceil_div(target, total_row_tiles));
-    c = std::min(c, kMaxCluster);
-    c = std::min(c, max_kt);
-    const int need = static_cast<int>(ceil_div(max_kt, kMaxKtPerCta));
-    c = std::max(c, need);
-    return std::max(c, 1);
+constexpr int kMaxCtas = 320;  // persistent CTAs per launch (>= 2 per SM on GB300)
+constexpr size_t kSlotBytes = 2ull * 16 * kTileN * 4;
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// Sections of the caller's workspace.  The activation tiles are sized for the
+// widest tile (16 fp16 rows, 4096 B per k tile) whatever path runs, and the
+// split-tile slots for the largest grid, so the size depends on shapes only.
+WorkspaceLayout layout_for(const GemmProblem* probs, int n) {
+    size_t nt = 0, tasks = 0, pre = 0, kt = 0;
+    for (int i = 0; i < n; ++i) {
+        if (probs[i].M == 0 || probs[i].N == 0) continue;
+        nt += probs[i].nt;
+        tasks += probs[i].M;
+        pre += static_cast<size_t>(probs[i].kt + 1) * 16;
+        kt += probs[i].kt;
+    }
+    WorkspaceLayout L;
+    L.gridbar = 0;
+    L.counters = 256;
+    L.ascale = L.counters + align256(nt * 4);
+    L.prefix = L.ascale + align256(tasks * 4);
+    L.slots = L.prefix + align256(pre * 4);
+    L.btiles = L.slots + kMaxCtas * kSlotBytes;
+    L.total = L.btiles + align256(kt * 4096);
+    return L;
 }
 
-int run_gemms(const GemmProblem* probs, int n, unsigned flags, cudaStream_t stream) {
+int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes, unsigned flags,
+              cudaStream_t stream) {
     bool any = false;
     for (int i = 0; i < n; ++i) any = any || (probs[i].M > 0 && probs[i].N > 0);
     if (!any) return BITMTP_OK;  // empty problems never touch the device
+    const WorkspaceLayout L = layout_for(probs, n);
+    if (!workspace) return BITMTP_ERR_INVALID;
+    if (!aligned16(workspace)) return BITMTP_ERR_ALIGN;
+    if (ws_bytes < L.total) return BITMTP_ERR_SHAPE;
     DevInfo* dev = nullptr;
     int st = current_device(&dev);
     if (st != BITMTP_OK) return st;
+
     GemmParams prm;
     std::memset(&prm, 0, sizeof(prm));
-    int total_rt = 0, max_kt = 1, max_m = 1, np = 0;
+    long long tiles = 0;
+    int tasks = 0, rt = 0, bt = 0, pre = 0, max_m = 1, np = 0;
     for (int i = 0; i < n; ++i) {
         if (probs[i].M == 0 || probs[i].N == 0) continue;
-        prm.p[np] = probs[i];
-        prm.p[np].cluster_begin = total_rt;
-        total_rt += probs[i].nt;
-        max_kt = std::max(max_kt, probs[i].kt);
-        max_m = std::max(max_m, probs[i].M);
-        ++np;
+        GemmProblem g = probs[i];
+        g.tile_begin = tiles;
+        g.task_begin = tasks;
+        g.rt_begin = rt;
+        g.bt_begin = bt;
+        g.pre_begin = pre;
+        tiles += static_cast<long long>(g.nt) * g.kt;
+        tasks += g.M;
+        rt += g.nt;
+        bt += g.kt;
+        pre += (g.kt + 1) * 16;
+        max_m = std::max(max_m, g.M);
+        prm.p[np++] = g;
     }
-    if (np == 0) return BITMTP_OK;
     int dp_rows = 1;
     const int path = choose_path(max_m, flags, &dp_rows);
     if (path < 0) return BITMTP_ERR_SHAPE;
+    const int cap = std::min(kMaxCtas, kCtasPerSm * dev->sms);
     prm.n_problems = np;
-    prm.csize = choose_csize(total_rt, max_kt, dev->sms);
-    prm.nkt_max = static_cast<int>(ceil_div(max_kt, prm.csize));
-    if (prm.nkt_max > kMaxKtPerCta) return BITMTP_ERR_SHAPE;
+    prm.rows_b = path == kPathTC16 ? 16 : path == kPathTC8 ? 8 : dp_rows;
+    prm.btile_bytes = path == kPathTC16 ? 4096 : path == kPathTC8 ? 2048 : dp_rows * 128;
+    prm.stages = gemm_stages(path, dp_rows);
+    prm.total_tasks = tasks;
+    prm.total_tiles = tiles;
+    prm.nctas = static_cast<int>(std::min<long long>(cap, tiles));  // every CTA range is non-empty
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    prm.gridbar = reinterpret_cast<unsigned*>(w + L.gridbar);
+    prm.counters = reinterpret_cast<unsigned*>(w + L.counters);
+    prm.ascale = reinterpret_cast<float*>(w + L.ascale);
+    prm.prefix = reinterpret_cast<int*>(w + L.prefix);
+    prm.slots = reinterpret_cast<int*>(w + L.slots);
+    prm.btiles = w + L.btiles;
     prm.err = dev->err;
-    return cuda_status(launch_gemm(prm, path, dp_rows, total_rt, (flags & BITMTP_FLAG_PDL) != 0, stream));
+    return cuda_status(launch_gemm(prm, path, dp_rows, (flags & BITMTP_FLAG_PDL) != 0, stream));
 }
 
 }  // namespace
@@ -297,18 +336,48 @@ int bitmtp_linear_quant_act(const void* x, int x_kind, int64_t M, int64_t K, int
     return cuda_status(cudaGetLastError());
 }
 
+size_t bitmtp_linear_workspace_bytes(int64_t N, int64_t K, int64_t M) {
+    if (M < 1 || M > BITMTP_MAX_M || N < 1 || N > BITMTP_MAX_N || K < 1 || K > BITMTP_MAX_K) return 0;
+    GemmProblem g;
+    std::memset(&g, 0, sizeof(g));
+    g.N = static_cast<int>(N);
+    g.K = static_cast<int>(K);
+    g.M = static_cast<int>(M);
+    g.nt = static_cast<int>(ceil_div(N, kTileN));
+    g.kt = static_cast<int>(ceil_div(K, kTileK));
+    return layout_for(&g, 1).total;
+}
+
+size_t bitmtp_linear_workspace_bytes_grouped(const bitmtp_gemm_desc* d, int n_desc) {
+    if (n_desc < 1 || n_desc > BITMTP_MAX_GROUP || !d) return 0;
+    GemmProblem g[BITMTP_MAX_GROUP];
+    std::memset(g, 0, sizeof(g));
+    for (int i = 0; i < n_desc; ++i) {
+        const int64_t N = d[i].N, K = d[i].K, M = d[i].M;
+        if (M < 0 || M > BITMTP_MAX_M || N < 0 || N > BITMTP_MAX_N || K < 1 || K > BITMTP_MAX_K) return 0;
+        g[i].N = static_cast<int>(N);
+        g[i].K = static_cast<int>(K);
+        g[i].M = static_cast<int>(M);
+        g[i].nt = static_cast<int>(ceil_div(N, kTileN));
+        g[i].kt = static_cast<int>(ceil_div(K, kTileK));
+    }
+    return layout_for(g, n_desc).total;
+}
+
 int bitmtp_linear_gemm(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M, const bitmtp_act* act,
-                       const bitmtp_out* out, unsigned flags, void* stream) {
+                       const bitmtp_out* out, void* workspace, size_t workspace_bytes, unsigned flags,
+                       void* stream) {
     GemmProblem g;
     std::memset(&g, 0, sizeof(g));
     int st = check_problem(pk, w_scale, N, K, M, act, out, &g);
     if (st != BITMTP_OK) return st;
     if ((flags & BITMTP_FLAG_FORCE_TC) && (flags & BITMTP_FLAG_FORCE_DP)) return BITMTP_ERR_INVALID;
     if (g.M == 0) return BITMTP_OK;
-    return run_gemms(&g, 1, flags, static_cast<cudaStream_t>(stream));
+    return run_gemms(&g, 1, workspace, workspace_bytes, flags, static_cast<cudaStream_t>(stream));
 }
 
-int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc, unsigned flags, void* stream) {
+int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc, void* workspace, size_t workspace_bytes,
+                               unsigned flags, void* stream) {
     if (n_desc < 0 || n_desc > BITMTP_MAX_GROUP) return BITMTP_ERR_SHAPE;
     if (n_desc > 0 && !d) return BITMTP_ERR_INVALID;
     if ((flags & BITMTP_FLAG_FORCE_TC) && (flags & BITMTP_FLAG_FORCE_DP)) return BITMTP_ERR_INVALID;
@@ -319,7 +388,7 @@ int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc, unsigned f
         if (st != BITMTP_OK) return st;
     }
     if (n_desc == 0) return BITMTP_OK;
-    return run_gemms(g, n_desc, flags, static_cast<cudaStream_t>(stream));
+    return run_gemms(g, n_desc, workspace, workspace_bytes, flags, static_cast<cudaStream_t>(stream));
 }
 
 int bitmtp_linear_device_error(void* stream) {

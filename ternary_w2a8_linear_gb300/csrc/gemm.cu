@@ -1,36 +1,44 @@
-// gemm.cu -- the W2A8 ternary linear on sm_103a.
+// gemm.cu -- the W2A8 ternary linear on sm_103a: a persistent stream-K kernel.
 //
-// One kernel template, two compute paths that share the weight stream, the
-// activation prologue and the split-K epilogue:
+// One launch computes one or several independent linears ("problems") with
+// the same compute path:
 //
-//   kPathTC  tcgen05 tensor cores, any block width 1..16.  Each producer
-//            thread owns one output row (one TMEM lane), unpacks its 2-bit
-//            codes straight into fp16 bit patterns with one mask per register
-//            (the codes land in the fp16 subnormal range, value u * 4^J * 2^-24),
-//            writes them to tensor memory (tcgen05.st) as the A operand, and one
-//            thread issues tcgen05.mma (M=128, N=16, K=16) against the
-//            activation block held in shared memory as fp16 pre-scaled by
-//            2^(9-2J) per k position.  Every product is u*q*2^-15 exactly and
-//            every partial sum stays below 2^24 * 2^-15, so the fp32
-//            accumulator holds the exact integer sum.
-//   kPathDP  integer dp4a for narrow blocks (1..4 rows): the same code words,
-//            four byte masks per word and four int32 accumulators per row.
+//  phase 0  every CTA starts streaming its first packed-weight tiles (4 KiB
+//           bulk copies, TMA engine) into a shared-memory ring; weights do
+//           not depend on the previous kernel on the stream;
+//  phase 1  activation rows are quantised (per-row absmax, fp32 round half to
+//           even, the same code as the standalone quantiser) one row per CTA
+//           task, written straight into the activation operand tiles the
+//           compute path consumes, with per-k-tile row sums of the codes;
+//  barrier  one grid-wide barrier (all CTAs are co-resident by construction);
+//  phase 2  the flattened (problem, row tile, k tile) space is split into
+//           equal contiguous ranges, one per CTA (stream-K), so every SM
+//           streams the same number of weight bytes whatever the mix of
+//           shapes.  A row tile whose k tiles span several CTAs is finished by
+//           the last of them to arrive, which sums the others' int32 partials
+//           from the workspace; the dequant epilogue is fused.
 //
-// With u = T + 1, sum_k T*q = sum_k u*q - sum_k q; the CTA subtracts the row
-// sums of its own k slice.
-//
-// Work split: a cluster of `csize` CTAs owns one 128-row tile of the output;
-// CTA r of the cluster owns k tiles [r*KT/csize, (r+1)*KT/csize).  The whole
-// k slice of packed weights is fetched up front with 4 KiB bulk copies (TMA),
-// so every byte the CTA needs is in flight from the first cycle.  Split-K
-// partials (exact int32) are summed through distributed shared memory; the
-// raw-activation absmax is exchanged the same way, so quantisation is fused
-// without a second kernel or any global scratch.
+// Compute paths (the same 2-bit code words feed both):
+//   tensor (kPathTC16 / kPathTC8): each of 128 threads owns one output row
+//     (one TMEM lane), turns its code words into fp16 bit patterns with one
+//     mask per register -- the 2-bit code u lands in the fp16 subnormal range,
+//     value u * 4^J * 2^-24 -- and writes them to tensor memory as the A
+//     operand (tcgen05.st); one thread issues tcgen05.mma kind::f16 (M=128,
+//     N=16, K=16) against the activation tile in shared memory, whose fp16
+//     entries are q * 2^(9-2J).  Every product is u*q*2^-15 and every partial
+//     sum an integer multiple of 2^-15 below 2^9, so the fp32 accumulator is
+//     exact in any order.  kPathTC8 keeps 8 activation rows (the second row
+//     group aliases the first through a zero stride).
+//   dp4a (kPathDP): four byte masks per code word, four int32 accumulators
+//     per row (scales 4^s, recombined with exact shifts).
+// With u = T + 1, sum_k T*q = sum_k u*q - sum_k q; the row sums come from the
+// quantisation phase.
 //
 // The operation is the packed W2A8 linear of "BitMTP: When Multi-Token
 // Prediction Meets Low-Bit Large Language Models" (AI summary: Main Findings,
 // first bullet -- 2-bit weights, 8-bit activations; Methodology in Plain
-// English -- width-specialised packed low-bit operators).
+// English -- width-specialised packed low-bit operators, role-dependent output
+// projections).
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -42,46 +50,50 @@
 namespace bitmtp {
 namespace {
 
+constexpr int kMaxStages = 24;
 constexpr int kCtrlBytes = 1024;
-constexpr int kPartBytes = 16 * kTileN * 4;   // int32 partials [16 rows][128 out-features]
+constexpr int kScratchBytes = 2048;
 constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t kAccCol = 0;               // D: columns 0..15 (fp32, one per block row)
-constexpr uint32_t kACol = 32;                // A: two buffers of 32 columns (64 k each)
+constexpr uint32_t kAccCol = 0;      // D: 16 fp32 columns, one per activation row
+constexpr uint32_t kACol = 32;       // A: three buffers of 32 columns (64 k each)
+constexpr int kABufs = 3;
 constexpr uint32_t kIdesc = idesc_f16_f32(128, 16);
-constexpr int kTcSmemFloor = 48 * 1024;       // caps residency at 4 CTAs/SM -> 4 x 128 TMEM columns
+constexpr int kSmemTarget = 56 * 1024;  // 2 CTAs of this kernel + 2 of the next fit on an SM
 
 enum : int {
-    kErrWaitFull = 0x101,
-    kErrWaitAFull = 0x102,
-    kErrWaitAEmpty = 0x103,
-    kErrWaitDone = 0x104,
+    kErrWaitW = 0x101,
+    kErrWaitB = 0x102,
+    kErrWaitAFull = 0x103,
+    kErrWaitAEmpty = 0x104,
+    kErrWaitD = 0x105,
+    kErrWaitEmpty = 0x106,
+    kErrGridBarrier = 0x107,
 };
 
 struct Ctrl {
-    uint64_t full[kMaxKtPerCta];
-    uint64_t a_full[2];
-    uint64_t a_empty[2];
-    uint64_t done;
+    uint64_t wfull[kMaxStages];
+    uint64_t bfull[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t a_full[kABufs];
+    uint64_t a_empty[kABufs];
+    uint64_t dfull;
     uint32_t tmem_base;
     int failed;
-    float amax_part[16];
-    float a_scale[16];
-    float qscale[16];
-    int rowsum_part[16];
+    int last;
+    float red_f[4];
+    int red_i[4];
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
-// fp16 pre-scale of the activation for code column c (J = 0,1,2,3,4,0,1,2).
-__device__ __forceinline__ int bscale_shift(int c) {
-    return 9 - 2 * ((c < 5) ? c : (c - 5));
-}
+__host__ __device__ constexpr int btile_lbo(int path) { return path == kPathTC16 ? 256 : 128; }
+__host__ __device__ constexpr int btile_sbo(int path) { return path == kPathTC16 ? 128 : 0; }
+
+// fp16 pre-scale shift of the activation for A column c (J = 0,1,2,3,4,0,1,2).
+__device__ __forceinline__ int bscale_shift(int c) { return 9 - 2 * ((c < 5) ? c : (c - 5)); }
 
 __device__ __forceinline__ void fail(Ctrl* c, int* err, int code) {
     *reinterpret_cast<volatile int*>(&c->failed) = 1;
     atomicCAS(err, 0, code);
-}
-__device__ __forceinline__ bool failed(Ctrl* c) {
-    return *reinterpret_cast<volatile int*>(&c->failed) != 0;
 }
 
 // One code word -> eight fp16x2 registers (A columns c = 0..7; half e of
@@ -98,8 +110,224 @@ __device__ __forceinline__ void unpack_word_f16(uint32_t w, uint32_t* r) {
     r[7] = t & 0x00300030u;
 }
 
-__device__ __forceinline__ void store_out(const GemmProblem& pr, int m, int n, int acc,
-                                          float a_scale) {
+__device__ __forceinline__ int find_problem_by_task(const GemmParams& P, int task) {
+    int pi = 0;
+#pragma unroll 1
+    for (int i = 1; i < P.n_problems; ++i)
+        if (task >= P.p[i].task_begin) pi = i;
+    return pi;
+}
+__device__ __forceinline__ int find_problem_by_tile(const GemmParams& P, long long t) {
+    int pi = 0;
+#pragma unroll 1
+    for (int i = 1; i < P.n_problems; ++i)
+        if (t >= P.p[i].tile_begin) pi = i;
+    return pi;
+}
+
+__device__ __forceinline__ long long range_start(int b, long long T, int n) {
+    return (static_cast<long long>(b) * T) / n;
+}
+// CTA whose range holds flattened tile t.
+__device__ __forceinline__ int range_owner(long long t, long long T, int n) {
+    return static_cast<int>(((t + 1) * n - 1) / T);
+}
+
+// Flattened-tile walker: (problem, row tile, k tile) advancing with k fastest.
+struct TileIter {
+    int pi, rt, kt;
+    __device__ void init(const GemmParams& P, long long t) {
+        pi = find_problem_by_tile(P, t);
+        const long long local = t - P.p[pi].tile_begin;
+        rt = static_cast<int>(local / P.p[pi].kt);
+        kt = static_cast<int>(local % P.p[pi].kt);
+    }
+    __device__ void next(const GemmParams& P) {
+        if (++kt == P.p[pi].kt) {
+            kt = 0;
+            if (++rt == P.p[pi].nt) {
+                rt = 0;
+                ++pi;
+            }
+        }
+    }
+};
+
+// Block-wide (128 threads, named barrier 1) max of non-negative floats.
+__device__ __forceinline__ float block128_max(float v, Ctrl* c, int tid) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((tid & 31) == 0) c->red_f[tid >> 5] = v;
+    named_bar_sync(1, 128);
+    const float r = fmaxf(fmaxf(c->red_f[0], c->red_f[1]), fmaxf(c->red_f[2], c->red_f[3]));
+    named_bar_sync(1, 128);
+    return r;
+}
+
+// Exclusive prefix sum over 128 threads (named barrier 1); returns the
+// exclusive sum and writes the block total to *total.
+__device__ __forceinline__ int block128_exscan(int v, Ctrl* c, int tid, int* total) {
+    const int lane = tid & 31;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) c->red_i[tid >> 5] = incl;
+    named_bar_sync(1, 128);
+    int base = 0;
+    for (int w = 0; w < (tid >> 5); ++w) base += c->red_i[w];
+    *total = c->red_i[0] + c->red_i[1] + c->red_i[2] + c->red_i[3];
+    named_bar_sync(1, 128);
+    return base + incl - v;
+}
+
+// Load 8 consecutive activations k0..k0+7 of one row (zero beyond K).
+__device__ __forceinline__ void load8(const GemmProblem& pr, const char* row, bool vec_ok, int k0,
+                                      float (&v)[8]) {
+    if (pr.act_kind == BITMTP_BF16) {
+        if (vec_ok && k0 + 8 <= pr.K) {
+            const uint4 u = *reinterpret_cast<const uint4*>(row + 2ll * k0);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __uint_as_float(w[i] << 16);
+                v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        } else {
+            const uint16_t* r = reinterpret_cast<const uint16_t*>(row);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = (k0 + i < pr.K) ? __uint_as_float(static_cast<uint32_t>(r[k0 + i]) << 16) : 0.f;
+        }
+    } else if (pr.act_kind == BITMTP_F32) {
+        if (vec_ok && k0 + 8 <= pr.K) {
+            const float4 a = *reinterpret_cast<const float4*>(row + 4ll * k0);
+            const float4 b = *reinterpret_cast<const float4*>(row + 4ll * k0 + 16);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+            const float* r = reinterpret_cast<const float*>(row);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = (k0 + i < pr.K) ? r[k0 + i] : 0.f;
+        }
+    } else {  // int8 codes
+        const int8_t* r = reinterpret_cast<const int8_t*>(row);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = (k0 + i < pr.K) ? static_cast<float>(r[k0 + i]) : 0.f;
+    }
+}
+
+// ------------------------------------------------ phase 1: one activation row --
+template <int PATH, int DPR>
+__device__ void quant_row_task(const GemmParams& P, int task, Ctrl* c, int* tsum, int tid) {
+    const int pi = find_problem_by_task(P, task);
+    const GemmProblem& pr = P.p[pi];
+    const int m = task - pr.task_begin;
+    const int KT = pr.kt;
+    const int esize = pr.act_kind == BITMTP_F32 ? 4 : (pr.act_kind == BITMTP_BF16 ? 2 : 1);
+    const char* row = static_cast<const char*>(pr.x) + static_cast<long long>(m) * pr.ldx * esize;
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+    const bool raw = pr.act_kind != BITMTP_Q8;
+
+    float s = 0.f;
+    if (raw) {
+        float a = 0.f;
+#pragma unroll 4
+        for (int g = tid; g * 8 < pr.K; g += 128) {
+            float v[8];
+            load8(pr, row, vec_ok, g * 8, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+        }
+        const float amax = block128_max(a, c, tid);
+        s = quant_scale(amax);
+        if (tid == 0) P.ascale[pr.task_begin + m] = dequant_scale(amax);
+    } else if (tid == 0) {
+        P.ascale[pr.task_begin + m] = pr.a_scale_in[m];
+    }
+
+    uint8_t* bt = P.btiles + static_cast<size_t>(pr.bt_begin) * P.btile_bytes;
+    if constexpr (PATH != kPathDP) {
+        // 8-k groups; 16 per k tile, one half-warp per tile per pass
+        const int ngroups = KT * 16;
+        for (int base = (tid & ~31); base < ngroups; base += 128) {
+            const int g = base + (tid & 31);
+            int rs = 0;
+            if (g < ngroups) {
+                float v[8];
+                load8(pr, row, vec_ok, g * 8, v);
+                uint32_t packed[4];
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    const int q0 = raw ? quantize(v[i], s) : static_cast<int>(v[i]);
+                    const int q1 = raw ? quantize(v[i + 1], s) : static_cast<int>(v[i + 1]);
+                    rs += q0 + q1;
+                    const int sh = bscale_shift((g & 1) * 4 + (i >> 1));
+                    const __half h0 = __int2half_rn(q0 * (1 << sh));
+                    const __half h1 = __int2half_rn(q1 * (1 << sh));
+                    packed[i >> 1] = static_cast<uint32_t>(__half_as_ushort(h0)) |
+                                     (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+                }
+                const int tile = g >> 4, kg = g & 15;
+                uint8_t* dst = bt + static_cast<size_t>(tile) * P.btile_bytes + kg * btile_lbo(PATH) +
+                               (m >> 3) * btile_sbo(PATH) + (m & 7) * 16;
+                *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+            if ((tid & 15) == 0 && g < ngroups) tsum[g >> 4] = rs;
+        }
+    } else {
+        // 16-k chunks; 8 per k tile, eight threads per tile per pass
+        const int nchunks = KT * 8;
+        for (int base = (tid & ~31); base < nchunks; base += 128) {
+            const int g = base + (tid & 31);
+            int rs = 0;
+            if (g < nchunks) {
+                float v[16];
+                float* v0 = v;
+                load8(pr, row, vec_ok, g * 16, *reinterpret_cast<float(*)[8]>(v0));
+                load8(pr, row, vec_ok, g * 16 + 8, *reinterpret_cast<float(*)[8]>(v0 + 8));
+                int q[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    q[i] = raw ? quantize(v[i], s) : static_cast<int>(v[i]);
+                    rs += q[i];
+                }
+                uint32_t reg[4];
+#pragma unroll
+                for (int sidx = 0; sidx < 4; ++sidx) {
+                    reg[sidx] = (static_cast<uint32_t>(q[2 * sidx]) & 0xFFu) |
+                                ((static_cast<uint32_t>(q[8 + 2 * sidx]) & 0xFFu) << 8) |
+                                ((static_cast<uint32_t>(q[2 * sidx + 1]) & 0xFFu) << 16) |
+                                ((static_cast<uint32_t>(q[9 + 2 * sidx]) & 0xFFu) << 24);
+                }
+                const int tile = g >> 3, ch = g & 7;
+                uint8_t* dst = bt + static_cast<size_t>(tile) * P.btile_bytes + ch * (DPR * 16) + m * 16;
+                *reinterpret_cast<uint4*>(dst) = make_uint4(reg[0], reg[1], reg[2], reg[3]);
+            }
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+            if ((tid & 7) == 0 && g < nchunks) tsum[g >> 3] = rs;
+        }
+    }
+    named_bar_sync(1, 128);
+    // prefix[kt] = sum of the row's codes over k tiles [0, kt), kt = 0..KT
+    int* pre = P.prefix + pr.pre_begin;
+    const int a0 = (2 * tid < KT) ? tsum[2 * tid] : 0;
+    const int a1 = (2 * tid + 1 < KT) ? tsum[2 * tid + 1] : 0;
+    int total = 0;
+    const int ex = block128_exscan(a0 + a1, c, tid, &total);
+    if (2 * tid < KT) pre[(2 * tid) * 16 + m] = ex;
+    if (2 * tid + 1 < KT) pre[(2 * tid + 1) * 16 + m] = ex + a0;
+    if (tid == 0) pre[KT * 16 + m] = total;
+    named_bar_sync(1, 128);
+}
+
+// ------------------------------------------------------------ epilogue --
+__device__ __forceinline__ void store_out(const GemmProblem& pr, int m, int n, int acc, float a_scale) {
     const float v = __fmul_rn(__fmul_rn(static_cast<float>(acc), a_scale), pr.w_scale);
     const long long o = static_cast<long long>(m) * pr.ldy + n;
     if (pr.out_dtype == BITMTP_F32) {
@@ -110,335 +338,350 @@ __device__ __forceinline__ void store_out(const GemmProblem& pr, int m, int n, i
     if (pr.acc) pr.acc[static_cast<long long>(m) * pr.lda + n] = acc;
 }
 
+// Finish one segment (k tiles [ka, kb) of row tile rt of problem pi) held by
+// this CTA.  part[m] = sum_k u*q for the thread's row over the segment.
+__device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int pi, int rt, int ka, int kb,
+                                 bool first_segment, const int (&part)[16], int tid, bool alive) {
+    const GemmProblem& pr = P.p[pi];
+    const int M = pr.M;
+    const int* pre = P.prefix + pr.pre_begin;
+    const float* asc = P.ascale + pr.task_begin;
+    const int n = rt * kTileN + tid;
+    int acc[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+        acc[m] = (m < M) ? part[m] - (pre[kb * 16 + m] - pre[ka * 16 + m]) : 0;
+
+    if (ka == 0 && kb == pr.kt) {
+        if (alive && n < pr.N) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                if (m < M) store_out(pr, m, n, acc[m], asc[m]);
+        }
+        return;
+    }
+    // split row tile: publish the partial, the last contributor finishes it
+    const int b = blockIdx.x;
+    int* my = P.slots + (static_cast<size_t>(b) * 2 + (first_segment ? 0 : 1)) * 16 * kTileN;
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+        if (alive && m < M) my[m * kTileN + tid] = acc[m];
+    __threadfence();
+    named_bar_sync(1, 128);
+    const long long T = P.total_tiles;
+    const long long t_first = pr.tile_begin + static_cast<long long>(rt) * pr.kt;
+    const int b_first = range_owner(t_first, T, P.nctas);
+    const int b_last = range_owner(t_first + pr.kt - 1, T, P.nctas);
+    if (tid == 0) {
+        const unsigned old = atomicAdd(P.counters + pr.rt_begin + rt, 1u);
+        c->last = (old == static_cast<unsigned>(b_last - b_first)) ? 1 : 0;
+    }
+    named_bar_sync(1, 128);
+    if (c->last) {
+        __threadfence();
+        for (int ob = b_first; ob <= b_last; ++ob) {
+            if (ob == b) continue;
+            const int slot = (range_start(ob, T, P.nctas) >= t_first) ? 0 : 1;
+            const int* os = P.slots + (static_cast<size_t>(ob) * 2 + slot) * 16 * kTileN;
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                if (m < M) acc[m] += __ldcg(os + m * kTileN + tid);
+        }
+        if (alive && n < pr.N) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                if (m < M) store_out(pr, m, n, acc[m], asc[m]);
+        }
+        if (tid == 0) atomicExch(P.counters + pr.rt_begin + rt, 0u);
+    }
+    named_bar_sync(1, 128);
+}
+
+// Grid-wide barrier: each CTA adds 1 except CTA 0, which adds 2^31 - (n-1), so
+// the top bit of the counter flips exactly once per barrier and the low bits
+// come back to their value.  Called by one thread per CTA.
+__device__ bool grid_barrier(unsigned* bar, int nblocks) {
+    __threadfence();
+    const unsigned inc = (blockIdx.x == 0) ? (0x80000000u - static_cast<unsigned>(nblocks - 1)) : 1u;
+    const unsigned old = atomicAdd(bar, inc);
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (((old ^ ld_acquire_gpu(bar)) & 0x80000000u) != 0) break;
+        if ((it & 63u) == 63u && global_ns() - t0 > 2000000000ull) return false;
+    }
+    __threadfence();
+    return true;
+}
+
 template <int PATH, int DPR>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-w2a8_gemm_kernel(const __grid_constant__ GemmParams P) {
+__global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
+w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem);
-    uint8_t* Ws = smem + kCtrlBytes;
-    uint8_t* Bs = Ws + static_cast<size_t>(P.nkt_max) * kTileBytes;
-    int* part = reinterpret_cast<int*>(Bs + static_cast<size_t>(P.nkt_max) * kTileBytes);
+    Ctrl* c = reinterpret_cast<Ctrl*>(smem);
+    int* tsum = reinterpret_cast<int*>(smem + kCtrlBytes);
+    uint8_t* Wr = smem + kCtrlBytes + kScratchBytes;
+    const int S = P.stages;
+    uint8_t* Br = Wr + static_cast<size_t>(S) * kTileBytes;
+    const int BT = P.btile_bytes;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int csize = P.csize;
-    const int rank = (csize > 1) ? static_cast<int>(cluster_ctarank()) : 0;
-    const int cl = blockIdx.x / csize;
-
-    int pi = 0;
-#pragma unroll 1
-    for (int i = 1; i < P.n_problems; ++i)
-        if (cl >= P.p[i].cluster_begin) pi = i;
-    const GemmProblem& pr = P.p[pi];
-
-    const int rt = cl - pr.cluster_begin;
-    const int KT = pr.kt;
-    const int kt0 = static_cast<int>(static_cast<long long>(rank) * KT / csize);
-    const int kt1 = static_cast<int>(static_cast<long long>(rank + 1) * KT / csize);
-    const int nkt = kt1 - kt0;
-    const int M = pr.M;
-    const int kbase = kt0 * kTileK;                    // first k of this CTA's slice
-    const int kend = min(kt1 * kTileK, pr.K);          // end of valid k in the slice
-    const bool raw = pr.act_kind != BITMTP_Q8;
+    const int b = blockIdx.x;
+    const long long T = P.total_tiles;
+    const long long t_begin = range_start(b, T, P.nctas);
+    const int nloc = static_cast<int>(range_start(b + 1, T, P.nctas) - t_begin);
+    constexpr bool kTC = PATH != kPathDP;
 
     // ------------------------------------------------------------ set-up --
     if (tid == 0) {
-        for (int s = 0; s < nkt; ++s) mbar_init(smem_u32(&ctrl->full[s]), 1);
-        mbar_init(smem_u32(&ctrl->a_full[0]), 4);
-        mbar_init(smem_u32(&ctrl->a_full[1]), 4);
-        mbar_init(smem_u32(&ctrl->a_empty[0]), 1);
-        mbar_init(smem_u32(&ctrl->a_empty[1]), 1);
-        mbar_init(smem_u32(&ctrl->done), 1);
-        ctrl->failed = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&c->wfull[s]), 1);
+            mbar_init(smem_u32(&c->bfull[s]), 1);
+            mbar_init(smem_u32(&c->empty[s]), kTC ? 1 : 4);
+        }
+        for (int a = 0; a < kABufs; ++a) {
+            mbar_init(smem_u32(&c->a_full[a]), 4);
+            mbar_init(smem_u32(&c->a_empty[a]), 1);
+        }
+        mbar_init(smem_u32(&c->dfull), 1);
+        c->failed = 0;
         fence_mbar_init();
     }
-    if (tid < 16) {
-        ctrl->rowsum_part[tid] = 0;
-        ctrl->amax_part[tid] = 0.f;
-    }
-    if constexpr (PATH == kPathTC) {
+    if constexpr (kTC) {
         if (warp == 0) {
-            tmem_alloc(smem_u32(&ctrl->tmem_base), kTmemCols);
+            tmem_alloc(smem_u32(&c->tmem_base), kTmemCols);
             tmem_relinquish();
         }
         tc_fence_before();
     }
     __syncthreads();
-    if constexpr (PATH == kPathTC) tc_fence_after();
-    const uint32_t tmem = (PATH == kPathTC) ? ctrl->tmem_base : 0u;
+    if constexpr (kTC) tc_fence_after();
+    const uint32_t tmem = kTC ? c->tmem_base : 0u;
 
-    // The packed weights do not depend on earlier kernels: start streaming now.
-    if (warp == 4 && lane == 0 && nkt > 0) {
-        const uint64_t pol = policy_evict_first();
-        const uint8_t* src = pr.pk + (static_cast<size_t>(rt) * KT + kt0) * kTileBytes;
-        for (int s = 0; s < nkt; ++s) {
-            const uint32_t bar = smem_u32(&ctrl->full[s]);
+    // ------------------------------- phase 0: start the weight stream --
+    const int npre = nloc < S ? nloc : S;
+    uint64_t pol = 0;
+    if (warp == 4 && lane == 0) {
+        pol = policy_evict_first();
+        TileIter it;
+        it.init(P, t_begin);
+        for (int i = 0; i < npre; ++i) {
+            const GemmProblem& pr = P.p[it.pi];
+            const uint32_t bar = smem_u32(&c->wfull[i]);
             mbar_arrive_expect_tx(bar, kTileBytes);
-            bulk_g2s(smem_u32(Ws + s * kTileBytes), src + static_cast<size_t>(s) * kTileBytes,
-                     kTileBytes, bar, pol);
+            bulk_g2s(smem_u32(Wr + static_cast<size_t>(i) * kTileBytes),
+                     pr.pk + (static_cast<size_t>(it.rt) * pr.kt + it.kt) * kTileBytes, kTileBytes, bar, pol);
+            it.next(P);
         }
     }
     __syncwarp();
     pdl_launch_dependents();
 
-    // ------------------------------------- activation prologue (warps 0-3) --
+    // --------------------------------- phase 1: quantise activation rows --
     if (warp < 4) {
-        pdl_wait();  // activations may come from the previous kernel on the stream
-        if (raw) {
-            for (int m = warp; m < M; m += 4) {
-                float a = 0.f;
-                for (int k = kbase + lane; k < kend; k += 32)
-                    a = fmaxf(a, fabsf(load_act(pr.x, pr.act_kind, static_cast<long long>(m) * pr.ldx + k)));
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-                if (lane == 0) ctrl->amax_part[m] = a;
-            }
-        }
+        pdl_wait();  // activations may be written by the previous kernel on the stream
+        for (int task = b; task < P.total_tasks; task += P.nctas)
+            quant_row_task<PATH, DPR>(P, task, c, tsum, tid);
+        fence_proxy_async_global();  // operand tiles are read back by bulk copies
+        __threadfence();
     }
-    __syncwarp();
-    if (raw && csize > 1) cluster_sync(); else __syncthreads();
-    if (tid < 16) {
-        const int m = tid;
-        if (raw) {
-            float a = ctrl->amax_part[m];
-            for (int q = 0; q < csize; ++q)
-                if (q != rank) a = fmaxf(a, ld_cluster_f32(mapa(smem_u32(&ctrl->amax_part[m]), q)));
-            ctrl->qscale[m] = quant_scale(a);
-            ctrl->a_scale[m] = dequant_scale(a);
-        } else {
-            ctrl->qscale[m] = 0.f;
-            ctrl->a_scale[m] = (m < M) ? pr.a_scale[m] : 0.f;
-        }
+    __syncthreads();
+    if (tid == 0) {
+        if (!grid_barrier(P.gridbar, P.nctas)) fail(c, P.err, kErrGridBarrier);
     }
     __syncthreads();
 
-    if (warp < 4) {
-        int rs = 0;
-        const int slice_k = nkt * kTileK;
-        if constexpr (PATH == kPathTC) {
-            // B: [8-k group g][row group m/8][row m%8][8 fp16], core matrices of 8 x 16 B.
-            const int units = (slice_k / 8) * 16;
-            for (int u = tid; u < units; u += 128) {
-                const int m = u & 15;
-                const int g = u >> 4;
-                const float s = ctrl->qscale[m];
-                uint32_t packed[4];
-#pragma unroll
-                for (int i = 0; i < 8; i += 2) {
-                    int qv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int k = kbase + g * 8 + i + e;
-                        int v = 0;
-                        if (m < M && k < kend) {
-                            const long long idx = static_cast<long long>(m) * pr.ldx + k;
-                            v = raw ? quantize(load_act(pr.x, pr.act_kind, idx), s)
-                                    : static_cast<int>(static_cast<const int8_t*>(pr.x)[idx]);
+    // ------------------------------------------------ phase 2: stream-K --
+    if (warp == 4) {
+        if (lane == 0 && nloc > 0) {
+            fence_proxy_async_global();
+            TileIter it;
+            it.init(P, t_begin);
+            for (int i = 0; i < nloc; ++i) {
+                const GemmProblem& pr = P.p[it.pi];
+                const int s = i % S;
+                if (i >= S) {
+                    if (!mbar_wait_bounded(smem_u32(&c->empty[s]), ((i / S) - 1) & 1)) {
+                        fail(c, P.err, kErrWaitEmpty);
+                        break;
+                    }
+                    const uint32_t wb = smem_u32(&c->wfull[s]);
+                    mbar_arrive_expect_tx(wb, kTileBytes);
+                    bulk_g2s(smem_u32(Wr + static_cast<size_t>(s) * kTileBytes),
+                             pr.pk + (static_cast<size_t>(it.rt) * pr.kt + it.kt) * kTileBytes, kTileBytes,
+                             wb, pol);
+                }
+                const uint32_t bb = smem_u32(&c->bfull[s]);
+                mbar_arrive_expect_tx(bb, BT);
+                bulk_g2s(smem_u32(Br + static_cast<size_t>(s) * BT),
+                         P.btiles + (static_cast<size_t>(pr.bt_begin) + it.kt) * BT, BT, bb, pol);
+                it.next(P);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        if constexpr (kTC) {
+            if (lane == 0 && nloc > 0) {
+                TileIter it;
+                it.init(P, t_begin);
+                const uint32_t bbase = smem_u32(Br);
+                bool seg_first = true;
+                bool ok = true;
+                for (int i = 0; i < nloc && ok; ++i) {
+                    const int s = i % S;
+                    const bool seg_last = (i == nloc - 1) || (it.kt == P.p[it.pi].kt - 1);
+                    if (!mbar_wait_bounded(smem_u32(&c->bfull[s]), (i / S) & 1)) {
+                        fail(c, P.err, kErrWaitB);
+                        break;
+                    }
+                    for (int h = 0; h < 2; ++h) {
+                        const int u = 2 * i + h;
+                        const int a = u % kABufs;
+                        if (!mbar_wait_bounded(smem_u32(&c->a_full[a]), (u / kABufs) & 1)) {
+                            fail(c, P.err, kErrWaitAFull);
+                            ok = false;
+                            break;
                         }
-                        qv[e] = v;
-                        rs += v;
-                    }
-                    const int c = (g & 1) * 4 + (i >> 1);
-                    const int sh = bscale_shift(c);
-                    const __half h0 = __int2half_rn(qv[0] * (1 << sh));
-                    const __half h1 = __int2half_rn(qv[1] * (1 << sh));
-                    packed[i >> 1] = static_cast<uint32_t>(__half_as_ushort(h0)) |
-                                     (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-                }
-                uint4* dst = reinterpret_cast<uint4*>(Bs + g * 256 + (m >> 3) * 128 + (m & 7) * 16);
-                *dst = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            }
-            fence_proxy_async_smem();
-        } else {
-            // B: [16-k chunk t][row m] 16 bytes = four int8x4 registers matching the
-            // byte lanes of the masked code word: s -> {2s, 8+2s, 2s+1, 9+2s}.
-            const int units = (slice_k / 16) * 16;
-            for (int u = tid; u < units; u += 128) {
-                const int m = u & 15;
-                const int t = u >> 4;
-                const float s = ctrl->qscale[m];
-                int qv[16];
+                        tc_fence_after();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int k = kbase + t * 16 + i;
-                    int v = 0;
-                    if (m < M && k < kend) {
-                        const long long idx = static_cast<long long>(m) * pr.ldx + k;
-                        v = raw ? quantize(load_act(pr.x, pr.act_kind, idx), s)
-                                : static_cast<int>(static_cast<const int8_t*>(pr.x)[idx]);
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int chunk = h * 4 + jj;  // 16-k chunk within the k tile
+                            const uint64_t bdesc = smem_desc_noswizzle(
+                                bbase + s * BT + chunk * 2 * btile_lbo(PATH), btile_lbo(PATH), btile_sbo(PATH));
+                            mma_f16_ts(tmem + kAccCol, tmem + kACol + a * 32 + jj * 8, bdesc, kIdesc,
+                                       (seg_first && h == 0 && jj == 0) ? 0u : 1u);
+                        }
+                        mma_commit(smem_u32(&c->a_empty[a]));
                     }
-                    qv[i] = v;
-                    rs += v;
+                    if (!ok) break;
+                    mma_commit(smem_u32(&c->empty[s]));
+                    if (seg_last) mma_commit(smem_u32(&c->dfull));
+                    seg_first = seg_last;
+                    it.next(P);
                 }
-                uint32_t reg[4];
-#pragma unroll
-                for (int sidx = 0; sidx < 4; ++sidx) {
-                    reg[sidx] = (static_cast<uint32_t>(qv[2 * sidx]) & 0xFFu) |
-                                ((static_cast<uint32_t>(qv[8 + 2 * sidx]) & 0xFFu) << 8) |
-                                ((static_cast<uint32_t>(qv[2 * sidx + 1]) & 0xFFu) << 16) |
-                                ((static_cast<uint32_t>(qv[9 + 2 * sidx]) & 0xFFu) << 24);
-                }
-                *reinterpret_cast<uint4*>(Bs + (t * 16 + m) * 16) = make_uint4(reg[0], reg[1], reg[2], reg[3]);
             }
         }
-        // every thread's units share one row m = tid % 16
-        if (rs != 0) atomicAdd(&ctrl->rowsum_part[tid & 15], rs);
-    }
-    __syncthreads();
-
-    // -------------------------------------------------------- main loop --
-    int part_acc[16];
+        __syncwarp();
+    } else {
+        // warps 0-3: one output row per thread.  A failed (timed-out) wait only
+        // clears `alive`; every named barrier is still executed by all four warps.
+        TileIter it;
+        it.pi = it.rt = it.kt = 0;
+        if (nloc > 0) it.init(P, t_begin);
+        int part[16];
 #pragma unroll
-    for (int m = 0; m < 16; ++m) part_acc[m] = 0;
-
-    if constexpr (PATH == kPathTC) {
-        if (warp < 4) {
-            const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-            bool ok = true;
-            for (int i = 0; i < nkt && ok; ++i) {
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctrl->full[i]), 0));
-                if (!ok) { if (lane == 0) fail(ctrl, P.err, kErrWaitFull); break; }
+        for (int m = 0; m < 16; ++m) part[m] = 0;
+        int ka = it.kt, seg_idx = 0, seg_first_i = 0;
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        int dacc[4][DPR];
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+            for (int m = 0; m < DPR; ++m) dacc[s4][m] = 0;
+        bool alive = true;
+        for (int i = 0; i < nloc; ++i) {
+            const int s = i % S;
+            const bool seg_last = (i == nloc - 1) || (it.kt == P.p[it.pi].kt - 1);
+            if (alive) {
+                alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[s]), (i / S) & 1));
+                if (!alive && lane == 0) fail(c, P.err, kErrWaitW);
+            }
+            const uint8_t* wst = Wr + static_cast<size_t>(s) * kTileBytes;
+            if constexpr (kTC) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int u = 2 * i + h;
-                    const int b = u & 1;
-                    if (u >= 2) {
-                        ok = __all_sync(0xffffffffu,
-                                        mbar_wait_bounded(smem_u32(&ctrl->a_empty[b]), ((u >> 1) - 1) & 1));
-                        if (!ok) { if (lane == 0) fail(ctrl, P.err, kErrWaitAEmpty); break; }
+                    const int a = u % kABufs;
+                    if (alive && u >= kABufs) {
+                        alive = __all_sync(0xffffffffu,
+                                           mbar_wait_bounded(smem_u32(&c->a_empty[a]), ((u / kABufs) - 1) & 1));
+                        if (!alive && lane == 0) fail(c, P.err, kErrWaitAEmpty);
                         tc_fence_after();
                     }
-                    const uint4 wv = *reinterpret_cast<const uint4*>(Ws + i * kTileBytes + h * 2048 + tid * 16);
-                    uint32_t r[32];
-                    unpack_word_f16(wv.x, r + 0);
-                    unpack_word_f16(wv.y, r + 8);
-                    unpack_word_f16(wv.z, r + 16);
-                    unpack_word_f16(wv.w, r + 24);
-                    tmem_st32(tmem + lane_base + kACol + b * 32, r);
-                    tc_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ctrl->a_full[b]));
-                }
-            }
-        } else if (lane == 0 && nkt > 0) {
-            const uint32_t bbase = smem_u32(Bs);
-            const int nu = 2 * nkt;
-            for (int u = 0; u < nu; ++u) {
-                const int b = u & 1;
-                if (!mbar_wait_bounded(smem_u32(&ctrl->a_full[b]), (u >> 1) & 1)) {
-                    fail(ctrl, P.err, kErrWaitAFull);
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int t = 4 * u + jj;  // 16-k chunk within the slice
-                    const uint64_t bdesc = smem_desc_noswizzle(bbase + t * 512, 256, 128);
-                    mma_f16_ts(tmem + kAccCol, tmem + kACol + b * 32 + jj * 8, bdesc, kIdesc,
-                               (u | jj) != 0 ? 1u : 0u);
-                }
-                mma_commit(smem_u32(&ctrl->a_empty[b]));
-            }
-            mma_commit(smem_u32(&ctrl->done));
-        }
-        __syncwarp();
-        if (warp < 4 && nkt > 0) {
-            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctrl->done), 0));
-            if (ok) {
-                tc_fence_after();
-                uint32_t v[16];
-                tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + kAccCol, v);
-                tc_wait_ld();
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    part_acc[m] = __float2int_rn(__uint_as_float(v[m]) * 32768.f);
-            } else if (lane == 0) {
-                fail(ctrl, P.err, kErrWaitDone);
-            }
-        }
-    } else {
-        if (warp < 4) {
-            int a0[DPR], a1[DPR], a2[DPR], a3[DPR];
-#pragma unroll
-            for (int m = 0; m < DPR; ++m) a0[m] = a1[m] = a2[m] = a3[m] = 0;
-            for (int i = 0; i < nkt; ++i) {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctrl->full[i]), 0))) {
-                    if (lane == 0) fail(ctrl, P.err, kErrWaitFull);
-                    break;
-                }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint4 wv = *reinterpret_cast<const uint4*>(Ws + i * kTileBytes + h * 2048 + tid * 16);
-                    const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int t = i * 8 + h * 4 + jj;
-                        const uint32_t w = wd[jj];
-                        const uint32_t m0 = w & 0x03030303u, m1 = w & 0x0C0C0C0Cu;
-                        const uint32_t m2 = w & 0x30303030u, m3 = w & 0xC0C0C0C0u;
-#pragma unroll
-                        for (int m = 0; m < DPR; ++m) {
-                            const int4 qv = *reinterpret_cast<const int4*>(Bs + (t * 16 + m) * 16);
-                            a0[m] = dp4a_us(m0, qv.x, a0[m]);
-                            a1[m] = dp4a_us(m1, qv.y, a1[m]);
-                            a2[m] = dp4a_us(m2, qv.z, a2[m]);
-                            a3[m] = dp4a_us(m3, qv.w, a3[m]);
-                        }
+                    if (alive) {
+                        const uint4 wv = *reinterpret_cast<const uint4*>(wst + h * 2048 + tid * 16);
+                        uint32_t r[32];
+                        unpack_word_f16(wv.x, r + 0);
+                        unpack_word_f16(wv.y, r + 8);
+                        unpack_word_f16(wv.z, r + 16);
+                        unpack_word_f16(wv.w, r + 24);
+                        tmem_st32(tmem + lane_base + kACol + a * 32, r);
+                        tc_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&c->a_full[a]));
                     }
                 }
+            } else {
+                if (alive) {
+                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[s]), (i / S) & 1));
+                    if (!alive && lane == 0) fail(c, P.err, kErrWaitB);
+                }
+                if (alive) {
+                    const uint8_t* bst = Br + static_cast<size_t>(s) * BT;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 wv = *reinterpret_cast<const uint4*>(wst + h * 2048 + tid * 16);
+                        const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int ch = h * 4 + jj;
+                            const uint32_t w = wd[jj];
+                            const uint32_t m0 = w & 0x03030303u, m1 = w & 0x0C0C0C0Cu;
+                            const uint32_t m2 = w & 0x30303030u, m3 = w & 0xC0C0C0C0u;
+#pragma unroll
+                            for (int m = 0; m < DPR; ++m) {
+                                const int4 qv = *reinterpret_cast<const int4*>(bst + ch * (DPR * 16) + m * 16);
+                                dacc[0][m] = dp4a_us(m0, qv.x, dacc[0][m]);
+                                dacc[1][m] = dp4a_us(m1, qv.y, dacc[1][m]);
+                                dacc[2][m] = dp4a_us(m2, qv.z, dacc[2][m]);
+                                dacc[3][m] = dp4a_us(m3, qv.w, dacc[3][m]);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&c->empty[s]));
+                }
             }
+            if (seg_last) {
+                if constexpr (kTC) {
+                    if (alive) {
+                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->dfull), seg_idx & 1));
+                        if (!alive && lane == 0) fail(c, P.err, kErrWaitD);
+                    }
+                    if (alive) {
+                        tc_fence_after();
+                        uint32_t v[16];
+                        tmem_ld16(tmem + lane_base + kAccCol, v);
+                        tc_wait_ld();
+                        tc_fence_before();
 #pragma unroll
-            for (int m = 0; m < DPR; ++m)
-                part_acc[m] = a0[m] + (a1[m] >> 2) + (a2[m] >> 4) + (a3[m] >> 6);
-        }
-    }
-
-    // ---------------------------------------------- split-K epilogue --
-    if (warp < 4) {
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            if (m < M) {
-                const int v = part_acc[m] - ctrl->rowsum_part[m];
-                if (csize == 1) {
-                    const int n = rt * kTileN + tid;
-                    if (n < pr.N) store_out(pr, m, n, v, ctrl->a_scale[m]);
+                        for (int m = 0; m < 16; ++m) part[m] = __float2int_rn(__uint_as_float(v[m]) * 32768.f);
+                    }
                 } else {
-                    part[m * kTileN + tid] = v;
+#pragma unroll
+                    for (int m = 0; m < DPR; ++m) {
+                        part[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6);
+                        dacc[0][m] = dacc[1][m] = dacc[2][m] = dacc[3][m] = 0;
+                    }
                 }
+                segment_epilogue(P, c, it.pi, it.rt, ka, it.kt + 1, seg_first_i == 0, part, tid, alive);
+                ++seg_idx;
+                seg_first_i = i + 1;
+                ka = 0;
             }
+            it.next(P);
         }
-    }
-    __syncwarp();
-    if (csize > 1) {
-        cluster_sync();
-        if (warp < 4) {
-            const int rows_per = (kTileN + csize - 1) / csize;
-            const int row0 = rank * rows_per;
-            const int nrows = min(rows_per, kTileN - row0);
-            if (nrows > 0) {
-                for (int idx = tid; idx < M * nrows; idx += 128) {
-                    const int m = idx / nrows;
-                    const int rr = row0 + idx % nrows;
-                    const uint32_t a = smem_u32(&part[m * kTileN + rr]);
-                    int sum = 0;
-                    for (int q = 0; q < csize; ++q) sum += ld_cluster_s32(mapa(a, q));
-                    const int n = rt * kTileN + rr;
-                    if (n < pr.N) store_out(pr, m, n, sum, ctrl->a_scale[m]);
-                }
-            }
-        }
-        cluster_sync();  // peers may still read this CTA's partials until here
     }
 
     // ------------------------------------------------------- tear-down --
-    if (warp == 4 && lane == 0 && failed(ctrl)) {
-        // never leave a bulk copy in flight into shared memory we are releasing
-        for (int s = 0; s < nkt; ++s) (void)mbar_wait_bounded(smem_u32(&ctrl->full[s]), 0);
+    __syncthreads();
+    if (warp == 4 && lane == 0 && c->failed) {
+        // never release shared memory with a bulk copy still in flight
+        for (int s = 0; s < npre; ++s) (void)mbar_wait_bounded(smem_u32(&c->wfull[s]), 0, 100000000ull);
     }
-    __syncwarp();
-    if constexpr (PATH == kPathTC) {
+    if constexpr (kTC) {
         tc_fence_before();
         __syncthreads();
         if (warp == 0) {
@@ -449,32 +692,25 @@ w2a8_gemm_kernel(const __grid_constant__ GemmParams P) {
 }
 
 template <int PATH, int DPR>
-cudaError_t launch_one(const GemmParams& prm, int total_clusters, bool pdl, cudaStream_t stream) {
-    auto kern = &w2a8_gemm_kernel<PATH, DPR>;
+cudaError_t launch_one(const GemmParams& prm, bool pdl, cudaStream_t stream) {
+    auto kern = &w2a8_streamk_kernel<PATH, DPR>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !configured[dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(gemm_smem_bytes(PATH, kMaxKtPerCta)));
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                                 static_cast<int>(gemm_smem_bytes(PATH, DPR, kMaxStages)));
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(total_clusters * prm.csize), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(prm.nctas), 1, 1);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
-    cfg.dynamicSmemBytes = gemm_smem_bytes(PATH, prm.nkt_max);
+    cfg.dynamicSmemBytes = gemm_smem_bytes(PATH, DPR, prm.stages);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     int na = 0;
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = static_cast<unsigned>(prm.csize);
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
     if (pdl) {
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
@@ -487,18 +723,25 @@ cudaError_t launch_one(const GemmParams& prm, int total_clusters, bool pdl, cuda
 
 }  // namespace
 
-size_t gemm_smem_bytes(int path, int nkt_max) {
-    size_t b = static_cast<size_t>(kCtrlBytes) + static_cast<size_t>(nkt_max) * 2 * kTileBytes + kPartBytes;
-    if (path == kPathTC && b < static_cast<size_t>(kTcSmemFloor)) b = kTcSmemFloor;
-    return b;
+int gemm_stages(int path, int dp_rows) {
+    const int bt = path == kPathTC16 ? 4096 : path == kPathTC8 ? 2048 : dp_rows * 128;
+    int s = (kSmemTarget - kCtrlBytes - kScratchBytes) / (kTileBytes + bt);
+    if (s > kMaxStages) s = kMaxStages;
+    if (s < 2) s = 2;
+    return s;
 }
 
-cudaError_t launch_gemm(const GemmParams& prm, int path, int dp_rows, int total_clusters,
-                        bool pdl, cudaStream_t stream) {
-    if (path == kPathTC) return launch_one<kPathTC, 1>(prm, total_clusters, pdl, stream);
-    if (dp_rows <= 1) return launch_one<kPathDP, 1>(prm, total_clusters, pdl, stream);
-    if (dp_rows <= 2) return launch_one<kPathDP, 2>(prm, total_clusters, pdl, stream);
-    return launch_one<kPathDP, 4>(prm, total_clusters, pdl, stream);
+size_t gemm_smem_bytes(int path, int dp_rows, int stages) {
+    const int bt = path == kPathTC16 ? 4096 : path == kPathTC8 ? 2048 : dp_rows * 128;
+    return static_cast<size_t>(kCtrlBytes) + kScratchBytes + static_cast<size_t>(stages) * (kTileBytes + bt);
+}
+
+cudaError_t launch_gemm(const GemmParams& prm, int path, int dp_rows, bool pdl, cudaStream_t stream) {
+    if (path == kPathTC16) return launch_one<kPathTC16, 1>(prm, pdl, stream);
+    if (path == kPathTC8) return launch_one<kPathTC8, 1>(prm, pdl, stream);
+    if (dp_rows <= 1) return launch_one<kPathDP, 1>(prm, pdl, stream);
+    if (dp_rows <= 2) return launch_one<kPathDP, 2>(prm, pdl, stream);
+    return launch_one<kPathDP, 4>(prm, pdl, stream);
 }
 
 }  // namespace bitmtp

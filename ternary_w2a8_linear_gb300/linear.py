@@ -67,9 +67,13 @@ def load() -> ctypes.CDLL:
                                          c.c_size_t, c.c_void_p]),
         "bitmtp_linear_quant_act": (c.c_int, [c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_int64,
                                               c.c_void_p, c.c_int64, c.c_void_p, c.c_void_p, c.c_void_p]),
+        "bitmtp_linear_workspace_bytes": (c.c_size_t, [c.c_int64, c.c_int64, c.c_int64]),
+        "bitmtp_linear_workspace_bytes_grouped": (c.c_size_t, [c.POINTER(GemmDesc), c.c_int]),
         "bitmtp_linear_gemm": (c.c_int, [c.c_void_p, c.c_float, c.c_int64, c.c_int64, c.c_int64,
-                                         c.POINTER(Act), c.POINTER(Out), c.c_uint, c.c_void_p]),
-        "bitmtp_linear_gemm_grouped": (c.c_int, [c.POINTER(GemmDesc), c.c_int, c.c_uint, c.c_void_p]),
+                                         c.POINTER(Act), c.POINTER(Out), c.c_void_p, c.c_size_t,
+                                         c.c_uint, c.c_void_p]),
+        "bitmtp_linear_gemm_grouped": (c.c_int, [c.POINTER(GemmDesc), c.c_int, c.c_void_p, c.c_size_t,
+                                                 c.c_uint, c.c_void_p]),
         "bitmtp_linear_device_error": (c.c_int, [c.c_void_p]),
         "bitmtp_linear_status_string": (c.c_char_p, [c.c_int]),
         "bitmtp_linear_version": (c.c_int, []),
@@ -102,13 +106,23 @@ def bitmtp_linear_quant_act(x_ptr, x_kind, M, K, ldx, q_ptr, ldq, a_scale_ptr, r
     return load().bitmtp_linear_quant_act(x_ptr, x_kind, M, K, ldx, q_ptr, ldq, a_scale_ptr, rowsum_ptr, stream)
 
 
-def bitmtp_linear_gemm(pk_ptr, w_scale, N, K, M, act: Act, out: Out, flags, stream) -> int:
-    return load().bitmtp_linear_gemm(pk_ptr, w_scale, N, K, M, ctypes.byref(act), ctypes.byref(out), flags, stream)
+def bitmtp_linear_workspace_bytes(N: int, K: int, M: int) -> int:
+    return int(load().bitmtp_linear_workspace_bytes(N, K, M))
 
 
-def bitmtp_linear_gemm_grouped(descs, flags, stream) -> int:
+def bitmtp_linear_workspace_bytes_grouped(descs) -> int:
     arr = (GemmDesc * max(1, len(descs)))(*descs)
-    return load().bitmtp_linear_gemm_grouped(arr, len(descs), flags, stream)
+    return int(load().bitmtp_linear_workspace_bytes_grouped(arr, len(descs)))
+
+
+def bitmtp_linear_gemm(pk_ptr, w_scale, N, K, M, act: Act, out: Out, ws_ptr, ws_bytes, flags, stream) -> int:
+    return load().bitmtp_linear_gemm(pk_ptr, w_scale, N, K, M, ctypes.byref(act), ctypes.byref(out),
+                                     ws_ptr, ws_bytes, flags, stream)
+
+
+def bitmtp_linear_gemm_grouped(descs, ws_ptr, ws_bytes, flags, stream) -> int:
+    arr = (GemmDesc * max(1, len(descs)))(*descs)
+    return load().bitmtp_linear_gemm_grouped(arr, len(descs), ws_ptr, ws_bytes, flags, stream)
 
 
 def bitmtp_linear_device_error(stream=None) -> int:
@@ -164,6 +178,25 @@ def packed_bytes(N: int, K: int) -> int:
     return bitmtp_linear_packed_bytes(N, K)
 
 
+_ws_cache: dict = {}
+
+
+def workspace(nbytes: int, device=None, stream=None) -> torch.Tensor:
+    """A zero-filled workspace of at least ``nbytes`` for GEMM calls on
+    ``stream`` (cached per device and stream; calls on one stream are ordered,
+    so they may share it)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    sptr = _stream(stream).value or 0
+    key = (dev.index, sptr)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        size = max(nbytes, 2 * ws.numel() if ws is not None else 0, 1 << 20)
+        ws = torch.zeros(size, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize(dev)  # zero-fill complete before any stream uses it
+        _ws_cache[key] = ws
+    return ws
+
+
 def pack(T: torch.Tensor, stream=None) -> torch.Tensor:
     """Pack ternary int8 weights [N, K] (device) -> uint8 packed buffer."""
     if T.dtype != torch.int8 or not T.is_cuda:
@@ -211,7 +244,8 @@ def make_out(y: torch.Tensor, acc: torch.Tensor | None = None) -> Out:
 
 def gemm(pk: torch.Tensor, w_scale: float, N: int, K: int, x: torch.Tensor,
          a_scale: torch.Tensor | None = None, out_dtype=torch.float32, y: torch.Tensor | None = None,
-         acc: torch.Tensor | bool | None = None, flags: int = 0, stream=None):
+         acc: torch.Tensor | bool | None = None, flags: int = 0, stream=None,
+         workspace_tensor: torch.Tensor | None = None):
     """y = W2A8 linear of x ([M, K] fp32 / bf16 raw, or int8 codes with a_scale).
 
     Returns y, or (y, acc) when ``acc`` is True or a tensor."""
@@ -223,11 +257,14 @@ def gemm(pk: torch.Tensor, w_scale: float, N: int, K: int, x: torch.Tensor,
         acc = torch.empty((M, N), dtype=torch.int32, device=x.device)
     act = make_act(x, a_scale)
     out = make_out(y, acc if want_acc else None)
-    _check(bitmtp_linear_gemm(_ptr(pk), float(w_scale), N, K, M, act, out, flags, _stream(stream)), "gemm")
+    nb = bitmtp_linear_workspace_bytes(N, K, max(M, 1))
+    ws = workspace_tensor if workspace_tensor is not None else (workspace(nb, x.device, stream) if M else None)
+    _check(bitmtp_linear_gemm(_ptr(pk), float(w_scale), N, K, M, act, out, _ptr(ws),
+                              ws.numel() if ws is not None else 0, flags, _stream(stream)), "gemm")
     return (y, acc) if want_acc else y
 
 
-def gemm_grouped(problems, flags: int = 0, stream=None):
+def gemm_grouped(problems, flags: int = 0, stream=None, workspace_tensor: torch.Tensor | None = None):
     """One launch over several problems.  Each problem is a dict with keys
     pk, w_scale, N, K, x, (a_scale), y, (acc)."""
     descs = []
@@ -235,4 +272,9 @@ def gemm_grouped(problems, flags: int = 0, stream=None):
         x = p["x"]
         descs.append(GemmDesc(p["pk"].data_ptr(), float(p["w_scale"]), p["N"], p["K"], x.shape[0],
                               make_act(x, p.get("a_scale")), make_out(p["y"], p.get("acc"))))
-    _check(bitmtp_linear_gemm_grouped(descs, flags, _stream(stream)), "gemm_grouped")
+    if not descs:
+        return
+    nb = bitmtp_linear_workspace_bytes_grouped(descs)
+    dev = problems[0]["x"].device
+    ws = workspace_tensor if workspace_tensor is not None else workspace(nb, dev, stream)
+    _check(bitmtp_linear_gemm_grouped(descs, _ptr(ws), ws.numel(), flags, _stream(stream)), "gemm_grouped")

@@ -25,7 +25,8 @@ def test_exports_every_header_symbol(lib):
     assert set(syms) == {
         "bitmtp_linear_packed_bytes", "bitmtp_linear_pack", "bitmtp_linear_quant_act",
         "bitmtp_linear_gemm", "bitmtp_linear_gemm_grouped", "bitmtp_linear_device_error",
-        "bitmtp_linear_status_string", "bitmtp_linear_version",
+        "bitmtp_linear_status_string", "bitmtp_linear_version", "bitmtp_linear_workspace_bytes",
+        "bitmtp_linear_workspace_bytes_grouped",
     }
     for s in syms:
         assert hasattr(lib, s), s
@@ -60,10 +61,13 @@ def _out(dtype=L.F32, y=FAKE, ldy=64, acc=None, lda=0):
     return L.Out(dtype, y, ldy, acc, lda)
 
 
-def gemm(pk=FAKE, w=0.02, N=64, K=64, M=4, act=None, out=None, flags=0):
+WS = 1 << 24  # claimed workspace size for validation-only calls
+
+
+def gemm(pk=FAKE, w=0.02, N=64, K=64, M=4, act=None, out=None, flags=0, ws=FAKE, ws_bytes=WS):
     act = act or _act()
     out = out or _out()
-    return L.bitmtp_linear_gemm(pk, w, N, K, M, act, out, flags, None)
+    return L.bitmtp_linear_gemm(pk, w, N, K, M, act, out, ws, ws_bytes, flags, None)
 
 
 def test_gemm_validation(lib):
@@ -84,7 +88,11 @@ def test_gemm_validation(lib):
     assert gemm(out=_out(acc=FAKE, lda=3)) == L.ERR_INVALID
     assert gemm(w=float("nan")) == L.ERR_INVALID
     assert gemm(flags=L.FLAG_FORCE_TC | L.FLAG_FORCE_DP) == L.ERR_INVALID
-    assert L.load().bitmtp_linear_gemm(FAKE, 0.02, 64, 64, 4, None, ctypes.byref(_out()), 0, None) == L.ERR_INVALID
+    assert L.load().bitmtp_linear_gemm(FAKE, 0.02, 64, 64, 4, None, ctypes.byref(_out()), FAKE, WS, 0,
+                                       None) == L.ERR_INVALID
+    assert gemm(ws=None) == L.ERR_INVALID
+    assert gemm(ws=FAKE + 4) == L.ERR_ALIGN
+    assert gemm(ws_bytes=L.bitmtp_linear_workspace_bytes(64, 64, 4) - 1) == L.ERR_SHAPE
     # empty problems are valid no-ops and never touch the device
     assert gemm(M=0) == L.OK
     assert gemm(N=0) == L.OK
@@ -93,11 +101,28 @@ def test_gemm_validation(lib):
 def test_grouped_validation(lib):
     good = L.GemmDesc(FAKE, 0.02, 64, 64, 4, _act(), _out())
     bad = L.GemmDesc(FAKE, 0.02, 64, 64, 20, _act(), _out())
-    assert L.bitmtp_linear_gemm_grouped([good, bad], 0, None) == L.ERR_SHAPE
-    assert L.bitmtp_linear_gemm_grouped([good] * (L.MAX_GROUP + 1), 0, None) == L.ERR_SHAPE
-    assert L.bitmtp_linear_gemm_grouped([], 0, None) == L.OK
+    grp = L.bitmtp_linear_gemm_grouped
+    assert grp([good, bad], FAKE, WS, 0, None) == L.ERR_SHAPE
+    assert grp([good] * (L.MAX_GROUP + 1), FAKE, WS, 0, None) == L.ERR_SHAPE
+    assert grp([], FAKE, WS, 0, None) == L.OK
     empty = L.GemmDesc(FAKE, 0.02, 64, 64, 0, _act(), _out())
-    assert L.bitmtp_linear_gemm_grouped([empty], 0, None) == L.OK
+    assert grp([empty], None, 0, 0, None) == L.OK
+    assert grp([good], None, 0, 0, None) == L.ERR_INVALID
+    need = L.bitmtp_linear_workspace_bytes_grouped([good, good])
+    assert grp([good, good], FAKE, need - 16, 0, None) == L.ERR_SHAPE
+
+
+def test_workspace_bytes(lib):
+    wb = L.bitmtp_linear_workspace_bytes
+    assert wb(0, 64, 4) == 0 and wb(64, 0, 4) == 0 and wb(64, 64, 0) == 0 and wb(64, 64, 17) == 0
+    small, big = wb(128, 128, 1), wb(32000, 2560, 16)
+    assert 0 < small < big
+    assert big - small >= (20 - 1) * 4096             # activation tiles: one per k tile
+    assert wb(2560, 2560, 1) == wb(2560, 2560, 16) or wb(2560, 2560, 1) < wb(2560, 2560, 16)
+    d = [L.GemmDesc(FAKE, 0.02, 2560, 2560, 8, _act(ldx=2560), _out(ldy=2560)),
+         L.GemmDesc(FAKE, 0.02, 640, 2560, 8, _act(ldx=2560), _out(ldy=640))]
+    g = L.bitmtp_linear_workspace_bytes_grouped(d)
+    assert g >= wb(2560, 2560, 8) and g > wb(640, 2560, 8)
 
 
 def test_pack_and_quant_validation(lib):
