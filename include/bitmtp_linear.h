@@ -141,14 +141,14 @@ typedef struct bitmtp_out {
     int64_t lda;           /* >= N when acc != NULL                                  */
 } bitmtp_out;
 
-/* Workspace of a GEMM call: a device buffer the caller allocates once,
- * 16-byte aligned, zero-filled before its first use (e.g. cudaMemset); every
- * call leaves it ready for the next call.  It holds the quantised activation
- * tiles, the split-row-tile partial sums and self-resetting arrival counters.
- * Calls that may execute concurrently on the GPU need distinct workspaces.
- * If a call reports BITMTP_ERR_DEVICE the workspace must be zero-filled again.
- * These return the bytes needed (0 for out-of-range arguments); the size
- * depends on the shapes only, not on the device. */
+/* Workspace of a GEMM call: a device buffer the caller allocates once and
+ * reuses, 16-byte aligned, of at least the size these queries return.  It
+ * holds the quantised activation tiles, split-row-tile partial sums and
+ * arrival counters, all written by a call before that call reads them, so it
+ * needs no initialisation.  Calls that may execute concurrently on the GPU
+ * need distinct workspaces; calls ordered on one stream may share one.  The
+ * size depends on the shapes only, not on the device (0 for out-of-range
+ * arguments). */
 size_t bitmtp_linear_workspace_bytes(int64_t N, int64_t K, int64_t M);
 
 /* y = dequant(T * q): the W2A8 linear at block width M.

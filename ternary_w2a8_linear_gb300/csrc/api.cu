@@ -205,6 +205,9 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 // Sections of the caller's workspace.  The activation tiles are sized for the
 // widest tile (16 fp16 rows, 4096 B per k tile) whatever path runs, and the
 // split-tile slots for the largest grid, so the size depends on shapes only.
+// Every section is written by a launch before that launch reads it (the grid
+// barrier word works from any value), so the workspace needs no
+// initialisation and section offsets may differ from call to call.
 WorkspaceLayout layout_for(const GemmProblem* probs, int n) {
     size_t nt = 0, tasks = 0, pre = 0, kt = 0;
     for (int i = 0; i < n; ++i) {
@@ -267,6 +270,7 @@ int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes,
     prm.btile_bytes = path == kPathTC16 ? 4096 : path == kPathTC8 ? 2048 : dp_rows * 128;
     prm.stages = gemm_stages(path, dp_rows);
     prm.total_tasks = tasks;
+    prm.total_rowtiles = rt;
     prm.total_tiles = tiles;
     prm.nctas = static_cast<int>(std::min<long long>(cap, tiles));  // every CTA range is non-empty
     uint8_t* w = static_cast<uint8_t*>(workspace);

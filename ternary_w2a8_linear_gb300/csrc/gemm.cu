@@ -15,8 +15,9 @@
 //           equal contiguous ranges, one per CTA (stream-K), so every SM
 //           streams the same number of weight bytes whatever the mix of
 //           shapes.  A row tile whose k tiles span several CTAs is finished by
-//           the last of them to arrive, which sums the others' int32 partials
-//           from the workspace; the dequant epilogue is fused.
+//           the last of them to arrive (arrival counters are zeroed in phase 1
+//           of every launch), which sums the others' int32 partials from the
+//           workspace; the dequant epilogue is fused.
 //
 // Compute paths (the same 2-bit code words feed both):
 //   tensor (kPathTC16 / kPathTC8): each of 128 threads owns one output row
@@ -392,7 +393,6 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int pi, int rt, i
             for (int m = 0; m < 16; ++m)
                 if (m < M) store_out(pr, m, n, acc[m], asc[m]);
         }
-        if (tid == 0) atomicExch(P.counters + pr.rt_begin + rt, 0u);
     }
     named_bar_sync(1, 128);
 }
@@ -481,6 +481,8 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     // --------------------------------- phase 1: quantise activation rows --
     if (warp < 4) {
         pdl_wait();  // activations may be written by the previous kernel on the stream
+        // this launch's split-row-tile arrival counters start at zero
+        for (int r = b * 128 + tid; r < P.total_rowtiles; r += P.nctas * 128) P.counters[r] = 0u;
         for (int task = b; task < P.total_tasks; task += P.nctas)
             quant_row_task<PATH, DPR>(P, task, c, tsum, tid);
         fence_proxy_async_global();  // operand tiles are read back by bulk copies

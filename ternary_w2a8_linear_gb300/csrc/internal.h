@@ -46,7 +46,8 @@ struct GemmParams {
     int rows_b;               // activation rows held per B tile
     int btile_bytes;
     int stages;               // shared-memory ring depth (k tiles)
-    int total_tasks;          // n_problems * rows_b
+    int total_tasks;          // activation rows to quantise (sum of M)
+    int total_rowtiles;       // arrival counters used by this launch
     int nctas;
     long long total_tiles;
     // workspace sections
