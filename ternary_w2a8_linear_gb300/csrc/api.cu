@@ -205,9 +205,9 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 // Sections of the caller's workspace.  The activation tiles are sized for the
 // widest tile (16 fp16 rows, 4096 B per k tile) whatever path runs, and the
 // split-tile slots for the largest grid, so the size depends on shapes only.
-// Every section is written by a launch before that launch reads it (the grid
-// barrier word works from any value), so the workspace needs no
-// initialisation and section offsets may differ from call to call.
+// Every section but the grid-barrier word is written by a launch before that
+// launch reads it, so section offsets may differ from call to call; the
+// barrier word (first 256 bytes) must start at zero and is left at zero.
 WorkspaceLayout layout_for(const GemmProblem* probs, int n) {
     size_t nt = 0, tasks = 0, pre = 0, kt = 0;
     for (int i = 0; i < n; ++i) {

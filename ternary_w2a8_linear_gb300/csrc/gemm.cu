@@ -398,8 +398,9 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int pi, int rt, i
 }
 
 // Grid-wide barrier: each CTA adds 1 except CTA 0, which adds 2^31 - (n-1), so
-// the top bit of the counter flips exactly once per barrier and the low bits
-// come back to their value.  Called by one thread per CTA.
+// the counter crosses a multiple of 2^31 -- its top bit flips -- exactly when
+// the last CTA arrives, provided its low 31 bits start at zero; they come back
+// to zero after every barrier.  Called by one thread per CTA.
 __device__ bool grid_barrier(unsigned* bar, int nblocks) {
     __threadfence();
     const unsigned inc = (blockIdx.x == 0) ? (0x80000000u - static_cast<unsigned>(nblocks - 1)) : 1u;

@@ -184,14 +184,16 @@ _ws_cache: dict = {}
 def workspace(nbytes: int, device=None, stream=None) -> torch.Tensor:
     """A workspace of at least ``nbytes`` for GEMM calls on ``stream`` (cached
     per device and stream; calls on one stream are ordered, so they may share
-    it; it needs no initialisation)."""
+    it).  Zero-filled once on allocation, as the library requires of its first
+    256 bytes."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     sptr = _stream(stream).value or 0
     key = (dev.index, sptr)
     ws = _ws_cache.get(key)
     if ws is None or ws.numel() < nbytes:
         size = max(nbytes, 2 * ws.numel() if ws is not None else 0, 1 << 20)
-        ws = torch.empty(size, dtype=torch.uint8, device=dev)
+        ws = torch.zeros(size, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize(dev)  # zero-fill complete before any stream uses it
         _ws_cache[key] = ws
     return ws
 

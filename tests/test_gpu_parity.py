@@ -255,14 +255,16 @@ def test_grouped_launch_two_roles():
     assert_bf16_within_ulp(bf16_bits(ydd), yd_ref)
 
 
-def test_workspace_needs_no_initialisation():
-    """A workspace full of garbage bytes, shared by alternating shapes, gives
-    exact results: every section a launch reads is written by that launch."""
+def test_workspace_reuse_across_shapes():
+    """A workspace whose bytes beyond the zeroed barrier word are garbage,
+    shared by alternating shapes, gives exact results: every other section a
+    launch reads is written by that launch."""
     probs = [inputs.random_problem(71, 8, 2560, 6912), inputs.random_problem(72, 3, 11008, 4096),
              inputs.random_problem(73, 1, 640, 2560)]
     packed = [L.pack(dev_tensor(T)) for T, _, _ in probs]
     nb = max(L.bitmtp_linear_workspace_bytes(T.shape[0], T.shape[1], x.shape[0]) for T, _, x in probs)
     ws = torch.full((nb,), 0xA7, dtype=torch.uint8, device="cuda")
+    ws[:256] = 0
     for rep in range(2):
         for (T, w, x), pk in zip(probs, packed):
             N, K = T.shape
@@ -270,3 +272,4 @@ def test_workspace_needs_no_initialisation():
             y_ref, acc_ref, _, _ = reference(T, w, x, False)
             assert np.array_equal(acc.cpu().numpy(), acc_ref), (rep, N, K)
             assert_f32_close(y.cpu().numpy(), y_ref, acc_ref)
+    assert L.bitmtp_linear_device_error() == 0
