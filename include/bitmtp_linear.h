@@ -141,16 +141,16 @@ typedef struct bitmtp_out {
     int64_t lda;           /* >= N when acc != NULL                                  */
 } bitmtp_out;
 
-/* Workspace of a GEMM call: a device buffer the caller allocates once and
- * reuses, 16-byte aligned, of at least the size these queries return.  Its
- * first 256 bytes (the grid-barrier word) must be zero before the first call;
- * every call leaves them so.  The rest holds the quantised activation tiles,
- * split-row-tile partial sums and arrival counters, which each call writes
- * before it reads them, so one workspace may serve calls of any shapes.
- * Calls that may execute concurrently on the GPU need distinct workspaces;
- * calls ordered on one stream may share one.  After a call that ends in
- * BITMTP_ERR_DEVICE, zero the first 256 bytes again.  The size depends on the
- * shapes only, not on the device (0 for out-of-range arguments). */
+/* Workspace of a GEMM call: a device buffer the caller allocates once,
+ * 16-byte aligned, of at least the size these queries return, and
+ * zero-fills before its first use (e.g. cudaMemset).  Every call leaves it
+ * ready for the next one, so one workspace serves calls of any shapes.  It
+ * holds the grid-barrier word, split-row-tile accumulators and counters
+ * (left at zero by each call) and the quantised activation tiles (written
+ * before they are read).  Calls that may execute concurrently on the GPU need
+ * distinct workspaces; calls ordered on one stream may share one.  After a
+ * call that ends in BITMTP_ERR_DEVICE, zero-fill it again.  The size depends
+ * on the shapes only, not on the device (0 for out-of-range arguments). */
 size_t bitmtp_linear_workspace_bytes(int64_t N, int64_t K, int64_t M);
 
 /* y = dequant(T * q): the W2A8 linear at block width M.

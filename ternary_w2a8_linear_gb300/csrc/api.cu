@@ -197,22 +197,19 @@ int choose_path(int max_m, unsigned flags, int* dp_rows) {
     return max_m <= 8 ? kPathTC8 : kPathTC16;
 }
 
-constexpr int kMaxCtas = 320;  // persistent CTAs per launch (>= 2 per SM on GB300)
-constexpr size_t kSlotBytes = 2ull * 16 * kTileN * 4;
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-// Sections of the caller's workspace.  The activation tiles are sized for the
-// widest tile (16 fp16 rows, 4096 B per k tile) whatever path runs, and the
-// split-tile slots for the largest grid, so the size depends on shapes only.
-// Every section but the grid-barrier word is written by a launch before that
-// launch reads it, so section offsets may differ from call to call; the
-// barrier word (first 256 bytes) must start at zero and is left at zero.
+// Sections of the caller's workspace.  A fixed prefix holds the state that
+// every launch leaves at zero: the grid-barrier word, one arrival counter and
+// one 128 x 16 accumulator per possible CTA.  The sections after it are
+// written by a launch before that launch reads them, so their offsets may
+// vary with the shapes.  Activation tiles are sized for the widest tile (16
+// fp16 rows, 4096 B per k tile) whatever path runs.
 WorkspaceLayout layout_for(const GemmProblem* probs, int n) {
-    size_t nt = 0, tasks = 0, pre = 0, kt = 0;
+    size_t tasks = 0, pre = 0, kt = 0;
     for (int i = 0; i < n; ++i) {
         if (probs[i].M == 0 || probs[i].N == 0) continue;
-        nt += probs[i].nt;
         tasks += probs[i].M;
         pre += static_cast<size_t>(probs[i].kt + 1) * 16;
         kt += probs[i].kt;
@@ -220,10 +217,10 @@ WorkspaceLayout layout_for(const GemmProblem* probs, int n) {
     WorkspaceLayout L;
     L.gridbar = 0;
     L.counters = 256;
-    L.ascale = L.counters + align256(nt * 4);
+    L.accum = L.counters + align256(kMaxCtas * 4);
+    L.ascale = L.accum + static_cast<size_t>(kMaxCtas) * kTileN * 16 * 4;
     L.prefix = L.ascale + align256(tasks * 4);
-    L.slots = L.prefix + align256(pre * 4);
-    L.btiles = L.slots + kMaxCtas * kSlotBytes;
+    L.btiles = L.prefix + align256(pre * 4);
     L.total = L.btiles + align256(kt * 4096);
     return L;
 }
@@ -270,7 +267,6 @@ int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes,
     prm.btile_bytes = path == kPathTC16 ? 4096 : path == kPathTC8 ? 2048 : dp_rows * 128;
     prm.stages = gemm_stages(path, dp_rows);
     prm.total_tasks = tasks;
-    prm.total_rowtiles = rt;
     prm.total_tiles = tiles;
     prm.nctas = static_cast<int>(std::min<long long>(cap, tiles));  // every CTA range is non-empty
     uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -278,7 +274,7 @@ int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes,
     prm.counters = reinterpret_cast<unsigned*>(w + L.counters);
     prm.ascale = reinterpret_cast<float*>(w + L.ascale);
     prm.prefix = reinterpret_cast<int*>(w + L.prefix);
-    prm.slots = reinterpret_cast<int*>(w + L.slots);
+    prm.accum = reinterpret_cast<float*>(w + L.accum);
     prm.btiles = w + L.btiles;
     prm.err = dev->err;
     return cuda_status(launch_gemm(prm, path, dp_rows, (flags & BITMTP_FLAG_PDL) != 0, stream));

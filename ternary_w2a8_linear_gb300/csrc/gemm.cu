@@ -15,9 +15,8 @@
 //           equal contiguous ranges, one per CTA (stream-K), so every SM
 //           streams the same number of weight bytes whatever the mix of
 //           shapes.  A row tile whose k tiles span several CTAs is finished by
-//           the last of them to arrive (arrival counters are zeroed in phase 1
-//           of every launch), which sums the others' int32 partials from the
-//           workspace; the dequant epilogue is fused.
+//           the last of them to arrive, after each added its partial into an
+//           accumulator in the workspace; the dequant epilogue is fused.
 //
 // Compute paths (the same 2-bit code words feed both):
 //   tensor (kPathTC16 / kPathTC8): each of 128 threads owns one output row
@@ -59,7 +58,7 @@ constexpr uint32_t kAccCol = 0;      // D: 16 fp32 columns, one per activation r
 constexpr uint32_t kACol = 32;       // A: three buffers of 32 columns (64 k each)
 constexpr int kABufs = 3;
 constexpr uint32_t kIdesc = idesc_f16_f32(128, 16);
-constexpr int kSmemTarget = 56 * 1024;  // 2 CTAs of this kernel + 2 of the next fit on an SM
+constexpr int kSmemTarget = 100 * 1024;  // two CTAs per SM, deep weight ring
 
 enum : int {
     kErrWaitW = 0x101,
@@ -221,6 +220,9 @@ __device__ __forceinline__ void load8(const GemmProblem& pr, const char* row, bo
 }
 
 // ------------------------------------------------ phase 1: one activation row --
+// One CTA task = one activation row: absmax over K (all loads of a batch in
+// flight), then the codes written into the operand tiles, with per-k-tile row
+// sums and their prefix over k tiles.
 template <int PATH, int DPR>
 __device__ void quant_row_task(const GemmParams& P, int task, Ctrl* c, int* tsum, int tid) {
     const int pi = find_problem_by_task(P, task);
@@ -232,38 +234,62 @@ __device__ void quant_row_task(const GemmParams& P, int task, Ctrl* c, int* tsum
     const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
     const bool raw = pr.act_kind != BITMTP_Q8;
 
+    for (int t = tid; t < KT; t += 128) tsum[t] = 0;
     float s = 0.f;
     if (raw) {
+        const int ng = (pr.K + 7) >> 3;
         float a = 0.f;
-#pragma unroll 4
-        for (int g = tid; g * 8 < pr.K; g += 128) {
-            float v[8];
-            load8(pr, row, vec_ok, g * 8, v);
+        for (int g0 = tid; g0 < ng; g0 += 512) {
+            float v[4][8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+            for (int j = 0; j < 4; ++j) {
+                const int g = g0 + j * 128;
+                if (g < ng) {
+                    load8(pr, row, vec_ok, g * 8, v[j]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[j][i]));
         }
-        const float amax = block128_max(a, c, tid);
+        const float amax = block128_max(a, c, tid);  // also orders the tsum zeroing
         s = quant_scale(amax);
         if (tid == 0) P.ascale[pr.task_begin + m] = dequant_scale(amax);
-    } else if (tid == 0) {
-        P.ascale[pr.task_begin + m] = pr.a_scale_in[m];
+    } else {
+        if (tid == 0) P.ascale[pr.task_begin + m] = pr.a_scale_in[m];
+        named_bar_sync(1, 128);
     }
 
     uint8_t* bt = P.btiles + static_cast<size_t>(pr.bt_begin) * P.btile_bytes;
     if constexpr (PATH != kPathDP) {
-        // 8-k groups; 16 per k tile, one half-warp per tile per pass
+        // 8-k groups, 16 per k tile
         const int ngroups = KT * 16;
-        for (int base = (tid & ~31); base < ngroups; base += 128) {
-            const int g = base + (tid & 31);
-            int rs = 0;
-            if (g < ngroups) {
-                float v[8];
-                load8(pr, row, vec_ok, g * 8, v);
+        for (int g0 = tid; g0 < ngroups; g0 += 256) {
+            float v[2][8];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int g = g0 + j * 128;
+                if (g < ngroups) {
+                    load8(pr, row, vec_ok, g * 8, v[j]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int g = g0 + j * 128;
+                if (g >= ngroups) continue;
+                int rs = 0;
                 uint32_t packed[4];
 #pragma unroll
                 for (int i = 0; i < 8; i += 2) {
-                    const int q0 = raw ? quantize(v[i], s) : static_cast<int>(v[i]);
-                    const int q1 = raw ? quantize(v[i + 1], s) : static_cast<int>(v[i + 1]);
+                    const int q0 = raw ? quantize(v[j][i], s) : static_cast<int>(v[j][i]);
+                    const int q1 = raw ? quantize(v[j][i + 1], s) : static_cast<int>(v[j][i + 1]);
                     rs += q0 + q1;
                     const int sh = bscale_shift((g & 1) * 4 + (i >> 1));
                     const __half h0 = __int2half_rn(q0 * (1 << sh));
@@ -275,43 +301,35 @@ __device__ void quant_row_task(const GemmParams& P, int task, Ctrl* c, int* tsum
                 uint8_t* dst = bt + static_cast<size_t>(tile) * P.btile_bytes + kg * btile_lbo(PATH) +
                                (m >> 3) * btile_sbo(PATH) + (m & 7) * 16;
                 *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                if (rs != 0) atomicAdd(&tsum[tile], rs);
             }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
-            if ((tid & 15) == 0 && g < ngroups) tsum[g >> 4] = rs;
         }
     } else {
-        // 16-k chunks; 8 per k tile, eight threads per tile per pass
+        // 16-k chunks, 8 per k tile
         const int nchunks = KT * 8;
-        for (int base = (tid & ~31); base < nchunks; base += 128) {
-            const int g = base + (tid & 31);
+        for (int g = tid; g < nchunks; g += 128) {
+            float v[16];
+            load8(pr, row, vec_ok, g * 16, *reinterpret_cast<float(*)[8]>(v));
+            load8(pr, row, vec_ok, g * 16 + 8, *reinterpret_cast<float(*)[8]>(v + 8));
+            int q[16];
             int rs = 0;
-            if (g < nchunks) {
-                float v[16];
-                float* v0 = v;
-                load8(pr, row, vec_ok, g * 16, *reinterpret_cast<float(*)[8]>(v0));
-                load8(pr, row, vec_ok, g * 16 + 8, *reinterpret_cast<float(*)[8]>(v0 + 8));
-                int q[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    q[i] = raw ? quantize(v[i], s) : static_cast<int>(v[i]);
-                    rs += q[i];
-                }
-                uint32_t reg[4];
-#pragma unroll
-                for (int sidx = 0; sidx < 4; ++sidx) {
-                    reg[sidx] = (static_cast<uint32_t>(q[2 * sidx]) & 0xFFu) |
-                                ((static_cast<uint32_t>(q[8 + 2 * sidx]) & 0xFFu) << 8) |
-                                ((static_cast<uint32_t>(q[2 * sidx + 1]) & 0xFFu) << 16) |
-                                ((static_cast<uint32_t>(q[9 + 2 * sidx]) & 0xFFu) << 24);
-                }
-                const int tile = g >> 3, ch = g & 7;
-                uint8_t* dst = bt + static_cast<size_t>(tile) * P.btile_bytes + ch * (DPR * 16) + m * 16;
-                *reinterpret_cast<uint4*>(dst) = make_uint4(reg[0], reg[1], reg[2], reg[3]);
+            for (int i = 0; i < 16; ++i) {
+                q[i] = raw ? quantize(v[i], s) : static_cast<int>(v[i]);
+                rs += q[i];
             }
+            uint32_t reg[4];
 #pragma unroll
-            for (int o = 4; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
-            if ((tid & 7) == 0 && g < nchunks) tsum[g >> 3] = rs;
+            for (int sidx = 0; sidx < 4; ++sidx) {
+                reg[sidx] = (static_cast<uint32_t>(q[2 * sidx]) & 0xFFu) |
+                            ((static_cast<uint32_t>(q[8 + 2 * sidx]) & 0xFFu) << 8) |
+                            ((static_cast<uint32_t>(q[2 * sidx + 1]) & 0xFFu) << 16) |
+                            ((static_cast<uint32_t>(q[9 + 2 * sidx]) & 0xFFu) << 24);
+            }
+            const int tile = g >> 3, ch = g & 7;
+            uint8_t* dst = bt + static_cast<size_t>(tile) * P.btile_bytes + ch * (DPR * 16) + m * 16;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(reg[0], reg[1], reg[2], reg[3]);
+            if (rs != 0) atomicAdd(&tsum[tile], rs);
         }
     }
     named_bar_sync(1, 128);
@@ -361,38 +379,51 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int pi, int rt, i
         }
         return;
     }
-    // split row tile: publish the partial, the last contributor finishes it
-    const int b = blockIdx.x;
-    int* my = P.slots + (static_cast<size_t>(b) * 2 + (first_segment ? 0 : 1)) * 16 * kTileN;
-#pragma unroll
-    for (int m = 0; m < 16; ++m)
-        if (alive && m < M) my[m * kTileN + tid] = acc[m];
-    __threadfence();
-    named_bar_sync(1, 128);
+    // Split row tile: every contributor adds its partial into the row tile's
+    // accumulator (fp32 vector atomics; all values are integers below 2^24, so
+    // every sum is exact in any order); the last to arrive reads the total,
+    // writes the output and leaves accumulator and counter at zero.  A split
+    // row tile is identified by the CTA holding its last k tile: a CTA is the
+    // last contributor of at most one split row tile.
     const long long T = P.total_tiles;
     const long long t_first = pr.tile_begin + static_cast<long long>(rt) * pr.kt;
     const int b_first = range_owner(t_first, T, P.nctas);
     const int b_last = range_owner(t_first + pr.kt - 1, T, P.nctas);
+    float4* accum = reinterpret_cast<float4*>(P.accum) + (static_cast<size_t>(b_last) * kTileN + tid) * 4;
+    if (alive) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            if (4 * g < M)
+                atomicAdd(accum + g, make_float4(static_cast<float>(acc[4 * g]), static_cast<float>(acc[4 * g + 1]),
+                                                 static_cast<float>(acc[4 * g + 2]),
+                                                 static_cast<float>(acc[4 * g + 3])));
+    }
+    __threadfence();
+    named_bar_sync(1, 128);
     if (tid == 0) {
-        const unsigned old = atomicAdd(P.counters + pr.rt_begin + rt, 1u);
+        const unsigned old = atomicAdd(P.counters + b_last, 1u);
         c->last = (old == static_cast<unsigned>(b_last - b_first)) ? 1 : 0;
     }
     named_bar_sync(1, 128);
     if (c->last) {
         __threadfence();
-        for (int ob = b_first; ob <= b_last; ++ob) {
-            if (ob == b) continue;
-            const int slot = (range_start(ob, T, P.nctas) >= t_first) ? 0 : 1;
-            const int* os = P.slots + (static_cast<size_t>(ob) * 2 + slot) * 16 * kTileN;
+        float tot[16];
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-                if (m < M) acc[m] += __ldcg(os + m * kTileN + tid);
+        for (int g = 0; g < 4; ++g) {
+            if (4 * g < M) {
+                const float4 v = __ldcg(accum + g);
+                tot[4 * g] = v.x; tot[4 * g + 1] = v.y; tot[4 * g + 2] = v.z; tot[4 * g + 3] = v.w;
+                __stcg(accum + g, make_float4(0.f, 0.f, 0.f, 0.f));
+            } else {
+                tot[4 * g] = tot[4 * g + 1] = tot[4 * g + 2] = tot[4 * g + 3] = 0.f;
+            }
         }
         if (alive && n < pr.N) {
 #pragma unroll
             for (int m = 0; m < 16; ++m)
-                if (m < M) store_out(pr, m, n, acc[m], asc[m]);
+                if (m < M) store_out(pr, m, n, static_cast<int>(tot[m]), asc[m]);
         }
+        if (tid == 0) P.counters[b_last] = 0u;
     }
     named_bar_sync(1, 128);
 }
@@ -482,9 +513,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     // --------------------------------- phase 1: quantise activation rows --
     if (warp < 4) {
         pdl_wait();  // activations may be written by the previous kernel on the stream
-        // this launch's split-row-tile arrival counters start at zero
-        for (int r = b * 128 + tid; r < P.total_rowtiles; r += P.nctas * 128) P.counters[r] = 0u;
-        for (int task = b; task < P.total_tasks; task += P.nctas)
+            for (int task = b; task < P.total_tasks; task += P.nctas)
             quant_row_task<PATH, DPR>(P, task, c, tsum, tid);
         fence_proxy_async_global();  // operand tiles are read back by bulk copies
         __threadfence();

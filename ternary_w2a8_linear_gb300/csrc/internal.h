@@ -47,7 +47,6 @@ struct GemmParams {
     int btile_bytes;
     int stages;               // shared-memory ring depth (k tiles)
     int total_tasks;          // activation rows to quantise (sum of M)
-    int total_rowtiles;       // arrival counters used by this launch
     int nctas;
     long long total_tiles;
     // workspace sections
@@ -55,15 +54,16 @@ struct GemmParams {
     unsigned* counters;
     float* ascale;            // [total_tasks]
     int* prefix;              // row-sum prefixes
-    int* slots;               // [nctas][2][16][128] split-row-tile partials
+    float* accum;             // [kMaxCtas][128][16] split-row-tile accumulators
     uint8_t* btiles;          // activation operand tiles
     int* err;                 // device error word
 };
 
 // Workspace layout for a launch (sizes in bytes, sections 256-byte aligned).
 struct WorkspaceLayout {
-    size_t gridbar, counters, ascale, prefix, slots, btiles, total;
+    size_t gridbar, counters, accum, ascale, prefix, btiles, total;
 };
+constexpr int kMaxCtas = 320;  // persistent CTAs per launch (>= 2 per SM on GB300)
 
 size_t gemm_smem_bytes(int path, int dp_rows, int stages);
 int gemm_stages(int path, int dp_rows);

@@ -184,8 +184,7 @@ _ws_cache: dict = {}
 def workspace(nbytes: int, device=None, stream=None) -> torch.Tensor:
     """A workspace of at least ``nbytes`` for GEMM calls on ``stream`` (cached
     per device and stream; calls on one stream are ordered, so they may share
-    it).  Zero-filled once on allocation, as the library requires of its first
-    256 bytes."""
+    it).  Zero-filled once on allocation, as the library requires."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     sptr = _stream(stream).value or 0
     key = (dev.index, sptr)
