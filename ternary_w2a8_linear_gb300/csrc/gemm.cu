@@ -3,9 +3,11 @@
 // One launch computes one or several independent linears ("problems") with
 // the same compute path:
 //
-//  phase 0  every CTA starts streaming its first packed-weight tiles (4 KiB
-//           bulk copies, TMA engine) into a shared-memory ring; weights do
-//           not depend on the previous kernel on the stream;
+//  phase 0  every CTA starts streaming its first packed-weight tiles into a
+//           shared-memory ring with bulk copies (TMA engine) of up to four
+//           contiguous 4 KiB tiles each -- the engine's cost is per copy, so
+//           16 KiB copies stream at HBM speed where 4 KiB ones do not;
+//           weights do not depend on the previous kernel on the stream;
 //  phase 1  activation rows are quantised (per-row absmax, fp32 round half to
 //           even, the same code as the standalone quantiser) one row per CTA
 //           task, written straight into the activation operand tiles the
@@ -50,7 +52,9 @@
 namespace bitmtp {
 namespace {
 
-constexpr int kMaxStages = 24;
+constexpr int kMaxStages = 24;   // tile slots in the shared-memory ring
+constexpr int kChunk = 4;        // tile slots per bulk-copy chunk (16 KiB of weights)
+constexpr int kMaxChunks = kMaxStages / kChunk;
 constexpr int kCtrlBytes = 1024;
 constexpr int kScratchBytes = 2048;
 constexpr uint32_t kTmemCols = 128;
@@ -71,9 +75,9 @@ enum : int {
 };
 
 struct Ctrl {
-    uint64_t wfull[kMaxStages];
-    uint64_t bfull[kMaxStages];
-    uint64_t empty[kMaxStages];
+    uint64_t wfull[kMaxChunks];
+    uint64_t bfull[kMaxChunks];
+    uint64_t empty[kMaxChunks];
     uint64_t a_full[kABufs];
     uint64_t a_empty[kABufs];
     uint64_t dfull;
@@ -152,6 +156,40 @@ struct TileIter {
         }
     }
 };
+
+// Bulk-copy the weight tiles (or the activation tiles) of tiles
+// [first, first + count) of this CTA's range into consecutive ring slots,
+// merging runs that are contiguous in global memory (weights: within one
+// problem; activation tiles: within one row tile) into single copies; all
+// copies complete on `bar`, which expects their total bytes.
+template <bool kW>
+__device__ void issue_chunk(const GemmParams& P, long long first, int count, uint8_t* dst, int slot_bytes,
+                            uint32_t bar, uint64_t pol) {
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(count * slot_bytes));
+    TileIter it;
+    it.init(P, first);
+    const uint8_t* run_src = nullptr;
+    int run_len = 0;
+    uint8_t* run_dst = dst;
+    int prev_pi = -1, prev_rt = -1;
+    for (int k = 0; k < count; ++k) {
+        const GemmProblem& pr = P.p[it.pi];
+        const uint8_t* src = kW ? pr.pk + (static_cast<size_t>(it.rt) * pr.kt + it.kt) * kTileBytes
+                                : P.btiles + (static_cast<size_t>(pr.bt_begin) + it.kt) * slot_bytes;
+        const bool contiguous = run_len > 0 && it.pi == prev_pi && (kW || it.rt == prev_rt);
+        if (!contiguous) {
+            if (run_len > 0) bulk_g2s(smem_u32(run_dst), run_src, run_len * slot_bytes, bar, pol);
+            run_dst = dst + k * slot_bytes;
+            run_src = src;
+            run_len = 0;
+        }
+        ++run_len;
+        prev_pi = it.pi;
+        prev_rt = it.rt;
+        it.next(P);
+    }
+    if (run_len > 0) bulk_g2s(smem_u32(run_dst), run_src, run_len * slot_bytes, bar, pol);
+}
 
 // Block-wide (128 threads, named barrier 1) max of non-negative floats.
 __device__ __forceinline__ float block128_max(float v, Ctrl* c, int tid) {
@@ -467,10 +505,10 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 
     // ------------------------------------------------------------ set-up --
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&c->wfull[s]), 1);
-            mbar_init(smem_u32(&c->bfull[s]), 1);
-            mbar_init(smem_u32(&c->empty[s]), kTC ? 1 : 4);
+        for (int q = 0; q < S / kChunk; ++q) {
+            mbar_init(smem_u32(&c->wfull[q]), 1);
+            mbar_init(smem_u32(&c->bfull[q]), 1);
+            mbar_init(smem_u32(&c->empty[q]), kTC ? 1 : 4);
         }
         for (int a = 0; a < kABufs; ++a) {
             mbar_init(smem_u32(&c->a_full[a]), 4);
@@ -492,19 +530,16 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     const uint32_t tmem = kTC ? c->tmem_base : 0u;
 
     // ------------------------------- phase 0: start the weight stream --
-    const int npre = nloc < S ? nloc : S;
+    const int R = S / kChunk;                         // chunks in the ring
+    const int nchunks = (nloc + kChunk - 1) / kChunk;
+    const int npre = nchunks < R ? nchunks : R;
     uint64_t pol = 0;
     if (warp == 4 && lane == 0) {
         pol = policy_evict_first();
-        TileIter it;
-        it.init(P, t_begin);
-        for (int i = 0; i < npre; ++i) {
-            const GemmProblem& pr = P.p[it.pi];
-            const uint32_t bar = smem_u32(&c->wfull[i]);
-            mbar_arrive_expect_tx(bar, kTileBytes);
-            bulk_g2s(smem_u32(Wr + static_cast<size_t>(i) * kTileBytes),
-                     pr.pk + (static_cast<size_t>(it.rt) * pr.kt + it.kt) * kTileBytes, kTileBytes, bar, pol);
-            it.next(P);
+        for (int j = 0; j < npre; ++j) {
+            const int cnt = min(kChunk, nloc - j * kChunk);
+            issue_chunk<true>(P, t_begin + j * kChunk, cnt, Wr + static_cast<size_t>(j) * kChunk * kTileBytes,
+                              kTileBytes, smem_u32(&c->wfull[j]), pol);
         }
     }
     __syncwarp();
@@ -528,27 +563,20 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     if (warp == 4) {
         if (lane == 0 && nloc > 0) {
             fence_proxy_async_global();
-            TileIter it;
-            it.init(P, t_begin);
-            for (int i = 0; i < nloc; ++i) {
-                const GemmProblem& pr = P.p[it.pi];
-                const int s = i % S;
-                if (i >= S) {
-                    if (!mbar_wait_bounded(smem_u32(&c->empty[s]), ((i / S) - 1) & 1)) {
+            for (int j = 0; j < nchunks; ++j) {
+                const int q = j % R;
+                const int cnt = min(kChunk, nloc - j * kChunk);
+                const long long first = t_begin + static_cast<long long>(j) * kChunk;
+                if (j >= R) {
+                    if (!mbar_wait_bounded(smem_u32(&c->empty[q]), ((j / R) - 1) & 1)) {
                         fail(c, P.err, kErrWaitEmpty);
                         break;
                     }
-                    const uint32_t wb = smem_u32(&c->wfull[s]);
-                    mbar_arrive_expect_tx(wb, kTileBytes);
-                    bulk_g2s(smem_u32(Wr + static_cast<size_t>(s) * kTileBytes),
-                             pr.pk + (static_cast<size_t>(it.rt) * pr.kt + it.kt) * kTileBytes, kTileBytes,
-                             wb, pol);
+                    issue_chunk<true>(P, first, cnt, Wr + static_cast<size_t>(q) * kChunk * kTileBytes, kTileBytes,
+                                      smem_u32(&c->wfull[q]), pol);
                 }
-                const uint32_t bb = smem_u32(&c->bfull[s]);
-                mbar_arrive_expect_tx(bb, BT);
-                bulk_g2s(smem_u32(Br + static_cast<size_t>(s) * BT),
-                         P.btiles + (static_cast<size_t>(pr.bt_begin) + it.kt) * BT, BT, bb, pol);
-                it.next(P);
+                issue_chunk<false>(P, first, cnt, Br + static_cast<size_t>(q) * kChunk * BT, BT,
+                                   smem_u32(&c->bfull[q]), pol);
             }
         }
         __syncwarp();
@@ -562,8 +590,9 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 bool ok = true;
                 for (int i = 0; i < nloc && ok; ++i) {
                     const int s = i % S;
+                    const int q = (i / kChunk) % R;
                     const bool seg_last = (i == nloc - 1) || (it.kt == P.p[it.pi].kt - 1);
-                    if (!mbar_wait_bounded(smem_u32(&c->bfull[s]), (i / S) & 1)) {
+                    if ((i % kChunk) == 0 && !mbar_wait_bounded(smem_u32(&c->bfull[q]), ((i / kChunk) / R) & 1)) {
                         fail(c, P.err, kErrWaitB);
                         break;
                     }
@@ -587,7 +616,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         mma_commit(smem_u32(&c->a_empty[a]));
                     }
                     if (!ok) break;
-                    mma_commit(smem_u32(&c->empty[s]));
+                    if ((i % kChunk) == kChunk - 1 || i == nloc - 1) mma_commit(smem_u32(&c->empty[q]));
                     if (seg_last) mma_commit(smem_u32(&c->dfull));
                     seg_first = seg_last;
                     it.next(P);
@@ -614,9 +643,12 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         bool alive = true;
         for (int i = 0; i < nloc; ++i) {
             const int s = i % S;
+            const int q = (i / kChunk) % R;
+            const bool chunk_first = (i % kChunk) == 0;
+            const bool chunk_last = (i % kChunk) == kChunk - 1 || i == nloc - 1;
             const bool seg_last = (i == nloc - 1) || (it.kt == P.p[it.pi].kt - 1);
-            if (alive) {
-                alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[s]), (i / S) & 1));
+            if (alive && chunk_first) {
+                alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[q]), ((i / kChunk) / R) & 1));
                 if (!alive && lane == 0) fail(c, P.err, kErrWaitW);
             }
             const uint8_t* wst = Wr + static_cast<size_t>(s) * kTileBytes;
@@ -646,8 +678,9 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                     }
                 }
             } else {
-                if (alive) {
-                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[s]), (i / S) & 1));
+                if (alive && chunk_first) {
+                    alive = __all_sync(0xffffffffu,
+                                       mbar_wait_bounded(smem_u32(&c->bfull[q]), ((i / kChunk) / R) & 1));
                     if (!alive && lane == 0) fail(c, P.err, kErrWaitB);
                 }
                 if (alive) {
@@ -673,7 +706,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         }
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&c->empty[s]));
+                    if (lane == 0 && chunk_last) mbar_arrive(smem_u32(&c->empty[q]));
                 }
             }
             if (seg_last) {
@@ -711,7 +744,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     __syncthreads();
     if (warp == 4 && lane == 0 && c->failed) {
         // never release shared memory with a bulk copy still in flight
-        for (int s = 0; s < npre; ++s) (void)mbar_wait_bounded(smem_u32(&c->wfull[s]), 0, 100000000ull);
+        for (int q = 0; q < npre; ++q) (void)mbar_wait_bounded(smem_u32(&c->wfull[q]), 0, 100000000ull);
     }
     if constexpr (kTC) {
         tc_fence_before();
@@ -759,7 +792,8 @@ int gemm_stages(int path, int dp_rows) {
     const int bt = path == kPathTC16 ? 4096 : path == kPathTC8 ? 2048 : dp_rows * 128;
     int s = (kSmemTarget - kCtrlBytes - kScratchBytes) / (kTileBytes + bt);
     if (s > kMaxStages) s = kMaxStages;
-    if (s < 2) s = 2;
+    s -= s % kChunk;
+    if (s < 2 * kChunk) s = 2 * kChunk;
     return s;
 }
 
