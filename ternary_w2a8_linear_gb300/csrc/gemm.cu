@@ -395,14 +395,24 @@ __device__ __forceinline__ void store_out(const GemmProblem& pr, int m, int n, i
     if (pr.acc) pr.acc[static_cast<long long>(m) * pr.lda + n] = acc;
 }
 
+// A split row tile this CTA contributed to, finished after the main loop.
+struct Pending {
+    int pi, rt, b_first, b_last;
+};
+
 // Finish one segment (k tiles [ka, kb) of row tile rt of problem pi) held by
-// this CTA.  part[m] = sum_k u*q for the thread's row over the segment.
-__device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int pi, int rt, int ka, int kb,
-                                 bool first_segment, const int (&part)[16], int tid, bool alive) {
+// this CTA.  part[m] = sum_k u*q for the thread's row over the segment.  A
+// whole row tile is written out at once.  For a split row tile the partial is
+// added into the row tile's accumulator in the workspace (fp32 vector
+// atomics; every value is an integer below 2^24, so every sum is exact in any
+// order) without waiting, and the tile is recorded in `pend` to be finished
+// after the main loop.  A split row tile is identified by the CTA holding its
+// last k tile: a CTA is the last contributor of at most one split row tile.
+__device__ void segment_epilogue(const GemmParams& P, int pi, int rt, int ka, int kb, const int (&part)[16],
+                                 int tid, bool alive, Pending* pend, int& npend) {
     const GemmProblem& pr = P.p[pi];
     const int M = pr.M;
     const int* pre = P.prefix + pr.pre_begin;
-    const float* asc = P.ascale + pr.task_begin;
     const int n = rt * kTileN + tid;
     int acc[16];
 #pragma unroll
@@ -411,21 +421,15 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int pi, int rt, i
 
     if (ka == 0 && kb == pr.kt) {
         if (alive && n < pr.N) {
+            const float* asc = P.ascale + pr.task_begin;
 #pragma unroll
             for (int m = 0; m < 16; ++m)
                 if (m < M) store_out(pr, m, n, acc[m], asc[m]);
         }
         return;
     }
-    // Split row tile: every contributor adds its partial into the row tile's
-    // accumulator (fp32 vector atomics; all values are integers below 2^24, so
-    // every sum is exact in any order); the last to arrive reads the total,
-    // writes the output and leaves accumulator and counter at zero.  A split
-    // row tile is identified by the CTA holding its last k tile: a CTA is the
-    // last contributor of at most one split row tile.
     const long long T = P.total_tiles;
     const long long t_first = pr.tile_begin + static_cast<long long>(rt) * pr.kt;
-    const int b_first = range_owner(t_first, T, P.nctas);
     const int b_last = range_owner(t_first + pr.kt - 1, T, P.nctas);
     float4* accum = reinterpret_cast<float4*>(P.accum) + (static_cast<size_t>(b_last) * kTileN + tid) * 4;
     if (alive) {
@@ -436,15 +440,36 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int pi, int rt, i
                                                  static_cast<float>(acc[4 * g + 2]),
                                                  static_cast<float>(acc[4 * g + 3])));
     }
+    pend[npend].pi = pi;
+    pend[npend].rt = rt;
+    pend[npend].b_first = range_owner(t_first, T, P.nctas);
+    pend[npend].b_last = b_last;
+    ++npend;
+}
+
+// After the main loop: publish this CTA's contributions to its split row
+// tiles (one fence, one counter increment each); the last contributor of a
+// tile reads the total, writes the output and leaves accumulator and counter
+// at zero.  Warps 0-3 only (named barrier 1).
+__device__ void finish_pending(const GemmParams& P, Ctrl* c, const Pending* pend, int npend, int tid, bool alive) {
+    if (npend == 0) return;  // uniform across the four warps
     __threadfence();
     named_bar_sync(1, 128);
     if (tid == 0) {
-        const unsigned old = atomicAdd(P.counters + b_last, 1u);
-        c->last = (old == static_cast<unsigned>(b_last - b_first)) ? 1 : 0;
+        for (int k = 0; k < npend; ++k) {
+            const unsigned old = atomicAdd(P.counters + pend[k].b_last, 1u);
+            c->red_i[k] = (old == static_cast<unsigned>(pend[k].b_last - pend[k].b_first)) ? 1 : 0;
+        }
     }
     named_bar_sync(1, 128);
-    if (c->last) {
-        __threadfence();
+    const int last0 = c->red_i[0], last1 = npend > 1 ? c->red_i[1] : 0;
+    if (last0 | last1) __threadfence();
+    for (int k = 0; k < npend; ++k) {
+        if (!(k == 0 ? last0 : last1)) continue;
+        const GemmProblem& pr = P.p[pend[k].pi];
+        const int M = pr.M;
+        const int n = pend[k].rt * kTileN + tid;
+        float4* accum = reinterpret_cast<float4*>(P.accum) + (static_cast<size_t>(pend[k].b_last) * kTileN + tid) * 4;
         float tot[16];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -457,11 +482,12 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int pi, int rt, i
             }
         }
         if (alive && n < pr.N) {
+            const float* asc = P.ascale + pr.task_begin;
 #pragma unroll
             for (int m = 0; m < 16; ++m)
                 if (m < M) store_out(pr, m, n, static_cast<int>(tot[m]), asc[m]);
         }
-        if (tid == 0) P.counters[b_last] = 0u;
+        if (tid == 0) P.counters[pend[k].b_last] = 0u;
     }
     named_bar_sync(1, 128);
 }
@@ -633,7 +659,9 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         int part[16];
 #pragma unroll
         for (int m = 0; m < 16; ++m) part[m] = 0;
-        int ka = it.kt, seg_idx = 0, seg_first_i = 0;
+        int ka = it.kt, seg_idx = 0;
+        Pending pend[2];
+        int npend = 0;
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         int dacc[4][DPR];
 #pragma unroll
@@ -731,13 +759,13 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         dacc[0][m] = dacc[1][m] = dacc[2][m] = dacc[3][m] = 0;
                     }
                 }
-                segment_epilogue(P, c, it.pi, it.rt, ka, it.kt + 1, seg_first_i == 0, part, tid, alive);
+                segment_epilogue(P, it.pi, it.rt, ka, it.kt + 1, part, tid, alive, pend, npend);
                 ++seg_idx;
-                seg_first_i = i + 1;
                 ka = 0;
             }
             it.next(P);
         }
+        finish_pending(P, c, pend, npend, tid, alive);
     }
 
     // ------------------------------------------------------- tear-down --
