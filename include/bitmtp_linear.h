@@ -143,14 +143,13 @@ typedef struct bitmtp_out {
 
 /* Workspace of a GEMM call: a device buffer the caller allocates once,
  * 16-byte aligned, of at least the size these queries return, and
- * zero-fills before its first use (e.g. cudaMemset).  Every call leaves it
- * ready for the next one, so one workspace serves calls of any shapes.  It
- * holds the grid-barrier word, split-row-tile accumulators and counters
- * (left at zero by each call) and the quantised activation tiles (written
- * before they are read).  Calls that may execute concurrently on the GPU need
- * distinct workspaces; calls ordered on one stream may share one.  After a
- * call that ends in BITMTP_ERR_DEVICE, zero-fill it again.  The size depends
- * on the shapes only, not on the device (0 for out-of-range arguments). */
+ * zero-fills before its first use (e.g. cudaMemset).  It holds split-row-tile
+ * partial sums and arrival counters; every call leaves the counters at zero,
+ * so one workspace serves calls of any shapes.  Calls that may execute
+ * concurrently on the GPU need distinct workspaces; calls ordered on one
+ * stream may share one.  After a call that ends in BITMTP_ERR_DEVICE,
+ * zero-fill it again.  The size is the same for every valid shape (0 for
+ * out-of-range arguments). */
 size_t bitmtp_linear_workspace_bytes(int64_t N, int64_t K, int64_t M);
 
 /* y = dequant(T * q): the W2A8 linear at block width M.

@@ -198,42 +198,15 @@ int choose_path(int max_m, unsigned flags, int* dp_rows) {
 }
 
 
-size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
-
-// Sections of the caller's workspace.  A fixed prefix holds the state that
-// every launch leaves at zero: the grid-barrier word, one arrival counter and
-// one 128 x 16 accumulator per possible CTA.  The sections after it are
-// written by a launch before that launch reads them, so their offsets may
-// vary with the shapes.  Activation tiles are sized for the widest tile (16
-// fp16 rows, 4096 B per k tile) whatever path runs.
-WorkspaceLayout layout_for(const GemmProblem* probs, int n) {
-    size_t tasks = 0, pre = 0, kt = 0;
-    for (int i = 0; i < n; ++i) {
-        if (probs[i].M == 0 || probs[i].N == 0) continue;
-        tasks += probs[i].M;
-        pre += static_cast<size_t>(probs[i].kt + 1) * 16;
-        kt += probs[i].kt;
-    }
-    WorkspaceLayout L;
-    L.gridbar = 0;
-    L.counters = 256;
-    L.accum = L.counters + align256(kMaxCtas * 4);
-    L.ascale = L.accum + static_cast<size_t>(kMaxCtas) * kTileN * 16 * 4;
-    L.prefix = L.ascale + align256(tasks * 4);
-    L.btiles = L.prefix + align256(pre * 4);
-    L.total = L.btiles + align256(kt * 4096);
-    return L;
-}
 
 int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes, unsigned flags,
               cudaStream_t stream) {
     bool any = false;
     for (int i = 0; i < n; ++i) any = any || (probs[i].M > 0 && probs[i].N > 0);
     if (!any) return BITMTP_OK;  // empty problems never touch the device
-    const WorkspaceLayout L = layout_for(probs, n);
     if (!workspace) return BITMTP_ERR_INVALID;
     if (!aligned16(workspace)) return BITMTP_ERR_ALIGN;
-    if (ws_bytes < L.total) return BITMTP_ERR_SHAPE;
+    if (ws_bytes < kWsBytes) return BITMTP_ERR_SHAPE;
     DevInfo* dev = nullptr;
     int st = current_device(&dev);
     if (st != BITMTP_OK) return st;
@@ -241,41 +214,28 @@ int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes,
     GemmParams prm;
     std::memset(&prm, 0, sizeof(prm));
     long long tiles = 0;
-    int tasks = 0, rt = 0, bt = 0, pre = 0, max_m = 1, np = 0;
+    int max_m = 1, np = 0;
     for (int i = 0; i < n; ++i) {
         if (probs[i].M == 0 || probs[i].N == 0) continue;
         GemmProblem g = probs[i];
         g.tile_begin = tiles;
-        g.task_begin = tasks;
-        g.rt_begin = rt;
-        g.bt_begin = bt;
-        g.pre_begin = pre;
         tiles += static_cast<long long>(g.nt) * g.kt;
-        tasks += g.M;
-        rt += g.nt;
-        bt += g.kt;
-        pre += (g.kt + 1) * 16;
         max_m = std::max(max_m, g.M);
         prm.p[np++] = g;
     }
     int dp_rows = 1;
     const int path = choose_path(max_m, flags, &dp_rows);
     if (path < 0) return BITMTP_ERR_SHAPE;
-    const int cap = std::min(kMaxCtas, kCtasPerSm * dev->sms);
+    const long long cap = std::min(kMaxCtas, kCtasPerSm * dev->sms);
     prm.n_problems = np;
-    prm.rows_b = path == kPathTC16 ? 16 : path == kPathTC8 ? 8 : dp_rows;
-    prm.btile_bytes = path == kPathTC16 ? 4096 : path == kPathTC8 ? 2048 : dp_rows * 128;
     prm.stages = gemm_stages(path, dp_rows);
-    prm.total_tasks = tasks;
     prm.total_tiles = tiles;
-    prm.nctas = static_cast<int>(std::min<long long>(cap, tiles));  // every CTA range is non-empty
+    // every CTA range is non-empty (nctas <= tiles) and, where the problem is
+    // large enough, at least kMinTilesPerCta long
+    prm.nctas = static_cast<int>(std::max(1ll, std::min(cap, (tiles + kMinTilesPerCta - 1) / kMinTilesPerCta)));
     uint8_t* w = static_cast<uint8_t*>(workspace);
-    prm.gridbar = reinterpret_cast<unsigned*>(w + L.gridbar);
-    prm.counters = reinterpret_cast<unsigned*>(w + L.counters);
-    prm.ascale = reinterpret_cast<float*>(w + L.ascale);
-    prm.prefix = reinterpret_cast<int*>(w + L.prefix);
-    prm.accum = reinterpret_cast<float*>(w + L.accum);
-    prm.btiles = w + L.btiles;
+    prm.counters = reinterpret_cast<unsigned*>(w + kWsCounters);
+    prm.slots = reinterpret_cast<int*>(w + kWsSlots);
     prm.err = dev->err;
     return cuda_status(launch_gemm(prm, path, dp_rows, (flags & BITMTP_FLAG_PDL) != 0, stream));
 }
@@ -338,30 +298,16 @@ int bitmtp_linear_quant_act(const void* x, int x_kind, int64_t M, int64_t K, int
 
 size_t bitmtp_linear_workspace_bytes(int64_t N, int64_t K, int64_t M) {
     if (M < 1 || M > BITMTP_MAX_M || N < 1 || N > BITMTP_MAX_N || K < 1 || K > BITMTP_MAX_K) return 0;
-    GemmProblem g;
-    std::memset(&g, 0, sizeof(g));
-    g.N = static_cast<int>(N);
-    g.K = static_cast<int>(K);
-    g.M = static_cast<int>(M);
-    g.nt = static_cast<int>(ceil_div(N, kTileN));
-    g.kt = static_cast<int>(ceil_div(K, kTileK));
-    return layout_for(&g, 1).total;
+    return kWsBytes;
 }
 
 size_t bitmtp_linear_workspace_bytes_grouped(const bitmtp_gemm_desc* d, int n_desc) {
     if (n_desc < 1 || n_desc > BITMTP_MAX_GROUP || !d) return 0;
-    GemmProblem g[BITMTP_MAX_GROUP];
-    std::memset(g, 0, sizeof(g));
     for (int i = 0; i < n_desc; ++i) {
         const int64_t N = d[i].N, K = d[i].K, M = d[i].M;
         if (M < 0 || M > BITMTP_MAX_M || N < 0 || N > BITMTP_MAX_N || K < 1 || K > BITMTP_MAX_K) return 0;
-        g[i].N = static_cast<int>(N);
-        g[i].K = static_cast<int>(K);
-        g[i].M = static_cast<int>(M);
-        g[i].nt = static_cast<int>(ceil_div(N, kTileN));
-        g[i].kt = static_cast<int>(ceil_div(K, kTileK));
     }
-    return layout_for(g, n_desc).total;
+    return kWsBytes;
 }
 
 int bitmtp_linear_gemm(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M, const bitmtp_act* act,

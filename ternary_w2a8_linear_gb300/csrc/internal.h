@@ -10,7 +10,7 @@ namespace bitmtp {
 constexpr int kTileN = 128;       // out-features per row tile (= TMEM lanes)
 constexpr int kTileK = 128;       // in-features per k tile
 constexpr int kTileBytes = 4096;  // packed bytes per (row tile, k tile)
-constexpr int kGemmThreads = 192; // warps 0-3 compute, warp 4 bulk copies, warp 5 MMA issue
+constexpr int kGemmThreads = 256; // warps 0-3 compute, 4 bulk copies, 5 MMA issue, 6-7 activation builders
 constexpr int kCtasPerSm = 2;     // persistent CTAs per SM
 
 // Compute paths.  The activation operand ("B tile", one per k tile) is laid
@@ -34,36 +34,26 @@ struct GemmProblem {
     int act_kind;             // BITMTP_F32 / BITMTP_BF16 / BITMTP_Q8
     int out_dtype;            // BITMTP_F32 / BITMTP_BF16
     long long tile_begin;     // first flattened (row tile, k tile) index of this problem
-    int task_begin;           // first activation-row task (rows_b per problem)
-    int rt_begin;             // first row-tile counter
-    int bt_begin;             // first B tile in the workspace
-    int pre_begin;            // first row-sum prefix entry ((kt + 1) * 16 per problem)
 };
 
 struct GemmParams {
     GemmProblem p[BITMTP_MAX_GROUP];
     int n_problems;
-    int rows_b;               // activation rows held per B tile
-    int btile_bytes;
-    int stages;               // shared-memory ring depth (k tiles)
-    int total_tasks;          // activation rows to quantise (sum of M)
+    int stages;               // chunks in the shared-memory ring
     int nctas;
     long long total_tiles;
-    // workspace sections
-    unsigned* gridbar;
-    unsigned* counters;
-    float* ascale;            // [total_tasks]
-    int* prefix;              // row-sum prefixes
-    float* accum;             // [kMaxCtas][128][16] split-row-tile accumulators
-    uint8_t* btiles;          // activation operand tiles
+    unsigned* counters;       // [kMaxCtas] split-row-tile arrival counters (left at zero)
+    int* slots;               // [kMaxCtas][2][16][128] split-row-tile partial sums
     int* err;                 // device error word
 };
 
-// Workspace layout for a launch (sizes in bytes, sections 256-byte aligned).
-struct WorkspaceLayout {
-    size_t gridbar, counters, accum, ascale, prefix, btiles, total;
-};
-constexpr int kMaxCtas = 320;  // persistent CTAs per launch (>= 2 per SM on GB300)
+constexpr int kMaxCtas = 320;         // persistent CTAs per launch (>= 2 per SM on GB300)
+constexpr int kMinTilesPerCta = 4;    // fewer CTAs on small problems: fewer split row tiles
+
+// Workspace: a fixed layout, independent of the shapes.
+constexpr size_t kWsCounters = 256;
+constexpr size_t kWsSlots = kWsCounters + ((static_cast<size_t>(kMaxCtas) * 4 + 255) & ~static_cast<size_t>(255));
+constexpr size_t kWsBytes = kWsSlots + static_cast<size_t>(kMaxCtas) * 2 * 16 * kTileN * 4;
 
 size_t gemm_smem_bytes(int path, int dp_rows, int stages);
 int gemm_stages(int path, int dp_rows);

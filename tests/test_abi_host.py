@@ -116,13 +116,13 @@ def test_workspace_bytes(lib):
     wb = L.bitmtp_linear_workspace_bytes
     assert wb(0, 64, 4) == 0 and wb(64, 0, 4) == 0 and wb(64, 64, 0) == 0 and wb(64, 64, 17) == 0
     small, big = wb(128, 128, 1), wb(32000, 2560, 16)
-    assert 0 < small < big
-    assert big - small >= (20 - 1) * 4096             # activation tiles: one per k tile
-    assert wb(2560, 2560, 1) == wb(2560, 2560, 16) or wb(2560, 2560, 1) < wb(2560, 2560, 16)
+    # fixed layout: split-row-tile slots and counters for the largest grid
+    assert small == big and small >= 320 * 2 * 16 * 128 * 4
     d = [L.GemmDesc(FAKE, 0.02, 2560, 2560, 8, _act(ldx=2560), _out(ldy=2560)),
          L.GemmDesc(FAKE, 0.02, 640, 2560, 8, _act(ldx=2560), _out(ldy=640))]
-    g = L.bitmtp_linear_workspace_bytes_grouped(d)
-    assert g >= wb(2560, 2560, 8) and g > wb(640, 2560, 8)
+    assert L.bitmtp_linear_workspace_bytes_grouped(d) == small
+    bad = [L.GemmDesc(FAKE, 0.02, 2560, 2560, 20, _act(ldx=2560), _out(ldy=2560))]
+    assert L.bitmtp_linear_workspace_bytes_grouped(bad) == 0
 
 
 def test_pack_and_quant_validation(lib):
