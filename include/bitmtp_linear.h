@@ -190,6 +190,42 @@ int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc,
                                void* workspace, size_t workspace_bytes,
                                unsigned flags, void* stream);
 
+/* Size of the library's built-in scratch array used by
+ * bitmtp_linear_gemm_noalloc: 5 MiB + 4 KiB of device memory, held on every
+ * device that loads the library until the process exits. */
+#define BITMTP_NOALLOC_SCRATCH_BYTES ((size_t)5 * 1024 * 1024 + 4096)
+
+/* bitmtp_linear_gemm without a workspace argument: for callers that cannot
+ * allocate device memory.  Examples: code called from another runtime's
+ * launch hook or plugin that forbids allocation; latency-bound loops where
+ * cudaMalloc/cudaFree would stall the device or the host thread; processes
+ * whose device memory is entirely owned by a caching allocator they cannot
+ * reach.  (The paper has no counterpart: this is a deployment convenience.)
+ *
+ * Arguments, results and the launched kernel are those of bitmtp_linear_gemm;
+ * instead of a caller workspace the call uses one static device array of
+ * BITMTP_NOALLOC_SCRATCH_BYTES that the library owns.  It allocates nothing.
+ *   - Limit: a shape whose workspace need (bitmtp_linear_workspace_bytes)
+ *     exceeds BITMTP_NOALLOC_SCRATCH_BYTES is rejected with BITMTP_ERR_SHAPE
+ *     before anything is enqueued.  Every shape inside the library's limits
+ *     (M <= BITMTP_MAX_M, K <= BITMTP_MAX_K, N <= BITMTP_MAX_N) fits.
+ *   - Set-up: the first call on a device, made with that device current,
+ *     looks up the array's device address (one CUDA runtime query, which may
+ *     load the library's device code).  Make that first call before any
+ *     stream capture begins.
+ *   - Sharing: all calls on a device share the one array and it keeps what
+ *     the previous call left.  Each call first clears, on `stream`, the part
+ *     that must start at zero (the split-row-tile arrival counters); the
+ *     partial-sum slots are always written before they are read.  Calls whose
+ *     work can overlap on the GPU (different streams without ordering between
+ *     them, or different host threads) race on the array and give wrong
+ *     results; order them on one stream or use bitmtp_linear_gemm with
+ *     distinct workspaces.
+ * Enqueues one small memset and the GEMM kernel on `stream`. */
+int bitmtp_linear_gemm_noalloc(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M,
+                               const bitmtp_act* act, const bitmtp_out* out,
+                               unsigned flags, void* stream);
+
 /* Synchronise `stream`, then return and clear the device error word that a
  * kernel sets when one of its bounded waits expires (0 = none; otherwise a
  * code naming the wait).  Never set by correct launches. */

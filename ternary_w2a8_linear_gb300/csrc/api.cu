@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "internal.h"
@@ -240,6 +241,35 @@ int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes,
     return cuda_status(launch_gemm(prm, path, dp_rows, (flags & BITMTP_FLAG_PDL) != 0, stream));
 }
 
+// ------------------------------------------------- no-allocation variant --
+// Built-in scratch of bitmtp_linear_gemm_noalloc, laid out like a caller's
+// workspace.  Host code must not pass the symbol itself to a kernel: on the
+// host it names a stand-in, not device memory.  Its device address is looked
+// up once per device (with that device current) and kept here.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[BITMTP_NOALLOC_SCRATCH_BYTES];
+static_assert(kWsBytes <= BITMTP_NOALLOC_SCRATCH_BYTES, "built-in scratch smaller than the workspace layout");
+
+std::atomic<void*> g_noalloc_addr[64];
+
+int noalloc_scratch(void** addr) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return BITMTP_ERR_UNSUPPORTED;
+    }
+    void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        // two threads racing here both obtain the same address
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return BITMTP_ERR_CUDA;
+        }
+        g_noalloc_addr[dev].store(p, std::memory_order_release);
+    }
+    *addr = p;
+    return BITMTP_OK;
+}
+
 }  // namespace
 }  // namespace bitmtp
 
@@ -335,6 +365,33 @@ int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc, void* work
     }
     if (n_desc == 0) return BITMTP_OK;
     return run_gemms(g, n_desc, workspace, workspace_bytes, flags, static_cast<cudaStream_t>(stream));
+}
+
+int bitmtp_linear_gemm_noalloc(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M,
+                               const bitmtp_act* act, const bitmtp_out* out, unsigned flags, void* stream) {
+    GemmProblem g;
+    std::memset(&g, 0, sizeof(g));
+    int st = check_problem(pk, w_scale, N, K, M, act, out, &g);
+    if (st != BITMTP_OK) return st;
+    if ((flags & BITMTP_FLAG_FORCE_TC) && (flags & BITMTP_FLAG_FORCE_DP)) return BITMTP_ERR_INVALID;
+    if (g.M == 0) return BITMTP_OK;
+    const size_t need = bitmtp_linear_workspace_bytes(N, K, M);
+    if (need == 0 || need > BITMTP_NOALLOC_SCRATCH_BYTES) return BITMTP_ERR_SHAPE;
+    int dp_rows = 1;
+    if (choose_path(g.M, flags, &dp_rows) < 0) return BITMTP_ERR_SHAPE;  // before anything is enqueued
+    DevInfo* dev = nullptr;
+    st = current_device(&dev);
+    if (st != BITMTP_OK) return st;
+    void* scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != BITMTP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the arrival counters must start at zero; a call that gave up a bounded
+    // wait may have left some set
+    st = cuda_status(cudaMemsetAsync(static_cast<uint8_t*>(scratch) + kWsCounters, 0,
+                                     kWsSlots - kWsCounters, s));
+    if (st != BITMTP_OK) return st;
+    return run_gemms(&g, 1, scratch, BITMTP_NOALLOC_SCRATCH_BYTES, flags, s);
 }
 
 int bitmtp_linear_device_error(void* stream) {

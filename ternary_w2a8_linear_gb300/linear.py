@@ -25,6 +25,7 @@ ERR_INVALID, ERR_ALIGN, ERR_SHAPE, ERR_NOT_TERNARY, ERR_UNSUPPORTED, ERR_CUDA, E
 F32, BF16, Q8 = 0, 1, 2
 FLAG_PDL, FLAG_FORCE_TC, FLAG_FORCE_DP = 0x1, 0x2, 0x4
 MAX_M, MAX_K, MAX_N, MAX_GROUP = 16, 32768, 16777216, 8
+NOALLOC_SCRATCH_BYTES = 5 * 1024 * 1024 + 4096
 
 
 class BitmtpError(RuntimeError):
@@ -74,6 +75,8 @@ def load() -> ctypes.CDLL:
                                          c.c_uint, c.c_void_p]),
         "bitmtp_linear_gemm_grouped": (c.c_int, [c.POINTER(GemmDesc), c.c_int, c.c_void_p, c.c_size_t,
                                                  c.c_uint, c.c_void_p]),
+        "bitmtp_linear_gemm_noalloc": (c.c_int, [c.c_void_p, c.c_float, c.c_int64, c.c_int64, c.c_int64,
+                                                 c.POINTER(Act), c.POINTER(Out), c.c_uint, c.c_void_p]),
         "bitmtp_linear_device_error": (c.c_int, [c.c_void_p]),
         "bitmtp_linear_status_string": (c.c_char_p, [c.c_int]),
         "bitmtp_linear_version": (c.c_int, []),
@@ -123,6 +126,13 @@ def bitmtp_linear_gemm(pk_ptr, w_scale, N, K, M, act: Act, out: Out, ws_ptr, ws_
 def bitmtp_linear_gemm_grouped(descs, ws_ptr, ws_bytes, flags, stream) -> int:
     arr = (GemmDesc * max(1, len(descs)))(*descs)
     return load().bitmtp_linear_gemm_grouped(arr, len(descs), ws_ptr, ws_bytes, flags, stream)
+
+
+def bitmtp_linear_gemm_noalloc(pk_ptr, w_scale, N, K, M, act: Act, out: Out, flags, stream) -> int:
+    """bitmtp_linear_gemm on the library's built-in scratch array (no workspace,
+    nothing allocated); calls on one device must not overlap on the GPU."""
+    return load().bitmtp_linear_gemm_noalloc(pk_ptr, w_scale, N, K, M, ctypes.byref(act), ctypes.byref(out),
+                                             flags, stream)
 
 
 def bitmtp_linear_device_error(stream=None) -> int:

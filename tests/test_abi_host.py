@@ -26,7 +26,7 @@ def test_exports_every_header_symbol(lib):
         "bitmtp_linear_packed_bytes", "bitmtp_linear_pack", "bitmtp_linear_quant_act",
         "bitmtp_linear_gemm", "bitmtp_linear_gemm_grouped", "bitmtp_linear_device_error",
         "bitmtp_linear_status_string", "bitmtp_linear_version", "bitmtp_linear_workspace_bytes",
-        "bitmtp_linear_workspace_bytes_grouped",
+        "bitmtp_linear_workspace_bytes_grouped", "bitmtp_linear_gemm_noalloc",
     }
     for s in syms:
         assert hasattr(lib, s), s
@@ -125,6 +125,18 @@ def test_workspace_bytes(lib):
     assert L.bitmtp_linear_workspace_bytes_grouped(bad) == 0
 
 
+def test_noalloc_validation(lib):
+    na = L.bitmtp_linear_gemm_noalloc
+    assert na(FAKE, 0.02, 64, 64, 17, _act(), _out(), 0, None) == L.ERR_SHAPE
+    assert na(FAKE, 0.02, 64, L.MAX_K + 1, 4, _act(), _out(), 0, None) == L.ERR_SHAPE
+    assert na(FAKE, 0.02, 64, 64, 8, _act(), _out(), L.FLAG_FORCE_DP, None) == L.ERR_SHAPE
+    assert na(None, 0.02, 64, 64, 4, _act(), _out(), 0, None) == L.ERR_INVALID
+    assert na(FAKE, 0.02, 64, 64, 0, _act(), _out(), 0, None) == L.OK
+    # the built-in array covers the workspace of every shape inside the limits
+    assert L.bitmtp_linear_workspace_bytes(L.MAX_N, L.MAX_K, L.MAX_M) <= L.NOALLOC_SCRATCH_BYTES
+    assert "NOALLOC_SCRATCH_BYTES ((size_t)5 * 1024 * 1024 + 4096)" in open(L.HEADER_PATH).read()
+
+
 def test_pack_and_quant_validation(lib):
     pk = L.bitmtp_linear_pack
     assert pk(FAKE, 0, 16, 16, FAKE, 4096 + 16, None) == L.ERR_SHAPE
@@ -143,6 +155,7 @@ def test_pack_and_quant_validation(lib):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")
 def test_valid_calls_without_device_report_unsupported(lib):
     assert gemm() == L.ERR_UNSUPPORTED
+    assert L.bitmtp_linear_gemm_noalloc(FAKE, 0.02, 64, 64, 4, _act(), _out(), 0, None) == L.ERR_UNSUPPORTED
     assert L.bitmtp_linear_quant_act(FAKE, L.F32, 2, 16, 16, FAKE, 16, FAKE, None, None) == L.ERR_UNSUPPORTED
     assert L.bitmtp_linear_pack(FAKE, 4, 16, 16, FAKE, 4096 + 16, None) == L.ERR_UNSUPPORTED
     assert L.bitmtp_linear_device_error(0) == L.ERR_UNSUPPORTED
