@@ -4,11 +4,13 @@ Default workload (one "step"): the BitNet-2B-shaped layer set -- projections
 q 2560->2560, k/v 2560->640, o 2560->2560, gate/up 2560->6912, down 6912->2560,
 ternary weights with P(0)=0.5, bf16 activations with 1% outliers x20 -- at
 block widths M = 1, 2, 4, 8.  One step runs, for each width, the seven
-projections back to back, each a single fused launch (absmax quantisation of
-the raw bf16 rows, 2-bit weight stream, exact integer product, dequant to
-bf16).  Weights rotate over enough distinct copies that no step finds its
-weights in L2.  Steps are replayed from CUDA graphs with programmatic
-dependent launch between consecutive linears.
+projections: by default as one grouped call per width, otherwise one call per
+projection.  A call is two launches: the activation preparation (absmax
+quantisation of the raw bf16 rows into the operand tiles) and the GEMM (2-bit
+weight stream, exact integer product, dequant to bf16), which starts
+streaming weights while the first runs.  Weights rotate over enough distinct
+copies that no step finds its weights in L2.  Steps are replayed from CUDA
+graphs with programmatic dependent launch between consecutive launches.
 
 Metric: achieved HBM GB/s on algorithmic bytes (packed weights + activations),
 also as a fraction of the measured copy bandwidth, plus rows/s per width.
@@ -233,7 +235,8 @@ def run_ours(args, rank, world):
     K = args.steps
     reps, rem = divmod(K, G)
     g_rem = capture(rem, 0) if rem else None
-    launches_per_step = len(WIDTHS) * (1 if args.mode == "grouped" else len(inputs.BITNET2B_PROJ))
+    # two kernels per call: activation preparation + GEMM
+    launches_per_step = 2 * len(WIDTHS) * (1 if args.mode == "grouped" else len(inputs.BITNET2B_PROJ))
 
     # warm-up
     with torch.cuda.stream(stream):

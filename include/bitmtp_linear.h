@@ -144,12 +144,13 @@ typedef struct bitmtp_out {
 /* Workspace of a GEMM call: a device buffer the caller allocates once,
  * 16-byte aligned, of at least the size these queries return, and
  * zero-fills before its first use (e.g. cudaMemset).  It holds split-row-tile
- * partial sums and arrival counters; every call leaves the counters at zero,
- * so one workspace serves calls of any shapes.  Calls that may execute
- * concurrently on the GPU need distinct workspaces; calls ordered on one
- * stream may share one.  After a call that ends in BITMTP_ERR_DEVICE,
- * zero-fill it again.  The size is the same for every valid shape (0 for
- * out-of-range arguments). */
+ * partial sums and arrival counters (a fixed 5 MiB part) and each problem's
+ * quantised activation operand (about 4 KiB per 128 in-features); every call
+ * leaves the counters at zero, so one workspace serves calls of any shapes
+ * that fit.  Calls that may execute concurrently on the GPU need distinct
+ * workspaces; calls ordered on one stream may share one.  After a call that
+ * ends in BITMTP_ERR_DEVICE, zero-fill it again.  Returns 0 for out-of-range
+ * arguments. */
 size_t bitmtp_linear_workspace_bytes(int64_t N, int64_t K, int64_t M);
 
 /* y = dequant(T * q): the W2A8 linear at block width M.
@@ -159,8 +160,10 @@ size_t bitmtp_linear_workspace_bytes(int64_t N, int64_t K, int64_t M);
  *   M         block width, 0 <= M <= BITMTP_MAX_M (0: no-op)
  *   workspace >= bitmtp_linear_workspace_bytes(N, K, M) bytes, see above
  *   flags     BITMTP_FLAG_* bits
- * One kernel launch: it quantises raw activation rows (BITMTP_F32/BF16) with
- * the quantiser above, streams the packed weights and writes y (and acc).
+ * Two kernel launches: the first quantises the activation rows
+ * (BITMTP_F32/BF16, with the quantiser above; BITMTP_Q8 rows are taken as
+ * they are) into the workspace, the second streams the packed weights and
+ * writes y (and acc); it starts streaming while the first one runs.
  * The compute path is chosen from M (width specialisation); results do not
  * depend on the choice. */
 int bitmtp_linear_gemm(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M,
@@ -180,7 +183,8 @@ typedef struct bitmtp_gemm_desc {
 /* Workspace bytes for a grouped launch of these descriptors (0 if invalid). */
 size_t bitmtp_linear_workspace_bytes_grouped(const bitmtp_gemm_desc* d, int n_desc);
 
-/* Run up to BITMTP_MAX_GROUP independent problems in ONE kernel launch --
+/* Run up to BITMTP_MAX_GROUP independent problems in one GEMM launch (after
+ * one activation-preparation launch covering all of them) --
  * e.g. the role-dependent output projections of one block step (verify rows
  * through one projection and draft rows through another), or the independent
  * projections of a layer.  `d` is a HOST array of n_desc descriptors (copied
@@ -191,9 +195,9 @@ int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc,
                                unsigned flags, void* stream);
 
 /* Size of the library's built-in scratch array used by
- * bitmtp_linear_gemm_noalloc: 5 MiB + 4 KiB of device memory, held on every
+ * bitmtp_linear_gemm_noalloc: 6.5 MiB of device memory, held on every
  * device that loads the library until the process exits. */
-#define BITMTP_NOALLOC_SCRATCH_BYTES ((size_t)5 * 1024 * 1024 + 4096)
+#define BITMTP_NOALLOC_SCRATCH_BYTES ((size_t)13 * 512 * 1024)
 
 /* bitmtp_linear_gemm without a workspace argument: for callers that cannot
  * allocate device memory.  Examples: code called from another runtime's

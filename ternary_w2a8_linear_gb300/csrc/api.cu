@@ -207,18 +207,27 @@ int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes,
     if (!any) return BITMTP_OK;  // empty problems never touch the device
     if (!workspace) return BITMTP_ERR_INVALID;
     if (!aligned16(workspace)) return BITMTP_ERR_ALIGN;
-    if (ws_bytes < kWsBytes) return BITMTP_ERR_SHAPE;
+    size_t need = kWsAct;
+    for (int i = 0; i < n; ++i)
+        if (probs[i].M > 0 && probs[i].N > 0) need += act_region_bytes(probs[i].kt);
+    if (ws_bytes < need) return BITMTP_ERR_SHAPE;
     DevInfo* dev = nullptr;
     int st = current_device(&dev);
     if (st != BITMTP_OK) return st;
 
     GemmParams prm;
     std::memset(&prm, 0, sizeof(prm));
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    size_t act_off = kWsAct;
     long long tiles = 0;
     int max_m = 1, np = 0;
     for (int i = 0; i < n; ++i) {
         if (probs[i].M == 0 || probs[i].N == 0) continue;
         GemmProblem g = probs[i];
+        g.actb = w + act_off;
+        g.rsp = reinterpret_cast<int*>(w + act_off + act_tiles_bytes(g.kt));
+        g.asc = reinterpret_cast<float*>(w + act_off + act_tiles_bytes(g.kt) + act_rsp_bytes(g.kt));
+        act_off += act_region_bytes(g.kt);
         g.tile_begin = tiles;
         tiles += static_cast<long long>(g.nt) * g.kt;
         max_m = std::max(max_m, g.M);
@@ -234,7 +243,6 @@ int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes,
     // every CTA range is non-empty (nctas <= tiles) and, where the problem is
     // large enough, at least kMinTilesPerCta long
     prm.nctas = static_cast<int>(std::max(1ll, std::min(cap, (tiles + kMinTilesPerCta - 1) / kMinTilesPerCta)));
-    uint8_t* w = static_cast<uint8_t*>(workspace);
     prm.counters = reinterpret_cast<unsigned*>(w + kWsCounters);
     prm.slots = reinterpret_cast<int*>(w + kWsSlots);
     prm.err = dev->err;
@@ -247,7 +255,8 @@ int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes,
 // host it names a stand-in, not device memory.  Its device address is looked
 // up once per device (with that device current) and kept here.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[BITMTP_NOALLOC_SCRATCH_BYTES];
-static_assert(kWsBytes <= BITMTP_NOALLOC_SCRATCH_BYTES, "built-in scratch smaller than the workspace layout");
+static_assert(kWsAct + act_region_bytes(BITMTP_MAX_K / kTileK) <= BITMTP_NOALLOC_SCRATCH_BYTES,
+              "built-in scratch smaller than the workspace of the largest single problem");
 
 std::atomic<void*> g_noalloc_addr[64];
 
@@ -328,7 +337,7 @@ int bitmtp_linear_quant_act(const void* x, int x_kind, int64_t M, int64_t K, int
 
 size_t bitmtp_linear_workspace_bytes(int64_t N, int64_t K, int64_t M) {
     if (M < 1 || M > BITMTP_MAX_M || N < 1 || N > BITMTP_MAX_N || K < 1 || K > BITMTP_MAX_K) return 0;
-    return kWsBytes;
+    return kWsAct + act_region_bytes(static_cast<int>(ceil_div(K, kTileK)));
 }
 
 size_t bitmtp_linear_workspace_bytes_grouped(const bitmtp_gemm_desc* d, int n_desc) {
@@ -337,7 +346,9 @@ size_t bitmtp_linear_workspace_bytes_grouped(const bitmtp_gemm_desc* d, int n_de
         const int64_t N = d[i].N, K = d[i].K, M = d[i].M;
         if (M < 0 || M > BITMTP_MAX_M || N < 0 || N > BITMTP_MAX_N || K < 1 || K > BITMTP_MAX_K) return 0;
     }
-    return kWsBytes;
+    size_t need = kWsAct;
+    for (int i = 0; i < n_desc; ++i) need += act_region_bytes(static_cast<int>(ceil_div(d[i].K, kTileK)));
+    return need;
 }
 
 int bitmtp_linear_gemm(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M, const bitmtp_act* act,

@@ -1,29 +1,31 @@
-// gemm.cu -- the W2A8 ternary linear on sm_103a: a persistent, warp-specialised
-// stream-K kernel.
+// gemm.cu -- the W2A8 ternary linear on sm_103a: an activation-operand
+// preparation kernel followed by a persistent, warp-specialised stream-K GEMM.
 //
-// One launch computes one or several independent linears ("problems") with
-// one compute path.  The flattened (problem, row tile, k tile) space is split
-// into equal contiguous ranges, one per CTA (stream-K), so every SM streams
-// the same number of weight bytes whatever the mix of shapes.  Each CTA:
+// Two launches per call, chained by programmatic dependent launch (PDL):
 //
-//   warp 4       streams its weight tiles with bulk copies (TMA engine) of up
-//                to four contiguous 4 KiB tiles -- the engine's cost is per
-//                copy, so 16 KiB copies keep up with HBM where 4 KiB ones do
-//                not -- into a ring of chunks; weights do not depend on the
-//                previous kernel on the stream, so this starts before the
-//                programmatic-dependent-launch wait;
-//   warps 0-3,6-7  first compute the per-row absmax of every activation row the
-//                CTA needs (batches of loads in flight), using the quantiser of
-//                the standalone kernel in the same fp32 operations;
-//   warps 6-7    then run ahead of the consumers, quantising the activation
-//                operand of each chunk into a shared-memory ring in the layout
-//                the compute path reads, with per-tile row sums of the codes;
-//   warps 0-3    one output row per thread: the compute path (below), and the
-//                epilogue -- a whole row tile is dequantised and written
-//                straight away; a row tile split between CTAs is finished by
-//                the last contributor, which sums the others' int32 partials
-//                from the workspace;
-//   warp 5       (tensor path) issues tcgen05.mma.
+//   act_prep_kernel   one CTA per (problem, activation row): the row's absmax
+//                     and int8 codes (the quantiser of the standalone kernel,
+//                     the same fp32 operations), written once into the
+//                     workspace as the GEMM's activation operand -- one tile
+//                     per k tile, in the layout the compute path reads --
+//                     with prefix sums over k tiles of the row's codes and the
+//                     row's dequant scale.
+//
+//   w2a8_streamk_kernel  the flattened (problem, row tile, k tile) space is
+//                     split into equal contiguous ranges, one per CTA
+//                     (stream-K), so every SM streams the same number of
+//                     weight bytes whatever the mix of shapes.  Each CTA:
+//     warp 4      bulk copies (TMA engine) into a ring of chunks of four
+//                 tiles: weight tiles first -- they do not depend on the
+//                 preparation kernel, so they are requested before the PDL
+//                 wait -- and, after it, the matching activation tiles; each
+//                 contiguous run is one copy (the engine's cost is per copy);
+//     warps 0-3   one output row per thread: the compute path (below), then
+//                 the epilogue -- a whole row tile is dequantised and written
+//                 straight away; a row tile split between CTAs is finished by
+//                 the last contributor, which sums the others' int32 partials
+//                 from the workspace;
+//     warp 5      (tensor path) issues tcgen05.mma.
 //
 // Compute paths (the same 2-bit code words feed both):
 //   tensor (kPathTC16 / kPathTC8): each thread turns its code words into fp16
@@ -38,7 +40,8 @@
 //     stride).
 //   dp4a (kPathDP): four byte masks per code word, four int32 accumulators
 //     per row (scales 4^s, recombined with exact shifts).
-// With u = T + 1, sum_k T*q = sum_k u*q - sum_k q.
+// With u = T + 1, sum_k T*q = sum_k u*q - sum_k q; the second sum comes from
+// the preparation kernel's prefix sums.
 //
 // The operation is the packed W2A8 linear of "BitMTP: When Multi-Token
 // Prediction Meets Low-Bit Large Language Models" (AI summary: Main Findings,
@@ -58,15 +61,14 @@ namespace {
 
 constexpr int kChunk = 4;            // k tiles per ring chunk (16 KiB of weights)
 constexpr int kMaxRing = 6;          // chunks in the ring (upper bound)
-constexpr int kCtrlBytes = 4096;
+constexpr int kCtrlBytes = 1024;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kAccCol = 0;      // D: 16 fp32 columns, one per activation row
 constexpr uint32_t kACol = 32;       // A: kABufs buffers of 32 columns (64 k each)
 constexpr int kABufs = 7;
 constexpr uint32_t kIdesc = idesc_f16_f32(128, 16);
 constexpr int kSmemTarget = 100 * 1024;
-constexpr int kBuilders = 64;        // warps 6-7
-constexpr int kAmaxThreads = 192;    // warps 0-3 and 6-7
+constexpr int kPrepThreads = 256;
 
 enum : int {
     kErrWaitW = 0x101,
@@ -78,8 +80,8 @@ enum : int {
 };
 
 struct Ctrl {
-    uint64_t wfull[kMaxRing];     // weight chunk landed (bulk copies)
-    uint64_t bfull[kMaxRing];     // activation chunk built (builder warps)
+    uint64_t wfull[kMaxRing];     // weight tiles of the chunk landed
+    uint64_t bfull[kMaxRing];     // activation tiles of the chunk landed
     uint64_t empty[kMaxRing];     // chunk slot free again (MMA commit / dp4a consumers)
     uint64_t a_full[kABufs];
     uint64_t a_empty[kABufs];
@@ -87,9 +89,7 @@ struct Ctrl {
     uint32_t tmem_base;
     int failed;
     int flag[2];
-    unsigned amax[BITMTP_MAX_GROUP][16];  // float bits, non-negative
-    float qscale[BITMTP_MAX_GROUP][16];
-    int rs[kMaxRing * kChunk][16];        // per tile slot: row sums of the codes
+    float asc[BITMTP_MAX_GROUP][16];  // dequant scale per (problem - p0, row)
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
@@ -98,6 +98,10 @@ __host__ __device__ constexpr int btile_bytes(int path, int dp_rows) {
 }
 __host__ __device__ constexpr int btile_lbo(int path) { return path == kPathTC16 ? 256 : 128; }
 __host__ __device__ constexpr int btile_sbo(int path) { return path == kPathTC16 ? 128 : 0; }
+// Activation rows an operand tile holds (rows from M on are zero).
+__host__ __device__ constexpr int btile_rows(int path, int dp_rows) {
+    return path == kPathTC16 ? 16 : path == kPathTC8 ? 8 : dp_rows;
+}
 
 // fp16 pre-scale shift of the activation for A column c (J = 0,1,2,3,4,0,1,2).
 __device__ __forceinline__ int bscale_shift(int c) { return 9 - 2 * ((c < 5) ? c : (c - 5)); }
@@ -183,6 +187,30 @@ __device__ void issue_weights(const GemmParams& P, long long first, int count, u
     if (run_len > 0) bulk_g2s(smem_u32(run_dst), run_src, run_len * kTileBytes, bar, pol);
 }
 
+// The same for the activation tiles (BT bytes each) of those tiles: a run
+// ends where the k index wraps to the next row tile or the problem changes.
+__device__ void issue_acts(const GemmParams& P, long long first, int count, int BT, uint8_t* dst, uint32_t bar,
+                           uint64_t pol) {
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(count * BT));
+    TileIter it;
+    it.init(P, first);
+    const uint8_t* run_src = nullptr;
+    int run_len = 0;
+    uint8_t* run_dst = dst;
+    for (int k = 0; k < count; ++k) {
+        const uint8_t* src = P.p[it.pi].actb + static_cast<size_t>(it.kt) * BT;
+        if (run_len == 0 || src != run_src + static_cast<size_t>(run_len) * BT) {
+            if (run_len > 0) bulk_g2s(smem_u32(run_dst), run_src, run_len * BT, bar, pol);
+            run_dst = dst + k * BT;
+            run_src = src;
+            run_len = 0;
+        }
+        ++run_len;
+        it.next(P);
+    }
+    if (run_len > 0) bulk_g2s(smem_u32(run_dst), run_src, run_len * BT, bar, pol);
+}
+
 // Load 8 consecutive activations k0..k0+7 of one row (zero beyond K).
 __device__ __forceinline__ void load8(const GemmProblem& pr, const char* row, bool vec_ok, int k0,
                                       float (&v)[8]) {
@@ -214,8 +242,17 @@ __device__ __forceinline__ void load8(const GemmProblem& pr, const char* row, bo
         }
     } else {  // int8 codes
         const int8_t* r = reinterpret_cast<const int8_t*>(row);
+        if (vec_ok && k0 + 8 <= pr.K) {
+            const uint2 u = *reinterpret_cast<const uint2*>(r + k0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = (k0 + i < pr.K) ? static_cast<float>(r[k0 + i]) : 0.f;
+            for (int i = 0; i < 4; ++i) {
+                v[i] = static_cast<float>(static_cast<int8_t>(u.x >> (8 * i)));
+                v[4 + i] = static_cast<float>(static_cast<int8_t>(u.y >> (8 * i)));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = (k0 + i < pr.K) ? static_cast<float>(r[k0 + i]) : 0.f;
+        }
     }
 }
 
@@ -224,112 +261,153 @@ __device__ __forceinline__ const char* act_row(const GemmProblem& pr, int m) {
     return static_cast<const char*>(pr.x) + static_cast<long long>(m) * pr.ldx * esize;
 }
 
-// ------------------------------------------------------------- absmax --
-// Per-row absmax of every activation row of problems [p0, p1] (raw kinds),
-// into c->amax[p - p0][m], by the kAmaxThreads threads (index at).  Batches
-// of eight 8-element loads per thread are in flight at once.
-__device__ void local_amax(const GemmParams& P, Ctrl* c, int p0, int p1, int at) {
-    for (int p = p0; p <= p1; ++p) {
-        const GemmProblem& pr = P.p[p];
-        if (pr.act_kind == BITMTP_Q8) continue;
-        const int ng = (pr.K + 7) >> 3;
-        const int total = pr.M * ng;
-        for (int base = at; base < total; base += kAmaxThreads * 8) {
-            float v[8][8];
-            int mrow[8];
+// ---------------------------------------------------- activation operand --
+// One CTA per (problem, row m < btile_rows).  Writes row m of every
+// activation tile of the problem (zeros for m >= M and beyond K), the prefix
+// sums rsp[m][0..kt] of the row's codes over k tiles, and asc[m].
+template <int PATH, int DPR>
+__global__ void __launch_bounds__(kPrepThreads)
+act_prep_kernel(const __grid_constant__ GemmParams P) {
+    constexpr int kRows = btile_rows(PATH, DPR);
+    constexpr int BT = btile_bytes(PATH, DPR);
+    __shared__ float red[kPrepThreads / 32];
+    __shared__ int tsum[BITMTP_MAX_K / kTileK];
+    pdl_launch_dependents();  // the GEMM may start streaming weights now
+
+    const int pi = blockIdx.x / kRows;
+    const int m = blockIdx.x - pi * kRows;
+    const GemmProblem& pr = P.p[pi];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool live = m < pr.M;
+    const bool raw = pr.act_kind != BITMTP_Q8;
+    const char* row = live ? act_row(pr, m) : nullptr;
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+    const int ngroups = pr.kt * 16;  // 8-element groups, the zero tail of the last tile included
+
+    // The activations may come from the previous kernel on the stream, and the
+    // previous GEMM on this workspace may still be reading it.
+    pdl_wait();
+
+    float amax = 0.f;
+    if (live && raw) {
+        for (int g0 = 0; g0 < ngroups; g0 += kPrepThreads * 4) {
+            float v[4][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int idx = base + j * kAmaxThreads;
-                mrow[j] = -1;
-                if (idx < total) {
-                    const int m = idx / ng, g = idx - m * ng;
-                    const char* row = act_row(pr, m);
-                    load8(pr, row, (reinterpret_cast<uintptr_t>(row) & 15u) == 0, g * 8, v[j]);
-                    mrow[j] = m;
+            for (int j = 0; j < 4; ++j) {
+                const int g = g0 + j * kPrepThreads + tid;
+                if (g < ngroups) {
+                    load8(pr, row, vec_ok, g * 8, v[j]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (mrow[j] < 0) continue;
-                float a = 0.f;
+            for (int j = 0; j < 4; ++j)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[j][i]));
-                if (a > 0.f) atomicMax(&c->amax[p - p0][mrow[j]], __float_as_uint(a));
-            }
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
         }
     }
-}
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    const float s = quant_scale(amax);
 
-// ---------------------------------------------------- activation builder --
-// Quantise the activation operand of `cnt` consecutive tiles of this CTA's
-// range (starting at walker position `it`) into ring chunk slot q, with the
-// per-tile row sums of the codes.  Builder threads only (bt in [0, 64)).
-template <int PATH, int DPR>
-__device__ void build_chunk(const GemmParams& P, Ctrl* c, TileIter it, int p0, int cnt, int q, uint8_t* Bq,
-                            int bt, bool alive) {
-    constexpr int BT = btile_bytes(PATH, DPR);
-    constexpr int kRows = PATH == kPathTC16 ? 16 : PATH == kPathTC8 ? 8 : DPR;
-    constexpr int kElems = PATH == kPathDP ? 16 : 8;     // k per unit
-    constexpr int kUnitsPerTile = (128 / kElems) * kRows;
-    for (int z = bt; z < cnt * 16; z += kBuilders) c->rs[q * kChunk + z / 16][z % 16] = 0;
-    named_bar_sync(2, kBuilders);
-    for (int t = 0; t < cnt && alive; ++t) {
-        const GemmProblem& pr = P.p[it.pi];
-        const bool raw = pr.act_kind != BITMTP_Q8;
-        uint8_t* tile = Bq + t * BT;
-        int* rs = c->rs[q * kChunk + t];
-        for (int u = bt; u < kUnitsPerTile; u += kBuilders) {
-            const int m = u % kRows;          // row fastest: conflict-free 16-byte stores
-            const int g = u / kRows;          // 8-k group (tensor) or 16-k chunk (dp4a)
-            if (m >= pr.M) continue;          // rows beyond M feed only ignored results
-            const char* row = act_row(pr, m);
-            const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-            const float s = c->qscale[it.pi - p0][m];
-            const int k0 = it.kt * kTileK + g * kElems;
-            int rsum = 0;
-            if constexpr (PATH != kPathDP) {
-                float v[8];
-                load8(pr, row, vec_ok, k0, v);
+    // Each group of 16 consecutive threads covers one k tile: ngroups is a
+    // multiple of 16, so the shuffles below always see whole groups.
+    for (int g0 = 0; g0 < ngroups; g0 += kPrepThreads) {
+        const int g = g0 + tid;
+        const bool gv = g < ngroups;
+        float v[8];
+        if (live && gv) {
+            load8(pr, row, vec_ok, g * 8, v);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        }
+        int qv[8];
+        int rsum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            qv[i] = !live ? 0 : raw ? ((amax > 0.f) ? quantize(v[i], s) : 0) : static_cast<int>(v[i]);
+            rsum += qv[i];
+        }
+        const int kt = g >> 4, gg = g & 15;
+        uint8_t* tile = pr.actb + static_cast<size_t>(kt) * BT;
+        if constexpr (PATH != kPathDP) {
+            if (gv) {
                 uint32_t packed[4];
 #pragma unroll
                 for (int i = 0; i < 8; i += 2) {
-                    const int q0 = raw ? quantize(v[i], s) : static_cast<int>(v[i]);
-                    const int q1 = raw ? quantize(v[i + 1], s) : static_cast<int>(v[i + 1]);
-                    rsum += q0 + q1;
-                    const int sh = bscale_shift((g & 1) * 4 + (i >> 1));
-                    const __half h0 = __int2half_rn(q0 * (1 << sh));
-                    const __half h1 = __int2half_rn(q1 * (1 << sh));
+                    const int sh = bscale_shift((gg & 1) * 4 + (i >> 1));
+                    const __half h0 = __int2half_rn(qv[i] * (1 << sh));
+                    const __half h1 = __int2half_rn(qv[i + 1] * (1 << sh));
                     packed[i >> 1] = static_cast<uint32_t>(__half_as_ushort(h0)) |
                                      (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
                 }
-                *reinterpret_cast<uint4*>(tile + g * btile_lbo(PATH) + (m >> 3) * btile_sbo(PATH) + (m & 7) * 16) =
+                *reinterpret_cast<uint4*>(tile + gg * btile_lbo(PATH) + (m >> 3) * btile_sbo(PATH) + (m & 7) * 16) =
                     make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            } else {
-                float v[16];
-                load8(pr, row, vec_ok, k0, *reinterpret_cast<float(*)[8]>(v));
-                load8(pr, row, vec_ok, k0 + 8, *reinterpret_cast<float(*)[8]>(v + 8));
-                int qv[16];
+            }
+        } else {
+            // A 16-k unit is two 8-groups (lanes 2i, 2i+1): the even lane
+            // interleaves its partner's codes with its own.
+            const uint32_t lo = (static_cast<uint32_t>(qv[0]) & 0xFFu) | ((static_cast<uint32_t>(qv[1]) & 0xFFu) << 8) |
+                                ((static_cast<uint32_t>(qv[2]) & 0xFFu) << 16) | (static_cast<uint32_t>(qv[3]) << 24);
+            const uint32_t hi = (static_cast<uint32_t>(qv[4]) & 0xFFu) | ((static_cast<uint32_t>(qv[5]) & 0xFFu) << 8) |
+                                ((static_cast<uint32_t>(qv[6]) & 0xFFu) << 16) | (static_cast<uint32_t>(qv[7]) << 24);
+            const uint32_t plo = __shfl_xor_sync(0xffffffffu, lo, 1);
+            const uint32_t phi = __shfl_xor_sync(0xffffffffu, hi, 1);
+            if (gv && (gg & 1) == 0) {
+                uint32_t b[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    qv[i] = raw ? quantize(v[i], s) : static_cast<int>(v[i]);
-                    rsum += qv[i];
+                for (int i = 0; i < 4; ++i) {
+                    b[i] = (lo >> (8 * i)) & 0xFFu;
+                    b[4 + i] = (hi >> (8 * i)) & 0xFFu;
+                    b[8 + i] = (plo >> (8 * i)) & 0xFFu;
+                    b[12 + i] = (phi >> (8 * i)) & 0xFFu;
                 }
                 uint32_t reg[4];
 #pragma unroll
-                for (int sidx = 0; sidx < 4; ++sidx) {
-                    reg[sidx] = (static_cast<uint32_t>(qv[2 * sidx]) & 0xFFu) |
-                                ((static_cast<uint32_t>(qv[8 + 2 * sidx]) & 0xFFu) << 8) |
-                                ((static_cast<uint32_t>(qv[2 * sidx + 1]) & 0xFFu) << 16) |
-                                ((static_cast<uint32_t>(qv[9 + 2 * sidx]) & 0xFFu) << 24);
-                }
-                *reinterpret_cast<uint4*>(tile + g * (DPR * 16) + m * 16) = make_uint4(reg[0], reg[1], reg[2], reg[3]);
+                for (int si = 0; si < 4; ++si)
+                    reg[si] = b[2 * si] | (b[8 + 2 * si] << 8) | (b[2 * si + 1] << 16) | (b[9 + 2 * si] << 24);
+                *reinterpret_cast<uint4*>(tile + (gg >> 1) * (DPR * 16) + m * 16) =
+                    make_uint4(reg[0], reg[1], reg[2], reg[3]);
             }
-            if (rsum != 0) atomicAdd(&rs[m], rsum);
         }
-        it.next(P);
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, o);
+        if (gv && (tid & 15) == 0) tsum[kt] = rsum;
     }
-    if constexpr (PATH != kPathDP) fence_proxy_async_smem();  // read by the tensor core
-    named_bar_sync(2, kBuilders);
+    __syncthreads();
+
+    // rsp[m][0] = 0, rsp[m][t + 1] = codes of k tiles 0..t summed
+    if (warp == 0) {
+        const int KT = pr.kt;
+        int* rsp = pr.rsp + m * (KT + 1);
+        const int per = (KT + 31) / 32;
+        const int t0 = lane * per, t1 = min(KT, t0 + per);
+        int loc = 0;
+        for (int t = t0; t < t1; ++t) loc += tsum[t];
+        int inc = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        int run = inc - loc;
+        if (lane == 0) rsp[0] = 0;
+        for (int t = t0; t < t1; ++t) {
+            run += tsum[t];
+            rsp[t + 1] = run;
+        }
+        if (lane == 0) pr.asc[m] = raw ? dequant_scale(amax) : (live ? pr.a_scale_in[m] : 0.f);
+    }
+    // the GEMM reads the tiles through the async proxy (bulk copies)
+    fence_proxy_async_global();
 }
 
 // ------------------------------------------------------------ epilogue --
@@ -342,10 +420,6 @@ __device__ __forceinline__ void store_out(const GemmProblem& pr, int m, int n, i
         static_cast<__nv_bfloat16*>(pr.y)[o] = __float2bfloat16_rn(v);
     }
     if (pr.acc) pr.acc[static_cast<long long>(m) * pr.lda + n] = acc;
-}
-
-__device__ __forceinline__ float row_ascale(const GemmProblem& pr, const Ctrl* c, int lp, int m) {
-    return pr.act_kind == BITMTP_Q8 ? pr.a_scale_in[m] : dequant_scale(__uint_as_float(c->amax[lp][m]));
 }
 
 // A split row tile this CTA contributed to, finished after the main loop.
@@ -369,7 +443,7 @@ __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int
         if (alive && n < pr.N) {
 #pragma unroll
             for (int m = 0; m < 16; ++m)
-                if (m < M) store_out(pr, m, n, acc[m], row_ascale(pr, c, pi - p0, m));
+                if (m < M) store_out(pr, m, n, acc[m], c->asc[pi - p0][m]);
         }
         return;
     }
@@ -437,11 +511,21 @@ __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pendi
         if (alive && n < pr.N) {
 #pragma unroll
             for (int m = 0; m < 16; ++m)
-                if (m < M) store_out(pr, m, n, tot[m], row_ascale(pr, c, pend[k].pi - p0, m));
+                if (m < M) store_out(pr, m, n, tot[m], c->asc[pend[k].pi - p0][m]);
         }
         if (tid == 0) P.counters[pend[k].b_last] = 0u;
     }
     named_bar_sync(1, 128);
+}
+
+// Codes of rows 0..15 summed over k tiles [ka, kb) of problem pr (zero for
+// rows >= M); read from the preparation kernel's prefix sums.
+__device__ __forceinline__ void segment_code_sums(const GemmProblem& pr, int ka, int kb, int (&rq)[16]) {
+    const int* rsp = pr.rsp;
+    const int stride = pr.kt + 1;
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+        rq[m] = (m < pr.M) ? __ldcg(rsp + m * stride + kb) - __ldcg(rsp + m * stride + ka) : 0;
 }
 
 template <int PATH, int DPR>
@@ -470,7 +554,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     if (tid == 0) {
         for (int q = 0; q < R; ++q) {
             mbar_init(smem_u32(&c->wfull[q]), 1);
-            mbar_init(smem_u32(&c->bfull[q]), 2);             // the two builder warps
+            mbar_init(smem_u32(&c->bfull[q]), 1);
             mbar_init(smem_u32(&c->empty[q]), kTC ? 1 : 4);
         }
         for (int a = 0; a < kABufs; ++a) {
@@ -481,7 +565,6 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         c->failed = 0;
         fence_mbar_init();
     }
-    for (int z = tid; z < BITMTP_MAX_GROUP * 16; z += kGemmThreads) (&c->amax[0][0])[z] = 0u;
     if constexpr (kTC) {
         if (warp == 0) {
             tmem_alloc(smem_u32(&c->tmem_base), kTmemCols);
@@ -492,68 +575,44 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     __syncthreads();
     if constexpr (kTC) tc_fence_after();
     const uint32_t tmem = kTC ? c->tmem_base : 0u;
-
-    // ------------------------- weight stream starts before the PDL wait --
-    uint64_t pol = 0;
-    const int npre = nchunks < R ? nchunks : R;
-    if (warp == 4 && lane == 0) {
-        pol = policy_evict_first();
-        for (int j = 0; j < npre; ++j)
-            issue_weights(P, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk),
-                          Wr + static_cast<size_t>(j) * kChunk * kTileBytes, smem_u32(&c->wfull[j]), pol);
-    }
-    __syncwarp();
     pdl_launch_dependents();
 
-    // --------------------------------------------- activation row absmax --
-    const bool amax_thread = warp < 4 || warp >= 6;
-    if (amax_thread) {
-        pdl_wait();  // activations may be written by the previous kernel on the stream
-        local_amax(P, c, p0, p1, warp < 4 ? tid : tid - 64);
-    }
-    __syncthreads();
-    if (tid < BITMTP_MAX_GROUP * 16) {
-        const int lp = tid / 16, m = tid % 16;
-        (&c->qscale[0][0])[tid] = quant_scale(__uint_as_float(c->amax[lp][m]));
-    }
-    __syncthreads();
+    const int npre = nchunks < R ? nchunks : R;
+    int w_issued = 0, b_issued = 0;  // chunks whose copies were requested (warp 4, lane 0)
 
     // -------------------------------------------------------- main loop --
     if (warp == 4) {
-        // weight producer: refill ring slots as they are released
         if (lane == 0) {
+            // weights first: they do not depend on the kernels before this one
+            const uint64_t pol = policy_evict_first();
+            for (int j = 0; j < npre; ++j)
+                issue_weights(P, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk),
+                              Wr + static_cast<size_t>(j) * kChunk * kTileBytes, smem_u32(&c->wfull[j]), pol);
+            w_issued = npre;
+            pdl_wait();  // the activation tiles are written by the preparation kernel
+            const uint64_t pol_b = policy_evict_last();
+            for (int j = 0; j < npre; ++j)
+                issue_acts(P, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk), BT,
+                           Br + static_cast<size_t>(j) * kChunk * BT, smem_u32(&c->bfull[j]), pol_b);
+            b_issued = npre;
+            // refill ring slots as they are released
             for (int j = npre; j < nchunks; ++j) {
                 const int q = j % R;
                 if (!mbar_wait_bounded(smem_u32(&c->empty[q]), ((j / R) - 1) & 1)) {
                     fail(c, P.err, kErrWaitEmpty);
                     break;
                 }
-                issue_weights(P, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk),
-                              Wr + static_cast<size_t>(q) * kChunk * kTileBytes, smem_u32(&c->wfull[q]), pol);
+                const long long first = t_begin + static_cast<long long>(j) * kChunk;
+                const int cnt = min(kChunk, nloc - j * kChunk);
+                issue_weights(P, first, cnt, Wr + static_cast<size_t>(q) * kChunk * kTileBytes,
+                              smem_u32(&c->wfull[q]), pol);
+                w_issued = j + 1;
+                issue_acts(P, first, cnt, BT, Br + static_cast<size_t>(q) * kChunk * BT, smem_u32(&c->bfull[q]),
+                           pol_b);
+                b_issued = j + 1;
             }
         }
         __syncwarp();
-    } else if (warp >= 6) {
-        // activation builders: run up to R chunks ahead of the consumers
-        const int bt = tid - 192;
-        TileIter it;
-        it.pi = it.rt = it.kt = 0;
-        if (nloc > 0) it.init(P, t_begin);
-        // A timed-out wait only clears `alive`; both builder warps still execute
-        // every named barrier of build_chunk.
-        bool alive = true;
-        for (int j = 0; j < nchunks; ++j) {
-            const int q = j % R;
-            const int cnt = min(kChunk, nloc - j * kChunk);
-            if (alive && j >= R) {
-                alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->empty[q]), ((j / R) - 1) & 1));
-                if (!alive && lane == 0) fail(c, P.err, kErrWaitEmpty);
-            }
-            build_chunk<PATH, DPR>(P, c, it, p0, cnt, q, Br + static_cast<size_t>(q) * kChunk * BT, bt, alive);
-            __syncwarp();
-            if (alive && lane == 0) mbar_arrive(smem_u32(&c->bfull[q]));
-            for (int k = 0; k < cnt; ++k) it.next(P);
-        }
     } else if (warp == 5) {
         if constexpr (kTC) {
             if (lane == 0 && nloc > 0) {
@@ -601,15 +660,20 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     } else {
         // warps 0-3: one output row per thread.  A failed (timed-out) wait only
         // clears `alive`; every named barrier is still executed by all four warps.
+        pdl_wait();  // outputs and workspace: the preparation kernel has finished
+        for (int z = tid; z < (p1 - p0 + 1) * 16; z += 128) {
+            const GemmProblem& pr = P.p[p0 + z / 16];
+            c->asc[z / 16][z % 16] = (z % 16 < pr.M) ? __ldcg(pr.asc + z % 16) : 0.f;
+        }
+        named_bar_sync(1, 128);
         TileIter it;
         it.pi = it.rt = it.kt = 0;
         if (nloc > 0) it.init(P, t_begin);
         int ka = it.kt, seg_idx = 0, seg_first_i = 0;
         Pending pend[2];
         int npend = 0;
-        int rsum[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) rsum[m] = 0;
+        int rq[16];
+        if (nloc > 0) segment_code_sums(P.p[it.pi], ka, min(P.p[it.pi].kt, ka + nloc), rq);
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         int dacc[4][DPR];
 #pragma unroll
@@ -626,14 +690,12 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             if (alive && chunk_first) {
                 alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[q]), (j / R) & 1));
                 if (!alive && lane == 0) fail(c, P.err, kErrWaitW);
-                if (alive) {
-                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[q]), (j / R) & 1));
-                    if (!alive && lane == 0) fail(c, P.err, kErrWaitB);
+                if constexpr (!kTC) {
+                    if (alive) {
+                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[q]), (j / R) & 1));
+                        if (!alive && lane == 0) fail(c, P.err, kErrWaitB);
+                    }
                 }
-            }
-            if (alive) {
-#pragma unroll
-                for (int m = 0; m < 16; ++m) rsum[m] += c->rs[s][m];
             }
             const uint8_t* wst = Wr + static_cast<size_t>(s) * kTileBytes;
             if constexpr (kTC) {
@@ -705,24 +767,24 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         tc_fence_before();
 #pragma unroll
                         for (int m = 0; m < 16; ++m)
-                            acc[m] = __float2int_rn(__uint_as_float(v[m]) * 32768.f) - rsum[m];
+                            acc[m] = __float2int_rn(__uint_as_float(v[m]) * 32768.f) - rq[m];
                     }
                 } else {
 #pragma unroll
                     for (int m = 0; m < DPR; ++m) {
-                        acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) - rsum[m];
+                        acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) - rq[m];
                         dacc[0][m] = dacc[1][m] = dacc[2][m] = dacc[3][m] = 0;
                     }
                 }
                 segment_epilogue(P, c, p0, it.pi, it.rt, ka, it.kt + 1, seg_first_i == 0, acc, tid, alive, pend,
                                  npend);
-#pragma unroll
-                for (int m = 0; m < 16; ++m) rsum[m] = 0;
                 ++seg_idx;
                 seg_first_i = i + 1;
                 ka = 0;
             }
             it.next(P);
+            if (seg_last && i + 1 < nloc)  // the next segment starts at k tile 0 of the next row tile
+                segment_code_sums(P.p[it.pi], 0, min(P.p[it.pi].kt, nloc - (i + 1)), rq);
         }
         finish_pending(P, c, p0, pend, npend, tid, alive);
     }
@@ -730,8 +792,14 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     // ------------------------------------------------------- tear-down --
     __syncthreads();
     if (warp == 4 && lane == 0 && c->failed) {
-        // never release shared memory with a bulk copy still in flight
-        for (int q = 0; q < npre; ++q) (void)mbar_wait_bounded(smem_u32(&c->wfull[q]), 0, 100000000ull);
+        // never release shared memory with a bulk copy still in flight: wait
+        // (bounded) for the last requested phase of every slot
+        for (int q = 0; q < R; ++q) {
+            if (q < w_issued)
+                (void)mbar_wait_bounded(smem_u32(&c->wfull[q]), ((w_issued - 1 - q) / R) & 1, 100000000ull);
+            if (q < b_issued)
+                (void)mbar_wait_bounded(smem_u32(&c->bfull[q]), ((b_issued - 1 - q) / R) & 1, 100000000ull);
+        }
     }
     if constexpr (kTC) {
         tc_fence_before();
@@ -741,6 +809,13 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             tmem_dealloc(tmem, kTmemCols);
         }
     }
+}
+
+cudaLaunchAttribute pdl_attr() {
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
 }
 
 template <int PATH, int DPR>
@@ -756,20 +831,25 @@ cudaError_t launch_one(const GemmParams& prm, bool pdl, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
+    cudaLaunchAttribute attr[1] = {pdl_attr()};
+
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3(static_cast<unsigned>(prm.n_problems * btile_rows(PATH, DPR)), 1, 1);
+    pc.blockDim = dim3(kPrepThreads, 1, 1);
+    pc.dynamicSmemBytes = 0;
+    pc.stream = stream;
+    pc.attrs = attr;
+    pc.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&pc, &act_prep_kernel<PATH, DPR>, prm);
+    if (e != cudaSuccess) return e;
+
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(prm.nctas), 1, 1);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = gemm_smem_bytes(PATH, DPR, prm.stages);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    int na = 0;
-    if (pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
     cfg.attrs = attr;
-    cfg.numAttrs = na;
+    cfg.numAttrs = 1;  // overlaps the preparation kernel: only weights are read before its wait
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 

@@ -10,7 +10,7 @@ namespace bitmtp {
 constexpr int kTileN = 128;       // out-features per row tile (= TMEM lanes)
 constexpr int kTileK = 128;       // in-features per k tile
 constexpr int kTileBytes = 4096;  // packed bytes per (row tile, k tile)
-constexpr int kGemmThreads = 256; // warps 0-3 compute, 4 bulk copies, 5 MMA issue, 6-7 activation builders
+constexpr int kGemmThreads = 192; // warps 0-3 compute + epilogue, 4 bulk copies, 5 MMA issue
 constexpr int kCtasPerSm = 2;     // persistent CTAs per SM
 
 // Compute paths.  The activation operand ("B tile", one per k tile) is laid
@@ -34,6 +34,10 @@ struct GemmProblem {
     int act_kind;             // BITMTP_F32 / BITMTP_BF16 / BITMTP_Q8
     int out_dtype;            // BITMTP_F32 / BITMTP_BF16
     long long tile_begin;     // first flattened (row tile, k tile) index of this problem
+    // Activation operand in the workspace, written by the preparation kernel:
+    uint8_t* actb;            // [kt] tiles in the compute path's layout
+    int* rsp;                 // [16][kt + 1] prefix sums over k tiles of each row's codes
+    float* asc;               // [16] per-row dequant scales (amax / 127)
 };
 
 struct GemmParams {
@@ -50,15 +54,23 @@ struct GemmParams {
 constexpr int kMaxCtas = 320;         // persistent CTAs per launch (>= 2 per SM on GB300)
 constexpr int kMinTilesPerCta = 4;    // fewer CTAs on small problems: fewer split row tiles
 
-// Workspace: a fixed layout, independent of the shapes.
+// Workspace: split-row-tile counters and partial-sum slots at fixed offsets,
+// then one activation region per problem (sized by its k tiles).
+constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 constexpr size_t kWsCounters = 256;
-constexpr size_t kWsSlots = kWsCounters + ((static_cast<size_t>(kMaxCtas) * 4 + 255) & ~static_cast<size_t>(255));
-constexpr size_t kWsBytes = kWsSlots + static_cast<size_t>(kMaxCtas) * 2 * 16 * kTileN * 4;
+constexpr size_t kWsSlots = kWsCounters + align256(static_cast<size_t>(kMaxCtas) * 4);
+constexpr size_t kWsAct = kWsSlots + static_cast<size_t>(kMaxCtas) * 2 * 16 * kTileN * 4;
+constexpr size_t act_tiles_bytes(int kt) { return align256(static_cast<size_t>(kt) * 4096); }
+constexpr size_t act_rsp_bytes(int kt) { return align256(static_cast<size_t>(16) * (kt + 1) * 4); }
+constexpr size_t act_region_bytes(int kt) { return act_tiles_bytes(kt) + act_rsp_bytes(kt) + 256; }
 
 size_t gemm_smem_bytes(int path, int dp_rows, int stages);
 int gemm_stages(int path, int dp_rows);
 
-// Launch the stream-K GEMM kernel (params validated and filled).
+// Launch the activation preparation kernel, then the stream-K GEMM kernel
+// (params validated and filled).  `pdl` lets the preparation kernel overlap
+// the kernel before it on the stream; the GEMM always overlaps the
+// preparation kernel (it only streams weights before waiting for it).
 cudaError_t launch_gemm(const GemmParams& prm, int path, int dp_rows, bool pdl, cudaStream_t stream);
 
 }  // namespace bitmtp

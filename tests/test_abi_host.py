@@ -116,11 +116,15 @@ def test_workspace_bytes(lib):
     wb = L.bitmtp_linear_workspace_bytes
     assert wb(0, 64, 4) == 0 and wb(64, 0, 4) == 0 and wb(64, 64, 0) == 0 and wb(64, 64, 17) == 0
     small, big = wb(128, 128, 1), wb(32000, 2560, 16)
-    # fixed layout: split-row-tile slots and counters for the largest grid
-    assert small == big and small >= 320 * 2 * 16 * 128 * 4
+    # split-row-tile slots and counters for the largest grid, plus one
+    # activation region (4 KiB per k tile, prefix sums, scales) per problem
+    assert small >= 320 * 2 * 16 * 128 * 4
+    assert big - small == 19 * 4096 + (16 * 21 * 4 + 255) // 256 * 256 - 256
+    assert wb(32000, 2560, 1) == big == wb(5, 2560, 16)   # depends on K only
     d = [L.GemmDesc(FAKE, 0.02, 2560, 2560, 8, _act(ldx=2560), _out(ldy=2560)),
          L.GemmDesc(FAKE, 0.02, 640, 2560, 8, _act(ldx=2560), _out(ldy=640))]
-    assert L.bitmtp_linear_workspace_bytes_grouped(d) == small
+    one = wb(2560, 2560, 8)
+    assert L.bitmtp_linear_workspace_bytes_grouped(d) == 2 * one - (small - (4096 + 256 + 256))
     bad = [L.GemmDesc(FAKE, 0.02, 2560, 2560, 20, _act(ldx=2560), _out(ldy=2560))]
     assert L.bitmtp_linear_workspace_bytes_grouped(bad) == 0
 
@@ -134,7 +138,7 @@ def test_noalloc_validation(lib):
     assert na(FAKE, 0.02, 64, 64, 0, _act(), _out(), 0, None) == L.OK
     # the built-in array covers the workspace of every shape inside the limits
     assert L.bitmtp_linear_workspace_bytes(L.MAX_N, L.MAX_K, L.MAX_M) <= L.NOALLOC_SCRATCH_BYTES
-    assert "NOALLOC_SCRATCH_BYTES ((size_t)5 * 1024 * 1024 + 4096)" in open(L.HEADER_PATH).read()
+    assert "NOALLOC_SCRATCH_BYTES ((size_t)13 * 512 * 1024)" in open(L.HEADER_PATH).read()
 
 
 def test_pack_and_quant_validation(lib):
