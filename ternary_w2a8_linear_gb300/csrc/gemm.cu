@@ -28,20 +28,26 @@
 //     warp 5      (tensor path) issues tcgen05.mma.
 //
 // Compute paths (the same 2-bit code words feed both):
-//   tensor (kPathTC16 / kPathTC8): each thread turns its code words into fp16
-//     bit patterns with one mask per register -- the 2-bit code u lands in the
-//     fp16 subnormal range, value u * 4^J * 2^-24 -- and writes them to tensor
-//     memory as the A operand (tcgen05.st, seven buffers in flight); one thread
-//     issues tcgen05.mma kind::f16 (M=128, N=16, K=16) against the activation
-//     tile in shared memory, whose fp16 entries are q * 2^(9-2J).  Every
-//     product is u*q*2^-15 and every partial sum an integer multiple of 2^-15
-//     below 2^9, so the fp32 accumulator is exact in any order.  kPathTC8 keeps
-//     8 activation rows (the second row group aliases the first through a zero
-//     stride).
+//   tensor (kPathTC16 / kPathTC8): each thread turns its code words into e4m3
+//     bytes with one shift and one mask per register -- the 2-bit code u is
+//     the mantissa of an e4m3 subnormal, value u * 2^-9 -- and writes them to
+//     tensor memory as the A operand (tcgen05.st, seven k-tile buffers in
+//     flight).  The activation operand splits every code exactly as
+//     q = 16*h + l (h in [-8, 7], l in [0, 15], both exact in e4m3) into two
+//     operand rows, so one tcgen05.mma kind::f8f6f4 (M=128, K=32, N = twice the
+//     activation rows: 32 or 16) yields both halves.  Products are integers
+//     times 2^-9 and every sum stays below 2^24 of those units, so the fp32
+//     accumulator is exact; the epilogue forms 2^9 * (16*D_h + D_l).  One
+//     thread issues the MMAs, two k tiles (eight MMAs, straight-line code)
+//     per wait: a branch or a wait between tcgen05.mma issues costs more than
+//     the MMAs themselves.
 //   dp4a (kPathDP): four byte masks per code word, four int32 accumulators
 //     per row (scales 4^s, recombined with exact shifts).
 // With u = T + 1, sum_k T*q = sum_k u*q - sum_k q; the second sum comes from
-// the preparation kernel's prefix sums.
+// the preparation kernel's prefix sums.  Both paths store the activation
+// operand in units of 16 k: per operand row 16 bytes, byte 4s + b holding
+// k = {2s, 2s+8, 2s+1, 2s+9}[b] of the unit -- the order in which one shift
+// and mask per register lays out the code word.
 //
 // The operation is the packed W2A8 linear of "BitMTP: When Multi-Token
 // Prediction Meets Low-Bit Large Language Models" (AI summary: Main Findings,
@@ -63,12 +69,14 @@ constexpr int kChunk = 4;            // k tiles per ring chunk (16 KiB of weight
 constexpr int kMaxRing = 6;          // chunks in the ring (upper bound)
 constexpr int kCtrlBytes = 1024;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kAccCol = 0;      // D: 16 fp32 columns, one per activation row
-constexpr uint32_t kACol = 32;       // A: kABufs buffers of 32 columns (64 k each)
-constexpr int kABufs = 7;
-constexpr uint32_t kIdesc = idesc_f16_f32(128, 16);
+constexpr uint32_t kAccCol = 0;      // D: one fp32 column per operand row (at most 32)
+constexpr uint32_t kACol = 32;       // A: kATiles buffers of one k tile each
+constexpr uint32_t kATileCols = 32;  // 128 k, one e4m3 byte each
+constexpr int kATiles = 7;
+constexpr int kMmaBatch = 2;         // k tiles per MMA-issuer wait
 constexpr int kSmemTarget = 100 * 1024;
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 512;
+constexpr int kPrepGroups = 8;     // 8-element groups of one row per preparation thread
 
 enum : int {
     kErrWaitW = 0x101,
@@ -83,8 +91,8 @@ struct Ctrl {
     uint64_t wfull[kMaxRing];     // weight tiles of the chunk landed
     uint64_t bfull[kMaxRing];     // activation tiles of the chunk landed
     uint64_t empty[kMaxRing];     // chunk slot free again (MMA commit / dp4a consumers)
-    uint64_t a_full[kABufs];
-    uint64_t a_empty[kABufs];
+    uint64_t a_full[kATiles];     // A buffer written (four consumer warps)
+    uint64_t a_empty[kATiles];    // A buffer free again (MMA commit)
     uint64_t dfull;
     uint32_t tmem_base;
     int failed;
@@ -93,36 +101,63 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
-__host__ __device__ constexpr int btile_bytes(int path, int dp_rows) {
-    return path == kPathTC16 ? 4096 : path == kPathTC8 ? 2048 : dp_rows * 128;
-}
-__host__ __device__ constexpr int btile_lbo(int path) { return path == kPathTC16 ? 256 : 128; }
-__host__ __device__ constexpr int btile_sbo(int path) { return path == kPathTC16 ? 128 : 0; }
 // Activation rows an operand tile holds (rows from M on are zero).
 __host__ __device__ constexpr int btile_rows(int path, int dp_rows) {
     return path == kPathTC16 ? 16 : path == kPathTC8 ? 8 : dp_rows;
 }
-
-// fp16 pre-scale shift of the activation for A column c (J = 0,1,2,3,4,0,1,2).
-__device__ __forceinline__ int bscale_shift(int c) { return 9 - 2 * ((c < 5) ? c : (c - 5)); }
+// Operand rows: the tensor paths keep two (h and l) per activation row.
+__host__ __device__ constexpr int btile_brows(int path, int dp_rows) {
+    return path == kPathDP ? dp_rows : 2 * btile_rows(path, dp_rows);
+}
+// Bytes of one k tile of the activation operand: 8 units of 16 k, each
+// holding 16 bytes per operand row.
+__host__ __device__ constexpr int btile_bytes(int path, int dp_rows) { return btile_brows(path, dp_rows) * 128; }
 
 __device__ __forceinline__ void fail(Ctrl* c, int* err, int code) {
     *reinterpret_cast<volatile int*>(&c->failed) = 1;
     atomicCAS(err, 0, code);
 }
 
-// One code word -> eight fp16x2 registers (A columns c = 0..7; half e of
-// column c is k = 2c + e of the word).
-__device__ __forceinline__ void unpack_word_f16(uint32_t w, uint32_t* r) {
-    r[0] = w & 0x00030003u;
-    r[1] = w & 0x000C000Cu;
-    r[2] = w & 0x00300030u;
-    r[3] = w & 0x00C000C0u;
-    r[4] = w & 0x03000300u;
-    const uint32_t t = w >> 10;
-    r[5] = t & 0x00030003u;
-    r[6] = t & 0x000C000Cu;
-    r[7] = t & 0x00300030u;
+// One code word (16 k) -> four registers of e4m3 bytes u * 2^-9: register s,
+// byte b holds k = {2s, 2s+8, 2s+1, 2s+9}[b] of the word.
+__device__ __forceinline__ void unpack_word_e4m3(uint32_t w, uint32_t* r) {
+    r[0] = w & 0x03030303u;
+    r[1] = (w >> 2) & 0x03030303u;
+    r[2] = (w >> 4) & 0x03030303u;
+    r[3] = (w >> 6) & 0x03030303u;
+}
+
+// e4m3 bit pattern of an integer v with |v| <= 15 (exact: sign, exponent
+// floor(log2|v|) + 7, three mantissa bits).
+__device__ __forceinline__ uint32_t e4m3_small_int(int v) {
+    const uint32_t a = static_cast<uint32_t>(v < 0 ? -v : v);
+    if (a == 0) return 0u;
+    const int e = 31 - __clz(static_cast<int>(a));
+    return (v < 0 ? 0x80u : 0u) | (static_cast<uint32_t>(e + 7) << 3) | (((a << 3) >> e) & 7u);
+}
+
+// Bytes (low 8 bits of each value) of eight values, as two words.
+__device__ __forceinline__ void bytes8(const uint32_t (&b)[8], uint32_t& lo, uint32_t& hi) {
+    lo = (b[0] & 0xFFu) | ((b[1] & 0xFFu) << 8) | ((b[2] & 0xFFu) << 16) | (b[3] << 24);
+    hi = (b[4] & 0xFFu) | ((b[5] & 0xFFu) << 8) | ((b[6] & 0xFFu) << 16) | (b[7] << 24);
+}
+
+// One 16-k unit of one operand row from the bytes of k 0..7 (lo, hi: this
+// lane) and k 8..15 (plo, phi: the partner lane), in the unit byte order.
+__device__ __forceinline__ uint4 unit16(uint32_t lo, uint32_t hi, uint32_t plo, uint32_t phi) {
+    uint32_t b[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        b[i] = (lo >> (8 * i)) & 0xFFu;
+        b[4 + i] = (hi >> (8 * i)) & 0xFFu;
+        b[8 + i] = (plo >> (8 * i)) & 0xFFu;
+        b[12 + i] = (phi >> (8 * i)) & 0xFFu;
+    }
+    uint32_t reg[4];
+#pragma unroll
+    for (int si = 0; si < 4; ++si)
+        reg[si] = b[2 * si] | (b[8 + 2 * si] << 8) | (b[2 * si + 1] << 16) | (b[9 + 2 * si] << 24);
+    return make_uint4(reg[0], reg[1], reg[2], reg[3]);
 }
 
 __device__ __forceinline__ int find_problem_by_tile(const GemmParams& P, long long t) {
@@ -158,6 +193,34 @@ struct TileIter {
             }
         }
     }
+};
+
+// Position of local tile i in the chunk ring and in the A buffers, advanced
+// one tile at a time (no division by the runtime ring size on the way to an
+// MMA issue or a barrier wait).
+struct RingPos {
+    int cp;          // i % kChunk
+    int q;           // (i / kChunk) % R: ring slot of the chunk
+    uint32_t qph;    // ((i / kChunk) / R) & 1: phase of that slot's barriers
+    int ab;          // i % kATiles: A buffer
+    uint32_t abph;   // (i / kATiles) & 1
+    int i;
+    __device__ void reset() { cp = q = ab = i = 0; qph = abph = 0u; }
+    __device__ void next(int R) {
+        ++i;
+        if (++cp == kChunk) {
+            cp = 0;
+            if (++q == R) {
+                q = 0;
+                qph ^= 1u;
+            }
+        }
+        if (++ab == kATiles) {
+            ab = 0;
+            abph ^= 1u;
+        }
+    }
+    __device__ int slot() const { return q * kChunk + cp; }  // tile slot in the ring
 };
 
 // Bulk-copy the weight tiles of tiles [first, first + count) of this CTA's
@@ -264,12 +327,17 @@ __device__ __forceinline__ const char* act_row(const GemmProblem& pr, int m) {
 // ---------------------------------------------------- activation operand --
 // One CTA per (problem, row m < btile_rows).  Writes row m of every
 // activation tile of the problem (zeros for m >= M and beyond K), the prefix
-// sums rsp[m][0..kt] of the row's codes over k tiles, and asc[m].
+// sums rsp[m][0..kt] of the row's codes over k tiles, and asc[m].  The whole
+// row stays in registers between the absmax and the quantisation (at most
+// kPrepGroups 8-element groups per thread: K <= 32768 with 512 threads), so
+// the row is read once, with all loads in flight together.
 template <int PATH, int DPR>
-__global__ void __launch_bounds__(kPrepThreads)
+__global__ void __launch_bounds__(kPrepThreads, 1)
 act_prep_kernel(const __grid_constant__ GemmParams P) {
     constexpr int kRows = btile_rows(PATH, DPR);
+    constexpr int kBRows = btile_brows(PATH, DPR);
     constexpr int BT = btile_bytes(PATH, DPR);
+    static_assert(kPrepThreads * kPrepGroups * 8 >= BITMTP_MAX_K, "row does not fit the registers");
     __shared__ float red[kPrepThreads / 32];
     __shared__ int tsum[BITMTP_MAX_K / kTileK];
     pdl_launch_dependents();  // the GEMM may start streaming weights now
@@ -288,25 +356,23 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     // previous GEMM on this workspace may still be reading it.
     pdl_wait();
 
-    float amax = 0.f;
-    if (live && raw) {
-        for (int g0 = 0; g0 < ngroups; g0 += kPrepThreads * 4) {
-            float v[4][8];
+    float v[kPrepGroups][8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int g = g0 + j * kPrepThreads + tid;
-                if (g < ngroups) {
-                    load8(pr, row, vec_ok, g * 8, v[j]);
-                } else {
+    for (int j = 0; j < kPrepGroups; ++j) {
+        const int g = j * kPrepThreads + tid;
+        if (live && g < ngroups) {
+            load8(pr, row, vec_ok, g * 8, v[j]);
+        } else {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
+            for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
         }
+    }
+    float amax = 0.f;
+    if (raw) {
+#pragma unroll
+        for (int j = 0; j < kPrepGroups; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -317,66 +383,47 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
     const float s = quant_scale(amax);
 
-    // Each group of 16 consecutive threads covers one k tile: ngroups is a
-    // multiple of 16, so the shuffles below always see whole groups.
-    for (int g0 = 0; g0 < ngroups; g0 += kPrepThreads) {
-        const int g = g0 + tid;
-        const bool gv = g < ngroups;
-        float v[8];
-        if (live && gv) {
-            load8(pr, row, vec_ok, g * 8, v);
-        } else {
+    // Each group of 16 consecutive threads covers one k tile: ngroups and
+    // kPrepThreads are multiples of 16, so the shuffles below always see
+    // whole groups.
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = 0.f;
-        }
+    for (int j = 0; j < kPrepGroups; ++j) {
+        if (j * kPrepThreads >= ngroups) break;  // uniform over the block
+        const int g = j * kPrepThreads + tid;
+        const bool gv = g < ngroups;
         int qv[8];
         int rsum = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            qv[i] = !live ? 0 : raw ? ((amax > 0.f) ? quantize(v[i], s) : 0) : static_cast<int>(v[i]);
+            qv[i] = raw ? ((amax > 0.f) ? quantize(v[j][i], s) : 0) : static_cast<int>(v[j][i]);
             rsum += qv[i];
         }
         const int kt = g >> 4, gg = g & 15;
-        uint8_t* tile = pr.actb + static_cast<size_t>(kt) * BT;
+        uint8_t* unit = pr.actb + static_cast<size_t>(kt) * BT + (gg >> 1) * (kBRows * 16);
+        // operand row m holds the codes (dp4a) or, on the tensor paths, the
+        // high parts h = q >> 4 (row m) and low parts l = q & 15 (row m + kRows)
+        uint32_t ba[8], bb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if constexpr (PATH == kPathDP) {
+                ba[i] = static_cast<uint32_t>(qv[i]);
+                bb[i] = 0u;
+            } else {
+                ba[i] = e4m3_small_int(qv[i] >> 4);
+                bb[i] = e4m3_small_int(qv[i] & 15);
+            }
+        }
+        uint32_t alo, ahi;
+        bytes8(ba, alo, ahi);
+        const uint32_t palo = __shfl_xor_sync(0xffffffffu, alo, 1);
+        const uint32_t pahi = __shfl_xor_sync(0xffffffffu, ahi, 1);
+        if (gv && (gg & 1) == 0) *reinterpret_cast<uint4*>(unit + m * 16) = unit16(alo, ahi, palo, pahi);
         if constexpr (PATH != kPathDP) {
-            if (gv) {
-                uint32_t packed[4];
-#pragma unroll
-                for (int i = 0; i < 8; i += 2) {
-                    const int sh = bscale_shift((gg & 1) * 4 + (i >> 1));
-                    const __half h0 = __int2half_rn(qv[i] * (1 << sh));
-                    const __half h1 = __int2half_rn(qv[i + 1] * (1 << sh));
-                    packed[i >> 1] = static_cast<uint32_t>(__half_as_ushort(h0)) |
-                                     (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-                }
-                *reinterpret_cast<uint4*>(tile + gg * btile_lbo(PATH) + (m >> 3) * btile_sbo(PATH) + (m & 7) * 16) =
-                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            }
-        } else {
-            // A 16-k unit is two 8-groups (lanes 2i, 2i+1): the even lane
-            // interleaves its partner's codes with its own.
-            const uint32_t lo = (static_cast<uint32_t>(qv[0]) & 0xFFu) | ((static_cast<uint32_t>(qv[1]) & 0xFFu) << 8) |
-                                ((static_cast<uint32_t>(qv[2]) & 0xFFu) << 16) | (static_cast<uint32_t>(qv[3]) << 24);
-            const uint32_t hi = (static_cast<uint32_t>(qv[4]) & 0xFFu) | ((static_cast<uint32_t>(qv[5]) & 0xFFu) << 8) |
-                                ((static_cast<uint32_t>(qv[6]) & 0xFFu) << 16) | (static_cast<uint32_t>(qv[7]) << 24);
-            const uint32_t plo = __shfl_xor_sync(0xffffffffu, lo, 1);
-            const uint32_t phi = __shfl_xor_sync(0xffffffffu, hi, 1);
-            if (gv && (gg & 1) == 0) {
-                uint32_t b[16];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    b[i] = (lo >> (8 * i)) & 0xFFu;
-                    b[4 + i] = (hi >> (8 * i)) & 0xFFu;
-                    b[8 + i] = (plo >> (8 * i)) & 0xFFu;
-                    b[12 + i] = (phi >> (8 * i)) & 0xFFu;
-                }
-                uint32_t reg[4];
-#pragma unroll
-                for (int si = 0; si < 4; ++si)
-                    reg[si] = b[2 * si] | (b[8 + 2 * si] << 8) | (b[2 * si + 1] << 16) | (b[9 + 2 * si] << 24);
-                *reinterpret_cast<uint4*>(tile + (gg >> 1) * (DPR * 16) + m * 16) =
-                    make_uint4(reg[0], reg[1], reg[2], reg[3]);
-            }
+            uint32_t blo, bhi;
+            bytes8(bb, blo, bhi);
+            const uint32_t pblo = __shfl_xor_sync(0xffffffffu, blo, 1);
+            const uint32_t pbhi = __shfl_xor_sync(0xffffffffu, bhi, 1);
+            if (gv && (gg & 1) == 0) *reinterpret_cast<uint4*>(unit + (m + kRows) * 16) = unit16(blo, bhi, pblo, pbhi);
         }
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, o);
@@ -469,17 +516,17 @@ __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int
 __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pending* pend, int npend, int tid,
                                bool alive) {
     if (npend == 0) return;  // uniform across the four warps
-    __threadfence();
-    named_bar_sync(1, 128);
+    named_bar_sync(1, 128);  // every slot store of this CTA is issued
     if (tid == 0) {
+        __threadfence();     // ... and made visible before the counters move
         for (int k = 0; k < npend; ++k) {
             const unsigned old = atomicAdd(P.counters + pend[k].b_last, 1u);
             c->flag[k] = (old == static_cast<unsigned>(pend[k].b_last - pend[k].b_first)) ? 1 : 0;
         }
+        __threadfence();     // the last contributor then sees every other slot
     }
     named_bar_sync(1, 128);
     const int last0 = c->flag[0], last1 = npend > 1 ? c->flag[1] : 0;
-    if (last0 | last1) __threadfence();
     const long long T = P.total_tiles;
     for (int k = 0; k < npend; ++k) {
         if (!(k == 0 ? last0 : last1)) continue;
@@ -518,14 +565,17 @@ __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pendi
     named_bar_sync(1, 128);
 }
 
-// Codes of rows 0..15 summed over k tiles [ka, kb) of problem pr (zero for
-// rows >= M); read from the preparation kernel's prefix sums.
-__device__ __forceinline__ void segment_code_sums(const GemmProblem& pr, int ka, int kb, int (&rq)[16]) {
+// The preparation kernel's prefix sums of rows 0..15 at k tiles ka and kb
+// (zero for rows >= M): their difference is the codes of k tiles [ka, kb)
+// summed.  Issued at the start of a segment, used at its end.
+__device__ __forceinline__ void load_code_sums(const GemmProblem& pr, int ka, int kb, int (&lo)[16], int (&hi)[16]) {
     const int* rsp = pr.rsp;
     const int stride = pr.kt + 1;
 #pragma unroll
-    for (int m = 0; m < 16; ++m)
-        rq[m] = (m < pr.M) ? __ldcg(rsp + m * stride + kb) - __ldcg(rsp + m * stride + ka) : 0;
+    for (int m = 0; m < 16; ++m) {
+        lo[m] = (m < pr.M) ? __ldcg(rsp + m * stride + ka) : 0;
+        hi[m] = (m < pr.M) ? __ldcg(rsp + m * stride + kb) : 0;
+    }
 }
 
 template <int PATH, int DPR>
@@ -557,7 +607,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             mbar_init(smem_u32(&c->bfull[q]), 1);
             mbar_init(smem_u32(&c->empty[q]), kTC ? 1 : 4);
         }
-        for (int a = 0; a < kABufs; ++a) {
+        for (int a = 0; a < kATiles; ++a) {
             mbar_init(smem_u32(&c->a_full[a]), 4);
             mbar_init(smem_u32(&c->a_empty[a]), 1);
         }
@@ -615,125 +665,156 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         __syncwarp();
     } else if (warp == 5) {
         if constexpr (kTC) {
-            if (lane == 0 && nloc > 0) {
+            if (lane == 0) {
+                // Segment by segment (k tiles of one row tile) in batches of up
+                // to kMmaBatch tiles: one wait (the batch's last A buffer: the
+                // consumer warps fill buffers in order), then the batch's MMAs
+                // as straight-line code, then the commits.
+                constexpr int kBR = btile_brows(PATH, DPR);
+                constexpr uint32_t kIdesc = idesc_f16_f32(128, kBR);
+                constexpr uint32_t kUnit = kBR * 16;      // bytes of one 16-k unit
+                const uint32_t bbase = smem_u32(Br);
                 TileIter it;
                 it.init(P, t_begin);
-                const uint32_t bbase = smem_u32(Br);
-                bool seg_first = true;
+                RingPos rp;
+                rp.reset();
                 bool ok = true;
-                for (int i = 0; i < nloc && ok; ++i) {
-                    const int j = i / kChunk, q = j % R;
-                    const int s = q * kChunk + (i % kChunk);
-                    const bool seg_last = (i == nloc - 1) || (it.kt == P.p[it.pi].kt - 1);
-                    if ((i % kChunk) == 0 && !mbar_wait_bounded(smem_u32(&c->bfull[q]), (j / R) & 1)) {
-                        fail(c, P.err, kErrWaitB);
-                        break;
-                    }
-                    for (int h = 0; h < 2; ++h) {
-                        const int u = 2 * i + h;
-                        const int a = u % kABufs;
-                        if (!mbar_wait_bounded(smem_u32(&c->a_full[a]), (u / kABufs) & 1)) {
+                while (rp.i < nloc && ok) {
+                    const int len = min(P.p[it.pi].kt - it.kt, nloc - rp.i);
+                    for (int e = 0; e < len && ok;) {
+                        const int nb = min(kMmaBatch, len - e);
+                        RingPos r1 = rp;
+                        if (nb == 2) r1.next(R);
+                        // activation tiles of any chunk the batch enters
+                        if (rp.cp == 0 && !mbar_wait_bounded(smem_u32(&c->bfull[rp.q]), rp.qph)) ok = false;
+                        if (ok && nb == 2 && r1.cp == 0 && !mbar_wait_bounded(smem_u32(&c->bfull[r1.q]), r1.qph))
+                            ok = false;
+                        if (!ok) {
+                            fail(c, P.err, kErrWaitB);
+                            break;
+                        }
+                        if (!mbar_wait_bounded(smem_u32(&c->a_full[r1.ab]), r1.abph)) {
                             fail(c, P.err, kErrWaitAFull);
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) {
-                            const int ch = h * 4 + jj;  // 16-k chunk within the k tile
-                            const uint64_t bdesc = smem_desc_noswizzle(
-                                bbase + s * BT + ch * 2 * btile_lbo(PATH), btile_lbo(PATH), btile_sbo(PATH));
-                            mma_f16_ts(tmem + kAccCol, tmem + kACol + a * 32 + jj * 8, bdesc, kIdesc,
-                                       (seg_first && h == 0 && jj == 0) ? 0u : 1u);
+                        const uint32_t acc0 = e == 0 ? 0u : 1u;
+                        const uint64_t bd0 = smem_desc_noswizzle(bbase + rp.slot() * BT, kUnit, 128);
+                        const uint32_t a0 = tmem + kACol + rp.ab * kATileCols;
+                        // chunk cc of 32 k: A columns 8*cc, B units 2cc and 2cc+1
+                        mma_f8_ts(tmem + kAccCol, a0, bd0, kIdesc, acc0);
+                        mma_f8_ts(tmem + kAccCol, a0 + 8, bd0 + ((2 * kUnit) >> 4), kIdesc, 1u);
+                        mma_f8_ts(tmem + kAccCol, a0 + 16, bd0 + ((4 * kUnit) >> 4), kIdesc, 1u);
+                        mma_f8_ts(tmem + kAccCol, a0 + 24, bd0 + ((6 * kUnit) >> 4), kIdesc, 1u);
+                        if (nb == 2) {
+                            const uint64_t bd1 = smem_desc_noswizzle(bbase + r1.slot() * BT, kUnit, 128);
+                            const uint32_t a1 = tmem + kACol + r1.ab * kATileCols;
+                            mma_f8_ts(tmem + kAccCol, a1, bd1, kIdesc, 1u);
+                            mma_f8_ts(tmem + kAccCol, a1 + 8, bd1 + ((2 * kUnit) >> 4), kIdesc, 1u);
+                            mma_f8_ts(tmem + kAccCol, a1 + 16, bd1 + ((4 * kUnit) >> 4), kIdesc, 1u);
+                            mma_f8_ts(tmem + kAccCol, a1 + 24, bd1 + ((6 * kUnit) >> 4), kIdesc, 1u);
                         }
-                        mma_commit(smem_u32(&c->a_empty[a]));
+                        mma_commit(smem_u32(&c->a_empty[rp.ab]));
+                        if (rp.cp == kChunk - 1 || rp.i == nloc - 1) mma_commit(smem_u32(&c->empty[rp.q]));
+                        if (nb == 2) {
+                            mma_commit(smem_u32(&c->a_empty[r1.ab]));
+                            if (r1.cp == kChunk - 1 || r1.i == nloc - 1) mma_commit(smem_u32(&c->empty[r1.q]));
+                        }
+                        rp = r1;
+                        rp.next(R);
+                        e += nb;
                     }
                     if (!ok) break;
-                    if ((i % kChunk) == kChunk - 1 || i == nloc - 1) mma_commit(smem_u32(&c->empty[q]));
-                    if (seg_last) mma_commit(smem_u32(&c->dfull));
-                    seg_first = seg_last;
-                    it.next(P);
+                    mma_commit(smem_u32(&c->dfull));
+                    // next segment: k tile 0 of the next row tile
+                    it.kt = 0;
+                    if (++it.rt == P.p[it.pi].nt) {
+                        it.rt = 0;
+                        ++it.pi;
+                    }
                 }
             }
         }
         __syncwarp();
     } else {
-        // warps 0-3: one output row per thread.  A failed (timed-out) wait only
-        // clears `alive`; every named barrier is still executed by all four warps.
+        // warps 0-3: one output row per thread, segment by segment.  A failed
+        // (timed-out) wait only clears `alive`; every named barrier is still
+        // executed by all four warps.
         pdl_wait();  // outputs and workspace: the preparation kernel has finished
+        // dequant scales of problems p0..p1, first needed by the first epilogue
+        // (the named barrier there publishes them)
         for (int z = tid; z < (p1 - p0 + 1) * 16; z += 128) {
             const GemmProblem& pr = P.p[p0 + z / 16];
             c->asc[z / 16][z % 16] = (z % 16 < pr.M) ? __ldcg(pr.asc + z % 16) : 0.f;
         }
-        named_bar_sync(1, 128);
         TileIter it;
-        it.pi = it.rt = it.kt = 0;
-        if (nloc > 0) it.init(P, t_begin);
-        int ka = it.kt, seg_idx = 0, seg_first_i = 0;
+        it.init(P, t_begin);
         Pending pend[2];
         int npend = 0;
-        int rq[16];
-        if (nloc > 0) segment_code_sums(P.p[it.pi], ka, min(P.p[it.pi].kt, ka + nloc), rq);
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        int dacc[4][DPR];
-#pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4)
-#pragma unroll
-            for (int m = 0; m < DPR; ++m) dacc[s4][m] = 0;
         bool alive = true;
-        for (int i = 0; i < nloc; ++i) {
-            const int j = i / kChunk, q = j % R;
-            const int s = q * kChunk + (i % kChunk);
-            const bool chunk_first = (i % kChunk) == 0;
-            const bool chunk_last = (i % kChunk) == kChunk - 1 || i == nloc - 1;
-            const bool seg_last = (i == nloc - 1) || (it.kt == P.p[it.pi].kt - 1);
-            if (alive && chunk_first) {
-                alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[q]), (j / R) & 1));
-                if (!alive && lane == 0) fail(c, P.err, kErrWaitW);
-                if constexpr (!kTC) {
-                    if (alive) {
-                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[q]), (j / R) & 1));
-                        if (!alive && lane == 0) fail(c, P.err, kErrWaitB);
+        int seg_idx = 0;
+        RingPos rp;
+        rp.reset();
+        while (rp.i < nloc) {
+            const GemmProblem& pr = P.p[it.pi];
+            const int ka = it.kt;
+            const int len = min(pr.kt - ka, nloc - rp.i);
+            int rlo[16], rhi[16];
+            load_code_sums(pr, ka, ka + len, rlo, rhi);
+            int dacc[4][DPR];
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+                for (int m = 0; m < DPR; ++m) dacc[s4][m] = 0;
+            for (int e = 0; e < len; ++e, rp.next(R)) {
+                const int s = rp.slot();
+                if (alive && rp.cp == 0) {
+                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[rp.q]), rp.qph));
+                    if (!alive && lane == 0) fail(c, P.err, kErrWaitW);
+                    if constexpr (!kTC) {
+                        if (alive) {
+                            alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[rp.q]), rp.qph));
+                            if (!alive && lane == 0) fail(c, P.err, kErrWaitB);
+                        }
                     }
                 }
-            }
-            const uint8_t* wst = Wr + static_cast<size_t>(s) * kTileBytes;
-            if constexpr (kTC) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int u = 2 * i + h;
-                    const int a = u % kABufs;
-                    if (alive && u >= kABufs) {
-                        alive = __all_sync(0xffffffffu,
-                                           mbar_wait_bounded(smem_u32(&c->a_empty[a]), ((u / kABufs) - 1) & 1));
+                const uint8_t* wst = Wr + static_cast<size_t>(s) * kTileBytes;
+                if constexpr (kTC) {
+                    const int ab = rp.ab;
+                    if (alive && rp.i >= kATiles) {
+                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->a_empty[ab]), rp.abph ^ 1u));
                         if (!alive && lane == 0) fail(c, P.err, kErrWaitAEmpty);
                         tc_fence_after();
                     }
                     if (alive) {
-                        const uint4 wv = *reinterpret_cast<const uint4*>(wst + h * 2048 + tid * 16);
-                        uint32_t r[32];
-                        unpack_word_f16(wv.x, r + 0);
-                        unpack_word_f16(wv.y, r + 8);
-                        unpack_word_f16(wv.z, r + 16);
-                        unpack_word_f16(wv.w, r + 24);
-                        tmem_st32(tmem + lane_base + kACol + a * 32, r);
+                        const uint4 w0 = *reinterpret_cast<const uint4*>(wst + tid * 16);
+                        const uint4 w1 = *reinterpret_cast<const uint4*>(wst + 2048 + tid * 16);
+                        uint32_t r[32];  // A columns 4w + s: word w (16 k), register s
+                        unpack_word_e4m3(w0.x, r + 0);
+                        unpack_word_e4m3(w0.y, r + 4);
+                        unpack_word_e4m3(w0.z, r + 8);
+                        unpack_word_e4m3(w0.w, r + 12);
+                        unpack_word_e4m3(w1.x, r + 16);
+                        unpack_word_e4m3(w1.y, r + 20);
+                        unpack_word_e4m3(w1.z, r + 24);
+                        unpack_word_e4m3(w1.w, r + 28);
+                        tmem_st32(tmem + lane_base + kACol + ab * kATileCols, r);
                         tc_wait_st();
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&c->a_full[a]));
+                        if (lane == 0) mbar_arrive(smem_u32(&c->a_full[ab]));
                     }
-                }
-            } else {
-                if (alive) {
-                    const uint8_t* bst = Br + static_cast<size_t>(s) * BT;
+                } else {
+                    if (alive) {
+                        const uint8_t* bst = Br + static_cast<size_t>(s) * BT;
+                        const uint4 w0 = *reinterpret_cast<const uint4*>(wst + tid * 16);
+                        const uint4 w1 = *reinterpret_cast<const uint4*>(wst + 2048 + tid * 16);
+                        const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint4 wv = *reinterpret_cast<const uint4*>(wst + h * 2048 + tid * 16);
-                        const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) {
-                            const int ch = h * 4 + jj;
-                            const uint32_t w = wd[jj];
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const uint32_t w = wd[ch];
                             const uint32_t m0 = w & 0x03030303u, m1 = w & 0x0C0C0C0Cu;
                             const uint32_t m2 = w & 0x30303030u, m3 = w & 0xC0C0C0C0u;
 #pragma unroll
@@ -745,46 +826,49 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                                 dacc[3][m] = dp4a_us(m3, qv.w, dacc[3][m]);
                             }
                         }
-                    }
-                    __syncwarp();
-                    if (lane == 0 && chunk_last) mbar_arrive(smem_u32(&c->empty[q]));
-                }
-            }
-            if (seg_last) {
-                int acc[16];
-#pragma unroll
-                for (int m = 0; m < 16; ++m) acc[m] = 0;
-                if constexpr (kTC) {
-                    if (alive) {
-                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->dfull), seg_idx & 1));
-                        if (!alive && lane == 0) fail(c, P.err, kErrWaitD);
-                    }
-                    if (alive) {
-                        tc_fence_after();
-                        uint32_t v[16];
-                        tmem_ld16(tmem + lane_base + kAccCol, v);
-                        tc_wait_ld();
-                        tc_fence_before();
-#pragma unroll
-                        for (int m = 0; m < 16; ++m)
-                            acc[m] = __float2int_rn(__uint_as_float(v[m]) * 32768.f) - rq[m];
-                    }
-                } else {
-#pragma unroll
-                    for (int m = 0; m < DPR; ++m) {
-                        acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) - rq[m];
-                        dacc[0][m] = dacc[1][m] = dacc[2][m] = dacc[3][m] = 0;
+                        __syncwarp();
+                        if (lane == 0 && (rp.cp == kChunk - 1 || rp.i == nloc - 1))
+                            mbar_arrive(smem_u32(&c->empty[rp.q]));
                     }
                 }
-                segment_epilogue(P, c, p0, it.pi, it.rt, ka, it.kt + 1, seg_first_i == 0, acc, tid, alive, pend,
-                                 npend);
-                ++seg_idx;
-                seg_first_i = i + 1;
-                ka = 0;
             }
-            it.next(P);
-            if (seg_last && i + 1 < nloc)  // the next segment starts at k tile 0 of the next row tile
-                segment_code_sums(P.p[it.pi], 0, min(P.p[it.pi].kt, nloc - (i + 1)), rq);
+            int acc[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc[m] = 0;
+            if constexpr (kTC) {
+                if (alive) {
+                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->dfull), seg_idx & 1));
+                    if (!alive && lane == 0) fail(c, P.err, kErrWaitD);
+                }
+                if (alive) {
+                    // D column m: high parts of row m; column m + kRows: low parts
+                    constexpr int kRows = btile_rows(PATH, DPR);
+                    tc_fence_after();
+                    uint32_t v[32];
+                    tmem_ld16(tmem + lane_base + kAccCol, *reinterpret_cast<uint32_t(*)[16]>(v));
+                    if constexpr (kRows == 16) tmem_ld16(tmem + lane_base + kAccCol + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+                    tc_wait_ld();
+                    tc_fence_before();
+#pragma unroll
+                    for (int m = 0; m < kRows; ++m) {
+                        const float d = __fadd_rn(__fmul_rn(__uint_as_float(v[m]), 16.f), __uint_as_float(v[m + kRows]));
+                        acc[m] = __float2int_rn(__fmul_rn(d, 512.f)) - (rhi[m] - rlo[m]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < DPR; ++m)
+                    acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) - (rhi[m] - rlo[m]);
+            }
+            if (seg_idx == 0) named_bar_sync(1, 128);  // c->asc written
+            segment_epilogue(P, c, p0, it.pi, it.rt, ka, ka + len, seg_idx == 0, acc, tid, alive, pend, npend);
+            ++seg_idx;
+            // next segment: k tile 0 of the next row tile
+            it.kt = 0;
+            if (++it.rt == pr.nt) {
+                it.rt = 0;
+                ++it.pi;
+            }
         }
         finish_pending(P, c, p0, pend, npend, tid, alive);
     }
