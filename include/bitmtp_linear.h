@@ -144,10 +144,10 @@ typedef struct bitmtp_out {
 /* Workspace of a GEMM call: a device buffer the caller allocates once,
  * 16-byte aligned, of at least the size these queries return, and
  * zero-fills before its first use (e.g. cudaMemset).  It holds split-row-tile
- * partial sums and arrival counters (a fixed 5 MiB part) and each problem's
+ * accumulators and arrival counters (a fixed 2.5 MiB part) and each problem's
  * quantised activation operand (about 4 KiB per 128 in-features); every call
- * leaves the counters at zero, so one workspace serves calls of any shapes
- * that fit.  Calls that may execute concurrently on the GPU need distinct
+ * leaves the accumulators and counters at zero, so one workspace serves calls
+ * of any shapes that fit.  Calls that may execute concurrently on the GPU need distinct
  * workspaces; calls ordered on one stream may share one.  After a call that
  * ends in BITMTP_ERR_DEVICE, zero-fill it again.  Returns 0 for out-of-range
  * arguments. */
@@ -195,9 +195,9 @@ int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc,
                                unsigned flags, void* stream);
 
 /* Size of the library's built-in scratch array used by
- * bitmtp_linear_gemm_noalloc: 6.5 MiB of device memory, held on every
- * device that loads the library until the process exits. */
-#define BITMTP_NOALLOC_SCRATCH_BYTES ((size_t)13 * 512 * 1024)
+ * bitmtp_linear_gemm_noalloc: 4 MiB of device memory, held on every device
+ * that loads the library until the process exits. */
+#define BITMTP_NOALLOC_SCRATCH_BYTES ((size_t)4 * 1024 * 1024)
 
 /* bitmtp_linear_gemm without a workspace argument: for callers that cannot
  * allocate device memory.  Examples: code called from another runtime's
@@ -219,8 +219,9 @@ int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc,
  *     stream capture begins.
  *   - Sharing: all calls on a device share the one array and it keeps what
  *     the previous call left.  Each call first clears, on `stream`, the part
- *     that must start at zero (the split-row-tile arrival counters); the
- *     partial-sum slots are always written before they are read.  Calls whose
+ *     that must start at zero (the split-row-tile accumulators and arrival
+ *     counters, 2.5 MiB); the activation part is always written before it is
+ *     read.  Calls whose
  *     work can overlap on the GPU (different streams without ordering between
  *     them, or different host threads) race on the array and give wrong
  *     results; order them on one stream or use bitmtp_linear_gemm with

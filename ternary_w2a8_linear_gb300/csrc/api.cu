@@ -397,10 +397,10 @@ int bitmtp_linear_gemm_noalloc(const void* pk, float w_scale, int64_t N, int64_t
     st = noalloc_scratch(&scratch);
     if (st != BITMTP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the arrival counters must start at zero; a call that gave up a bounded
-    // wait may have left some set
+    // the split-row-tile counters and accumulators must start at zero; a call
+    // that gave up a bounded wait may have left some set
     st = cuda_status(cudaMemsetAsync(static_cast<uint8_t*>(scratch) + kWsCounters, 0,
-                                     kWsSlots - kWsCounters, s));
+                                     kWsAct - kWsCounters, s));
     if (st != BITMTP_OK) return st;
     return run_gemms(&g, 1, scratch, BITMTP_NOALLOC_SCRATCH_BYTES, flags, s);
 }

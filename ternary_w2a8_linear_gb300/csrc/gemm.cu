@@ -75,8 +75,8 @@ constexpr uint32_t kATileCols = 32;  // 128 k, one e4m3 byte each
 constexpr int kATiles = 7;
 constexpr int kMmaBatch = 2;         // k tiles per MMA-issuer wait
 constexpr int kSmemTarget = 100 * 1024;
-constexpr int kPrepThreads = 512;
-constexpr int kPrepGroups = 8;     // 8-element groups of one row per preparation thread
+constexpr int kPrepThreads = 256;
+constexpr int kPrepGroups = 4;     // 8-element groups of one row per thread and pass
 
 enum : int {
     kErrWaitW = 0x101,
@@ -127,37 +127,27 @@ __device__ __forceinline__ void unpack_word_e4m3(uint32_t w, uint32_t* r) {
     r[3] = (w >> 6) & 0x03030303u;
 }
 
-// e4m3 bit pattern of an integer v with |v| <= 15 (exact: sign, exponent
-// floor(log2|v|) + 7, three mantissa bits).
-__device__ __forceinline__ uint32_t e4m3_small_int(int v) {
-    const uint32_t a = static_cast<uint32_t>(v < 0 ? -v : v);
-    if (a == 0) return 0u;
-    const int e = 31 - __clz(static_cast<int>(a));
-    return (v < 0 ? 0x80u : 0u) | (static_cast<uint32_t>(e + 7) << 3) | (((a << 3) >> e) & 7u);
+// Two small integers (|v| <= 15, exact in e4m3) -> their e4m3 bytes: a in
+// bits 0-7, b in bits 8-15 (hardware conversion; no rounding happens).
+__device__ __forceinline__ uint32_t e4m3x2_small_int(int a, int b) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+        : "=h"(r) : "f"(static_cast<float>(b)), "f"(static_cast<float>(a)));
+    return r;
 }
 
 // Bytes (low 8 bits of each value) of eight values, as two words.
 __device__ __forceinline__ void bytes8(const uint32_t (&b)[8], uint32_t& lo, uint32_t& hi) {
-    lo = (b[0] & 0xFFu) | ((b[1] & 0xFFu) << 8) | ((b[2] & 0xFFu) << 16) | (b[3] << 24);
-    hi = (b[4] & 0xFFu) | ((b[5] & 0xFFu) << 8) | ((b[6] & 0xFFu) << 16) | (b[7] << 24);
+    lo = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+    hi = __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
 }
 
 // One 16-k unit of one operand row from the bytes of k 0..7 (lo, hi: this
-// lane) and k 8..15 (plo, phi: the partner lane), in the unit byte order.
+// lane) and k 8..15 (plo, phi: the partner lane), in the unit byte order:
+// register s = bytes {k 2s, k 2s+8, k 2s+1, k 2s+9}.
 __device__ __forceinline__ uint4 unit16(uint32_t lo, uint32_t hi, uint32_t plo, uint32_t phi) {
-    uint32_t b[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        b[i] = (lo >> (8 * i)) & 0xFFu;
-        b[4 + i] = (hi >> (8 * i)) & 0xFFu;
-        b[8 + i] = (plo >> (8 * i)) & 0xFFu;
-        b[12 + i] = (phi >> (8 * i)) & 0xFFu;
-    }
-    uint32_t reg[4];
-#pragma unroll
-    for (int si = 0; si < 4; ++si)
-        reg[si] = b[2 * si] | (b[8 + 2 * si] << 8) | (b[2 * si + 1] << 16) | (b[9 + 2 * si] << 24);
-    return make_uint4(reg[0], reg[1], reg[2], reg[3]);
+    return make_uint4(__byte_perm(lo, plo, 0x5140), __byte_perm(lo, plo, 0x7362),
+                      __byte_perm(hi, phi, 0x5140), __byte_perm(hi, phi, 0x7362));
 }
 
 __device__ __forceinline__ int find_problem_by_tile(const GemmParams& P, long long t) {
@@ -332,12 +322,12 @@ __device__ __forceinline__ const char* act_row(const GemmProblem& pr, int m) {
 // kPrepGroups 8-element groups per thread: K <= 32768 with 512 threads), so
 // the row is read once, with all loads in flight together.
 template <int PATH, int DPR>
-__global__ void __launch_bounds__(kPrepThreads, 1)
+__global__ void __launch_bounds__(kPrepThreads, 4)
 act_prep_kernel(const __grid_constant__ GemmParams P) {
     constexpr int kRows = btile_rows(PATH, DPR);
     constexpr int kBRows = btile_brows(PATH, DPR);
     constexpr int BT = btile_bytes(PATH, DPR);
-    static_assert(kPrepThreads * kPrepGroups * 8 >= BITMTP_MAX_K, "row does not fit the registers");
+    constexpr int kPass = kPrepThreads * kPrepGroups;  // 8-element groups per pass
     __shared__ float red[kPrepThreads / 32];
     __shared__ int tsum[BITMTP_MAX_K / kTileK];
     pdl_launch_dependents();  // the GEMM may start streaming weights now
@@ -351,28 +341,33 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     const char* row = live ? act_row(pr, m) : nullptr;
     const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
     const int ngroups = pr.kt * 16;  // 8-element groups, the zero tail of the last tile included
+    const int npass = (ngroups + kPass - 1) / kPass;
 
     // The activations may come from the previous kernel on the stream, and the
     // previous GEMM on this workspace may still be reading it.
     pdl_wait();
 
+    // Rows of up to kPass groups (K <= 8192) stay in registers between the
+    // absmax and the quantisation; longer rows are read twice.
     float v[kPrepGroups][8];
-#pragma unroll
-    for (int j = 0; j < kPrepGroups; ++j) {
-        const int g = j * kPrepThreads + tid;
-        if (live && g < ngroups) {
-            load8(pr, row, vec_ok, g * 8, v[j]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
-        }
-    }
     float amax = 0.f;
-    if (raw) {
+    for (int ps = 0; ps < npass; ++ps) {
 #pragma unroll
-        for (int j = 0; j < kPrepGroups; ++j)
+        for (int j = 0; j < kPrepGroups; ++j) {
+            const int g = ps * kPass + j * kPrepThreads + tid;
+            if (live && g < ngroups) {
+                load8(pr, row, vec_ok, g * 8, v[j]);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
+                for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
+            }
+        }
+        if (raw) {
+#pragma unroll
+            for (int j = 0; j < kPrepGroups; ++j)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -386,10 +381,23 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     // Each group of 16 consecutive threads covers one k tile: ngroups and
     // kPrepThreads are multiples of 16, so the shuffles below always see
     // whole groups.
+    for (int ps = 0; ps < npass; ++ps) {
+      if (npass > 1) {
 #pragma unroll
-    for (int j = 0; j < kPrepGroups; ++j) {
-        if (j * kPrepThreads >= ngroups) break;  // uniform over the block
-        const int g = j * kPrepThreads + tid;
+        for (int j = 0; j < kPrepGroups; ++j) {
+            const int g = ps * kPass + j * kPrepThreads + tid;
+            if (live && g < ngroups) {
+                load8(pr, row, vec_ok, g * 8, v[j]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
+            }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kPrepGroups; ++j) {
+        if (ps * kPass + j * kPrepThreads >= ngroups) break;  // uniform over the block
+        const int g = ps * kPass + j * kPrepThreads + tid;
         const bool gv = g < ngroups;
         int qv[8];
         int rsum = 0;
@@ -402,25 +410,28 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
         uint8_t* unit = pr.actb + static_cast<size_t>(kt) * BT + (gg >> 1) * (kBRows * 16);
         // operand row m holds the codes (dp4a) or, on the tensor paths, the
         // high parts h = q >> 4 (row m) and low parts l = q & 15 (row m + kRows)
-        uint32_t ba[8], bb[8];
+        uint32_t alo, ahi, blo = 0u, bhi = 0u;
+        if constexpr (PATH == kPathDP) {
+            uint32_t ba[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if constexpr (PATH == kPathDP) {
-                ba[i] = static_cast<uint32_t>(qv[i]);
-                bb[i] = 0u;
-            } else {
-                ba[i] = e4m3_small_int(qv[i] >> 4);
-                bb[i] = e4m3_small_int(qv[i] & 15);
+            for (int i = 0; i < 8; ++i) ba[i] = static_cast<uint32_t>(qv[i]);
+            bytes8(ba, alo, ahi);
+        } else {
+            uint32_t hp[4], lp[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                hp[i] = e4m3x2_small_int(qv[2 * i] >> 4, qv[2 * i + 1] >> 4);
+                lp[i] = e4m3x2_small_int(qv[2 * i] & 15, qv[2 * i + 1] & 15);
             }
+            alo = hp[0] | (hp[1] << 16);
+            ahi = hp[2] | (hp[3] << 16);
+            blo = lp[0] | (lp[1] << 16);
+            bhi = lp[2] | (lp[3] << 16);
         }
-        uint32_t alo, ahi;
-        bytes8(ba, alo, ahi);
         const uint32_t palo = __shfl_xor_sync(0xffffffffu, alo, 1);
         const uint32_t pahi = __shfl_xor_sync(0xffffffffu, ahi, 1);
         if (gv && (gg & 1) == 0) *reinterpret_cast<uint4*>(unit + m * 16) = unit16(alo, ahi, palo, pahi);
         if constexpr (PATH != kPathDP) {
-            uint32_t blo, bhi;
-            bytes8(bb, blo, bhi);
             const uint32_t pblo = __shfl_xor_sync(0xffffffffu, blo, 1);
             const uint32_t pbhi = __shfl_xor_sync(0xffffffffu, bhi, 1);
             if (gv && (gg & 1) == 0) *reinterpret_cast<uint4*>(unit + (m + kRows) * 16) = unit16(blo, bhi, pblo, pbhi);
@@ -428,6 +439,7 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, o);
         if (gv && (tid & 15) == 0) tsum[kt] = rsum;
+      }
     }
     __syncthreads();
 
@@ -472,17 +484,15 @@ __device__ __forceinline__ void store_out(const GemmProblem& pr, int m, int n, i
 // A split row tile this CTA contributed to, finished after the main loop.
 struct Pending {
     int pi, rt, b_first, b_last;
-    long long t_first;
 };
 
 // Finish one segment (k tiles [ka, kb) of row tile rt of problem pi).
 // acc[m] is the exact partial sum_k T*q for the thread's row.  A whole row
-// tile is written out at once; a split one is stored to this CTA's slot in
-// the workspace (slot 0 if it is the first segment of the range, else 1) and
-// recorded in `pend`.
+// tile is written out at once; a split one is added (integer atomics, no
+// return value) into its accumulator in the workspace -- the one of the CTA
+// holding the row tile's last k tile -- and recorded in `pend`.
 __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int pi, int rt, int ka, int kb,
-                                 bool first_segment, const int (&acc)[16], int tid, bool alive, Pending* pend,
-                                 int& npend) {
+                                 const int (&acc)[16], int tid, bool alive, Pending* pend, int& npend) {
     const GemmProblem& pr = P.p[pi];
     const int M = pr.M;
     const int n = rt * kTileN + tid;
@@ -494,71 +504,60 @@ __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int
         }
         return;
     }
-    int* slot = P.slots + (static_cast<size_t>(blockIdx.x) * 2 + (first_segment ? 0 : 1)) * 16 * kTileN;
-#pragma unroll
-    for (int m = 0; m < 16; ++m)
-        if (alive && m < M) slot[m * kTileN + tid] = acc[m];
     const long long T = P.total_tiles;
     const long long t_first = pr.tile_begin + static_cast<long long>(rt) * pr.kt;
     Pending& pe = pend[npend++];
     pe.pi = pi;
     pe.rt = rt;
-    pe.t_first = t_first;
     pe.b_first = range_owner(t_first, T, P.nctas);
     pe.b_last = range_owner(t_first + pr.kt - 1, T, P.nctas);
+    int* sum = P.slots + static_cast<size_t>(pe.b_last) * 16 * kTileN;
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+        if (alive && m < M) atomicAdd(sum + m * kTileN + tid, acc[m]);
 }
 
 // After the main loop: one fence, one counter increment per split row tile;
-// the last contributor of a tile sums every contributor's slot (loads of four
-// contributors in flight at a time), writes the output and leaves the counter
-// at zero.  A split row tile is identified by the CTA holding its last k tile
-// (a CTA is the last contributor of at most one split row tile).  Warps 0-3.
+// the last contributor of a tile reads the accumulated sum, writes the output
+// and leaves the accumulator and the counter at zero.  A split row tile is
+// identified by the CTA holding its last k tile (a CTA is the last k tile's
+// holder for at most one split row tile).  Warps 0-3.
 __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pending* pend, int npend, int tid,
                                bool alive) {
     if (npend == 0) return;  // uniform across the four warps
-    named_bar_sync(1, 128);  // every slot store of this CTA is issued
+    named_bar_sync(1, 128);  // every atomic add of this CTA is issued
     if (tid == 0) {
-        __threadfence();     // ... and made visible before the counters move
+        __threadfence();     // ... and performed before the counters move
         for (int k = 0; k < npend; ++k) {
             const unsigned old = atomicAdd(P.counters + pend[k].b_last, 1u);
             c->flag[k] = (old == static_cast<unsigned>(pend[k].b_last - pend[k].b_first)) ? 1 : 0;
         }
-        __threadfence();     // the last contributor then sees every other slot
+        __threadfence();     // the last contributor then sees every addition
     }
     named_bar_sync(1, 128);
     const int last0 = c->flag[0], last1 = npend > 1 ? c->flag[1] : 0;
-    const long long T = P.total_tiles;
-    for (int k = 0; k < npend; ++k) {
-        if (!(k == 0 ? last0 : last1)) continue;
+    int tot[2][16];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const bool mine = k < npend && (k == 0 ? last0 : last1);
+        const int M = mine ? P.p[pend[k].pi].M : 0;
+        const int* sum = P.slots + (mine ? static_cast<size_t>(pend[k].b_last) * 16 * kTileN : 0);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) tot[k][m] = (m < M) ? __ldcg(sum + m * kTileN + tid) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        if (!(k < npend && (k == 0 ? last0 : last1))) continue;
         const GemmProblem& pr = P.p[pend[k].pi];
         const int M = pr.M;
-        int tot[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) tot[m] = 0;
-        for (int ob0 = pend[k].b_first; ob0 <= pend[k].b_last; ob0 += 4) {
-            int v[4][16];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int ob = ob0 + j;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) v[j][m] = 0;
-                if (ob > pend[k].b_last) continue;
-                const int sl = (range_start(ob, T, P.nctas) >= pend[k].t_first) ? 0 : 1;
-                const int* os = P.slots + (static_cast<size_t>(ob) * 2 + sl) * 16 * kTileN;
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    if (m < M) v[j][m] = __ldcg(os + m * kTileN + tid);
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int m = 0; m < 16; ++m) tot[m] += v[j][m];
-        }
+        int* sum = P.slots + static_cast<size_t>(pend[k].b_last) * 16 * kTileN;
         const int n = pend[k].rt * kTileN + tid;
-        if (alive && n < pr.N) {
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-                if (m < M) store_out(pr, m, n, tot[m], c->asc[pend[k].pi - p0][m]);
+        for (int m = 0; m < 16; ++m) {
+            if (m < M) {
+                if (alive && n < pr.N) store_out(pr, m, n, tot[k][m], c->asc[pend[k].pi - p0][m]);
+                sum[m * kTileN + tid] = 0;
+            }
         }
         if (tid == 0) P.counters[pend[k].b_last] = 0u;
     }
@@ -742,11 +741,13 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         // (timed-out) wait only clears `alive`; every named barrier is still
         // executed by all four warps.
         pdl_wait();  // outputs and workspace: the preparation kernel has finished
-        // dequant scales of problems p0..p1, first needed by the first epilogue
-        // (the named barrier there publishes them)
-        for (int z = tid; z < (p1 - p0 + 1) * 16; z += 128) {
-            const GemmProblem& pr = P.p[p0 + z / 16];
-            c->asc[z / 16][z % 16] = (z % 16 < pr.M) ? __ldcg(pr.asc + z % 16) : 0.f;
+        // dequant scales of problems p0..p1 (at most 8 x 16: one per thread),
+        // first needed by the first epilogue, which stores and publishes them
+        float asc_reg = 0.f;
+        const bool asc_mine = tid < (p1 - p0 + 1) * 16;
+        if (asc_mine) {
+            const GemmProblem& pr = P.p[p0 + tid / 16];
+            if (tid % 16 < pr.M) asc_reg = __ldcg(pr.asc + tid % 16);
         }
         TileIter it;
         it.init(P, t_begin);
@@ -860,8 +861,11 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 for (int m = 0; m < DPR; ++m)
                     acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) - (rhi[m] - rlo[m]);
             }
-            if (seg_idx == 0) named_bar_sync(1, 128);  // c->asc written
-            segment_epilogue(P, c, p0, it.pi, it.rt, ka, ka + len, seg_idx == 0, acc, tid, alive, pend, npend);
+            if (seg_idx == 0) {
+                if (asc_mine) c->asc[tid / 16][tid % 16] = asc_reg;
+                named_bar_sync(1, 128);
+            }
+            segment_epilogue(P, c, p0, it.pi, it.rt, ka, ka + len, acc, tid, alive, pend, npend);
             ++seg_idx;
             // next segment: k tile 0 of the next row tile
             it.kt = 0;

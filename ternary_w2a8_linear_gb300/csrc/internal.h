@@ -47,19 +47,20 @@ struct GemmParams {
     int nctas;
     long long total_tiles;
     unsigned* counters;       // [kMaxCtas] split-row-tile arrival counters (left at zero)
-    int* slots;               // [kMaxCtas][2][16][128] split-row-tile partial sums
+    int* slots;               // [kMaxCtas][16][128] split-row-tile accumulators (left at zero)
     int* err;                 // device error word
 };
 
 constexpr int kMaxCtas = 320;         // persistent CTAs per launch (>= 2 per SM on GB300)
 constexpr int kMinTilesPerCta = 4;    // fewer CTAs on small problems: fewer split row tiles
 
-// Workspace: split-row-tile counters and partial-sum slots at fixed offsets,
-// then one activation region per problem (sized by its k tiles).
+// Workspace: split-row-tile counters and accumulators at fixed offsets (both
+// must be zero when a launch starts; every launch leaves them at zero), then
+// one activation region per problem (sized by its k tiles).
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 constexpr size_t kWsCounters = 256;
 constexpr size_t kWsSlots = kWsCounters + align256(static_cast<size_t>(kMaxCtas) * 4);
-constexpr size_t kWsAct = kWsSlots + static_cast<size_t>(kMaxCtas) * 2 * 16 * kTileN * 4;
+constexpr size_t kWsAct = kWsSlots + static_cast<size_t>(kMaxCtas) * 16 * kTileN * 4;
 constexpr size_t act_tiles_bytes(int kt) { return align256(static_cast<size_t>(kt) * 4096); }
 constexpr size_t act_rsp_bytes(int kt) { return align256(static_cast<size_t>(16) * (kt + 1) * 4); }
 constexpr size_t act_region_bytes(int kt) { return act_tiles_bytes(kt) + act_rsp_bytes(kt) + 256; }
