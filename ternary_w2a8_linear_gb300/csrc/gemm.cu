@@ -74,6 +74,7 @@ constexpr uint32_t kACol = 32;       // A: kATiles buffers of one k tile each
 constexpr uint32_t kATileCols = 32;  // 128 k, one e4m3 byte each
 constexpr int kATiles = 7;
 constexpr int kMmaBatch = 2;         // k tiles per MMA-issuer wait
+constexpr int kBatchBars = 8;        // MMA batch completion barriers (> kATiles)
 constexpr int kSmemTarget = 100 * 1024;
 constexpr int kPrepThreads = 256;
 constexpr int kPrepGroups = 4;     // 8-element groups of one row per thread and pass
@@ -92,7 +93,7 @@ struct Ctrl {
     uint64_t bfull[kMaxRing];     // activation tiles of the chunk landed
     uint64_t empty[kMaxRing];     // chunk slot free again (MMA commit / dp4a consumers)
     uint64_t a_full[kATiles];     // A buffer written (four consumer warps)
-    uint64_t a_empty[kATiles];    // A buffer free again (MMA commit)
+    uint64_t mma_done[kBatchBars]; // MMA batch b complete: barrier b % kBatchBars
     uint64_t dfull;
     uint32_t tmem_base;
     int failed;
@@ -127,12 +128,11 @@ __device__ __forceinline__ void unpack_word_e4m3(uint32_t w, uint32_t* r) {
     r[3] = (w >> 6) & 0x03030303u;
 }
 
-// Two small integers (|v| <= 15, exact in e4m3) -> their e4m3 bytes: a in
-// bits 0-7, b in bits 8-15 (hardware conversion; no rounding happens).
-__device__ __forceinline__ uint32_t e4m3x2_small_int(int a, int b) {
+// Two integer-valued floats (|v| <= 15, exact in e4m3) -> their e4m3 bytes:
+// a in bits 0-7, b in bits 8-15 (hardware conversion; no rounding happens).
+__device__ __forceinline__ uint32_t e4m3x2_small(float a, float b) {
     uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
-        : "=h"(r) : "f"(static_cast<float>(b)), "f"(static_cast<float>(a)));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
     return r;
 }
 
@@ -215,10 +215,11 @@ struct RingPos {
 
 // Bulk-copy the weight tiles of tiles [first, first + count) of this CTA's
 // range into consecutive ring slots, one copy per run that is contiguous in
-// global memory (within one problem); all copies complete on `bar`.
+// global memory (within one problem); all copies complete on `bar`.  Run by
+// a whole converged warp; only the lane with `on` set issues.
 __device__ void issue_weights(const GemmParams& P, long long first, int count, uint8_t* dst, uint32_t bar,
-                              uint64_t pol) {
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(count * kTileBytes));
+                              uint64_t pol, uint32_t on) {
+    mbar_arrive_expect_tx_if(on, bar, static_cast<uint32_t>(count * kTileBytes));
     TileIter it;
     it.init(P, first);
     const uint8_t* run_src = nullptr;
@@ -228,7 +229,7 @@ __device__ void issue_weights(const GemmParams& P, long long first, int count, u
         const GemmProblem& pr = P.p[it.pi];
         const uint8_t* src = pr.pk + (static_cast<size_t>(it.rt) * pr.kt + it.kt) * kTileBytes;
         if (run_len == 0 || it.pi != run_pi) {
-            if (run_len > 0) bulk_g2s(smem_u32(run_dst), run_src, run_len * kTileBytes, bar, pol);
+            if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * kTileBytes, bar, pol);
             run_dst = dst + k * kTileBytes;
             run_src = src;
             run_len = 0;
@@ -237,14 +238,14 @@ __device__ void issue_weights(const GemmParams& P, long long first, int count, u
         ++run_len;
         it.next(P);
     }
-    if (run_len > 0) bulk_g2s(smem_u32(run_dst), run_src, run_len * kTileBytes, bar, pol);
+    if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * kTileBytes, bar, pol);
 }
 
 // The same for the activation tiles (BT bytes each) of those tiles: a run
 // ends where the k index wraps to the next row tile or the problem changes.
 __device__ void issue_acts(const GemmParams& P, long long first, int count, int BT, uint8_t* dst, uint32_t bar,
-                           uint64_t pol) {
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(count * BT));
+                           uint64_t pol, uint32_t on) {
+    mbar_arrive_expect_tx_if(on, bar, static_cast<uint32_t>(count * BT));
     TileIter it;
     it.init(P, first);
     const uint8_t* run_src = nullptr;
@@ -253,7 +254,7 @@ __device__ void issue_acts(const GemmParams& P, long long first, int count, int 
     for (int k = 0; k < count; ++k) {
         const uint8_t* src = P.p[it.pi].actb + static_cast<size_t>(it.kt) * BT;
         if (run_len == 0 || src != run_src + static_cast<size_t>(run_len) * BT) {
-            if (run_len > 0) bulk_g2s(smem_u32(run_dst), run_src, run_len * BT, bar, pol);
+            if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * BT, bar, pol);
             run_dst = dst + k * BT;
             run_src = src;
             run_len = 0;
@@ -261,7 +262,7 @@ __device__ void issue_acts(const GemmParams& P, long long first, int count, int 
         ++run_len;
         it.next(P);
     }
-    if (run_len > 0) bulk_g2s(smem_u32(run_dst), run_src, run_len * BT, bar, pol);
+    if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * BT, bar, pol);
 }
 
 // Load 8 consecutive activations k0..k0+7 of one row (zero beyond K).
@@ -399,13 +400,17 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
         if (ps * kPass + j * kPrepThreads >= ngroups) break;  // uniform over the block
         const int g = ps * kPass + j * kPrepThreads + tid;
         const bool gv = g < ngroups;
-        int qv[8];
-        int rsum = 0;
+        // codes as exact small floats: clamp(rint(RN(x * s))) gives the same
+        // values as the integer quantiser (quant.cuh), without conversions
+        float qf[8];
+        float fsum = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            qv[i] = raw ? ((amax > 0.f) ? quantize(v[j][i], s) : 0) : static_cast<int>(v[j][i]);
-            rsum += qv[i];
+            qf[i] = raw ? ((amax > 0.f) ? fminf(fmaxf(rintf(__fmul_rn(v[j][i], s)), -127.f), 127.f) : 0.f)
+                        : v[j][i];
+            fsum += qf[i];
         }
+        int rsum = static_cast<int>(fsum);  // |sum| <= 1016: exact
         const int kt = g >> 4, gg = g & 15;
         uint8_t* unit = pr.actb + static_cast<size_t>(kt) * BT + (gg >> 1) * (kBRows * 16);
         // operand row m holds the codes (dp4a) or, on the tensor paths, the
@@ -414,14 +419,16 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
         if constexpr (PATH == kPathDP) {
             uint32_t ba[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ba[i] = static_cast<uint32_t>(qv[i]);
+            for (int i = 0; i < 8; ++i) ba[i] = static_cast<uint32_t>(static_cast<int>(qf[i]));
             bytes8(ba, alo, ahi);
         } else {
+            // h = floor(q / 16), l = q - 16 h, both exact small floats
             uint32_t hp[4], lp[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                hp[i] = e4m3x2_small_int(qv[2 * i] >> 4, qv[2 * i + 1] >> 4);
-                lp[i] = e4m3x2_small_int(qv[2 * i] & 15, qv[2 * i + 1] & 15);
+                const float h0 = floorf(qf[2 * i] * 0.0625f), h1 = floorf(qf[2 * i + 1] * 0.0625f);
+                hp[i] = e4m3x2_small(h0, h1);
+                lp[i] = e4m3x2_small(fmaf(h0, -16.f, qf[2 * i]), fmaf(h1, -16.f, qf[2 * i + 1]));
             }
             alo = hp[0] | (hp[1] << 16);
             ahi = hp[2] | (hp[3] << 16);
@@ -606,10 +613,8 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             mbar_init(smem_u32(&c->bfull[q]), 1);
             mbar_init(smem_u32(&c->empty[q]), kTC ? 1 : 4);
         }
-        for (int a = 0; a < kATiles; ++a) {
-            mbar_init(smem_u32(&c->a_full[a]), 4);
-            mbar_init(smem_u32(&c->a_empty[a]), 1);
-        }
+        for (int a = 0; a < kATiles; ++a) mbar_init(smem_u32(&c->a_full[a]), 4);
+        for (int a = 0; a < kBatchBars; ++a) mbar_init(smem_u32(&c->mma_done[a]), 1);
         mbar_init(smem_u32(&c->dfull), 1);
         c->failed = 0;
         fence_mbar_init();
@@ -627,111 +632,117 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     pdl_launch_dependents();
 
     const int npre = nchunks < R ? nchunks : R;
-    int w_issued = 0, b_issued = 0;  // chunks whose copies were requested (warp 4, lane 0)
+    int w_issued = 0, b_issued = 0;  // chunks whose copies were requested (warp 4)
 
     // -------------------------------------------------------- main loop --
     if (warp == 4) {
-        if (lane == 0) {
-            // weights first: they do not depend on the kernels before this one
-            const uint64_t pol = policy_evict_first();
-            for (int j = 0; j < npre; ++j)
-                issue_weights(P, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk),
-                              Wr + static_cast<size_t>(j) * kChunk * kTileBytes, smem_u32(&c->wfull[j]), pol);
-            w_issued = npre;
-            pdl_wait();  // the activation tiles are written by the preparation kernel
-            const uint64_t pol_b = policy_evict_last();
-            for (int j = 0; j < npre; ++j)
-                issue_acts(P, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk), BT,
-                           Br + static_cast<size_t>(j) * kChunk * BT, smem_u32(&c->bfull[j]), pol_b);
-            b_issued = npre;
-            // refill ring slots as they are released
-            for (int j = npre; j < nchunks; ++j) {
-                const int q = j % R;
-                if (!mbar_wait_bounded(smem_u32(&c->empty[q]), ((j / R) - 1) & 1)) {
-                    fail(c, P.err, kErrWaitEmpty);
-                    break;
-                }
-                const long long first = t_begin + static_cast<long long>(j) * kChunk;
-                const int cnt = min(kChunk, nloc - j * kChunk);
-                issue_weights(P, first, cnt, Wr + static_cast<size_t>(q) * kChunk * kTileBytes,
-                              smem_u32(&c->wfull[q]), pol);
-                w_issued = j + 1;
-                issue_acts(P, first, cnt, BT, Br + static_cast<size_t>(q) * kChunk * BT, smem_u32(&c->bfull[q]),
-                           pol_b);
-                b_issued = j + 1;
+        // The whole warp runs the producer loop; the elected lane issues.
+        const uint32_t leader = elect_one();
+        // weights first: they do not depend on the kernels before this one
+        const uint64_t pol = policy_evict_first();
+        for (int j = 0; j < npre; ++j)
+            issue_weights(P, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk),
+                          Wr + static_cast<size_t>(j) * kChunk * kTileBytes, smem_u32(&c->wfull[j]), pol, leader);
+        w_issued = npre;
+        pdl_wait();  // the activation tiles are written by the preparation kernel
+        const uint64_t pol_b = policy_evict_last();
+        for (int j = 0; j < npre; ++j)
+            issue_acts(P, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk), BT,
+                       Br + static_cast<size_t>(j) * kChunk * BT, smem_u32(&c->bfull[j]), pol_b, leader);
+        b_issued = npre;
+        // refill ring slots as they are released
+        for (int j = npre; j < nchunks; ++j) {
+            const int q = j % R;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->empty[q]), ((j / R) - 1) & 1))) {
+                if (leader) fail(c, P.err, kErrWaitEmpty);
+                break;
             }
+            const long long first = t_begin + static_cast<long long>(j) * kChunk;
+            const int cnt = min(kChunk, nloc - j * kChunk);
+            issue_weights(P, first, cnt, Wr + static_cast<size_t>(q) * kChunk * kTileBytes,
+                          smem_u32(&c->wfull[q]), pol, leader);
+            w_issued = j + 1;
+            issue_acts(P, first, cnt, BT, Br + static_cast<size_t>(q) * kChunk * BT, smem_u32(&c->bfull[q]),
+                       pol_b, leader);
+            b_issued = j + 1;
         }
         __syncwarp();
     } else if (warp == 5) {
         if constexpr (kTC) {
-            if (lane == 0) {
-                // Segment by segment (k tiles of one row tile) in batches of up
-                // to kMmaBatch tiles: one wait (the batch's last A buffer: the
-                // consumer warps fill buffers in order), then the batch's MMAs
-                // as straight-line code, then the commits.
-                constexpr int kBR = btile_brows(PATH, DPR);
-                constexpr uint32_t kIdesc = idesc_f16_f32(128, kBR);
-                constexpr uint32_t kUnit = kBR * 16;      // bytes of one 16-k unit
-                const uint32_t bbase = smem_u32(Br);
-                TileIter it;
-                it.init(P, t_begin);
-                RingPos rp;
-                rp.reset();
-                bool ok = true;
-                while (rp.i < nloc && ok) {
-                    const int len = min(P.p[it.pi].kt - it.kt, nloc - rp.i);
-                    for (int e = 0; e < len && ok;) {
-                        const int nb = min(kMmaBatch, len - e);
-                        RingPos r1 = rp;
-                        if (nb == 2) r1.next(R);
-                        // activation tiles of any chunk the batch enters
-                        if (rp.cp == 0 && !mbar_wait_bounded(smem_u32(&c->bfull[rp.q]), rp.qph)) ok = false;
-                        if (ok && nb == 2 && r1.cp == 0 && !mbar_wait_bounded(smem_u32(&c->bfull[r1.q]), r1.qph))
-                            ok = false;
-                        if (!ok) {
-                            fail(c, P.err, kErrWaitB);
-                            break;
-                        }
-                        if (!mbar_wait_bounded(smem_u32(&c->a_full[r1.ab]), r1.abph)) {
-                            fail(c, P.err, kErrWaitAFull);
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t acc0 = e == 0 ? 0u : 1u;
-                        const uint64_t bd0 = smem_desc_noswizzle(bbase + rp.slot() * BT, kUnit, 128);
-                        const uint32_t a0 = tmem + kACol + rp.ab * kATileCols;
-                        // chunk cc of 32 k: A columns 8*cc, B units 2cc and 2cc+1
-                        mma_f8_ts(tmem + kAccCol, a0, bd0, kIdesc, acc0);
-                        mma_f8_ts(tmem + kAccCol, a0 + 8, bd0 + ((2 * kUnit) >> 4), kIdesc, 1u);
-                        mma_f8_ts(tmem + kAccCol, a0 + 16, bd0 + ((4 * kUnit) >> 4), kIdesc, 1u);
-                        mma_f8_ts(tmem + kAccCol, a0 + 24, bd0 + ((6 * kUnit) >> 4), kIdesc, 1u);
-                        if (nb == 2) {
-                            const uint64_t bd1 = smem_desc_noswizzle(bbase + r1.slot() * BT, kUnit, 128);
-                            const uint32_t a1 = tmem + kACol + r1.ab * kATileCols;
-                            mma_f8_ts(tmem + kAccCol, a1, bd1, kIdesc, 1u);
-                            mma_f8_ts(tmem + kAccCol, a1 + 8, bd1 + ((2 * kUnit) >> 4), kIdesc, 1u);
-                            mma_f8_ts(tmem + kAccCol, a1 + 16, bd1 + ((4 * kUnit) >> 4), kIdesc, 1u);
-                            mma_f8_ts(tmem + kAccCol, a1 + 24, bd1 + ((6 * kUnit) >> 4), kIdesc, 1u);
-                        }
-                        mma_commit(smem_u32(&c->a_empty[rp.ab]));
-                        if (rp.cp == kChunk - 1 || rp.i == nloc - 1) mma_commit(smem_u32(&c->empty[rp.q]));
-                        if (nb == 2) {
-                            mma_commit(smem_u32(&c->a_empty[r1.ab]));
-                            if (r1.cp == kChunk - 1 || r1.i == nloc - 1) mma_commit(smem_u32(&c->empty[r1.q]));
-                        }
-                        rp = r1;
-                        rp.next(R);
-                        e += nb;
+            // The whole warp runs the loop (uniform control flow, waits by every
+            // lane); the elected lane issues the MMAs and commits through guard
+            // predicates, so the warp never diverges around a tcgen05 issue.
+            // Segment by segment (k tiles of one row tile) in batches of up to
+            // kMmaBatch tiles: one wait (the batch's last A buffer: the consumer
+            // warps fill buffers in order), the batch's MMAs as straight-line
+            // code, one commit for the batch.
+            const uint32_t leader = elect_one();
+            constexpr int kBR = btile_brows(PATH, DPR);
+            constexpr uint32_t kIdesc = idesc_f16_f32(128, kBR);
+            constexpr uint32_t kUnit = kBR * 16;      // bytes of one 16-k unit
+            const uint32_t bbase = smem_u32(Br);
+            TileIter it;
+            it.init(P, t_begin);
+            RingPos rp;
+            rp.reset();
+            int nbatch = 0;
+            bool ok = true;
+            while (rp.i < nloc && ok) {
+                const int len = min(P.p[it.pi].kt - it.kt, nloc - rp.i);
+                for (int e = 0; e < len && ok;) {
+                    const int nb = min(kMmaBatch, len - e);
+                    RingPos r[kMmaBatch];
+                    r[0] = rp;
+#pragma unroll
+                    for (int t = 1; t < kMmaBatch; ++t) {
+                        r[t] = r[t - 1];
+                        if (t < nb) r[t].next(R);
                     }
-                    if (!ok) break;
-                    mma_commit(smem_u32(&c->dfull));
-                    // next segment: k tile 0 of the next row tile
-                    it.kt = 0;
-                    if (++it.rt == P.p[it.pi].nt) {
-                        it.rt = 0;
-                        ++it.pi;
+                    // activation tiles of every chunk the batch enters
+#pragma unroll
+                    for (int t = 0; t < kMmaBatch; ++t)
+                        if (ok && t < nb && r[t].cp == 0)
+                            ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[r[t].q]), r[t].qph));
+                    if (!ok) {
+                        if (leader) fail(c, P.err, kErrWaitB);
+                        break;
                     }
+                    const RingPos& rl = r[nb - 1];
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->a_full[rl.ab]), rl.abph));
+                    if (!ok) {
+                        if (leader) fail(c, P.err, kErrWaitAFull);
+                        break;
+                    }
+                    tc_fence_after();
+                    // chunk cc of 32 k of tile t: A columns 8*cc, B units 2cc and 2cc+1
+#pragma unroll
+                    for (int t = 0; t < kMmaBatch; ++t) {
+                        const uint32_t on = (t < nb) ? leader : 0u;
+                        const uint64_t bd = smem_desc_noswizzle(bbase + r[t].slot() * BT, kUnit, 128);
+                        const uint32_t at = tmem + kACol + r[t].ab * kATileCols;
+                        mma_f8_ts_if(on, tmem + kAccCol, at, bd, kIdesc, (t == 0 && e == 0) ? 0u : 1u);
+                        mma_f8_ts_if(on, tmem + kAccCol, at + 8, bd + ((2 * kUnit) >> 4), kIdesc, 1u);
+                        mma_f8_ts_if(on, tmem + kAccCol, at + 16, bd + ((4 * kUnit) >> 4), kIdesc, 1u);
+                        mma_f8_ts_if(on, tmem + kAccCol, at + 24, bd + ((6 * kUnit) >> 4), kIdesc, 1u);
+                    }
+                    mma_commit_if(leader, smem_u32(&c->mma_done[nbatch % kBatchBars]));
+#pragma unroll
+                    for (int t = 0; t < kMmaBatch; ++t) {
+                        const bool chunk_end = t < nb && (r[t].cp == kChunk - 1 || r[t].i == nloc - 1);
+                        mma_commit_if(chunk_end ? leader : 0u, smem_u32(&c->empty[r[t].q]));
+                    }
+                    ++nbatch;
+                    rp = rl;
+                    rp.next(R);
+                    e += nb;
+                }
+                if (!ok) break;
+                mma_commit_if(leader, smem_u32(&c->dfull));
+                // next segment: k tile 0 of the next row tile
+                it.kt = 0;
+                if (++it.rt == P.p[it.pi].nt) {
+                    it.rt = 0;
+                    ++it.pi;
                 }
             }
         }
@@ -740,6 +751,8 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         // warps 0-3: one output row per thread, segment by segment.  A failed
         // (timed-out) wait only clears `alive`; every named barrier is still
         // executed by all four warps.
+        TileIter it;
+        it.init(P, t_begin);
         pdl_wait();  // outputs and workspace: the preparation kernel has finished
         // dequant scales of problems p0..p1 (at most 8 x 16: one per thread),
         // first needed by the first epilogue, which stores and publishes them
@@ -749,8 +762,6 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             const GemmProblem& pr = P.p[p0 + tid / 16];
             if (tid % 16 < pr.M) asc_reg = __ldcg(pr.asc + tid % 16);
         }
-        TileIter it;
-        it.init(P, t_begin);
         Pending pend[2];
         int npend = 0;
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
@@ -758,6 +769,13 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         int seg_idx = 0;
         RingPos rp;
         rp.reset();
+        // MMA batch of each of the last kATiles tiles (the batch that must
+        // complete before an A buffer is written again); batches never span
+        // segments and hold up to kMmaBatch tiles, as in the MMA thread
+        int hist[kATiles];
+#pragma unroll
+        for (int k = 0; k < kATiles; ++k) hist[k] = 0;
+        int nbatch = 0;
         while (rp.i < nloc) {
             const GemmProblem& pr = P.p[it.pi];
             const int ka = it.kt;
@@ -784,8 +802,13 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 const uint8_t* wst = Wr + static_cast<size_t>(s) * kTileBytes;
                 if constexpr (kTC) {
                     const int ab = rp.ab;
+                    const int prev = hist[0];  // batch that read the tile kATiles back
+#pragma unroll
+                    for (int k = 0; k + 1 < kATiles; ++k) hist[k] = hist[k + 1];
+                    hist[kATiles - 1] = nbatch + e / kMmaBatch;
                     if (alive && rp.i >= kATiles) {
-                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->a_empty[ab]), rp.abph ^ 1u));
+                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->mma_done[prev % kBatchBars]),
+                                                                          (prev / kBatchBars) & 1));
                         if (!alive && lane == 0) fail(c, P.err, kErrWaitAEmpty);
                         tc_fence_after();
                     }
@@ -805,7 +828,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         tc_wait_st();
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&c->a_full[ab]));
+                        mbar_arrive_if(lane == 0, smem_u32(&c->a_full[ab]));
                     }
                 } else {
                     if (alive) {
@@ -828,8 +851,8 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                             }
                         }
                         __syncwarp();
-                        if (lane == 0 && (rp.cp == kChunk - 1 || rp.i == nloc - 1))
-                            mbar_arrive(smem_u32(&c->empty[rp.q]));
+                        mbar_arrive_if(lane == 0 && (rp.cp == kChunk - 1 || rp.i == nloc - 1),
+                                       smem_u32(&c->empty[rp.q]));
                     }
                 }
             }
@@ -867,6 +890,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             }
             segment_epilogue(P, c, p0, it.pi, it.rt, ka, ka + len, acc, tid, alive, pend, npend);
             ++seg_idx;
+            nbatch += (len + kMmaBatch - 1) / kMmaBatch;
             // next segment: k tile 0 of the next row tile
             it.kt = 0;
             if (++it.rt == pr.nt) {

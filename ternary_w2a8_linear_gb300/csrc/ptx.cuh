@@ -28,9 +28,19 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
                  :: "r"(bar) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive_if(uint32_t on, uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\t.reg .pred g;\n\tsetp.ne.b32 g, %1, 0;\n\t"
+                 "@g mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+                 :: "r"(bar), "r"(on) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
                  :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(uint32_t on, uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\t.reg .pred g;\n\tsetp.ne.b32 g, %2, 0;\n\t"
+                 "@g mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 :: "r"(bar), "r"(bytes), "r"(on) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -61,6 +71,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
                  " [%0], [%1], %2, [%3], %4;"
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
+}
+// The same, issued only where `on` is non-zero (guard predicate).
+__device__ __forceinline__ void bulk_g2s_if(uint32_t on, uint32_t dst, const void* src, uint32_t bytes,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile("{\n\t.reg .pred g;\n\tsetp.ne.b32 g, %5, 0;\n\t"
+                 "@g cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;\n\t}"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy), "r"(on) : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
@@ -194,6 +212,31 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
                  "setp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
                  :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// The same, issued only where `on` is non-zero (a guard predicate, no branch).
+__device__ __forceinline__ void mma_f8_ts_if(uint32_t on, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p, g;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "setp.ne.b32 g, %5, 0;\n\t"
+                 "@g tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(on) : "memory");
+}
+// One lane of a converged warp: 1 in the elected lane, 0 elsewhere.  Single-lane
+// tcgen05 work issued from a converged warp under this predicate (no branch)
+// is several times cheaper than from a lane running alone.
+__device__ __forceinline__ uint32_t elect_one() {
+    uint32_t pred = 0;
+    asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+                 : "=r"(pred));
+    return pred;
+}
+// Arrive on an mbarrier once all previously issued tcgen05.mma of this thread
+// complete, issued only where `on` is non-zero.
+__device__ __forceinline__ void mma_commit_if(uint32_t on, uint32_t bar) {
+    asm volatile("{\n\t.reg .pred g;\n\tsetp.ne.b32 g, %1, 0;\n\t"
+                 "@g tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+                 :: "r"(bar), "r"(on) : "memory");
 }
 // Arrive on an mbarrier once all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
