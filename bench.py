@@ -38,6 +38,10 @@ if ROOT not in sys.path:
 from ternary_w2a8_linear_gb300 import inputs  # noqa: E402
 
 WIDTHS = (1, 2, 4, 8)
+# DRAM bytes (read + write) of one step's GEMM launches, summed over the four
+# widths, from the ncu capture summarised in profiles/; None while the kernel
+# differs from the one captured.
+STEP_DRAM_TRAFFIC = None
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "W2A8 linear achieved HBM GB/s (% of roofline) and rows/s at widths 1-16"
 
@@ -289,7 +293,8 @@ def run_ours(args, rank, world):
             t = a.elapsed_time(b) / 1e3 / (n_rep * G)  # seconds per width-pass (7 linears)
             byt = sum(algorithmic_bytes(Kp, Np, M) for _, Kp, Np in inputs.BITNET2B_PROJ)
             per_width[mode][str(M)] = {"gbs": round(byt / t / 1e9, 1), "us_per_layer_set": round(t * 1e6, 2),
-                                       "rows_per_s": round(M / t, 1)}
+                                       "rows_per_s": round(M / t, 1),
+                                       "frac": round(byt / t / 1e9 / load_peaks()[0], 4)}
             del g
 
     e2e = None
@@ -473,8 +478,10 @@ def main():
                                          "graph_steps": res["graph_steps"],
                                          "launch": f"{args.mode}; CUDA graph + PDL"}),
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(per_gpu / peak, 4), "peak_kind": peak_kind, "traffic": None,
-                     "kernel": "w2a8_gemm_kernel (all launches of the step)"},
+                     "frac": round(per_gpu / peak, 4), "peak_kind": peak_kind,
+                     "traffic": STEP_DRAM_TRAFFIC,
+                     "kernel": "act_prep_kernel + w2a8_streamk_kernel: the two launches of each grouped call, "
+                               "4 calls per step; achieved = algorithmic bytes per step / mean step time"},
         "per_width": res["per_width"],
         "e2e": res["e2e"],
         "gpu_launches": res["gpu_launches"],
