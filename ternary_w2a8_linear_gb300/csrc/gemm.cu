@@ -69,10 +69,11 @@ constexpr int kChunk = 4;            // k tiles per ring chunk (16 KiB of weight
 constexpr int kMaxRing = 6;          // chunks in the ring (upper bound)
 constexpr int kCtrlBytes = 1024;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kAccCol = 0;      // D: one fp32 column per operand row (at most 32)
-constexpr uint32_t kACol = 32;       // A: kATiles buffers of one k tile each
+constexpr uint32_t kAccCol = 0;      // D: two accumulators (alternate segments) of 32 fp32 columns
+constexpr uint32_t kACol = 64;       // A: kATiles buffers of one k tile each
 constexpr uint32_t kATileCols = 32;  // 128 k, one e4m3 byte each
-constexpr int kATiles = 7;
+constexpr int kATiles = 6;
+constexpr int kDeferTiles = 5;       // a segment's epilogue runs this many tiles into the next one
 constexpr int kMmaBatch = 2;         // k tiles per MMA-issuer wait
 constexpr int kBatchBars = 8;        // MMA batch completion barriers (> kATiles)
 constexpr int kSmemTarget = 100 * 1024;
@@ -94,7 +95,7 @@ struct Ctrl {
     uint64_t empty[kMaxRing];     // chunk slot free again (MMA commit / dp4a consumers)
     uint64_t a_full[kATiles];     // A buffer written (four consumer warps)
     uint64_t mma_done[kBatchBars]; // MMA batch b complete: barrier b % kBatchBars
-    uint64_t dfull;
+    uint64_t dfull[2];            // accumulator of segment s (D buffer s & 1) complete
     uint32_t tmem_base;
     int failed;
     int flag[2];
@@ -615,7 +616,8 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         }
         for (int a = 0; a < kATiles; ++a) mbar_init(smem_u32(&c->a_full[a]), 4);
         for (int a = 0; a < kBatchBars; ++a) mbar_init(smem_u32(&c->mma_done[a]), 1);
-        mbar_init(smem_u32(&c->dfull), 1);
+        mbar_init(smem_u32(&c->dfull[0]), 1);
+        mbar_init(smem_u32(&c->dfull[1]), 1);
         c->failed = 0;
         fence_mbar_init();
     }
@@ -685,10 +687,11 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             it.init(P, t_begin);
             RingPos rp;
             rp.reset();
-            int nbatch = 0;
+            int nbatch = 0, seg = 0;
             bool ok = true;
             while (rp.i < nloc && ok) {
                 const int len = min(P.p[it.pi].kt - it.kt, nloc - rp.i);
+                const uint32_t dcol = tmem + kAccCol + (seg & 1) * 32;
                 for (int e = 0; e < len && ok;) {
                     const int nb = min(kMmaBatch, len - e);
                     RingPos r[kMmaBatch];
@@ -720,10 +723,10 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         const uint32_t on = (t < nb) ? leader : 0u;
                         const uint64_t bd = smem_desc_noswizzle(bbase + r[t].slot() * BT, kUnit, 128);
                         const uint32_t at = tmem + kACol + r[t].ab * kATileCols;
-                        mma_f8_ts_if(on, tmem + kAccCol, at, bd, kIdesc, (t == 0 && e == 0) ? 0u : 1u);
-                        mma_f8_ts_if(on, tmem + kAccCol, at + 8, bd + ((2 * kUnit) >> 4), kIdesc, 1u);
-                        mma_f8_ts_if(on, tmem + kAccCol, at + 16, bd + ((4 * kUnit) >> 4), kIdesc, 1u);
-                        mma_f8_ts_if(on, tmem + kAccCol, at + 24, bd + ((6 * kUnit) >> 4), kIdesc, 1u);
+                        mma_f8_ts_if(on, dcol, at, bd, kIdesc, (t == 0 && e == 0) ? 0u : 1u);
+                        mma_f8_ts_if(on, dcol, at + 8, bd + ((2 * kUnit) >> 4), kIdesc, 1u);
+                        mma_f8_ts_if(on, dcol, at + 16, bd + ((4 * kUnit) >> 4), kIdesc, 1u);
+                        mma_f8_ts_if(on, dcol, at + 24, bd + ((6 * kUnit) >> 4), kIdesc, 1u);
                     }
                     mma_commit_if(leader, smem_u32(&c->mma_done[nbatch % kBatchBars]));
 #pragma unroll
@@ -737,7 +740,8 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                     e += nb;
                 }
                 if (!ok) break;
-                mma_commit_if(leader, smem_u32(&c->dfull));
+                mma_commit_if(leader, smem_u32(&c->dfull[seg & 1]));
+                ++seg;
                 // next segment: k tile 0 of the next row tile
                 it.kt = 0;
                 if (++it.rt == P.p[it.pi].nt) {
@@ -776,6 +780,52 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
         for (int k = 0; k < kATiles; ++k) hist[k] = 0;
         int nbatch = 0;
+        bool first_epi = true;
+        // Tensor paths: a segment's epilogue is deferred until kDeferTiles tiles
+        // of the next segment are written (the accumulator is double-buffered),
+        // so the MMA pipeline does not drain at row-tile boundaries.
+        bool dv = false;
+        int d_pi = 0, d_rt = 0, d_ka = 0, d_kb = 0, d_seg = 0;
+        int d_rq[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) d_rq[m] = 0;
+        auto epilogue = [&](int e_pi, int e_rt, int e_ka, int e_kb, const int (&acc)[16]) {
+            if (first_epi) {  // publish the dequant scales once
+                if (asc_mine) c->asc[tid / 16][tid % 16] = asc_reg;
+                named_bar_sync(1, 128);
+                first_epi = false;
+            }
+            segment_epilogue(P, c, p0, e_pi, e_rt, e_ka, e_kb, acc, tid, alive, pend, npend);
+        };
+        auto finish_deferred = [&]() {
+            int acc[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc[m] = 0;
+            if constexpr (kTC) {
+                if (alive) {
+                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->dfull[d_seg & 1]), (d_seg >> 1) & 1));
+                    if (!alive && lane == 0) fail(c, P.err, kErrWaitD);
+                }
+                if (alive) {
+                    // D column m: high parts of row m; column m + kRows: low parts
+                    constexpr int kRows = btile_rows(PATH, DPR);
+                    const uint32_t dcol = tmem + lane_base + kAccCol + (d_seg & 1) * 32;
+                    tc_fence_after();
+                    uint32_t v[32];
+                    tmem_ld16(dcol, *reinterpret_cast<uint32_t(*)[16]>(v));
+                    if constexpr (kRows == 16) tmem_ld16(dcol + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+                    tc_wait_ld();
+                    tc_fence_before();
+#pragma unroll
+                    for (int m = 0; m < kRows; ++m) {
+                        const float d = __fadd_rn(__fmul_rn(__uint_as_float(v[m]), 16.f), __uint_as_float(v[m + kRows]));
+                        acc[m] = __float2int_rn(__fmul_rn(d, 512.f)) - d_rq[m];
+                    }
+                }
+            }
+            epilogue(d_pi, d_rt, d_ka, d_kb, acc);
+            dv = false;
+        };
         while (rp.i < nloc) {
             const GemmProblem& pr = P.p[it.pi];
             const int ka = it.kt;
@@ -788,6 +838,9 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
                 for (int m = 0; m < DPR; ++m) dacc[s4][m] = 0;
             for (int e = 0; e < len; ++e, rp.next(R)) {
+                if constexpr (kTC) {
+                    if (dv && e == kDeferTiles) finish_deferred();
+                }
                 const int s = rp.slot();
                 if (alive && rp.cp == 0) {
                     alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[rp.q]), rp.qph));
@@ -856,39 +909,25 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                     }
                 }
             }
-            int acc[16];
-#pragma unroll
-            for (int m = 0; m < 16; ++m) acc[m] = 0;
             if constexpr (kTC) {
-                if (alive) {
-                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->dfull), seg_idx & 1));
-                    if (!alive && lane == 0) fail(c, P.err, kErrWaitD);
-                }
-                if (alive) {
-                    // D column m: high parts of row m; column m + kRows: low parts
-                    constexpr int kRows = btile_rows(PATH, DPR);
-                    tc_fence_after();
-                    uint32_t v[32];
-                    tmem_ld16(tmem + lane_base + kAccCol, *reinterpret_cast<uint32_t(*)[16]>(v));
-                    if constexpr (kRows == 16) tmem_ld16(tmem + lane_base + kAccCol + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-                    tc_wait_ld();
-                    tc_fence_before();
+                if (dv) finish_deferred();  // the previous segment, if this one was short
+                d_pi = it.pi;
+                d_rt = it.rt;
+                d_ka = ka;
+                d_kb = ka + len;
+                d_seg = seg_idx;
 #pragma unroll
-                    for (int m = 0; m < kRows; ++m) {
-                        const float d = __fadd_rn(__fmul_rn(__uint_as_float(v[m]), 16.f), __uint_as_float(v[m + kRows]));
-                        acc[m] = __float2int_rn(__fmul_rn(d, 512.f)) - (rhi[m] - rlo[m]);
-                    }
-                }
+                for (int m = 0; m < 16; ++m) d_rq[m] = rhi[m] - rlo[m];
+                dv = true;
             } else {
+                int acc[16];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) acc[m] = 0;
 #pragma unroll
                 for (int m = 0; m < DPR; ++m)
                     acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) - (rhi[m] - rlo[m]);
+                epilogue(it.pi, it.rt, ka, ka + len, acc);
             }
-            if (seg_idx == 0) {
-                if (asc_mine) c->asc[tid / 16][tid % 16] = asc_reg;
-                named_bar_sync(1, 128);
-            }
-            segment_epilogue(P, c, p0, it.pi, it.rt, ka, ka + len, acc, tid, alive, pend, npend);
             ++seg_idx;
             nbatch += (len + kMmaBatch - 1) / kMmaBatch;
             // next segment: k tile 0 of the next row tile
@@ -898,6 +937,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 ++it.pi;
             }
         }
+        if (dv) finish_deferred();
         finish_pending(P, c, p0, pend, npend, tid, alive);
     }
 
