@@ -67,7 +67,7 @@ namespace {
 
 constexpr int kChunk = 4;            // k tiles per ring chunk (16 KiB of weights)
 constexpr int kMaxRing = 6;          // chunks in the ring (upper bound)
-constexpr int kCtrlBytes = 1024;
+constexpr int kCtrlBytes = 2048;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kAccCol = 0;      // D: two accumulators (alternate segments) of 32 fp32 columns
 constexpr uint32_t kACol = 64;       // A: kATiles buffers of one k tile each
@@ -76,7 +76,7 @@ constexpr int kATiles = 6;
 constexpr int kDeferTiles = 5;       // a segment's epilogue runs this many tiles into the next one
 constexpr int kMmaBatch = 2;         // k tiles per MMA-issuer wait
 constexpr int kBatchBars = 8;        // MMA batch completion barriers (> kATiles)
-constexpr int kSmemTarget = 100 * 1024;
+constexpr int kSmemTarget = 101 * 1024;
 constexpr int kPrepThreads = 256;
 constexpr int kPrepGroups = 4;     // 8-element groups of one row per thread and pass
 
@@ -100,6 +100,7 @@ struct Ctrl {
     int failed;
     int flag[2];
     float asc[BITMTP_MAX_GROUP][16];  // dequant scale per (problem - p0, row)
+    GemmProblem prob[BITMTP_MAX_GROUP];  // copy of the problem table
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
@@ -151,11 +152,14 @@ __device__ __forceinline__ uint4 unit16(uint32_t lo, uint32_t hi, uint32_t plo, 
                       __byte_perm(hi, phi, 0x5140), __byte_perm(hi, phi, 0x7362));
 }
 
-__device__ __forceinline__ int find_problem_by_tile(const GemmParams& P, long long t) {
+// Problem holding flattened tile t.  pp: the problem table (a shared-memory
+// copy in the GEMM: indexing the kernel parameter with a runtime index costs
+// a slow dependent load per field).
+__device__ __forceinline__ int find_problem_by_tile(const GemmProblem* pp, int np, long long t) {
     int pi = 0;
 #pragma unroll 1
-    for (int i = 1; i < P.n_problems; ++i)
-        if (t >= P.p[i].tile_begin) pi = i;
+    for (int i = 1; i < np; ++i)
+        if (t >= pp[i].tile_begin) pi = i;
     return pi;
 }
 __device__ __forceinline__ long long range_start(int b, long long T, int n) {
@@ -169,16 +173,16 @@ __device__ __forceinline__ int range_owner(long long t, long long T, int n) {
 // Flattened-tile walker: (problem, row tile, k tile) advancing with k fastest.
 struct TileIter {
     int pi, rt, kt;
-    __device__ void init(const GemmParams& P, long long t) {
-        pi = find_problem_by_tile(P, t);
-        const long long local = t - P.p[pi].tile_begin;
-        rt = static_cast<int>(local / P.p[pi].kt);
-        kt = static_cast<int>(local % P.p[pi].kt);
+    __device__ void init(const GemmProblem* pp, int np, long long t) {
+        pi = find_problem_by_tile(pp, np, t);
+        const int local = static_cast<int>(t - pp[pi].tile_begin);  // < nt * kt < 2^31
+        rt = local / pp[pi].kt;
+        kt = local - rt * pp[pi].kt;
     }
-    __device__ void next(const GemmParams& P) {
-        if (++kt == P.p[pi].kt) {
+    __device__ void next(const GemmProblem* pp) {
+        if (++kt == pp[pi].kt) {
             kt = 0;
-            if (++rt == P.p[pi].nt) {
+            if (++rt == pp[pi].nt) {
                 rt = 0;
                 ++pi;
             }
@@ -218,16 +222,16 @@ struct RingPos {
 // range into consecutive ring slots, one copy per run that is contiguous in
 // global memory (within one problem); all copies complete on `bar`.  Run by
 // a whole converged warp; only the lane with `on` set issues.
-__device__ void issue_weights(const GemmParams& P, long long first, int count, uint8_t* dst, uint32_t bar,
+__device__ void issue_weights(const GemmProblem* pp, int np, long long first, int count, uint8_t* dst, uint32_t bar,
                               uint64_t pol, uint32_t on) {
     mbar_arrive_expect_tx_if(on, bar, static_cast<uint32_t>(count * kTileBytes));
     TileIter it;
-    it.init(P, first);
+    it.init(pp, np, first);
     const uint8_t* run_src = nullptr;
     int run_len = 0, run_pi = -1;
     uint8_t* run_dst = dst;
     for (int k = 0; k < count; ++k) {
-        const GemmProblem& pr = P.p[it.pi];
+        const GemmProblem& pr = pp[it.pi];
         const uint8_t* src = pr.pk + (static_cast<size_t>(it.rt) * pr.kt + it.kt) * kTileBytes;
         if (run_len == 0 || it.pi != run_pi) {
             if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * kTileBytes, bar, pol);
@@ -237,23 +241,23 @@ __device__ void issue_weights(const GemmParams& P, long long first, int count, u
             run_pi = it.pi;
         }
         ++run_len;
-        it.next(P);
+        it.next(pp);
     }
     if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * kTileBytes, bar, pol);
 }
 
 // The same for the activation tiles (BT bytes each) of those tiles: a run
 // ends where the k index wraps to the next row tile or the problem changes.
-__device__ void issue_acts(const GemmParams& P, long long first, int count, int BT, uint8_t* dst, uint32_t bar,
-                           uint64_t pol, uint32_t on) {
+__device__ void issue_acts(const GemmProblem* pp, int np, long long first, int count, int BT, uint8_t* dst,
+                           uint32_t bar, uint64_t pol, uint32_t on) {
     mbar_arrive_expect_tx_if(on, bar, static_cast<uint32_t>(count * BT));
     TileIter it;
-    it.init(P, first);
+    it.init(pp, np, first);
     const uint8_t* run_src = nullptr;
     int run_len = 0;
     uint8_t* run_dst = dst;
     for (int k = 0; k < count; ++k) {
-        const uint8_t* src = P.p[it.pi].actb + static_cast<size_t>(it.kt) * BT;
+        const uint8_t* src = pp[it.pi].actb + static_cast<size_t>(it.kt) * BT;
         if (run_len == 0 || src != run_src + static_cast<size_t>(run_len) * BT) {
             if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * BT, bar, pol);
             run_dst = dst + k * BT;
@@ -261,7 +265,7 @@ __device__ void issue_acts(const GemmParams& P, long long first, int count, int 
             run_len = 0;
         }
         ++run_len;
-        it.next(P);
+        it.next(pp);
     }
     if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * BT, bar, pol);
 }
@@ -501,7 +505,7 @@ struct Pending {
 // holding the row tile's last k tile -- and recorded in `pend`.
 __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int pi, int rt, int ka, int kb,
                                  const int (&acc)[16], int tid, bool alive, Pending* pend, int& npend) {
-    const GemmProblem& pr = P.p[pi];
+    const GemmProblem& pr = c->prob[pi];
     const int M = pr.M;
     const int n = rt * kTileN + tid;
     if (ka == 0 && kb == pr.kt) {
@@ -548,7 +552,7 @@ __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pendi
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const bool mine = k < npend && (k == 0 ? last0 : last1);
-        const int M = mine ? P.p[pend[k].pi].M : 0;
+        const int M = mine ? c->prob[pend[k].pi].M : 0;
         const int* sum = P.slots + (mine ? static_cast<size_t>(pend[k].b_last) * 16 * kTileN : 0);
 #pragma unroll
         for (int m = 0; m < 16; ++m) tot[k][m] = (m < M) ? __ldcg(sum + m * kTileN + tid) : 0;
@@ -556,7 +560,7 @@ __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pendi
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         if (!(k < npend && (k == 0 ? last0 : last1))) continue;
-        const GemmProblem& pr = P.p[pend[k].pi];
+        const GemmProblem& pr = c->prob[pend[k].pi];
         const int M = pr.M;
         int* sum = P.slots + static_cast<size_t>(pend[k].b_last) * 16 * kTileN;
         const int n = pend[k].rt * kTileN + tid;
@@ -604,10 +608,18 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     const long long t_begin = range_start(b, T, P.nctas);
     const int nloc = static_cast<int>(range_start(b + 1, T, P.nctas) - t_begin);
     const int nchunks = (nloc + kChunk - 1) / kChunk;
-    const int p0 = find_problem_by_tile(P, t_begin);
-    const int p1 = find_problem_by_tile(P, t_begin + nloc - 1);
+    const int np = P.n_problems;
 
     // ------------------------------------------------------------ set-up --
+    // the problem table, copied once into shared memory (word by word)
+    static_assert(sizeof(GemmProblem) % 4 == 0, "problem record not word-sized");
+    {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(&P.p[0]);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&c->prob[0]);
+        const int words = np * static_cast<int>(sizeof(GemmProblem) / 4);
+        for (int z = tid; z < words; z += kGemmThreads) dst[z] = src[z];
+    }
+    const GemmProblem* pp = c->prob;
     if (tid == 0) {
         for (int q = 0; q < R; ++q) {
             mbar_init(smem_u32(&c->wfull[q]), 1);
@@ -632,6 +644,8 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     if constexpr (kTC) tc_fence_after();
     const uint32_t tmem = kTC ? c->tmem_base : 0u;
     pdl_launch_dependents();
+    const int p0 = find_problem_by_tile(pp, np, t_begin);
+    const int p1 = find_problem_by_tile(pp, np, t_begin + nloc - 1);
 
     const int npre = nchunks < R ? nchunks : R;
     int w_issued = 0, b_issued = 0;  // chunks whose copies were requested (warp 4)
@@ -643,13 +657,13 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         // weights first: they do not depend on the kernels before this one
         const uint64_t pol = policy_evict_first();
         for (int j = 0; j < npre; ++j)
-            issue_weights(P, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk),
+            issue_weights(pp, np, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk),
                           Wr + static_cast<size_t>(j) * kChunk * kTileBytes, smem_u32(&c->wfull[j]), pol, leader);
         w_issued = npre;
         pdl_wait();  // the activation tiles are written by the preparation kernel
         const uint64_t pol_b = policy_evict_last();
         for (int j = 0; j < npre; ++j)
-            issue_acts(P, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk), BT,
+            issue_acts(pp, np, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk), BT,
                        Br + static_cast<size_t>(j) * kChunk * BT, smem_u32(&c->bfull[j]), pol_b, leader);
         b_issued = npre;
         // refill ring slots as they are released
@@ -661,10 +675,10 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             }
             const long long first = t_begin + static_cast<long long>(j) * kChunk;
             const int cnt = min(kChunk, nloc - j * kChunk);
-            issue_weights(P, first, cnt, Wr + static_cast<size_t>(q) * kChunk * kTileBytes,
+            issue_weights(pp, np, first, cnt, Wr + static_cast<size_t>(q) * kChunk * kTileBytes,
                           smem_u32(&c->wfull[q]), pol, leader);
             w_issued = j + 1;
-            issue_acts(P, first, cnt, BT, Br + static_cast<size_t>(q) * kChunk * BT, smem_u32(&c->bfull[q]),
+            issue_acts(pp, np, first, cnt, BT, Br + static_cast<size_t>(q) * kChunk * BT, smem_u32(&c->bfull[q]),
                        pol_b, leader);
             b_issued = j + 1;
         }
@@ -684,13 +698,13 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             constexpr uint32_t kUnit = kBR * 16;      // bytes of one 16-k unit
             const uint32_t bbase = smem_u32(Br);
             TileIter it;
-            it.init(P, t_begin);
+            it.init(pp, np, t_begin);
             RingPos rp;
             rp.reset();
             int nbatch = 0, seg = 0;
             bool ok = true;
             while (rp.i < nloc && ok) {
-                const int len = min(P.p[it.pi].kt - it.kt, nloc - rp.i);
+                const int len = min(pp[it.pi].kt - it.kt, nloc - rp.i);
                 const uint32_t dcol = tmem + kAccCol + (seg & 1) * 32;
                 for (int e = 0; e < len && ok;) {
                     const int nb = min(kMmaBatch, len - e);
@@ -744,7 +758,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 ++seg;
                 // next segment: k tile 0 of the next row tile
                 it.kt = 0;
-                if (++it.rt == P.p[it.pi].nt) {
+                if (++it.rt == pp[it.pi].nt) {
                     it.rt = 0;
                     ++it.pi;
                 }
@@ -756,14 +770,14 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         // (timed-out) wait only clears `alive`; every named barrier is still
         // executed by all four warps.
         TileIter it;
-        it.init(P, t_begin);
+        it.init(pp, np, t_begin);
         pdl_wait();  // outputs and workspace: the preparation kernel has finished
         // dequant scales of problems p0..p1 (at most 8 x 16: one per thread),
         // first needed by the first epilogue, which stores and publishes them
         float asc_reg = 0.f;
         const bool asc_mine = tid < (p1 - p0 + 1) * 16;
         if (asc_mine) {
-            const GemmProblem& pr = P.p[p0 + tid / 16];
+            const GemmProblem& pr = pp[p0 + tid / 16];
             if (tid % 16 < pr.M) asc_reg = __ldcg(pr.asc + tid % 16);
         }
         Pending pend[2];
@@ -827,7 +841,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             dv = false;
         };
         while (rp.i < nloc) {
-            const GemmProblem& pr = P.p[it.pi];
+            const GemmProblem& pr = pp[it.pi];
             const int ka = it.kt;
             const int len = min(pr.kt - ka, nloc - rp.i);
             int rlo[16], rhi[16];
