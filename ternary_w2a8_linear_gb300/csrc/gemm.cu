@@ -576,17 +576,17 @@ __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pendi
     named_bar_sync(1, 128);
 }
 
-// The preparation kernel's prefix sums of rows 0..15 at k tiles ka and kb
-// (zero for rows >= M): their difference is the codes of k tiles [ka, kb)
-// summed.  Issued at the start of a segment, used at its end.
-__device__ __forceinline__ void load_code_sums(const GemmProblem& pr, int ka, int kb, int (&lo)[16], int (&hi)[16]) {
-    const int* rsp = pr.rsp;
-    const int stride = pr.kt + 1;
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        lo[m] = (m < pr.M) ? __ldcg(rsp + m * stride + ka) : 0;
-        hi[m] = (m < pr.M) ? __ldcg(rsp + m * stride + kb) : 0;
-    }
+// The preparation kernel's prefix sums at k tiles ka and kb: lane m < 16
+// loads row m at ka, lane 16 + m row m at kb (zero for rows >= M).  One load
+// per lane, issued at the start of a segment; code_sum() reads the
+// difference at its end.
+__device__ __forceinline__ int load_code_sum_lane(const GemmProblem& pr, int ka, int kb, int lane) {
+    const int m = lane & 15;
+    return (m < pr.M) ? __ldcg(pr.rsp + m * (pr.kt + 1) + ((lane & 16) ? kb : ka)) : 0;
+}
+// Codes of row m summed over the segment (every lane must take part).
+__device__ __forceinline__ int code_sum(int v, int m) {
+    return __shfl_sync(0xffffffffu, v, 16 + m) - __shfl_sync(0xffffffffu, v, m);
 }
 
 template <int PATH, int DPR>
@@ -844,8 +844,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             const GemmProblem& pr = pp[it.pi];
             const int ka = it.kt;
             const int len = min(pr.kt - ka, nloc - rp.i);
-            int rlo[16], rhi[16];
-            load_code_sums(pr, ka, ka + len, rlo, rhi);
+            const int rsl = load_code_sum_lane(pr, ka, ka + len, lane);
             int dacc[4][DPR];
 #pragma unroll
             for (int s4 = 0; s4 < 4; ++s4)
@@ -931,7 +930,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 d_kb = ka + len;
                 d_seg = seg_idx;
 #pragma unroll
-                for (int m = 0; m < 16; ++m) d_rq[m] = rhi[m] - rlo[m];
+                for (int m = 0; m < 16; ++m) d_rq[m] = code_sum(rsl, m);
                 dv = true;
             } else {
                 int acc[16];
@@ -939,7 +938,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 for (int m = 0; m < 16; ++m) acc[m] = 0;
 #pragma unroll
                 for (int m = 0; m < DPR; ++m)
-                    acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) - (rhi[m] - rlo[m]);
+                    acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) - code_sum(rsl, m);
                 epilogue(it.pi, it.rt, ka, ka + len, acc);
             }
             ++seg_idx;
