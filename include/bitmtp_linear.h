@@ -79,8 +79,10 @@ extern "C" {
  * integer dot-product path (dp4a, widths 1..4). */
 #define BITMTP_FLAG_FORCE_TC   0x2u
 #define BITMTP_FLAG_FORCE_DP   0x4u
-/* (Forcing the tensor path at widths 1..2 uses its 8-row activation tile;
- * forcing dp4a is valid for widths 1..4.) */
+/* (The default table: dp4a for widths 1..4, tensor cores with an 8-row
+ * activation tile for 5..8 and a 16-row tile for 9..16.  Forcing the tensor
+ * path at widths 1..4 uses its 8-row tile; forcing dp4a is valid for widths
+ * 1..4.) */
 
 /*
  * Packed ternary weights (this library's own layout; the pages only say the

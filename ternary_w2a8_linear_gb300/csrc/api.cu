@@ -182,8 +182,9 @@ int check_problem(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M
 }
 
 // Width-specialised operator choice (the analogue of picking packed low-bit
-// operators by replay width and input/output dimensions): dp4a for one or two
-// rows, tensor cores with an 8-row activation tile up to 8 rows, 16 rows above.
+// operators by replay width and input/output dimensions), from measured call
+// times on GB300: dp4a up to four rows, tensor cores with an 8-row activation
+// tile up to 8 rows, 16 rows above.
 int choose_path(int max_m, unsigned flags, int* dp_rows) {
     const int r = max_m <= 1 ? 1 : (max_m <= 2 ? 2 : 4);
     if (flags & BITMTP_FLAG_FORCE_DP) {
@@ -191,7 +192,7 @@ int choose_path(int max_m, unsigned flags, int* dp_rows) {
         *dp_rows = r;
         return kPathDP;
     }
-    if (!(flags & BITMTP_FLAG_FORCE_TC) && max_m <= 2) {
+    if (!(flags & BITMTP_FLAG_FORCE_TC) && max_m <= 4) {
         *dp_rows = r;
         return kPathDP;
     }
