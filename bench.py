@@ -57,7 +57,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-per-width", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
-    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--e2e-steps", type=int, default=1000)
     p.add_argument("--mode", choices=["grouped", "chained"], default="grouped",
                    help="grouped: each width's seven projections in one launch; chained: one launch each")
     return p.parse_args()
@@ -76,14 +76,6 @@ def step_bytes():
         for _, K, N in inputs.BITNET2B_PROJ:
             tot += algorithmic_bytes(K, N, M)
     return tot
-
-
-def out_bytes_per_step():
-    return sum(M * N * 2 for M in WIDTHS for _, _, N in inputs.BITNET2B_PROJ)
-
-
-def in_bytes_per_step():
-    return sum(M * K * 2 for M in WIDTHS for _, K, _ in inputs.BITNET2B_PROJ)
 
 
 def load_peaks():
@@ -306,29 +298,53 @@ def run_ours(args, rank, world):
 
 
 def run_e2e(args, L, torch, dev, stream, weights, rank, world):
-    """Same workload through the binding with host buffers: every step copies
-    its activations host->device from pinned memory and reads the outputs back."""
+    """Same workload through the library's C ABI with host buffers: every step
+    copies its activations host->device from pinned memory (one copy of the
+    16 rows of every projection; each width reads its first M rows), runs the
+    four grouped calls and reads every output back device->host (one copy),
+    then synchronises."""
     R = len(weights)
-    hx = [torch.from_numpy(inputs.bitnet2b_act(p, 16).view(np.int16)).view(torch.bfloat16).pin_memory()
-          for p in range(len(inputs.BITNET2B_PROJ))]
-    dx = [torch.empty_like(h, device=dev) for h in hx]
-    dy = [torch.empty((16, N), dtype=torch.bfloat16, device=dev) for _, _, N in inputs.BITNET2B_PROJ]
-    hy = [torch.empty((16, N), dtype=torch.bfloat16).pin_memory() for _, _, N in inputs.BITNET2B_PROJ]
+    proj = inputs.BITNET2B_PROJ
+    kofs, off = [], 0
+    for _, K, _ in proj:
+        kofs.append(off)
+        off += 16 * K
+    x_host = torch.empty(off, dtype=torch.int16).pin_memory()
+    for p in range(len(proj)):
+        _, K, _ = proj[p]
+        x_host[kofs[p]:kofs[p] + 16 * K] = torch.from_numpy(inputs.bitnet2b_act(p, 16).view(np.int16).reshape(-1))
+    x_dev = torch.empty_like(x_host, device=dev)
+    yofs, off = {}, 0
+    for M in WIDTHS:
+        for p, (_, _, N) in enumerate(proj):
+            yofs[(M, p)] = off
+            off += M * N
+    y_dev = torch.empty(off, dtype=torch.int16, device=dev)
+    y_host = torch.empty(off, dtype=torch.int16).pin_memory()
+    descs = {}
+    for c in range(R):
+        for M in WIDTHS:
+            d = [L.GemmDesc(pk.data_ptr(), w, N, K, M,
+                            L.Act(L.BF16, x_dev.data_ptr() + 2 * kofs[p], K, None),
+                            L.Out(L.BF16, y_dev.data_ptr() + 2 * yofs[(M, p)], N, None, 0))
+                 for p, (pk, w, K, N) in enumerate(weights[c])]
+            descs[(c, M)] = ((L.GemmDesc * len(d))(*d), len(d))
+    nb = L.bitmtp_linear_workspace_bytes_grouped(list(descs[(0, max(WIDTHS))][0]))
+    ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    lib = L.load()
+    cs = L.ctypes.c_void_p(stream.cuda_stream)
+    wsp = L.ctypes.c_void_p(ws.data_ptr())
     steps = args.e2e_steps
 
     def one(s):
+        x_dev.copy_(x_host, non_blocking=True)
         for M in WIDTHS:
-            c = (s * len(WIDTHS) + WIDTHS.index(M)) % R
-            for p in range(len(weights[c])):
-                dx[p][:M].copy_(hx[p][:M], non_blocking=True)
-            if args.mode == "grouped":
-                L.gemm_grouped([dict(pk=pk, w_scale=w, N=N, K=K, x=dx[p][:M], y=dy[p][:M])
-                                for p, (pk, w, K, N) in enumerate(weights[c])], stream=stream)
-            else:
-                for p, (pk, w, K, N) in enumerate(weights[c]):
-                    L.gemm(pk, w, N, K, dx[p][:M], y=dy[p][:M], stream=stream)
-            for p in range(len(weights[c])):
-                hy[p][:M].copy_(dy[p][:M], non_blocking=True)
+            arr, n = descs[((s * len(WIDTHS) + WIDTHS.index(M)) % R, M)]
+            st = lib.bitmtp_linear_gemm_grouped(arr, n, wsp, nb, L.FLAG_PDL, cs)
+            if st != L.OK:
+                raise L.BitmtpError(st, "gemm_grouped")
+        y_host.copy_(y_dev, non_blocking=True)
         stream.synchronize()
 
     with torch.cuda.stream(stream):
@@ -341,7 +357,7 @@ def run_e2e(args, L, torch, dev, stream, weights, rank, world):
         t1 = time.perf_counter()
     sec = dist_max(t1 - t0, world)
     return {"value": round(step_bytes() * steps * world / sec / 1e9, 2), "unit": "GB/s",
-            "h2d_bytes_per_step": in_bytes_per_step(), "d2h_bytes_per_step": out_bytes_per_step(),
+            "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
             "steps": steps, "ms_per_step": round(sec * 1e3 / steps, 4)}
 
 
