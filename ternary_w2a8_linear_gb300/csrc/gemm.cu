@@ -78,7 +78,7 @@ constexpr int kMmaBatch = 2;         // k tiles per MMA-issuer wait
 constexpr int kBatchBars = 8;        // MMA batch completion barriers (> kATiles)
 constexpr int kSmemTarget = 101 * 1024;
 constexpr int kPrepThreads = 256;
-constexpr int kPrepGroups = 4;     // 8-element groups of one row per thread and pass
+constexpr int kPrepUnits = 2;      // 16-element units of one row per thread and pass
 
 enum : int {
     kErrWaitW = 0x101,
@@ -136,20 +136,6 @@ __device__ __forceinline__ uint32_t e4m3x2_small(float a, float b) {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
     return r;
-}
-
-// Bytes (low 8 bits of each value) of eight values, as two words.
-__device__ __forceinline__ void bytes8(const uint32_t (&b)[8], uint32_t& lo, uint32_t& hi) {
-    lo = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
-    hi = __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
-}
-
-// One 16-k unit of one operand row from the bytes of k 0..7 (lo, hi: this
-// lane) and k 8..15 (plo, phi: the partner lane), in the unit byte order:
-// register s = bytes {k 2s, k 2s+8, k 2s+1, k 2s+9}.
-__device__ __forceinline__ uint4 unit16(uint32_t lo, uint32_t hi, uint32_t plo, uint32_t phi) {
-    return make_uint4(__byte_perm(lo, plo, 0x5140), __byte_perm(lo, plo, 0x7362),
-                      __byte_perm(hi, phi, 0x5140), __byte_perm(hi, phi, 0x7362));
 }
 
 // Problem holding flattened tile t.  pp: the problem table (a shared-memory
@@ -323,17 +309,17 @@ __device__ __forceinline__ const char* act_row(const GemmProblem& pr, int m) {
 // ---------------------------------------------------- activation operand --
 // One CTA per (problem, row m < btile_rows).  Writes row m of every
 // activation tile of the problem (zeros for m >= M and beyond K), the prefix
-// sums rsp[m][0..kt] of the row's codes over k tiles, and asc[m].  The whole
-// row stays in registers between the absmax and the quantisation (at most
-// kPrepGroups 8-element groups per thread: K <= 32768 with 512 threads), so
-// the row is read once, with all loads in flight together.
+// sums rsp[m][0..kt] of the row's codes over k tiles, and asc[m].  Each
+// thread owns whole 16-k units; rows of up to kPass units (K <= 8192) stay in
+// registers between the absmax and the quantisation, longer rows are read
+// twice.
 template <int PATH, int DPR>
 __global__ void __launch_bounds__(kPrepThreads, 4)
 act_prep_kernel(const __grid_constant__ GemmParams P) {
     constexpr int kRows = btile_rows(PATH, DPR);
     constexpr int kBRows = btile_brows(PATH, DPR);
     constexpr int BT = btile_bytes(PATH, DPR);
-    constexpr int kPass = kPrepThreads * kPrepGroups;  // 8-element groups per pass
+    constexpr int kPass = kPrepThreads * kPrepUnits;  // 16-element units per pass
     __shared__ float red[kPrepThreads / 32];
     __shared__ int tsum[BITMTP_MAX_K / kTileK];
     pdl_launch_dependents();  // the GEMM may start streaming weights now
@@ -346,33 +332,35 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     const bool raw = pr.act_kind != BITMTP_Q8;
     const char* row = live ? act_row(pr, m) : nullptr;
     const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-    const int ngroups = pr.kt * 16;  // 8-element groups, the zero tail of the last tile included
-    const int npass = (ngroups + kPass - 1) / kPass;
+    const int nunits = pr.kt * 8;  // 16-element units, the zero tail of the last tile included
+    const int npass = (nunits + kPass - 1) / kPass;
 
     // The activations may come from the previous kernel on the stream, and the
     // previous GEMM on this workspace may still be reading it.
     pdl_wait();
 
-    // Rows of up to kPass groups (K <= 8192) stay in registers between the
-    // absmax and the quantisation; longer rows are read twice.
-    float v[kPrepGroups][8];
-    float amax = 0.f;
-    for (int ps = 0; ps < npass; ++ps) {
+    float v[kPrepUnits][16];
+    auto load_pass = [&](int ps) {
 #pragma unroll
-        for (int j = 0; j < kPrepGroups; ++j) {
-            const int g = ps * kPass + j * kPrepThreads + tid;
-            if (live && g < ngroups) {
-                load8(pr, row, vec_ok, g * 8, v[j]);
+        for (int j = 0; j < kPrepUnits; ++j) {
+            const int u = ps * kPass + j * kPrepThreads + tid;
+            if (live && u < nunits) {
+                load8(pr, row, vec_ok, u * 16, *reinterpret_cast<float(*)[8]>(&v[j][0]));
+                load8(pr, row, vec_ok, u * 16 + 8, *reinterpret_cast<float(*)[8]>(&v[j][8]));
             } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
+                for (int i = 0; i < 16; ++i) v[j][i] = 0.f;
             }
         }
+    };
+    float amax = 0.f;
+    for (int ps = 0; ps < npass; ++ps) {
+        load_pass(ps);
         if (raw) {
 #pragma unroll
-            for (int j = 0; j < kPrepGroups; ++j)
+            for (int j = 0; j < kPrepUnits; ++j)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
+                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
         }
     }
 #pragma unroll
@@ -384,74 +372,63 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
     const float s = quant_scale(amax);
 
-    // Each group of 16 consecutive threads covers one k tile: ngroups and
-    // kPrepThreads are multiples of 16, so the shuffles below always see
-    // whole groups.
+    // Eight consecutive threads cover one k tile; units per pass and units of
+    // the row are multiples of 8, so the 8-lane sums below see whole tiles.
     for (int ps = 0; ps < npass; ++ps) {
-      if (npass > 1) {
+        if (npass > 1) load_pass(ps);
 #pragma unroll
-        for (int j = 0; j < kPrepGroups; ++j) {
-            const int g = ps * kPass + j * kPrepThreads + tid;
-            if (live && g < ngroups) {
-                load8(pr, row, vec_ok, g * 8, v[j]);
+        for (int j = 0; j < kPrepUnits; ++j) {
+            if (ps * kPass + j * kPrepThreads >= nunits) break;  // uniform over the block
+            const int u = ps * kPass + j * kPrepThreads + tid;
+            const bool uv = u < nunits;
+            // codes as exact small floats: clamp(rint(RN(x * s))) gives the same
+            // values as the integer quantiser (quant.cuh), without conversions
+            float qf[16];
+            float fsum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                qf[i] = raw ? ((amax > 0.f) ? fminf(fmaxf(rintf(__fmul_rn(v[j][i], s)), -127.f), 127.f) : 0.f)
+                            : v[j][i];
+                fsum += qf[i];
+            }
+            int rsum = static_cast<int>(fsum);  // |sum| <= 2032: exact
+            const int kt = u >> 3;
+            uint8_t* unit = pr.actb + static_cast<size_t>(kt) * BT + (u & 7) * (kBRows * 16);
+            // register si of a unit row holds k = {2si, 2si+8, 2si+1, 2si+9}
+            if constexpr (PATH == kPathDP) {
+                uint32_t reg[4];
+#pragma unroll
+                for (int si = 0; si < 4; ++si) {
+                    const uint32_t b0 = static_cast<uint32_t>(static_cast<int>(qf[2 * si])) & 0xFFu;
+                    const uint32_t b1 = static_cast<uint32_t>(static_cast<int>(qf[2 * si + 8])) & 0xFFu;
+                    const uint32_t b2 = static_cast<uint32_t>(static_cast<int>(qf[2 * si + 1])) & 0xFFu;
+                    const uint32_t b3 = static_cast<uint32_t>(static_cast<int>(qf[2 * si + 9]));
+                    reg[si] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                }
+                if (uv) *reinterpret_cast<uint4*>(unit + m * 16) = make_uint4(reg[0], reg[1], reg[2], reg[3]);
             } else {
+                // operand row m: high parts h = floor(q / 16); row m + kRows: low
+                // parts l = q - 16 h; both exact small floats, e4m3 bytes
+                float h[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
+                for (int i = 0; i < 16; ++i) h[i] = floorf(qf[i] * 0.0625f);
+                uint32_t hr[4], lr[4];
+#pragma unroll
+                for (int si = 0; si < 4; ++si) {
+                    const int k0 = 2 * si, k1 = 2 * si + 8, k2 = 2 * si + 1, k3 = 2 * si + 9;
+                    hr[si] = e4m3x2_small(h[k0], h[k1]) | (e4m3x2_small(h[k2], h[k3]) << 16);
+                    lr[si] = e4m3x2_small(fmaf(h[k0], -16.f, qf[k0]), fmaf(h[k1], -16.f, qf[k1])) |
+                             (e4m3x2_small(fmaf(h[k2], -16.f, qf[k2]), fmaf(h[k3], -16.f, qf[k3])) << 16);
+                }
+                if (uv) {
+                    *reinterpret_cast<uint4*>(unit + m * 16) = make_uint4(hr[0], hr[1], hr[2], hr[3]);
+                    *reinterpret_cast<uint4*>(unit + (m + kRows) * 16) = make_uint4(lr[0], lr[1], lr[2], lr[3]);
+                }
             }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, o);
+            if (uv && (tid & 7) == 0) tsum[kt] = rsum;
         }
-      }
-#pragma unroll
-      for (int j = 0; j < kPrepGroups; ++j) {
-        if (ps * kPass + j * kPrepThreads >= ngroups) break;  // uniform over the block
-        const int g = ps * kPass + j * kPrepThreads + tid;
-        const bool gv = g < ngroups;
-        // codes as exact small floats: clamp(rint(RN(x * s))) gives the same
-        // values as the integer quantiser (quant.cuh), without conversions
-        float qf[8];
-        float fsum = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            qf[i] = raw ? ((amax > 0.f) ? fminf(fmaxf(rintf(__fmul_rn(v[j][i], s)), -127.f), 127.f) : 0.f)
-                        : v[j][i];
-            fsum += qf[i];
-        }
-        int rsum = static_cast<int>(fsum);  // |sum| <= 1016: exact
-        const int kt = g >> 4, gg = g & 15;
-        uint8_t* unit = pr.actb + static_cast<size_t>(kt) * BT + (gg >> 1) * (kBRows * 16);
-        // operand row m holds the codes (dp4a) or, on the tensor paths, the
-        // high parts h = q >> 4 (row m) and low parts l = q & 15 (row m + kRows)
-        uint32_t alo, ahi, blo = 0u, bhi = 0u;
-        if constexpr (PATH == kPathDP) {
-            uint32_t ba[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ba[i] = static_cast<uint32_t>(static_cast<int>(qf[i]));
-            bytes8(ba, alo, ahi);
-        } else {
-            // h = floor(q / 16), l = q - 16 h, both exact small floats
-            uint32_t hp[4], lp[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float h0 = floorf(qf[2 * i] * 0.0625f), h1 = floorf(qf[2 * i + 1] * 0.0625f);
-                hp[i] = e4m3x2_small(h0, h1);
-                lp[i] = e4m3x2_small(fmaf(h0, -16.f, qf[2 * i]), fmaf(h1, -16.f, qf[2 * i + 1]));
-            }
-            alo = hp[0] | (hp[1] << 16);
-            ahi = hp[2] | (hp[3] << 16);
-            blo = lp[0] | (lp[1] << 16);
-            bhi = lp[2] | (lp[3] << 16);
-        }
-        const uint32_t palo = __shfl_xor_sync(0xffffffffu, alo, 1);
-        const uint32_t pahi = __shfl_xor_sync(0xffffffffu, ahi, 1);
-        if (gv && (gg & 1) == 0) *reinterpret_cast<uint4*>(unit + m * 16) = unit16(alo, ahi, palo, pahi);
-        if constexpr (PATH != kPathDP) {
-            const uint32_t pblo = __shfl_xor_sync(0xffffffffu, blo, 1);
-            const uint32_t pbhi = __shfl_xor_sync(0xffffffffu, bhi, 1);
-            if (gv && (gg & 1) == 0) *reinterpret_cast<uint4*>(unit + (m + kRows) * 16) = unit16(blo, bhi, pblo, pbhi);
-        }
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, o);
-        if (gv && (tid & 15) == 0) tsum[kt] = rsum;
-      }
     }
     __syncthreads();
 
