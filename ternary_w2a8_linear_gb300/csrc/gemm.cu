@@ -500,10 +500,15 @@ __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int
     pe.rt = rt;
     pe.b_first = range_owner(t_first, T, P.nctas);
     pe.b_last = range_owner(t_first + pr.kt - 1, T, P.nctas);
-    int* sum = P.slots + static_cast<size_t>(pe.b_last) * 16 * kTileN;
+    // column tid of the row tile: 16 fp32 slots, four per vector atomic (the
+    // partial sums are integers below 2^24 in magnitude, so fp32 adds are
+    // exact in any order)
+    float4* sum = reinterpret_cast<float4*>(P.slots) + (static_cast<size_t>(pe.b_last) * kTileN + tid) * 4;
 #pragma unroll
-    for (int m = 0; m < 16; ++m)
-        if (alive && m < M) atomicAdd(sum + m * kTileN + tid, acc[m]);
+    for (int g = 0; g < 4; ++g)
+        if (alive && 4 * g < M)
+            atomicAdd(sum + g, make_float4(static_cast<float>(acc[4 * g]), static_cast<float>(acc[4 * g + 1]),
+                                           static_cast<float>(acc[4 * g + 2]), static_cast<float>(acc[4 * g + 3])));
 }
 
 // After the main loop: one fence, one counter increment per split row tile;
@@ -525,29 +530,30 @@ __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pendi
     }
     named_bar_sync(1, 128);
     const int last0 = c->flag[0], last1 = npend > 1 ? c->flag[1] : 0;
-    int tot[2][16];
+    float4 tot[2][4];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const bool mine = k < npend && (k == 0 ? last0 : last1);
         const int M = mine ? c->prob[pend[k].pi].M : 0;
-        const int* sum = P.slots + (mine ? static_cast<size_t>(pend[k].b_last) * 16 * kTileN : 0);
+        const float4* sum = reinterpret_cast<const float4*>(P.slots) +
+                            (mine ? (static_cast<size_t>(pend[k].b_last) * kTileN + tid) * 4 : 0);
 #pragma unroll
-        for (int m = 0; m < 16; ++m) tot[k][m] = (m < M) ? __ldcg(sum + m * kTileN + tid) : 0;
+        for (int g = 0; g < 4; ++g) tot[k][g] = (4 * g < M) ? __ldcg(sum + g) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         if (!(k < npend && (k == 0 ? last0 : last1))) continue;
         const GemmProblem& pr = c->prob[pend[k].pi];
         const int M = pr.M;
-        int* sum = P.slots + static_cast<size_t>(pend[k].b_last) * 16 * kTileN;
+        float4* sum = reinterpret_cast<float4*>(P.slots) + (static_cast<size_t>(pend[k].b_last) * kTileN + tid) * 4;
         const int n = pend[k].rt * kTileN + tid;
+        const float* t = reinterpret_cast<const float*>(&tot[k][0]);
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            if (m < M) {
-                if (alive && n < pr.N) store_out(pr, m, n, tot[k][m], c->asc[pend[k].pi - p0][m]);
-                sum[m * kTileN + tid] = 0;
-            }
-        }
+        for (int m = 0; m < 16; ++m)
+            if (alive && m < M && n < pr.N) store_out(pr, m, n, __float2int_rn(t[m]), c->asc[pend[k].pi - p0][m]);
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            if (4 * g < M) sum[g] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (tid == 0) P.counters[pend[k].b_last] = 0u;
     }
     named_bar_sync(1, 128);
