@@ -475,10 +475,18 @@ struct Pending {
     int pi, rt, b_first, b_last;
 };
 
+// Accumulator of the split row tile whose last k tile CTA b holds: four groups
+// of four rows, one float4 per column in each, columns consecutive.  A warp's
+// vector atomics then cover 512 contiguous bytes, and a narrow block touches
+// only the groups its rows occupy.
+__device__ __forceinline__ float4* acc_slot(const GemmParams& P, int b, int g, int col) {
+    return reinterpret_cast<float4*>(P.slots) + (static_cast<size_t>(b) * 4 + g) * kTileN + col;
+}
+
 // Finish one segment (k tiles [ka, kb) of row tile rt of problem pi).
 // acc[m] is the exact partial sum_k T*q for the thread's row.  A whole row
-// tile is written out at once; a split one is added (integer atomics, no
-// return value) into its accumulator in the workspace -- the one of the CTA
+// tile is written out at once; a split one is added (fp32 vector atomics of
+// integer values, no return value) into its accumulator in the workspace -- the one of the CTA
 // holding the row tile's last k tile -- and recorded in `pend`.
 __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int pi, int rt, int ka, int kb,
                                  const int (&acc)[16], int tid, bool alive, Pending* pend, int& npend) {
@@ -500,14 +508,13 @@ __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int
     pe.rt = rt;
     pe.b_first = range_owner(t_first, T, P.nctas);
     pe.b_last = range_owner(t_first + pr.kt - 1, T, P.nctas);
-    // column tid of the row tile: 16 fp32 slots, four per vector atomic (the
+    // column tid of the row tile: one vector atomic per group of four rows (the
     // partial sums are integers below 2^24 in magnitude, so fp32 adds are
     // exact in any order)
-    float4* sum = reinterpret_cast<float4*>(P.slots) + (static_cast<size_t>(pe.b_last) * kTileN + tid) * 4;
 #pragma unroll
     for (int g = 0; g < 4; ++g)
         if (alive && 4 * g < M)
-            atomicAdd(sum + g, make_float4(static_cast<float>(acc[4 * g]), static_cast<float>(acc[4 * g + 1]),
+            atomicAdd(acc_slot(P, pe.b_last, g, tid), make_float4(static_cast<float>(acc[4 * g]), static_cast<float>(acc[4 * g + 1]),
                                            static_cast<float>(acc[4 * g + 2]), static_cast<float>(acc[4 * g + 3])));
 }
 
@@ -535,17 +542,16 @@ __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pendi
     for (int k = 0; k < 2; ++k) {
         const bool mine = k < npend && (k == 0 ? last0 : last1);
         const int M = mine ? c->prob[pend[k].pi].M : 0;
-        const float4* sum = reinterpret_cast<const float4*>(P.slots) +
-                            (mine ? (static_cast<size_t>(pend[k].b_last) * kTileN + tid) * 4 : 0);
+        const int b = mine ? pend[k].b_last : 0;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) tot[k][g] = (4 * g < M) ? __ldcg(sum + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int g = 0; g < 4; ++g)
+            tot[k][g] = (4 * g < M) ? __ldcg(acc_slot(P, b, g, tid)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         if (!(k < npend && (k == 0 ? last0 : last1))) continue;
         const GemmProblem& pr = c->prob[pend[k].pi];
         const int M = pr.M;
-        float4* sum = reinterpret_cast<float4*>(P.slots) + (static_cast<size_t>(pend[k].b_last) * kTileN + tid) * 4;
         const int n = pend[k].rt * kTileN + tid;
         const float* t = reinterpret_cast<const float*>(&tot[k][0]);
 #pragma unroll
@@ -553,7 +559,7 @@ __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pendi
             if (alive && m < M && n < pr.N) store_out(pr, m, n, __float2int_rn(t[m]), c->asc[pend[k].pi - p0][m]);
 #pragma unroll
         for (int g = 0; g < 4; ++g)
-            if (4 * g < M) sum[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (4 * g < M) *acc_slot(P, pend[k].b_last, g, tid) = make_float4(0.f, 0.f, 0.f, 0.f);
         if (tid == 0) P.counters[pend[k].b_last] = 0u;
     }
     named_bar_sync(1, 128);

@@ -47,7 +47,7 @@ struct GemmParams {
     int nctas;
     long long total_tiles;
     unsigned* counters;       // [kMaxCtas] split-row-tile arrival counters (left at zero)
-    int* slots;               // [kMaxCtas][128][16] split-row-tile accumulators, fp32 (left at zero)
+    int* slots;               // [kMaxCtas][4][128][4] split-row-tile accumulators, fp32 (left at zero)
     int* err;                 // device error word
 };
 

@@ -65,7 +65,8 @@ def _check_quant(x_np, is_bf16):
     assert np.array_equal(r.cpu().numpy(), r_ref)
 
 
-@pytest.mark.parametrize("M,K", [(1, 1), (3, 17), (16, 2560), (5, 6912), (2, 11008), (16, 300)])
+@pytest.mark.parametrize("M,K", [(1, 1), (3, 17), (16, 2560), (5, 6912), (2, 11008), (16, 300),
+                                 (3, 32768), (1, 32767)])
 @pytest.mark.parametrize("is_bf16", [False, True])
 def test_quant_act_bitexact(M, K, is_bf16):
     rng = np.random.default_rng(M * 1000 + K)
@@ -217,6 +218,28 @@ def test_degenerate_cases():
     pk = L.pack(dev_tensor(T))
     yz = torch.full((0, N), 1.0, device="cuda")
     L.gemm(pk, w, N, K, torch.zeros((0, K), device="cuda"), y=yz)
+
+
+@pytest.mark.parametrize("K", [32768, 32767])
+@pytest.mark.parametrize("M", [1, 4, 8, 16])
+def test_gemm_max_in_features(K, M):
+    """The largest in-feature count the library accepts (one dp4a width and the
+    three tensor widths): 256 k-tiles per row, the last one ragged for K=32767."""
+    T, w, x = inputs.random_problem(7000 + 10 * M + K % 2, M, 130, K, outliers=True)
+    check_gemm(T, w, x, False, "f32")
+
+
+@pytest.mark.parametrize("M", [1, 4, 8, 16])
+def test_gemm_max_in_features_extreme_sums(M):
+    """All +1 (then all -1) weights against constant rows at the maximum K: every
+    activation code is 127 and acc = +-127 * 32768, the largest magnitude a
+    call can produce."""
+    K = 32768
+    xc = np.full((M, K), -0.61, dtype=np.float32)
+    for sign in (1, -1):
+        T = np.full((130, K), sign, dtype=np.int8)
+        y, acc = run_gemm(T, np.float32(0.02), xc, "f32", "f32")
+        assert torch.all(acc == -sign * 127 * K)
 
 
 def test_pdl_flag_same_result():

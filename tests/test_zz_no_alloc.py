@@ -32,12 +32,14 @@ def lib():
 
 # (N, K, M, activation kind, output dtype, with int32 accumulators):
 # 16 rows on the 16-row tensor tile with row tiles split between CTAs,
-# 5 rows on the 8-row tensor tile, 1 row on the dp4a path.
+# 5 rows on the 8-row tensor tile, 1 row on the dp4a path, 16 rows at the
+# maximum in-feature count.
 CASES = [
     (2560, 6912, 16, "bf16", torch.float32, True),
     (2560, 2560, 5, "f32", torch.bfloat16, False),
     (640, 2560, 1, "bf16", torch.float32, True),
     (1000, 3000, 9, "f32", torch.float32, True),
+    (130, 32768, 16, "f32", torch.float32, True),  # the largest K the array holds
 ]
 
 
