@@ -514,7 +514,7 @@ __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int
 #pragma unroll
     for (int g = 0; g < 4; ++g)
         if (alive && 4 * g < M)
-            atomicAdd(acc_slot(P, pe.b_last, g, tid), make_float4(static_cast<float>(acc[4 * g]), static_cast<float>(acc[4 * g + 1]),
+            red_add_v4(acc_slot(P, pe.b_last, g, tid), make_float4(static_cast<float>(acc[4 * g]), static_cast<float>(acc[4 * g + 1]),
                                            static_cast<float>(acc[4 * g + 2]), static_cast<float>(acc[4 * g + 3])));
 }
 
