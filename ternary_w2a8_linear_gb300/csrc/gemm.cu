@@ -487,9 +487,12 @@ __device__ __forceinline__ float4* acc_slot(const GemmParams& P, int b, int g, i
 // acc[m] is the exact partial sum_k T*q for the thread's row.  A whole row
 // tile is written out at once; a split one is added (fp32 vector atomics of
 // integer values, no return value) into its accumulator in the workspace -- the one of the CTA
-// holding the row tile's last k tile -- and recorded in `pend`.
+// holding the row tile's last k tile -- and recorded in `pend`.  b_first and
+// b_last: the CTAs holding the row tile's first and last k tiles (used only
+// for a split tile).
 __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int pi, int rt, int ka, int kb,
-                                 const int (&acc)[16], int tid, bool alive, Pending* pend, int& npend) {
+                                 int b_first, int b_last, const int (&acc)[16], int tid, bool alive,
+                                 Pending* pend, int& npend) {
     const GemmProblem& pr = c->prob[pi];
     const int M = pr.M;
     const int n = rt * kTileN + tid;
@@ -501,13 +504,11 @@ __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int
         }
         return;
     }
-    const long long T = P.total_tiles;
-    const long long t_first = pr.tile_begin + static_cast<long long>(rt) * pr.kt;
     Pending& pe = pend[npend++];
     pe.pi = pi;
     pe.rt = rt;
-    pe.b_first = range_owner(t_first, T, P.nctas);
-    pe.b_last = range_owner(t_first + pr.kt - 1, T, P.nctas);
+    pe.b_first = b_first;
+    pe.b_last = b_last;
     // column tid of the row tile: one vector atomic per group of four rows (the
     // partial sums are integers below 2^24 in magnitude, so fp32 adds are
     // exact in any order)
@@ -760,6 +761,22 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         // executed by all four warps.
         TileIter it;
         it.init(pp, np, t_begin);
+        // Only a range's first and last segments can be split row tiles.  The
+        // CTAs holding their first and last k tiles take 64-bit divisions, so
+        // they are worked out here, while the preparation kernel still runs.
+        int own_f0, own_l0, own_f1, own_l1;
+        {
+            const GemmProblem& pa = pp[it.pi];
+            const long long fa = pa.tile_begin + static_cast<long long>(it.rt) * pa.kt;
+            own_f0 = range_owner(fa, T, P.nctas);
+            own_l0 = range_owner(fa + pa.kt - 1, T, P.nctas);
+            TileIter z;
+            z.init(pp, np, t_begin + nloc - 1);
+            const GemmProblem& pz = pp[z.pi];
+            const long long fz = pz.tile_begin + static_cast<long long>(z.rt) * pz.kt;
+            own_f1 = range_owner(fz, T, P.nctas);
+            own_l1 = range_owner(fz + pz.kt - 1, T, P.nctas);
+        }
         pdl_wait();  // outputs and workspace: the preparation kernel has finished
         // dequant scales of problems p0..p1 (at most 8 x 16: one per thread),
         // first needed by the first epilogue, which stores and publishes them
@@ -792,13 +809,14 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         int d_rq[16];
 #pragma unroll
         for (int m = 0; m < 16; ++m) d_rq[m] = 0;
-        auto epilogue = [&](int e_pi, int e_rt, int e_ka, int e_kb, const int (&acc)[16]) {
+        auto epilogue = [&](int e_pi, int e_rt, int e_ka, int e_kb, int e_seg, const int (&acc)[16]) {
             if (first_epi) {  // publish the dequant scales once
                 if (asc_mine) c->asc[tid / 16][tid % 16] = asc_reg;
                 named_bar_sync(1, 128);
                 first_epi = false;
             }
-            segment_epilogue(P, c, p0, e_pi, e_rt, e_ka, e_kb, acc, tid, alive, pend, npend);
+            segment_epilogue(P, c, p0, e_pi, e_rt, e_ka, e_kb, e_seg == 0 ? own_f0 : own_f1,
+                             e_seg == 0 ? own_l0 : own_l1, acc, tid, alive, pend, npend);
         };
         auto finish_deferred = [&]() {
             int acc[16];
@@ -826,7 +844,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                     }
                 }
             }
-            epilogue(d_pi, d_rt, d_ka, d_kb, acc);
+            epilogue(d_pi, d_rt, d_ka, d_kb, d_seg, acc);
             dv = false;
         };
         while (rp.i < nloc) {
@@ -928,7 +946,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
                 for (int m = 0; m < DPR; ++m)
                     acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) - code_sum(rsl, m);
-                epilogue(it.pi, it.rt, ka, ka + len, acc);
+                epilogue(it.pi, it.rt, ka, ka + len, seg_idx, acc);
             }
             ++seg_idx;
             nbatch += (len + kMmaBatch - 1) / kMmaBatch;
