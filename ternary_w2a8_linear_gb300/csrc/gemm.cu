@@ -489,7 +489,9 @@ __device__ __forceinline__ float4* acc_slot(const GemmParams& P, int b, int g, i
 // integer values, no return value) into its accumulator in the workspace -- the one of the CTA
 // holding the row tile's last k tile -- and recorded in `pend`.  b_first and
 // b_last: the CTAs holding the row tile's first and last k tiles (used only
-// for a split tile).
+// for a split tile).  kRows: the compute path's rows per tile, a compile-time
+// bound on M that keeps the unrolled row loops (and the code) short.
+template <int kRows>
 __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int pi, int rt, int ka, int kb,
                                  int b_first, int b_last, const int (&acc)[16], int tid, bool alive,
                                  Pending* pend, int& npend) {
@@ -499,7 +501,7 @@ __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int
     if (ka == 0 && kb == pr.kt) {
         if (alive && n < pr.N) {
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
+            for (int m = 0; m < kRows; ++m)
                 if (m < M) store_out(pr, m, n, acc[m], c->asc[pi - p0][m]);
         }
         return;
@@ -513,7 +515,7 @@ __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int
     // partial sums are integers below 2^24 in magnitude, so fp32 adds are
     // exact in any order)
 #pragma unroll
-    for (int g = 0; g < 4; ++g)
+    for (int g = 0; g < (kRows + 3) / 4; ++g)
         if (alive && 4 * g < M)
             red_add_v4(acc_slot(P, pe.b_last, g, tid), make_float4(static_cast<float>(acc[4 * g]), static_cast<float>(acc[4 * g + 1]),
                                            static_cast<float>(acc[4 * g + 2]), static_cast<float>(acc[4 * g + 3])));
@@ -523,7 +525,9 @@ __device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int
 // the last contributor of a tile reads the accumulated sum, writes the output
 // and leaves the accumulator and the counter at zero.  A split row tile is
 // identified by the CTA holding its last k tile (a CTA is the last k tile's
-// holder for at most one split row tile).  Warps 0-3.
+// holder for at most one split row tile).  Warps 0-3.  kRows as for
+// segment_epilogue.
+template <int kRows>
 __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pending* pend, int npend, int tid,
                                bool alive) {
     if (npend == 0) return;  // uniform across the four warps
@@ -538,14 +542,15 @@ __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pendi
     }
     named_bar_sync(1, 128);
     const int last0 = c->flag[0], last1 = npend > 1 ? c->flag[1] : 0;
-    float4 tot[2][4];
+    constexpr int kGroups = (kRows + 3) / 4;
+    float4 tot[2][kGroups];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const bool mine = k < npend && (k == 0 ? last0 : last1);
         const int M = mine ? c->prob[pend[k].pi].M : 0;
         const int b = mine ? pend[k].b_last : 0;
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
+        for (int g = 0; g < kGroups; ++g)
             tot[k][g] = (4 * g < M) ? __ldcg(acc_slot(P, b, g, tid)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
@@ -556,10 +561,10 @@ __device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pendi
         const int n = pend[k].rt * kTileN + tid;
         const float* t = reinterpret_cast<const float*>(&tot[k][0]);
 #pragma unroll
-        for (int m = 0; m < 16; ++m)
+        for (int m = 0; m < kRows; ++m)
             if (alive && m < M && n < pr.N) store_out(pr, m, n, __float2int_rn(t[m]), c->asc[pend[k].pi - p0][m]);
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
+        for (int g = 0; g < kGroups; ++g)
             if (4 * g < M) *acc_slot(P, pend[k].b_last, g, tid) = make_float4(0.f, 0.f, 0.f, 0.f);
         if (tid == 0) P.counters[pend[k].b_last] = 0u;
     }
@@ -585,6 +590,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr bool kTC = PATH != kPathDP;
     constexpr int BT = btile_bytes(PATH, DPR);
+    constexpr int kOutRows = btile_rows(PATH, DPR);  // M <= kOutRows (the host's path choice)
     Ctrl* c = reinterpret_cast<Ctrl*>(smem);
     const int R = P.stages;                                  // chunks in the ring
     uint8_t* Wr = smem + kCtrlBytes;                         // [R][kChunk][4096]
@@ -815,7 +821,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 named_bar_sync(1, 128);
                 first_epi = false;
             }
-            segment_epilogue(P, c, p0, e_pi, e_rt, e_ka, e_kb, e_seg == 0 ? own_f0 : own_f1,
+            segment_epilogue<kOutRows>(P, c, p0, e_pi, e_rt, e_ka, e_kb, e_seg == 0 ? own_f0 : own_f1,
                              e_seg == 0 ? own_l0 : own_l1, acc, tid, alive, pend, npend);
         };
         auto finish_deferred = [&]() {
@@ -937,7 +943,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 d_kb = ka + len;
                 d_seg = seg_idx;
 #pragma unroll
-                for (int m = 0; m < 16; ++m) d_rq[m] = code_sum(rsl, m);
+                for (int m = 0; m < kOutRows; ++m) d_rq[m] = code_sum(rsl, m);
                 dv = true;
             } else {
                 int acc[16];
@@ -958,7 +964,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             }
         }
         if (dv) finish_deferred();
-        finish_pending(P, c, p0, pend, npend, tid, alive);
+        finish_pending<kOutRows>(P, c, p0, pend, npend, tid, alive);
     }
 
     // ------------------------------------------------------- tear-down --
