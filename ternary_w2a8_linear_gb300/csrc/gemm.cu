@@ -256,48 +256,54 @@ __device__ void issue_acts(const GemmProblem* pp, int np, long long first, int c
     if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * BT, bar, pol);
 }
 
-// Load 8 consecutive activations k0..k0+7 of one row (zero beyond K).
-__device__ __forceinline__ void load8(const GemmProblem& pr, const char* row, bool vec_ok, int k0,
-                                      float (&v)[8]) {
-    if (pr.act_kind == BITMTP_BF16) {
-        if (vec_ok && k0 + 8 <= pr.K) {
-            const uint4 u = *reinterpret_cast<const uint4*>(row + 2ll * k0);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// Element k of one activation row as fp32 (exact for all three kinds).
+__device__ __forceinline__ float load_elem(int kind, const char* row, int k) {
+    if (kind == BITMTP_F32) return reinterpret_cast<const float*>(row)[k];
+    if (kind == BITMTP_BF16) return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(row)[k]) << 16);
+    return static_cast<float>(reinterpret_cast<const int8_t*>(row)[k]);
+}
+
+// The unit k0..k0+15 element by element (zero beyond K): the row's tail or a
+// row that is not 16-byte aligned.  Kept out of line: rarely run, and its 48
+// predicated loads would otherwise sit in every copy of the hot path.
+__device__ __noinline__ void load16_tail(int kind, const char* row, int K, int k0, float* v) {
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) v[i] = (k0 + i < K) ? load_elem(kind, row, k0 + i) : 0.f;
+}
+
+// Load the 16-element unit k0..k0+15 of one row (zero beyond K): vector loads
+// when the row is 16-byte aligned and the unit lies inside it, else element
+// by element.
+__device__ __forceinline__ void load16(const GemmProblem& pr, const char* row, bool vec_ok, int k0,
+                                       float (&v)[16]) {
+    if (vec_ok && k0 + 16 <= pr.K) {
+        if (pr.act_kind == BITMTP_BF16) {
+            const uint4* q = reinterpret_cast<const uint4*>(row + 2ll * k0);
+            const uint4 a = q[0], b = q[1];
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 v[2 * i] = __uint_as_float(w[i] << 16);
                 v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
             }
-        } else {
-            const uint16_t* r = reinterpret_cast<const uint16_t*>(row);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                v[i] = (k0 + i < pr.K) ? __uint_as_float(static_cast<uint32_t>(r[k0 + i]) << 16) : 0.f;
-        }
-    } else if (pr.act_kind == BITMTP_F32) {
-        if (vec_ok && k0 + 8 <= pr.K) {
-            const float4 a = *reinterpret_cast<const float4*>(row + 4ll * k0);
-            const float4 b = *reinterpret_cast<const float4*>(row + 4ll * k0 + 16);
-            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        } else {
-            const float* r = reinterpret_cast<const float*>(row);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = (k0 + i < pr.K) ? r[k0 + i] : 0.f;
-        }
-    } else {  // int8 codes
-        const int8_t* r = reinterpret_cast<const int8_t*>(row);
-        if (vec_ok && k0 + 8 <= pr.K) {
-            const uint2 u = *reinterpret_cast<const uint2*>(r + k0);
+        } else if (pr.act_kind == BITMTP_F32) {
+            const float4* q = reinterpret_cast<const float4*>(row + 4ll * k0);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                v[i] = static_cast<float>(static_cast<int8_t>(u.x >> (8 * i)));
-                v[4 + i] = static_cast<float>(static_cast<int8_t>(u.y >> (8 * i)));
+                const float4 a = q[i];
+                v[4 * i] = a.x; v[4 * i + 1] = a.y; v[4 * i + 2] = a.z; v[4 * i + 3] = a.w;
             }
-        } else {
+        } else {  // int8 codes
+            const uint4 a = *reinterpret_cast<const uint4*>(row + k0);
+            const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = (k0 + i < pr.K) ? static_cast<float>(r[k0 + i]) : 0.f;
+            for (int i = 0; i < 16; ++i) v[i] = static_cast<float>(static_cast<int8_t>(w[i / 4] >> (8 * (i % 4))));
         }
+    } else {
+        float t[16];
+        load16_tail(pr.act_kind, row, pr.K, k0, t);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = t[i];
     }
 }
 
@@ -340,42 +346,46 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     pdl_wait();
 
     float v[kPrepUnits][16];
-    auto load_pass = [&](int ps) {
+    float amax = 0.f, s = 0.f;
+    // Passes 0..npass-1 find the row's absmax, passes npass..2*npass-1
+    // quantise it (reading the row again only when it spans several passes).
+    // One loop, so that the loads are compiled once.
+    for (int it = 0; it < 2 * npass; ++it) {
+        const bool quant = it >= npass;
+        const int ps = quant ? it - npass : it;
+        if (!quant || npass > 1) {
 #pragma unroll
-        for (int j = 0; j < kPrepUnits; ++j) {
-            const int u = ps * kPass + j * kPrepThreads + tid;
-            if (live && u < nunits) {
-                load8(pr, row, vec_ok, u * 16, *reinterpret_cast<float(*)[8]>(&v[j][0]));
-                load8(pr, row, vec_ok, u * 16 + 8, *reinterpret_cast<float(*)[8]>(&v[j][8]));
-            } else {
+            for (int j = 0; j < kPrepUnits; ++j) {
+                const int u = ps * kPass + j * kPrepThreads + tid;
+                if (live && u < nunits) {
+                    load16(pr, row, vec_ok, u * 16, v[j]);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[j][i] = 0.f;
+                    for (int i = 0; i < 16; ++i) v[j][i] = 0.f;
+                }
             }
         }
-    };
-    float amax = 0.f;
-    for (int ps = 0; ps < npass; ++ps) {
-        load_pass(ps);
-        if (raw) {
+        if (!quant) {
+            if (raw) {
 #pragma unroll
-            for (int j = 0; j < kPrepUnits; ++j)
+                for (int j = 0; j < kPrepUnits; ++j)
 #pragma unroll
-                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
+                    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
+            }
+            if (it == npass - 1) {  // uniform over the block
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                if (lane == 0) red[warp] = amax;
+                __syncthreads();
+                amax = red[0];
+#pragma unroll
+                for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+                s = quant_scale(amax);
+            }
+            continue;
         }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (lane == 0) red[warp] = amax;
-    __syncthreads();
-    amax = red[0];
-#pragma unroll
-    for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
-    const float s = quant_scale(amax);
-
-    // Eight consecutive threads cover one k tile; units per pass and units of
-    // the row are multiples of 8, so the 8-lane sums below see whole tiles.
-    for (int ps = 0; ps < npass; ++ps) {
-        if (npass > 1) load_pass(ps);
+        // Eight consecutive threads cover one k tile; units per pass and units
+        // of the row are multiples of 8, so the 8-lane sums below see whole tiles.
 #pragma unroll
         for (int j = 0; j < kPrepUnits; ++j) {
             if (ps * kPass + j * kPrepThreads >= nunits) break;  // uniform over the block
