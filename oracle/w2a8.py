@@ -39,6 +39,8 @@ exact int64; dequant is fp64 then rounded to fp32.
 """
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 F32 = np.float32
@@ -73,15 +75,18 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 def ternarize_absmean(W: np.ndarray) -> tuple[np.ndarray, np.float32]:
     """T = clamp(round_half_even(W / gamma), -1, 1), gamma = max(mean|W|, 1e-5).
 
-    mean|W| is summed in fp64 and rounded once to fp32; the division and the
-    rounding are fp32 IEEE operations.  Returns (T int8 [N, K], w_scale fp32)
-    with W ~= w_scale * T."""
+    mean|W|: the exact sum of |W|, rounded once to fp64 (math.fsum, so that
+    the value does not depend on a summation order), divided by the count in
+    fp64 and rounded once to fp32.  The division W / gamma and the rounding
+    are fp32 IEEE operations.  Returns (T int8 [N, K], w_scale fp32) with
+    W ~= w_scale * T."""
     W = np.asarray(W, dtype=F32)
     if W.size == 0:
         raise ValueError("empty weight matrix")
     if not np.all(np.isfinite(W)):
         raise ValueError("non-finite weight")
-    gamma = F32(np.sum(np.abs(W.astype(F64))) / W.size)
+    total = math.fsum(np.abs(W.astype(F64)).ravel())
+    gamma = F32(F64(total) / F64(W.size))
     gamma = max(gamma, WEIGHT_EPS)
     ratio = (W / gamma).astype(F32)
     T = np.clip(np.rint(ratio), -1, 1).astype(np.int8)

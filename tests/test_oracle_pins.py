@@ -141,6 +141,42 @@ def test_ternarize_ties_and_clamp():
     assert T.tolist() == [[1, -1, 1, 1, -1, 0]]
 
 
+def test_ternarize_sum_exact_then_rounded():
+    """mean|W| must not depend on the summation order.  For
+    W = [2^30, 64, 2^-23, 2^-23] the exact sum 2^30 + 64 + 2^-22 is an fp64
+    number; divided by 4 it is 2^28 + 16 + 2^-24, just above the fp32 midpoint
+    2^28 + 16 between 2^28 and 2^28 + 32, so gamma = 2^28 + 32.  Adding the
+    terms left to right in fp64 loses both 2^-23 (each a tie to even) and
+    would give the midpoint, rounded down to 2^28."""
+    W = np.array([[2.0 ** 30, 64.0, 2.0 ** -23, 2.0 ** -23]], dtype=np.float32)
+    T, g = oracle.ternarize_absmean(W)
+    assert g == np.float32(2.0 ** 28 + 32)
+    assert T.tolist() == [[1, 0, 0, 0]]
+    seq = np.float64(0.0)
+    for v in W.ravel().astype(np.float64):
+        seq += v
+    assert np.float32(seq / 4) == np.float32(2.0 ** 28)  # the order-dependent value differs
+
+
+def test_ternarize_gamma_against_exact_rationals():
+    """gamma against the sum of |W| taken in exact rational arithmetic, rounded
+    once to fp64 (Fraction -> float rounds correctly), over a wide range of
+    magnitudes, subnormals and zeros included."""
+    from fractions import Fraction
+    rng = np.random.default_rng(23)
+    for trial in range(6):
+        n = int(rng.integers(1, 400))
+        mag = np.exp2(rng.uniform(-140, 100, n)).astype(np.float32)
+        W = (mag * np.where(rng.random(n) < 0.5, -1, 1)).astype(np.float32).reshape(1, n)
+        W[0, rng.random(n) < 0.1] = 0.0
+        if trial == 0:
+            W[0, :3] = np.float32(1e-45)  # the smallest subnormal
+        exact = sum((Fraction(float(abs(v))) for v in W.ravel()), Fraction(0))
+        want = max(np.float32(np.float64(float(exact)) / np.float64(n)), np.float32(1e-5))
+        _, g = oracle.ternarize_absmean(W)
+        assert g == want
+
+
 def test_ternarize_epsilon():
     T, g = oracle.ternarize_absmean(np.zeros((3, 4), dtype=np.float32))
     assert g == np.float32(1e-5) and not T.any()
