@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-per-width", action="store_true")
+    p.add_argument("--no-ternarize", action="store_true",
+                   help="skip the device ternarisation + pack figure (the offline step before the path)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--e2e-steps", type=int, default=1000)
     p.add_argument("--mode", choices=["grouped", "chained"], default="grouped",
@@ -292,9 +294,51 @@ def run_ours(args, rank, world):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, L, torch, dev, stream, weights, rank, world)
+    tern = None if args.no_ternarize else run_ternarize(L, torch, dev, stream)
 
-    return dict(value=value, ms_per_step=ms_per_step, clocks=clocks, per_width=per_width, e2e=e2e,
+    return dict(value=value, ms_per_step=ms_per_step, clocks=clocks, per_width=per_width, e2e=e2e, tern=tern,
                 gpu_launches=K * launches_per_step, copies=R, graph_steps=G)
+
+
+def run_ternarize(L, torch, dev, stream):
+    """Device absmean ternarisation + pack of the layer set's seven projections
+    from fp32 weights, through the C ABI on preallocated buffers (each call is
+    three launches and ends in a stream sync).  Algorithmic bytes: the fp32
+    weights read once plus the packed tiles written (278 MB + 17.4 MB, larger
+    than L2, so one pass over the set flushes the previous one)."""
+    projs = []
+    for p, (_, K, N) in enumerate(inputs.BITNET2B_PROJ):
+        W = torch.from_numpy(inputs.bitnet2b_dense_weights(p)).to(dev)
+        nb = L.packed_bytes(N, K)
+        wb = L.bitmtp_linear_ternarize_workspace_bytes(N, K)
+        projs.append((W, N, K, torch.empty(nb, dtype=torch.uint8, device=dev), nb,
+                      torch.empty(1, dtype=torch.float32, device=dev),
+                      torch.empty(wb, dtype=torch.uint8, device=dev), wb))
+    torch.cuda.synchronize()
+    cs = L.ctypes.c_void_p(stream.cuda_stream)
+
+    def one_pass():
+        for W, N, K, pk, nb, g, ws, wb in projs:
+            st = L.bitmtp_linear_ternarize_pack(L._ptr(W), N, K, K, L._ptr(pk), nb, L._ptr(g), L._ptr(ws), wb, cs)
+            if st != L.OK:
+                raise RuntimeError(L.status_string(st))
+
+    one_pass()
+    n_rep = 5
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n_rep):
+        one_pass()
+    b.record(stream)
+    b.synchronize()
+    t = a.elapsed_time(b) / 1e3 / n_rep
+    byt = sum(4 * N * K + L.packed_bytes(N, K) for _, K, N in inputs.BITNET2B_PROJ)
+    peak = load_peaks()[0]
+    return {"gbs": round(byt / t / 1e9, 1), "frac": round(byt / t / 1e9 / peak, 4),
+            "ms_per_layer_set": round(t * 1e3, 3), "bytes_per_layer_set": byt,
+            "gpu_launches_per_projection": 3,
+            "what": "bitmtp_linear_ternarize_pack of the 7 projections from fp32 N(0, 0.02^2) weights"}
 
 
 def run_e2e(args, L, torch, dev, stream, weights, rank, world):
@@ -500,6 +544,7 @@ def main():
                                "4 calls per step; achieved = algorithmic bytes per step / mean step time"},
         "per_width": res["per_width"],
         "e2e": res["e2e"],
+        "ternarize_pack": res["tern"],
         "gpu_launches": res["gpu_launches"],
         "clocks": res["clocks"],
         "cpu_baseline": cpu,

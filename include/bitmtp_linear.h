@@ -55,6 +55,7 @@ extern "C" {
 #define BITMTP_ERR_CUDA        (-6) /* a CUDA runtime call failed                 */
 #define BITMTP_ERR_DEVICE      (-7) /* a kernel gave up a bounded wait (see
                                        bitmtp_linear_device_error)               */
+#define BITMTP_ERR_NOT_FINITE  (-8) /* ternarize_pack: a weight is NaN or +-inf  */
 
 /* ---- element kinds --------------------------------------------------------- */
 #define BITMTP_F32  0   /* IEEE fp32                                   */
@@ -110,6 +111,29 @@ size_t bitmtp_linear_packed_bytes(int64_t N, int64_t K);
  * entry was outside {-1, 0, +1}. */
 int bitmtp_linear_pack(const int8_t* T, int64_t N, int64_t K, int64_t ldt,
                        void* pk, size_t pk_bytes, void* stream);
+
+/* Absmean ternarisation and pack of fp32 weights, on the device (the offline
+ * step before bitmtp_linear_pack's input exists).  The pages describe the
+ * backbone as BitNet b1.58-style ternary ("BitMTP: When Multi-Token Prediction
+ * Meets Low-Bit Large Language Models", "What This Paper Is About" and
+ * "Overview") but print no formula; this follows the BitNet b1.58 weight
+ * quantiser:
+ *   gamma = max(mean|W|, 1e-5),  T = clamp(round_half_even(W / gamma), -1, 1)
+ * where mean|W| is the exact sum of |W| rounded once to fp64, divided by N*K
+ * in fp64 and rounded to fp32 (so no summation order enters), and W / gamma is
+ * one IEEE fp32 division.
+ *   W          device fp32 [N][ldw], ldw >= K, finite values
+ *   pk         as for bitmtp_linear_pack; receives the packing of T
+ *   w_scale    device float, receives gamma (the per-tensor weight scale)
+ *   workspace  device scratch of ws_bytes >= bitmtp_linear_ternarize_workspace_bytes(N, K),
+ *              16-byte aligned, caller-owned; need not be zeroed, left dirty
+ * Stream-ordered; synchronises `stream` at the end to read the non-finite
+ * flag and returns BITMTP_ERR_NOT_FINITE (pk and *w_scale then unspecified)
+ * if W holds a NaN or an infinity. */
+size_t bitmtp_linear_ternarize_workspace_bytes(int64_t N, int64_t K);
+int bitmtp_linear_ternarize_pack(const float* W, int64_t N, int64_t K, int64_t ldw,
+                                 void* pk, size_t pk_bytes, float* w_scale,
+                                 void* workspace, size_t ws_bytes, void* stream);
 
 /* Quantise a block of activation rows to int8 codes with per-row scales
  * (the quantiser defined at the top of this file).

@@ -1,6 +1,6 @@
 // api.cu -- the C ABI (include/bitmtp_linear.h): argument validation, device
-// checks, the width/shape dispatch table and the pack / activation-quantisation
-// kernels.  The GEMM kernels live in gemm.cu.
+// checks, the width/shape dispatch table and the pack, absmean-ternarisation
+// and activation-quantisation kernels.  The GEMM kernels live in gemm.cu.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -20,10 +20,63 @@ namespace {
 constexpr uint32_t kTrailerMagic = 0x38413242u;
 
 // ----------------------------------------------------------------- pack --
+// Sources of ternary entries for the pack kernel: load16 gives the codes of
+// entries k0..k0+15 of row n (zero beyond N or K).
+
+// int8 T: entries outside {-1, 0, +1} are counted into `bad` and clamped.
+struct Int8Source {
+    const int8_t* T;
+    long long ld;
+    __device__ void load16(int n, int k0, int N, int K, int (&t)[16], int& bad) const {
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            const int k = k0 + kk;
+            int v = 0;
+            if (n < N && k < K) v = T[static_cast<long long>(n) * ld + k];
+            if (v < -1 || v > 1) {
+                ++bad;
+                v = v < 0 ? -1 : 1;
+            }
+            t[kk] = v;
+        }
+    }
+};
+
+// fp32 W under the absmean scale *g: clamp(round_half_even(w / g), -1, 1)
+// with one IEEE fp32 division.
+__device__ __forceinline__ int ternary_code(float w, float g) {
+    return static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(w, g)), -1.f), 1.f));
+}
+struct F32Source {
+    const float* W;
+    long long ld;
+    const float* g;  // device scalar written by absmean_finish_kernel
+    bool vec;        // W 16-byte aligned and ld a multiple of 4: float4 loads
+    __device__ void load16(int n, int k0, int N, int K, int (&t)[16], int&) const {
+        const float gs = *g;
+        const float* row = W + static_cast<long long>(n) * ld;
+        if (n < N && vec && k0 + 16 <= K) {
+            const float4* p = reinterpret_cast<const float4*>(row + k0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 v = p[i];
+                t[4 * i] = ternary_code(v.x, gs);
+                t[4 * i + 1] = ternary_code(v.y, gs);
+                t[4 * i + 2] = ternary_code(v.z, gs);
+                t[4 * i + 3] = ternary_code(v.w, gs);
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                t[kk] = (n < N && k0 + kk < K) ? ternary_code(row[k0 + kk], gs) : 0;
+        }
+    }
+};
+
 // Grid (KT, NT); each block writes one 4 KiB tile, each thread four words.
+template <class Src>
 __global__ void __launch_bounds__(256)
-pack_kernel(const int8_t* __restrict__ T, long long ldt, int N, int K, int KT,
-            uint32_t* __restrict__ pk, uint32_t* __restrict__ invalid) {
+pack_kernel(Src src, int N, int K, int KT, uint32_t* __restrict__ pk, uint32_t* __restrict__ invalid) {
     const int kt = blockIdx.x;
     const int rt = blockIdx.y;
     uint32_t* tile = pk + (static_cast<size_t>(rt) * KT + kt) * (kTileBytes / 4);
@@ -32,25 +85,126 @@ pack_kernel(const int8_t* __restrict__ T, long long ldt, int N, int K, int KT,
         const int half = widx >> 9;
         const int r = (widx & 511) >> 2;
         const int j = half * 4 + (widx & 3);
-        const int n = rt * kTileN + r;
-        const int k0 = kt * kTileK + 16 * j;
+        int t[16];
+        src.load16(rt * kTileN + r, kt * kTileK + 16 * j, N, K, t, bad);
         uint32_t word = 0;
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            const int k = k0 + kk;
-            int t = 0;
-            if (n < N && k < K) t = T[static_cast<long long>(n) * ldt + k];
-            if (t < -1 || t > 1) {
-                ++bad;
-                t = t < 0 ? -1 : 1;
-            }
-            word |= static_cast<uint32_t>(t + 1) << (16 * (kk & 1) + 2 * (kk >> 1));
-        }
+        for (int kk = 0; kk < 16; ++kk)
+            word |= static_cast<uint32_t>(t[kk] + 1) << (16 * (kk & 1) + 2 * (kk >> 1));
         tile[widx] = word;
     }
     // block-reduce the invalid count
     for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
     if ((threadIdx.x & 31) == 0 && bad) atomicAdd(invalid, static_cast<uint32_t>(bad));
+}
+
+// --------------------------------------------------- absmean ternarisation --
+// mean|W| is the exact sum of |W| rounded once to fp64, divided by the count
+// in fp64 and rounded to fp32; no summation order enters.  Each block adds the
+// significands of its entries into 256 integer bins by biased exponent: bin e
+// (1..254) holds significands m (with the implicit bit) of value m * 2^(e-150),
+// bin 0 the subnormal fractions (value m * 2^-149), bin 255 counts non-finite
+// entries.  Integer sums are exact and order-free; a bin never exceeds
+// 2^39 entries * 2^24 < 2^64.
+constexpr int kHistBins = 256;
+constexpr int kHistMaxBlocks = 512;
+
+int hist_blocks(int64_t N) { return static_cast<int>(std::min<int64_t>(N, kHistMaxBlocks)); }
+
+__global__ void __launch_bounds__(256)
+absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, unsigned long long* __restrict__ part) {
+    __shared__ unsigned long long h[kHistBins];
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = 0ull;
+    __syncthreads();
+    for (int n = blockIdx.x; n < N; n += gridDim.x) {
+        const float* row = W + static_cast<long long>(n) * ldw;
+        for (int k = threadIdx.x; k < K; k += blockDim.x) {
+            const uint32_t b = __float_as_uint(row[k]) & 0x7FFFFFFFu;
+            const uint32_t e = b >> 23;
+            const uint32_t m = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+            if (e == 255u)
+                atomicAdd(&h[255], 1ull);
+            else if (m)
+                atomicAdd(&h[e], static_cast<unsigned long long>(m));
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
+        part[static_cast<size_t>(blockIdx.x) * kHistBins + i] = h[i];
+}
+
+// 384-bit unsigned integer in 64-bit limbs, least significant first.
+constexpr int kLimbs = 6;
+
+__device__ void wide_add_shifted(unsigned long long (&L)[kLimbs], unsigned long long v, int sh) {
+    const int i = sh >> 6, o = sh & 63;  // sh <= 253: i + 1 < kLimbs
+    const unsigned long long lo = v << o;
+    const unsigned long long hi = o ? (v >> (64 - o)) : 0ull;
+    unsigned long long s = L[i] + lo;
+    unsigned long long c = s < lo;
+    L[i] = s;
+    s = L[i + 1] + hi;
+    unsigned long long c1 = s < hi;
+    s += c;
+    c1 |= (s < c);
+    L[i + 1] = s;
+    for (int j = i + 2; c1 && j < kLimbs; ++j) {
+        L[j] += 1ull;
+        c1 = (L[j] == 0ull);
+    }
+}
+
+__device__ unsigned long long wide_bits(const unsigned long long (&L)[kLimbs], int pos) {  // 64 bits from pos
+    const int i = pos >> 6, o = pos & 63;
+    unsigned long long v = L[i] >> o;
+    if (o && i + 1 < kLimbs) v |= L[i + 1] << (64 - o);
+    return v;
+}
+
+// L (in units of 2^-149) rounded to the nearest fp64, ties to even.
+__device__ double wide_to_double(const unsigned long long (&L)[kLimbs]) {
+    int top = -1;
+    for (int j = kLimbs - 1; j >= 0 && top < 0; --j)
+        if (L[j]) top = 64 * j + 63 - __clzll(static_cast<long long>(L[j]));
+    if (top < 0) return 0.0;
+    if (top < 53) return ldexp(static_cast<double>(L[0]), -149);  // exact
+    int lo = top - 52;  // the 53 bits [lo, top]
+    unsigned long long mant = wide_bits(L, lo) & ((1ull << 53) - 1ull);
+    const unsigned long long round = (L[(lo - 1) >> 6] >> ((lo - 1) & 63)) & 1ull;
+    bool sticky = false;
+    const int sb = lo - 1;  // bits [0, sb) below the round bit
+    for (int j = 0; j < (sb >> 6); ++j) sticky = sticky || L[j] != 0ull;
+    if (sb & 63) sticky = sticky || (L[sb >> 6] & ((1ull << (sb & 63)) - 1ull)) != 0ull;
+    if (round && (sticky || (mant & 1ull))) {
+        ++mant;
+        if (mant == (1ull << 53)) {
+            mant >>= 1;
+            ++lo;
+        }
+    }
+    return ldexp(static_cast<double>(mant), lo - 149);  // exact: a normal fp64
+}
+
+// One block of 256 threads: bin totals over the partial histograms, the exact
+// sum, gamma = max(RN32(RN64(sum) / count), 1e-5) into *w_scale, and the
+// non-finite flag.
+__global__ void __launch_bounds__(256)
+absmean_finish_kernel(const unsigned long long* __restrict__ part, int nblocks, long long count,
+                      float* __restrict__ w_scale, uint32_t* __restrict__ nonfinite) {
+    __shared__ unsigned long long H[kHistBins];
+    const int e = threadIdx.x;
+    unsigned long long s = 0ull;
+    for (int b = 0; b < nblocks; ++b) s += part[static_cast<size_t>(b) * kHistBins + e];
+    H[e] = s;
+    __syncthreads();
+    if (e == 0) {
+        unsigned long long L[kLimbs] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+        for (int b = 0; b < 255; ++b)
+            if (H[b]) wide_add_shifted(L, H[b], b == 0 ? 0 : b - 1);
+        const double mean = __ddiv_rn(wide_to_double(L), static_cast<double>(count));
+        *w_scale = fmaxf(__double2float_rn(mean), 1e-5f);
+        *nonfinite = H[255] ? 1u : 0u;
+    }
 }
 
 // ------------------------------------------------------------ quant_act --
@@ -310,8 +464,9 @@ int bitmtp_linear_pack(const int8_t* T, int64_t N, int64_t K, int64_t ldt, void*
     const uint32_t head[4] = {kTrailerMagic, static_cast<uint32_t>(N), static_cast<uint32_t>(K), 0u};
     st = cuda_status(cudaMemcpyAsync(trailer, head, sizeof(head), cudaMemcpyHostToDevice, s));
     if (st != BITMTP_OK) return st;
-    pack_kernel<<<dim3(KT, NT), 256, 0, s>>>(T, ldt, static_cast<int>(N), static_cast<int>(K), KT,
-                                             reinterpret_cast<uint32_t*>(base), trailer + 3);
+    pack_kernel<Int8Source><<<dim3(KT, NT), 256, 0, s>>>(Int8Source{T, ldt}, static_cast<int>(N),
+                                                         static_cast<int>(K), KT,
+                                                         reinterpret_cast<uint32_t*>(base), trailer + 3);
     st = cuda_status(cudaGetLastError());
     if (st != BITMTP_OK) return st;
     uint32_t invalid = 0;
@@ -320,6 +475,53 @@ int bitmtp_linear_pack(const int8_t* T, int64_t N, int64_t K, int64_t ldt, void*
     st = cuda_status(cudaStreamSynchronize(s));
     if (st != BITMTP_OK) return st;
     return invalid ? BITMTP_ERR_NOT_TERNARY : BITMTP_OK;
+}
+
+size_t bitmtp_linear_ternarize_workspace_bytes(int64_t N, int64_t K) {
+    if (N < 1 || K < 1 || N > BITMTP_MAX_N || K > BITMTP_MAX_K) return 0;
+    return static_cast<size_t>(hist_blocks(N)) * kHistBins * sizeof(unsigned long long) + 256;
+}
+
+int bitmtp_linear_ternarize_pack(const float* W, int64_t N, int64_t K, int64_t ldw, void* pk, size_t pk_bytes,
+                                 float* w_scale, void* workspace, size_t ws_bytes, void* stream) {
+    if (N < 1 || K < 1 || N > BITMTP_MAX_N || K > BITMTP_MAX_K) return BITMTP_ERR_SHAPE;
+    if (!W || !pk || !w_scale || !workspace || ldw < K) return BITMTP_ERR_INVALID;
+    if (!aligned16(pk) || !aligned16(workspace)) return BITMTP_ERR_ALIGN;
+    const size_t need = bitmtp_linear_packed_bytes(N, K);
+    if (pk_bytes < need || ws_bytes < bitmtp_linear_ternarize_workspace_bytes(N, K)) return BITMTP_ERR_SHAPE;
+    DevInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != BITMTP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int NT = static_cast<int>(ceil_div(N, kTileN));
+    const int KT = static_cast<int>(ceil_div(K, kTileK));
+    const int G = hist_blocks(N);
+    unsigned long long* part = static_cast<unsigned long long*>(workspace);
+    uint32_t* nonfinite = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) +
+                                                      static_cast<size_t>(G) * kHistBins * sizeof(unsigned long long));
+    absmean_hist_kernel<<<G, 256, 0, s>>>(W, ldw, static_cast<int>(N), static_cast<int>(K), part);
+    st = cuda_status(cudaGetLastError());
+    if (st != BITMTP_OK) return st;
+    absmean_finish_kernel<<<1, kHistBins, 0, s>>>(part, G, static_cast<long long>(N * K), w_scale, nonfinite);
+    st = cuda_status(cudaGetLastError());
+    if (st != BITMTP_OK) return st;
+    uint8_t* base = static_cast<uint8_t*>(pk);
+    uint32_t* trailer = reinterpret_cast<uint32_t*>(base + need - 16);
+    const uint32_t head[4] = {kTrailerMagic, static_cast<uint32_t>(N), static_cast<uint32_t>(K), 0u};
+    st = cuda_status(cudaMemcpyAsync(trailer, head, sizeof(head), cudaMemcpyHostToDevice, s));
+    if (st != BITMTP_OK) return st;
+    const bool vec = aligned16(W) && (ldw % 4) == 0;
+    pack_kernel<F32Source><<<dim3(KT, NT), 256, 0, s>>>(F32Source{W, ldw, w_scale, vec}, static_cast<int>(N),
+                                                        static_cast<int>(K), KT,
+                                                        reinterpret_cast<uint32_t*>(base), trailer + 3);
+    st = cuda_status(cudaGetLastError());
+    if (st != BITMTP_OK) return st;
+    uint32_t bad = 0;
+    st = cuda_status(cudaMemcpyAsync(&bad, nonfinite, 4, cudaMemcpyDeviceToHost, s));
+    if (st != BITMTP_OK) return st;
+    st = cuda_status(cudaStreamSynchronize(s));
+    if (st != BITMTP_OK) return st;
+    return bad ? BITMTP_ERR_NOT_FINITE : BITMTP_OK;
 }
 
 int bitmtp_linear_quant_act(const void* x, int x_kind, int64_t M, int64_t K, int64_t ldx, int8_t* q,
@@ -433,6 +635,7 @@ const char* bitmtp_linear_status_string(int status) {
         case BITMTP_ERR_UNSUPPORTED: return "BITMTP_ERR_UNSUPPORTED: no sm_103 device is current";
         case BITMTP_ERR_CUDA: return "BITMTP_ERR_CUDA: a CUDA runtime call failed";
         case BITMTP_ERR_DEVICE: return "BITMTP_ERR_DEVICE: a kernel gave up a bounded wait";
+        case BITMTP_ERR_NOT_FINITE: return "BITMTP_ERR_NOT_FINITE: a weight is NaN or infinite";
         default: return "BITMTP: unknown status";
     }
 }

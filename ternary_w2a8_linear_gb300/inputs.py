@@ -89,6 +89,14 @@ def bitnet2b_weights(proj_idx: int, layer: int | None = None):
     return T, w_scale
 
 
+def bitnet2b_dense_weights(proj_idx: int) -> np.ndarray:
+    """fp32 weights [N, K] of one BitNet-2B projection before ternarisation:
+    N(0, 0.02^2), seed 6000 + proj (input of the device ternarisation)."""
+    _, K, N = BITNET2B_PROJ[proj_idx]
+    rng = np.random.default_rng(6000 + proj_idx)
+    return (rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02)).astype(np.float32)
+
+
 def bitnet2b_act(proj_idx: int, M: int, layer: int | None = None) -> np.ndarray:
     """bf16 bits [M, K]; the first M of 16 seeded rows (seed 2100 + proj, or
     7000 + 10*layer + proj for the 30-layer stack)."""

@@ -21,7 +21,8 @@ LIB_PATH = os.path.join(_PKG, "libbitmtp_linear.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "bitmtp_linear.h")
 
 OK = 0
-ERR_INVALID, ERR_ALIGN, ERR_SHAPE, ERR_NOT_TERNARY, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE = range(-1, -8, -1)
+ERR_INVALID, ERR_ALIGN, ERR_SHAPE, ERR_NOT_TERNARY, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE, ERR_NOT_FINITE = \
+    range(-1, -9, -1)
 F32, BF16, Q8 = 0, 1, 2
 FLAG_PDL, FLAG_FORCE_TC, FLAG_FORCE_DP = 0x1, 0x2, 0x4
 MAX_M, MAX_K, MAX_N, MAX_GROUP = 16, 32768, 16777216, 8
@@ -66,6 +67,10 @@ def load() -> ctypes.CDLL:
         "bitmtp_linear_packed_bytes": (c.c_size_t, [c.c_int64, c.c_int64]),
         "bitmtp_linear_pack": (c.c_int, [c.c_void_p, c.c_int64, c.c_int64, c.c_int64, c.c_void_p,
                                          c.c_size_t, c.c_void_p]),
+        "bitmtp_linear_ternarize_workspace_bytes": (c.c_size_t, [c.c_int64, c.c_int64]),
+        "bitmtp_linear_ternarize_pack": (c.c_int, [c.c_void_p, c.c_int64, c.c_int64, c.c_int64, c.c_void_p,
+                                                   c.c_size_t, c.c_void_p, c.c_void_p, c.c_size_t,
+                                                   c.c_void_p]),
         "bitmtp_linear_quant_act": (c.c_int, [c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_int64,
                                               c.c_void_p, c.c_int64, c.c_void_p, c.c_void_p, c.c_void_p]),
         "bitmtp_linear_workspace_bytes": (c.c_size_t, [c.c_int64, c.c_int64, c.c_int64]),
@@ -103,6 +108,15 @@ def bitmtp_linear_packed_bytes(N: int, K: int) -> int:
 
 def bitmtp_linear_pack(T_ptr, N, K, ldt, pk_ptr, pk_bytes, stream) -> int:
     return load().bitmtp_linear_pack(T_ptr, N, K, ldt, pk_ptr, pk_bytes, stream)
+
+
+def bitmtp_linear_ternarize_workspace_bytes(N: int, K: int) -> int:
+    return int(load().bitmtp_linear_ternarize_workspace_bytes(N, K))
+
+
+def bitmtp_linear_ternarize_pack(W_ptr, N, K, ldw, pk_ptr, pk_bytes, w_scale_ptr, ws_ptr, ws_bytes, stream) -> int:
+    return load().bitmtp_linear_ternarize_pack(W_ptr, N, K, ldw, pk_ptr, pk_bytes, w_scale_ptr, ws_ptr, ws_bytes,
+                                               stream)
 
 
 def bitmtp_linear_quant_act(x_ptr, x_kind, M, K, ldx, q_ptr, ldq, a_scale_ptr, rowsum_ptr, stream) -> int:
@@ -219,6 +233,26 @@ def pack(T: torch.Tensor, stream=None) -> torch.Tensor:
     pk = torch.empty(nb, dtype=torch.uint8, device=T.device)
     _check(bitmtp_linear_pack(_ptr(T), N, K, ldt, _ptr(pk), nb, _stream(stream)), "pack")
     return pk
+
+
+def ternarize_pack(W: torch.Tensor, stream=None):
+    """Absmean-ternarise fp32 weights [N, K] (device) and pack them on the
+    device -> (packed uint8 buffer, w_scale as a Python float).  The scratch is
+    a fresh tensor, not the GEMM workspace (which must stay zero-filled)."""
+    if W.dtype != torch.float32 or not W.is_cuda:
+        raise TypeError("W must be a CUDA float32 tensor")
+    N, K = W.shape
+    ldw = _rowmajor(W, "W")
+    nb = packed_bytes(N, K)
+    wb = bitmtp_linear_ternarize_workspace_bytes(N, K)
+    if nb == 0 or wb == 0:
+        raise BitmtpError(ERR_SHAPE, "ternarize_pack")
+    pk = torch.empty(nb, dtype=torch.uint8, device=W.device)
+    ws = torch.empty(wb, dtype=torch.uint8, device=W.device)
+    g = torch.empty(1, dtype=torch.float32, device=W.device)
+    _check(bitmtp_linear_ternarize_pack(_ptr(W), N, K, ldw, _ptr(pk), nb, _ptr(g), _ptr(ws), wb, _stream(stream)),
+           "ternarize_pack")
+    return pk, float(g.item())
 
 
 def quant_act(x: torch.Tensor, stream=None):

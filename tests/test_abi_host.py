@@ -27,6 +27,7 @@ def test_exports_every_header_symbol(lib):
         "bitmtp_linear_gemm", "bitmtp_linear_gemm_grouped", "bitmtp_linear_device_error",
         "bitmtp_linear_status_string", "bitmtp_linear_version", "bitmtp_linear_workspace_bytes",
         "bitmtp_linear_workspace_bytes_grouped", "bitmtp_linear_gemm_noalloc",
+        "bitmtp_linear_ternarize_workspace_bytes", "bitmtp_linear_ternarize_pack",
     }
     for s in syms:
         assert hasattr(lib, s), s
@@ -36,7 +37,7 @@ def test_exports_every_header_symbol(lib):
 def test_version_and_status_strings(lib):
     assert L.bitmtp_linear_version() == 0x000100
     for st in (L.OK, L.ERR_INVALID, L.ERR_ALIGN, L.ERR_SHAPE, L.ERR_NOT_TERNARY,
-               L.ERR_UNSUPPORTED, L.ERR_CUDA, L.ERR_DEVICE):
+               L.ERR_UNSUPPORTED, L.ERR_CUDA, L.ERR_DEVICE, L.ERR_NOT_FINITE):
         assert L.status_string(st).startswith("BITMTP")
     assert "unknown" in L.status_string(12345)
 
@@ -45,6 +46,31 @@ def test_version_and_status_strings(lib):
                                  (129, 130), (7, 300)])
 def test_packed_bytes_matches_oracle_definition(lib, N, K):
     assert L.packed_bytes(N, K) == oracle.packed_bytes(N, K)
+
+
+def test_ternarize_validation(lib):
+    """Argument checks of the device ternarisation, all before any CUDA call."""
+    wb = L.bitmtp_linear_ternarize_workspace_bytes
+    assert wb(0, 5) == 0 and wb(5, 0) == 0 and wb(5, L.MAX_K + 1) == 0
+    assert wb(1, 1) == 256 * 8 + 256                 # one histogram block
+    assert wb(700, 64) == wb(100000, 64) == 512 * 256 * 8 + 256  # at most 512 blocks
+    nb = L.packed_bytes(64, 64)
+    tp = L.bitmtp_linear_ternarize_pack
+
+    def call(W=FAKE, N=64, K=64, ldw=64, pk=FAKE, pk_bytes=nb, g=FAKE, ws=FAKE, ws_bytes=None):
+        return tp(W, N, K, ldw, pk, pk_bytes, g, ws, wb(64, 64) if ws_bytes is None else ws_bytes, None)
+
+    assert call(N=0) == L.ERR_SHAPE
+    assert call(K=L.MAX_K + 1) == L.ERR_SHAPE
+    assert call(W=None) == L.ERR_INVALID
+    assert call(g=None) == L.ERR_INVALID
+    assert call(ws=None) == L.ERR_INVALID
+    assert call(ldw=63) == L.ERR_INVALID
+    assert call(pk=FAKE + 8) == L.ERR_ALIGN
+    assert call(ws=FAKE + 4) == L.ERR_ALIGN
+    assert call(pk_bytes=nb - 1) == L.ERR_SHAPE
+    assert call(ws_bytes=wb(64, 64) - 1) == L.ERR_SHAPE
+    assert "NaN" in L.status_string(L.ERR_NOT_FINITE)
 
 
 def test_packed_bytes_rejects(lib):

@@ -1,0 +1,103 @@
+"""GPU parity of the device absmean ternarisation + pack
+(bitmtp_linear_ternarize_pack, through the C ABI) against the oracle: the
+per-tensor scale bit for bit and the packed bytes byte for byte, on normal
+weights of several shapes (ragged tiles included), strided and unaligned
+rows, a wide range of magnitudes with subnormals and zeros, the summation-
+order case, ties, the epsilon floor and a full-size projection, which then
+feeds the GEMM."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ternary_w2a8_linear_gb300 import build, inputs
+from ternary_w2a8_linear_gb300 import linear as L
+from gpu_util import assert_f32_close, dev_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    yield L.load()
+    assert L.bitmtp_linear_device_error() == 0
+
+
+def _bits(v) -> int:
+    return int(np.float32(v).view(np.uint32))
+
+
+def _check(W: np.ndarray, W_dev: torch.Tensor | None = None):
+    pk, g = L.ternarize_pack(dev_tensor(W) if W_dev is None else W_dev)
+    T_ref, g_ref = oracle.ternarize_absmean(W)
+    assert _bits(g) == _bits(g_ref), (g, g_ref)
+    assert np.array_equal(pk.cpu().numpy(), oracle.pack_tiles(T_ref))
+    return pk, g, T_ref
+
+
+@pytest.mark.parametrize("N,K", [(1, 1), (5, 17), (130, 129), (300, 1000), (640, 2560), (257, 4097),
+                                 (3000, 300)])
+def test_normal_weights(N, K):
+    W = (np.random.default_rng(N * 31 + K).standard_normal((N, K)) * 0.02).astype(np.float32)
+    _check(W)
+
+
+def test_wide_magnitude_range_subnormals_and_zeros():
+    rng = np.random.default_rng(5)
+    N, K = 200, 777
+    mag = np.exp2(rng.uniform(-149, 100, (N, K))).astype(np.float32)
+    W = (mag * np.where(rng.random((N, K)) < 0.5, -1, 1)).astype(np.float32)
+    W[rng.random((N, K)) < 0.05] = 0.0
+    W[0, :5] = np.float32(1e-45)
+    _check(W)
+
+
+def test_summation_order_case():
+    W = np.array([[2.0 ** 30, 64.0, 2.0 ** -23, 2.0 ** -23]], dtype=np.float32)
+    pk, g, T = _check(W)
+    assert g == 2.0 ** 28 + 32
+    assert T.tolist() == [[1, 0, 0, 0]]
+
+
+def test_ties_and_epsilon():
+    _check(np.array([[1.0, 3.0, -1.0, -3.0]], dtype=np.float32))        # ratios +-0.5, +-1.5
+    _check(np.array([[2.0, -2.0, 1.0, 3.0, -1.0, 0.0]], dtype=np.float32))
+    pk, g, T = _check(np.zeros((3, 40), dtype=np.float32))
+    assert g == np.float32(1e-5) and not T.any()
+    _check(np.full((2, 2), 1e-7, dtype=np.float32))
+
+
+def test_strided_and_unaligned_rows():
+    rng = np.random.default_rng(8)
+    W = (rng.standard_normal((150, 300)) * 0.05).astype(np.float32)
+    for pad in (4, 1):  # 16-byte aligned rows (vector loads), then odd row pitch
+        big = np.zeros((150, 300 + pad), dtype=np.float32)
+        big[:, :300] = W
+        t = dev_tensor(big)[:, :300]
+        assert t.stride(0) == 300 + pad
+        _check(W, t)
+
+
+def test_non_finite_rejected():
+    W = np.ones((4, 40), dtype=np.float32)
+    for bad in (np.nan, np.inf, -np.inf):
+        W[2, 7] = bad
+        with pytest.raises(L.BitmtpError) as e:
+            L.ternarize_pack(dev_tensor(W))
+        assert e.value.status == L.ERR_NOT_FINITE
+
+
+def test_full_size_projection_then_gemm():
+    """The gate projection of the BitNet-2B layer set (2560 -> 6912) from fp32
+    weights, then a width-8 linear on the result against the oracle."""
+    _, K, N = inputs.BITNET2B_PROJ[4]
+    W = (np.random.default_rng(77).standard_normal((N, K)) * 0.02).astype(np.float32)
+    pk, g, T = _check(W)
+    x = np.random.default_rng(78).standard_normal((8, K)).astype(np.float32)
+    y, acc = L.gemm(pk, g, N, K, dev_tensor(x), acc=True)
+    y_ref, acc_ref, _, _, _ = oracle.w2a8_linear(T, np.float32(g), x, "f32")
+    assert np.array_equal(acc.cpu().numpy(), acc_ref.astype(np.int32))
+    assert_f32_close(y.cpu().numpy(), y_ref, acc_ref)
