@@ -100,13 +100,22 @@ pack_kernel(Src src, int N, int K, int KT, uint32_t* __restrict__ pk, uint32_t* 
 
 // --------------------------------------------------- absmean ternarisation --
 // mean|W| is the exact sum of |W| rounded once to fp64, divided by the count
-// in fp64 and rounded to fp32; no summation order enters.  Each block adds the
-// significands of its entries into 256 integer bins by biased exponent: bin e
-// (1..254) holds significands m (with the implicit bit) of value m * 2^(e-150),
-// bin 0 the subnormal fractions (value m * 2^-149), bin 255 counts non-finite
-// entries.  Integer sums are exact and order-free; a bin never exceeds
-// 2^39 entries * 2^24 < 2^64.
-constexpr int kHistBins = 256;
+// in fp64 and rounded to fp32; no summation order enters.  An entry is
+// m * 2^(e-150) with e = max(biased exponent, 1) and m its significand (the
+// implicit bit included for normals).  Integer sums of such terms are exact
+// and order-free:
+// * each thread adds m << (e - b) into a 128-bit register accumulator, b
+//   fixed by its first non-zero entry (b = e - 40, so exponents e - 40 ..
+//   e + 23 fit; at most 2^22 entries per thread keep it below 2^110);
+// * entries outside that window go to shared bins: bin j holds an integer
+//   sum at scale 2^(j - kBinOff - 150), entry (m, e) into bin e + kBinOff;
+// * at the end each thread adds its accumulator, in four 32-bit pieces, to
+//   bins b + 32 i + kBinOff (i = 0..3).
+// Bins 89..438 are the only ones used; bin 511 counts non-finite entries.  A
+// bin stays below 2^39 * 2^24 + 2^17 * 2^32 < 2^64.
+constexpr int kHistBins = 512;
+constexpr int kBinOff = 128;
+constexpr int kNonFiniteBin = 511;
 constexpr int kHistMaxBlocks = 512;
 
 int hist_blocks(int64_t N) { return static_cast<int>(std::min<int64_t>(N, kHistMaxBlocks)); }
@@ -116,28 +125,55 @@ absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, un
     __shared__ unsigned long long h[kHistBins];
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = 0ull;
     __syncthreads();
+    unsigned long long acc_lo = 0ull, acc_hi = 0ull;
+    int base = 0;
+    bool have_base = false;
     for (int n = blockIdx.x; n < N; n += gridDim.x) {
         const float* row = W + static_cast<long long>(n) * ldw;
         for (int k = threadIdx.x; k < K; k += blockDim.x) {
             const uint32_t b = __float_as_uint(row[k]) & 0x7FFFFFFFu;
-            const uint32_t e = b >> 23;
-            const uint32_t m = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
-            if (e == 255u)
-                atomicAdd(&h[255], 1ull);
-            else if (m)
-                atomicAdd(&h[e], static_cast<unsigned long long>(m));
+            const int eb = static_cast<int>(b >> 23);
+            if (eb == 255) {
+                atomicAdd(&h[kNonFiniteBin], 1ull);
+                continue;
+            }
+            const unsigned long long m = (b & 0x7FFFFFu) | (eb ? 0x800000u : 0u);
+            if (m == 0ull) continue;
+            const int e = eb ? eb : 1;
+            if (!have_base) {
+                base = e - 40;
+                have_base = true;
+            }
+            const int d = e - base;
+            if (d >= 0 && d < 64) {
+                const unsigned long long lo = m << d;
+                const unsigned long long hi = d > 40 ? (m >> (64 - d)) : 0ull;
+                acc_lo += lo;
+                acc_hi += hi + (acc_lo < lo ? 1ull : 0ull);
+            } else {
+                atomicAdd(&h[e + kBinOff], m);
+            }
         }
+    }
+    if (have_base) {
+        const unsigned long long piece[4] = {acc_lo & 0xFFFFFFFFull, acc_lo >> 32, acc_hi & 0xFFFFFFFFull, acc_hi >> 32};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (piece[i]) atomicAdd(&h[base + 32 * i + kBinOff], piece[i]);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
         part[static_cast<size_t>(blockIdx.x) * kHistBins + i] = h[i];
 }
 
-// 384-bit unsigned integer in 64-bit limbs, least significant first.
-constexpr int kLimbs = 6;
+// 512-bit unsigned integer in 64-bit limbs, least significant first, in units
+// of 2^-213: bin j adds at bit j - kBinOff - 150 + 213 = j - 65 (>= 24 for the
+// bins in use; every bin below 511 fits, shift <= 445).
+constexpr int kLimbs = 8;
+constexpr int kUnitExp = -213;
 
 __device__ void wide_add_shifted(unsigned long long (&L)[kLimbs], unsigned long long v, int sh) {
-    const int i = sh >> 6, o = sh & 63;  // sh <= 253: i + 1 < kLimbs
+    const int i = sh >> 6, o = sh & 63;  // sh <= 445: i + 1 < kLimbs
     const unsigned long long lo = v << o;
     const unsigned long long hi = o ? (v >> (64 - o)) : 0ull;
     unsigned long long s = L[i] + lo;
@@ -161,13 +197,13 @@ __device__ unsigned long long wide_bits(const unsigned long long (&L)[kLimbs], i
     return v;
 }
 
-// L (in units of 2^-149) rounded to the nearest fp64, ties to even.
+// L * 2^kUnitExp rounded to the nearest fp64, ties to even.
 __device__ double wide_to_double(const unsigned long long (&L)[kLimbs]) {
     int top = -1;
     for (int j = kLimbs - 1; j >= 0 && top < 0; --j)
         if (L[j]) top = 64 * j + 63 - __clzll(static_cast<long long>(L[j]));
     if (top < 0) return 0.0;
-    if (top < 53) return ldexp(static_cast<double>(L[0]), -149);  // exact
+    if (top < 53) return ldexp(static_cast<double>(L[0]), kUnitExp);  // exact
     int lo = top - 52;  // the 53 bits [lo, top]
     unsigned long long mant = wide_bits(L, lo) & ((1ull << 53) - 1ull);
     const unsigned long long round = (L[(lo - 1) >> 6] >> ((lo - 1) & 63)) & 1ull;
@@ -182,15 +218,15 @@ __device__ double wide_to_double(const unsigned long long (&L)[kLimbs]) {
             ++lo;
         }
     }
-    return ldexp(static_cast<double>(mant), lo - 149);  // exact: a normal fp64
+    return ldexp(static_cast<double>(mant), lo + kUnitExp);  // exact: a normal fp64
 }
 
-// One block of 256 threads: bin totals over the partial histograms, the exact
-// sum, gamma = max(RN32(RN64(sum) / count), 1e-5) into *w_scale, and the
-// non-finite flag.
-__global__ void __launch_bounds__(256)
-absmean_finish_kernel(const unsigned long long* __restrict__ part, int nblocks, long long count,
-                      float* __restrict__ w_scale, uint32_t* __restrict__ nonfinite) {
+// One block of kHistBins threads: bin totals over the partial histograms, the
+// exact sum, gamma = max(RN32(RN64(sum) / count), 1e-5) into *w_scale, the
+// non-finite flag, and the packed buffer's trailer {magic, N, K, 0}.
+__global__ void __launch_bounds__(kHistBins)
+absmean_finish_kernel(const unsigned long long* __restrict__ part, int nblocks, int N, int K,
+                      float* __restrict__ w_scale, uint32_t* __restrict__ nonfinite, uint32_t* __restrict__ trailer) {
     __shared__ unsigned long long H[kHistBins];
     const int e = threadIdx.x;
     unsigned long long s = 0ull;
@@ -198,12 +234,17 @@ absmean_finish_kernel(const unsigned long long* __restrict__ part, int nblocks, 
     H[e] = s;
     __syncthreads();
     if (e == 0) {
-        unsigned long long L[kLimbs] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
-        for (int b = 0; b < 255; ++b)
-            if (H[b]) wide_add_shifted(L, H[b], b == 0 ? 0 : b - 1);
+        unsigned long long L[kLimbs] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+        for (int j = 65; j < kNonFiniteBin; ++j)
+            if (H[j]) wide_add_shifted(L, H[j], j - 65);
+        const long long count = static_cast<long long>(N) * K;
         const double mean = __ddiv_rn(wide_to_double(L), static_cast<double>(count));
         *w_scale = fmaxf(__double2float_rn(mean), 1e-5f);
-        *nonfinite = H[255] ? 1u : 0u;
+        *nonfinite = H[kNonFiniteBin] ? 1u : 0u;
+        trailer[0] = kTrailerMagic;
+        trailer[1] = static_cast<uint32_t>(N);
+        trailer[2] = static_cast<uint32_t>(K);
+        trailer[3] = 0u;
     }
 }
 
@@ -502,13 +543,11 @@ int bitmtp_linear_ternarize_pack(const float* W, int64_t N, int64_t K, int64_t l
     absmean_hist_kernel<<<G, 256, 0, s>>>(W, ldw, static_cast<int>(N), static_cast<int>(K), part);
     st = cuda_status(cudaGetLastError());
     if (st != BITMTP_OK) return st;
-    absmean_finish_kernel<<<1, kHistBins, 0, s>>>(part, G, static_cast<long long>(N * K), w_scale, nonfinite);
-    st = cuda_status(cudaGetLastError());
-    if (st != BITMTP_OK) return st;
     uint8_t* base = static_cast<uint8_t*>(pk);
     uint32_t* trailer = reinterpret_cast<uint32_t*>(base + need - 16);
-    const uint32_t head[4] = {kTrailerMagic, static_cast<uint32_t>(N), static_cast<uint32_t>(K), 0u};
-    st = cuda_status(cudaMemcpyAsync(trailer, head, sizeof(head), cudaMemcpyHostToDevice, s));
+    absmean_finish_kernel<<<1, kHistBins, 0, s>>>(part, G, static_cast<int>(N), static_cast<int>(K), w_scale,
+                                                  nonfinite, trailer);
+    st = cuda_status(cudaGetLastError());
     if (st != BITMTP_OK) return st;
     const bool vec = aligned16(W) && (ldw % 4) == 0;
     pack_kernel<F32Source><<<dim3(KT, NT), 256, 0, s>>>(F32Source{W, ldw, w_scale, vec}, static_cast<int>(N),
