@@ -110,7 +110,8 @@ pack_kernel(Src src, int N, int K, int KT, uint32_t* __restrict__ pk, uint32_t* 
 // * entries outside that window go to shared bins: bin j holds an integer
 //   sum at scale 2^(j - kBinOff - 150), entry (m, e) into bin e + kBinOff;
 // * at the end each thread adds its accumulator, in four 32-bit pieces, to
-//   bins b + 32 i + kBinOff (i = 0..3).
+//   bins b + 32 i + kBinOff (i = 0..3), and each block adds its non-zero bins
+//   into one global set of bins (zeroed by the host before the launch).
 // Bins 89..438 are the only ones used; bin 511 counts non-finite entries.  A
 // bin stays below 2^39 * 2^24 + 2^17 * 2^32 < 2^64.
 constexpr int kHistBins = 512;
@@ -120,40 +121,54 @@ constexpr int kHistMaxBlocks = 512;
 
 int hist_blocks(int64_t N) { return static_cast<int>(std::min<int64_t>(N, kHistMaxBlocks)); }
 
+// Grid-stride over rows; vec: rows 16-byte aligned (W aligned, ldw % 4 == 0),
+// read as float4 with the row's last K % 4 entries one by one.
 __global__ void __launch_bounds__(256)
-absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, unsigned long long* __restrict__ part) {
+absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, bool vec,
+                    unsigned long long* __restrict__ gbins) {
     __shared__ unsigned long long h[kHistBins];
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = 0ull;
     __syncthreads();
     unsigned long long acc_lo = 0ull, acc_hi = 0ull;
     int base = 0;
     bool have_base = false;
+    auto add = [&](float w) {
+        const uint32_t b = __float_as_uint(w) & 0x7FFFFFFFu;
+        const int eb = static_cast<int>(b >> 23);
+        if (eb == 255) {
+            atomicAdd(&h[kNonFiniteBin], 1ull);
+            return;
+        }
+        const unsigned long long m = (b & 0x7FFFFFu) | (eb ? 0x800000u : 0u);
+        if (m == 0ull) return;
+        const int e = eb ? eb : 1;
+        if (!have_base) {
+            base = e - 40;
+            have_base = true;
+        }
+        const int d = e - base;
+        if (d >= 0 && d < 64) {
+            const unsigned long long lo = m << d;
+            const unsigned long long hi = d > 40 ? (m >> (64 - d)) : 0ull;
+            acc_lo += lo;
+            acc_hi += hi + (acc_lo < lo ? 1ull : 0ull);
+        } else {
+            atomicAdd(&h[e + kBinOff], m);
+        }
+    };
+    const int K4 = vec ? K / 4 : 0;
     for (int n = blockIdx.x; n < N; n += gridDim.x) {
         const float* row = W + static_cast<long long>(n) * ldw;
-        for (int k = threadIdx.x; k < K; k += blockDim.x) {
-            const uint32_t b = __float_as_uint(row[k]) & 0x7FFFFFFFu;
-            const int eb = static_cast<int>(b >> 23);
-            if (eb == 255) {
-                atomicAdd(&h[kNonFiniteBin], 1ull);
-                continue;
-            }
-            const unsigned long long m = (b & 0x7FFFFFu) | (eb ? 0x800000u : 0u);
-            if (m == 0ull) continue;
-            const int e = eb ? eb : 1;
-            if (!have_base) {
-                base = e - 40;
-                have_base = true;
-            }
-            const int d = e - base;
-            if (d >= 0 && d < 64) {
-                const unsigned long long lo = m << d;
-                const unsigned long long hi = d > 40 ? (m >> (64 - d)) : 0ull;
-                acc_lo += lo;
-                acc_hi += hi + (acc_lo < lo ? 1ull : 0ull);
-            } else {
-                atomicAdd(&h[e + kBinOff], m);
-            }
+        const float4* row4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 4
+        for (int k4 = threadIdx.x; k4 < K4; k4 += blockDim.x) {
+            const float4 v = row4[k4];
+            add(v.x);
+            add(v.y);
+            add(v.z);
+            add(v.w);
         }
+        for (int k = 4 * K4 + threadIdx.x; k < K; k += blockDim.x) add(row[k]);
     }
     if (have_base) {
         const unsigned long long piece[4] = {acc_lo & 0xFFFFFFFFull, acc_lo >> 32, acc_hi & 0xFFFFFFFFull, acc_hi >> 32};
@@ -163,7 +178,7 @@ absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, un
     }
     __syncthreads();
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
-        part[static_cast<size_t>(blockIdx.x) * kHistBins + i] = h[i];
+        if (h[i]) atomicAdd(&gbins[i], h[i]);
 }
 
 // 512-bit unsigned integer in 64-bit limbs, least significant first, in units
@@ -221,17 +236,15 @@ __device__ double wide_to_double(const unsigned long long (&L)[kLimbs]) {
     return ldexp(static_cast<double>(mant), lo + kUnitExp);  // exact: a normal fp64
 }
 
-// One block of kHistBins threads: bin totals over the partial histograms, the
-// exact sum, gamma = max(RN32(RN64(sum) / count), 1e-5) into *w_scale, the
-// non-finite flag, and the packed buffer's trailer {magic, N, K, 0}.
+// One block of kHistBins threads: the exact sum from the global bins,
+// gamma = max(RN32(RN64(sum) / count), 1e-5) into *w_scale, the non-finite
+// flag, and the packed buffer's trailer {magic, N, K, 0}.
 __global__ void __launch_bounds__(kHistBins)
-absmean_finish_kernel(const unsigned long long* __restrict__ part, int nblocks, int N, int K,
-                      float* __restrict__ w_scale, uint32_t* __restrict__ nonfinite, uint32_t* __restrict__ trailer) {
+absmean_finish_kernel(const unsigned long long* __restrict__ gbins, int N, int K, float* __restrict__ w_scale,
+                      uint32_t* __restrict__ nonfinite, uint32_t* __restrict__ trailer) {
     __shared__ unsigned long long H[kHistBins];
     const int e = threadIdx.x;
-    unsigned long long s = 0ull;
-    for (int b = 0; b < nblocks; ++b) s += part[static_cast<size_t>(b) * kHistBins + e];
-    H[e] = s;
+    H[e] = gbins[e];
     __syncthreads();
     if (e == 0) {
         unsigned long long L[kLimbs] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
@@ -520,7 +533,7 @@ int bitmtp_linear_pack(const int8_t* T, int64_t N, int64_t K, int64_t ldt, void*
 
 size_t bitmtp_linear_ternarize_workspace_bytes(int64_t N, int64_t K) {
     if (N < 1 || K < 1 || N > BITMTP_MAX_N || K > BITMTP_MAX_K) return 0;
-    return static_cast<size_t>(hist_blocks(N)) * kHistBins * sizeof(unsigned long long) + 256;
+    return kHistBins * sizeof(unsigned long long) + 256;  // the bins, then the non-finite flag
 }
 
 int bitmtp_linear_ternarize_pack(const float* W, int64_t N, int64_t K, int64_t ldw, void* pk, size_t pk_bytes,
@@ -537,19 +550,21 @@ int bitmtp_linear_ternarize_pack(const float* W, int64_t N, int64_t K, int64_t l
     const int NT = static_cast<int>(ceil_div(N, kTileN));
     const int KT = static_cast<int>(ceil_div(K, kTileK));
     const int G = hist_blocks(N);
-    unsigned long long* part = static_cast<unsigned long long*>(workspace);
+    unsigned long long* gbins = static_cast<unsigned long long*>(workspace);
     uint32_t* nonfinite = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) +
-                                                      static_cast<size_t>(G) * kHistBins * sizeof(unsigned long long));
-    absmean_hist_kernel<<<G, 256, 0, s>>>(W, ldw, static_cast<int>(N), static_cast<int>(K), part);
+                                                      kHistBins * sizeof(unsigned long long));
+    const bool vec = aligned16(W) && (ldw % 4) == 0;
+    st = cuda_status(cudaMemsetAsync(gbins, 0, kHistBins * sizeof(unsigned long long), s));
+    if (st != BITMTP_OK) return st;
+    absmean_hist_kernel<<<G, 256, 0, s>>>(W, ldw, static_cast<int>(N), static_cast<int>(K), vec, gbins);
     st = cuda_status(cudaGetLastError());
     if (st != BITMTP_OK) return st;
     uint8_t* base = static_cast<uint8_t*>(pk);
     uint32_t* trailer = reinterpret_cast<uint32_t*>(base + need - 16);
-    absmean_finish_kernel<<<1, kHistBins, 0, s>>>(part, G, static_cast<int>(N), static_cast<int>(K), w_scale,
+    absmean_finish_kernel<<<1, kHistBins, 0, s>>>(gbins, static_cast<int>(N), static_cast<int>(K), w_scale,
                                                   nonfinite, trailer);
     st = cuda_status(cudaGetLastError());
     if (st != BITMTP_OK) return st;
-    const bool vec = aligned16(W) && (ldw % 4) == 0;
     pack_kernel<F32Source><<<dim3(KT, NT), 256, 0, s>>>(F32Source{W, ldw, w_scale, vec}, static_cast<int>(N),
                                                         static_cast<int>(K), KT,
                                                         reinterpret_cast<uint32_t*>(base), trailer + 3);

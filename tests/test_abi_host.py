@@ -52,8 +52,7 @@ def test_ternarize_validation(lib):
     """Argument checks of the device ternarisation, all before any CUDA call."""
     wb = L.bitmtp_linear_ternarize_workspace_bytes
     assert wb(0, 5) == 0 and wb(5, 0) == 0 and wb(5, L.MAX_K + 1) == 0
-    assert wb(1, 1) == 512 * 8 + 256                 # one block of 512 bins
-    assert wb(700, 64) == wb(100000, 64) == 512 * 512 * 8 + 256  # at most 512 blocks
+    assert wb(1, 1) == wb(700, 64) == wb(100000, L.MAX_K) == 512 * 8 + 256  # 512 bins + flag
     nb = L.packed_bytes(64, 64)
     tp = L.bitmtp_linear_ternarize_pack
 
