@@ -15,6 +15,11 @@ graphs with programmatic dependent launch between consecutive launches.
 Metric: achieved HBM GB/s on algorithmic bytes (packed weights + activations),
 also as a fraction of the measured copy bandwidth, plus rows/s per width.
 
+The line also carries ``ternarize_pack``: the offline step before the path,
+device absmean ternarisation + pack of the layer set's seven projections from
+fp32 weights, in GB/s of algorithmic bytes (fp32 weights once + packed tiles),
+outside the timed steps (``--no-ternarize`` skips it).
+
 ``--impl reference`` times the CPU oracle on a bounded sample of the same
 workload (its only use of the oracle besides the cpu_baseline field).
 """
