@@ -25,10 +25,11 @@ oracle writes out directly:
 * integer accumulation acc[m, n] = sum_k T[n, k] * q[m, k]  (``gemm_acc``);
 * dequant epilogue y = acc * a_scale[m] * w_scale  (``dequant``).
 
-Readings taken where the pages are silent are listed in the design doc (zero row ->
-all-zero codes and a_scale 0; clamp to +-127; s multiplied, not divided; the
-weight epsilon 1e-5; exact bf16 widening; dequant evaluated in fp64 and rounded
-once to fp32, then to bf16 for bf16 output).
+Readings taken where the pages are silent: a zero row gives all-zero codes
+and a_scale 0; codes are clamped to +-127; s is multiplied, not divided; the
+weight epsilon is 1e-5; mean|W| is the exact sum rounded once to fp64; bf16
+widens exactly; dequant is evaluated in fp64 and rounded once to fp32, then
+to bf16 for bf16 output.
 
 The packed-weight format (``pack_tiles`` / ``unpack_tiles``) is this library's
 own internal layout, not the pages'; it is restated here from its written
