@@ -29,6 +29,12 @@ def test_step_bytes():
     assert pk == 4 * 17_367_040
 
 
+def test_ternarize_bytes():
+    # fp32 weights of the seven projections once (69.47 M entries) plus their
+    # packed form (17,367,040 bytes of tiles and seven 16-byte trailers)
+    assert bench.ternarize_bytes() == 4 * 69_468_160 + 17_367_040 + 7 * 16 == 295_239_792
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
