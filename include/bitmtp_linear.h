@@ -11,7 +11,9 @@
  * the library implements the BitNet b1.58 definitions:
  *
  *   weights      T[n][k] in {-1, 0, +1}, one fp32 per-tensor scale w_scale,
- *                W ~= w_scale * T;
+ *                W ~= w_scale * T (from fp32 W: w_scale = max(mean|W|, 1e-5),
+ *                T = clamp(rint(W / w_scale), -1, 1); see
+ *                bitmtp_linear_ternarize_pack);
  *   activations  per row m: amax = max_k |x[m][k]|, s = RN(127 / amax),
  *                q[m][k] = clamp(rint(RN(x * s)), -127, 127) (fp32, round
  *                half to even), a_scale[m] = RN(amax / 127); a zero row gives
@@ -27,7 +29,8 @@
  *     a caller-owned workspace (see bitmtp_linear_workspace_bytes).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is enqueued asynchronously on it; only
- *     bitmtp_linear_pack and bitmtp_linear_device_error synchronise it.
+ *     bitmtp_linear_pack, bitmtp_linear_ternarize_pack and
+ *     bitmtp_linear_device_error synchronise it.
  *   - Arguments are validated on the host before any CUDA call; an invalid
  *     call returns a negative status and enqueues nothing.  Nothing is thrown
  *     across the ABI.
