@@ -22,25 +22,28 @@
 //                 contiguous run is one copy (the engine's cost is per copy);
 //     warps 0-3   one output row per thread: the compute path (below), then
 //                 the epilogue -- a whole row tile is dequantised and written
-//                 straight away; a row tile split between CTAs is finished by
-//                 the last contributor, which sums the others' int32 partials
-//                 from the workspace;
+//                 straight away; a row tile split between CTAs is added by
+//                 every contributor into one workspace accumulator (no-return
+//                 fp32 vector reductions of integer partial sums, exact in any
+//                 order) and finished by the last contributor to arrive;
 //     warp 5      (tensor path) issues tcgen05.mma.
 //
 // Compute paths (the same 2-bit code words feed both):
 //   tensor (kPathTC16 / kPathTC8): each thread turns its code words into e4m3
 //     bytes with one shift and one mask per register -- the 2-bit code u is
 //     the mantissa of an e4m3 subnormal, value u * 2^-9 -- and writes them to
-//     tensor memory as the A operand (tcgen05.st, seven k-tile buffers in
+//     tensor memory as the A operand (tcgen05.st, six k-tile buffers in
 //     flight).  The activation operand splits every code exactly as
 //     q = 16*h + l (h in [-8, 7], l in [0, 15], both exact in e4m3) into two
 //     operand rows, so one tcgen05.mma kind::f8f6f4 (M=128, K=32, N = twice the
 //     activation rows: 32 or 16) yields both halves.  Products are integers
 //     times 2^-9 and every sum stays below 2^24 of those units, so the fp32
-//     accumulator is exact; the epilogue forms 2^9 * (16*D_h + D_l).  One
-//     thread issues the MMAs, two k tiles (eight MMAs, straight-line code)
-//     per wait: a branch or a wait between tcgen05.mma issues costs more than
-//     the MMAs themselves.
+//     accumulator is exact; the epilogue forms 2^9 * (16*D_h + D_l).  The
+//     elected lane of a converged warp issues the MMAs under a predicate, two
+//     k tiles (eight MMAs, straight-line code) per wait: a branch or a wait
+//     between tcgen05.mma issues costs more than the MMAs themselves.  Two
+//     accumulators alternate between consecutive row-tile segments, so a
+//     segment's epilogue runs while the next segment's MMAs go on.
 //   dp4a (kPathDP): four byte masks per code word, four int32 accumulators
 //     per row (scales 4^s, recombined with exact shifts).
 // With u = T + 1, sum_k T*q = sum_k u*q - sum_k q; the second sum comes from
