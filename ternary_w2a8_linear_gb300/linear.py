@@ -2,8 +2,9 @@
 
 Argument marshalling only: every step of the linear runs in the library's CUDA
 kernels.  PyTorch provides device memory and the current stream.  The raw
-entry points keep the C names (``bitmtp_linear_*``); ``pack``, ``quant_act``,
-``gemm`` and ``gemm_grouped`` are tensor conveniences over them.
+entry points keep the C names (``bitmtp_linear_*``); ``pack``,
+``ternarize_pack``, ``quant_act``, ``gemm`` and ``gemm_grouped`` are tensor
+conveniences over them.
 
 The library must have been built (``ternary_w2a8_linear_gb300.build``); if it
 is missing this module raises instead of falling back to anything else.
