@@ -34,6 +34,19 @@ def test_exports_every_header_symbol(lib):
         assert hasattr(L, s), s  # binding keeps the C names
 
 
+def test_binding_constants_match_header():
+    """Every integer #define of the header has the same value in the binding."""
+    import re
+    text = open(L.HEADER_PATH).read()
+    defs = {}
+    for name, val in re.findall(r"^#define BITMTP_(\w+)\s+(\(?-?(?:0x)?[0-9a-fA-F]+u?\)?)", text, re.M):
+        defs[name] = int(val.strip("()").rstrip("u"), 0)
+    assert len(defs) >= 18
+    for name, val in defs.items():
+        assert getattr(L, name) == val, name
+    assert L.NOALLOC_SCRATCH_BYTES == 4 * 1024 * 1024
+
+
 def test_version_and_status_strings(lib):
     assert L.bitmtp_linear_version() == 0x000100
     for st in (L.OK, L.ERR_INVALID, L.ERR_ALIGN, L.ERR_SHAPE, L.ERR_NOT_TERNARY,
