@@ -87,6 +87,14 @@ extern "C" {
  * activation tile for 5..8 and a 16-row tile for 9..16.  Forcing the tensor
  * path at widths 1..4 uses its 8-row tile; forcing dp4a is valid for widths
  * 1..4.) */
+/* Test only, never for production calls: CTA 0 of the launch never requests
+ * its first chunk of packed weights and every wait of the launch gives up
+ * after 1 ms instead of 2 s, so the launch exercises its bounded-wait error
+ * path: it ends without hanging, sets the device error word (see
+ * bitmtp_linear_device_error) and leaves its outputs unspecified.  Zero-fill
+ * the workspace before the next call (the no-alloc entry point does this
+ * itself once bitmtp_linear_device_error has reported the error). */
+#define BITMTP_FLAG_TEST_WITHHOLD 0x100u
 
 /*
  * Packed ternary weights (this library's own layout; the pages only say the
@@ -172,13 +180,14 @@ typedef struct bitmtp_out {
 
 /* Workspace of a GEMM call: a device buffer the caller allocates once,
  * 16-byte aligned, of at least the size these queries return, and
- * zero-fills before its first use (e.g. cudaMemset).  It holds split-row-tile
- * accumulators and arrival counters (a fixed 2.5 MiB part) and each problem's
- * quantised activation operand (about 4 KiB per 128 in-features); every call
- * leaves the accumulators and counters at zero, so one workspace serves calls
- * of any shapes that fit.  Calls that may execute concurrently on the GPU need distinct
- * workspaces; calls ordered on one stream may share one.  After a call that
- * ends in BITMTP_ERR_DEVICE, zero-fill it again.  Returns 0 for out-of-range
+ * zero-fills before its first use (e.g. cudaMemset).  It holds a fixed part
+ * of about 2.5 MiB -- one slot of partial sums per CTA for row tiles split
+ * between CTAs, and a ready flag per slot -- and each problem's quantised
+ * activation operand (about 4 KiB per 128 in-features).  Every call leaves
+ * the flags at zero, so one workspace serves calls of any shapes that fit.
+ * Calls that may execute concurrently on the GPU need distinct workspaces;
+ * calls ordered on one stream may share one.  After a call that ends in
+ * BITMTP_ERR_DEVICE, zero-fill it again.  Returns 0 for out-of-range
  * arguments. */
 size_t bitmtp_linear_workspace_bytes(int64_t N, int64_t K, int64_t M);
 
@@ -247,15 +256,16 @@ int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc,
  *     load the library's device code).  Make that first call before any
  *     stream capture begins.
  *   - Sharing: all calls on a device share the one array and it keeps what
- *     the previous call left.  Each call first clears, on `stream`, the part
- *     that must start at zero (the split-row-tile accumulators and arrival
- *     counters, 2.5 MiB); the activation part is always written before it is
- *     read.  Calls whose
- *     work can overlap on the GPU (different streams without ordering between
- *     them, or different host threads) race on the array and give wrong
- *     results; order them on one stream or use bitmtp_linear_gemm with
- *     distinct workspaces.
- * Enqueues one small memset and the GEMM kernel on `stream`. */
+ *     the previous call left.  The part that must start at zero (the ready
+ *     flags, 1.25 KiB) starts zeroed and every call leaves it at zero; only a
+ *     call that gave up a bounded wait can leave it dirty, and once
+ *     bitmtp_linear_device_error has reported that, the next call clears it
+ *     first (one memset on `stream`).  Calls whose work can overlap on the GPU
+ *     (different streams without ordering between them, or different host
+ *     threads) race on the array and give wrong results; order them on one
+ *     stream or use bitmtp_linear_gemm with distinct workspaces.
+ * Enqueues the two kernels of bitmtp_linear_gemm on `stream` (preceded by
+ * that memset only after a reported error). */
 int bitmtp_linear_gemm_noalloc(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M,
                                const bitmtp_act* act, const bitmtp_out* out,
                                unsigned flags, void* stream);

@@ -298,10 +298,14 @@ quant_act_kernel(const void* __restrict__ x, int kind, int K, long long ldx, int
 }
 
 // ------------------------------------------------------------- device --
+// Per-device facts, looked up once per device: the first caller fills them
+// and publishes `state` with release order; later callers read it with
+// acquire order (concurrent first callers only repeat the same queries).
 struct DevInfo {
-    int checked = 0;   // 0 unknown, 1 ok, -1 unsupported
+    std::atomic<int> state{0};   // 0 unknown, 1 ok, -1 unsupported
     int sms = 0;
     int* err = nullptr;
+    std::atomic<int> dirty{0};   // the no-alloc scratch may hold flags of a launch that gave up
 };
 DevInfo g_dev[64];
 
@@ -313,7 +317,8 @@ int current_device(DevInfo** info) {
     }
     if (dev >= 64) return BITMTP_ERR_UNSUPPORTED;
     DevInfo& d = g_dev[dev];
-    if (d.checked == 0) {
+    int st = d.state.load(std::memory_order_acquire);
+    if (st == 0) {
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -322,7 +327,7 @@ int current_device(DevInfo** info) {
             return BITMTP_ERR_UNSUPPORTED;
         }
         if (major != 10 || minor != 3) {
-            d.checked = -1;
+            st = -1;
         } else {
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
@@ -331,10 +336,11 @@ int current_device(DevInfo** info) {
             }
             d.err = static_cast<int*>(p);
             d.sms = sms;
-            d.checked = 1;
+            st = 1;
         }
+        d.state.store(st, std::memory_order_release);
     }
-    if (d.checked != 1) return BITMTP_ERR_UNSUPPORTED;
+    if (st != 1) return BITMTP_ERR_UNSUPPORTED;
     *info = &d;
     return BITMTP_OK;
 }
@@ -386,6 +392,8 @@ int check_problem(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M
     g->kt = static_cast<int>(ceil_div(K, kTileK));
     g->act_kind = act->kind;
     g->out_dtype = out->dtype;
+    const int64_t esize = act->kind == BITMTP_F32 ? 4 : (act->kind == BITMTP_BF16 ? 2 : 1);
+    g->vec_ok = (aligned16(act->x) && (act->ldx * esize) % 16 == 0) ? 1 : 0;
     return BITMTP_OK;
 }
 
@@ -452,9 +460,14 @@ int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes,
     // every CTA range is non-empty (nctas <= tiles) and, where the problem is
     // large enough, at least kMinTilesPerCta long
     prm.nctas = static_cast<int>(std::max(1ll, std::min(cap, (tiles + kMinTilesPerCta - 1) / kMinTilesPerCta)));
-    prm.counters = reinterpret_cast<unsigned*>(w + kWsCounters);
+    prm.tiles_q = static_cast<int>(tiles / prm.nctas);
+    prm.tiles_r = static_cast<int>(tiles % prm.nctas);
+    prm.flags = reinterpret_cast<unsigned*>(w + kWsFlags);
     prm.slots = reinterpret_cast<int*>(w + kWsSlots);
     prm.err = dev->err;
+    const bool test_withhold = (flags & BITMTP_FLAG_TEST_WITHHOLD) != 0;
+    prm.withhold = test_withhold ? 0 : -1;
+    prm.wait_ns = test_withhold ? kTestWaitNs : kWaitNs;
     return cuda_status(launch_gemm(prm, path, dp_rows, (flags & BITMTP_FLAG_PDL) != 0, stream));
 }
 
@@ -654,11 +667,16 @@ int bitmtp_linear_gemm_noalloc(const void* pk, float w_scale, int64_t N, int64_t
     st = noalloc_scratch(&scratch);
     if (st != BITMTP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the split-row-tile counters and accumulators must start at zero; a call
-    // that gave up a bounded wait may have left some set
-    st = cuda_status(cudaMemsetAsync(static_cast<uint8_t*>(scratch) + kWsCounters, 0,
-                                     kWsAct - kWsCounters, s));
-    if (st != BITMTP_OK) return st;
+    // The flags must start at zero.  The array starts zeroed and every launch
+    // leaves them at zero, except one that gave up a bounded wait: once
+    // bitmtp_linear_device_error has reported that, the next call clears them.
+    if (dev->dirty.exchange(0, std::memory_order_acq_rel) != 0) {
+        st = cuda_status(cudaMemsetAsync(static_cast<uint8_t*>(scratch) + kWsFlags, 0, kWsSlots - kWsFlags, s));
+        if (st != BITMTP_OK) {
+            dev->dirty.store(1, std::memory_order_release);
+            return st;
+        }
+    }
     return run_gemms(&g, 1, scratch, BITMTP_NOALLOC_SCRATCH_BYTES, flags, s);
 }
 
@@ -672,6 +690,7 @@ int bitmtp_linear_device_error(void* stream) {
     st = cuda_status(cudaMemcpy(&v, dev->err, sizeof(int), cudaMemcpyDeviceToHost));
     if (st != BITMTP_OK) return st;
     if (v != 0) {
+        dev->dirty.store(1, std::memory_order_release);
         const int zero = 0;
         st = cuda_status(cudaMemcpy(dev->err, &zero, sizeof(int), cudaMemcpyHostToDevice));
         if (st != BITMTP_OK) return st;

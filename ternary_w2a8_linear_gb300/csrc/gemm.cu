@@ -14,18 +14,27 @@
 //   w2a8_streamk_kernel  the flattened (problem, row tile, k tile) space is
 //                     split into equal contiguous ranges, one per CTA
 //                     (stream-K), so every SM streams the same number of
-//                     weight bytes whatever the mix of shapes.  Each CTA:
+//                     weight bytes whatever the mix of shapes.  A range is a
+//                     run of "segments" (the k tiles of one row tile it
+//                     covers), worked from the range's end back to its start:
+//                     its last segment, the head of a row tile the next CTA
+//                     finishes ("contributor"), comes first, and its partial
+//                     sums go to the CTA's slot in the workspace, published
+//                     by a flag early on; its first segment, the tail of a row
+//                     tile that earlier CTAs began ("owner"), comes last, when
+//                     the contributors' flags are normally set: it adds their
+//                     slots and writes the output.  Whole row tiles in between
+//                     are written directly.  Only owners wait for other CTAs,
+//                     and contributors never wait, so nothing can deadlock;
+//                     every wait is bounded.  Each CTA:
 //     warp 4      bulk copies (TMA engine) into a ring of chunks of four
 //                 tiles: weight tiles first -- they do not depend on the
 //                 preparation kernel, so they are requested before the PDL
 //                 wait -- and, after it, the matching activation tiles; each
 //                 contiguous run is one copy (the engine's cost is per copy);
+//                 and the flag that publishes a contributor's partial sums;
 //     warps 0-3   one output row per thread: the compute path (below), then
-//                 the epilogue -- a whole row tile is dequantised and written
-//                 straight away; a row tile split between CTAs is added by
-//                 every contributor into one workspace accumulator (no-return
-//                 fp32 vector reductions of integer partial sums, exact in any
-//                 order) and finished by the last contributor to arrive;
+//                 the segment epilogues;
 //     warp 5      (tensor path) issues tcgen05.mma.
 //
 // Compute paths (the same 2-bit code words feed both):
@@ -61,6 +70,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+#include <cstddef>
+
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant.cuh"
@@ -71,6 +83,7 @@ namespace {
 constexpr int kChunk = 4;            // k tiles per ring chunk (16 KiB of weights)
 constexpr int kMaxRing = 6;          // chunks in the ring (upper bound)
 constexpr int kCtrlBytes = 2048;
+constexpr int kBarEpi = 1;           // named barrier: the four consumer warps
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kAccCol = 0;      // D: two accumulators (alternate segments) of 32 fp32 columns
 constexpr uint32_t kACol = 64;       // A: kATiles buffers of one k tile each
@@ -90,6 +103,8 @@ enum : int {
     kErrWaitAEmpty = 0x104,
     kErrWaitD = 0x105,
     kErrWaitEmpty = 0x106,
+    kErrWaitFlag = 0x107,
+    kErrWaitSlot = 0x108,
 };
 
 struct Ctrl {
@@ -99,9 +114,10 @@ struct Ctrl {
     uint64_t a_full[kATiles];     // A buffer written (four consumer warps)
     uint64_t mma_done[kBatchBars]; // MMA batch b complete: barrier b % kBatchBars
     uint64_t dfull[2];            // accumulator of segment s (D buffer s & 1) complete
+    uint64_t slot_done;           // contributor partial sums stored (four consumer warps)
     uint32_t tmem_base;
     int failed;
-    int flag[2];
+    int owner_ok;
     float asc[BITMTP_MAX_GROUP][16];  // dequant scale per (problem - p0, row)
     GemmProblem prob[BITMTP_MAX_GROUP];  // copy of the problem table
 };
@@ -142,8 +158,8 @@ __device__ __forceinline__ uint32_t e4m3x2_small(float a, float b) {
 }
 
 // Problem holding flattened tile t.  pp: the problem table (a shared-memory
-// copy in the GEMM: indexing the kernel parameter with a runtime index costs
-// a slow dependent load per field).
+// copy: indexing the kernel parameter with a runtime index costs a slow
+// dependent load per field).
 __device__ __forceinline__ int find_problem_by_tile(const GemmProblem* pp, int np, long long t) {
     int pi = 0;
 #pragma unroll 1
@@ -151,37 +167,59 @@ __device__ __forceinline__ int find_problem_by_tile(const GemmProblem* pp, int n
         if (t >= pp[i].tile_begin) pi = i;
     return pi;
 }
-__device__ __forceinline__ long long range_start(int b, long long T, int n) {
-    return (static_cast<long long>(b) * T) / n;
-}
-// CTA whose range holds flattened tile t (every range is non-empty: n <= T).
-__device__ __forceinline__ int range_owner(long long t, long long T, int n) {
-    return static_cast<int>(((t + 1) * n - 1) / T);
+// Stream-K split of the flattened tiles: CTA b holds q tiles, plus one if
+// b < r (q = T / nctas, r = T % nctas, worked out on the host; T < 2^31).
+__device__ __forceinline__ int range_start(int b, int q, int r) { return b * q + min(b, r); }
+// CTA whose range holds flattened tile t.
+__device__ __forceinline__ int range_owner(int t, int q, int r) {
+    const int big = r * (q + 1);  // tiles of the first r CTAs
+    return t < big ? t / (q + 1) : r + (t - big) / q;
 }
 
-// Flattened-tile walker: (problem, row tile, k tile) advancing with k fastest.
-struct TileIter {
-    int pi, rt, kt;
-    __device__ void init(const GemmProblem* pp, int np, long long t) {
-        pi = find_problem_by_tile(pp, np, t);
-        const int local = static_cast<int>(t - pp[pi].tile_begin);  // < nt * kt < 2^31
-        rt = local / pp[pi].kt;
-        kt = local - rt * pp[pi].kt;
+// k tiles [ka, kb) of row tile rt of problem pi; flattened index of k tile ka.
+struct Seg {
+    int pi, rt, ka, kb;
+    long long t0;
+};
+
+// The segment that holds flattened tile t_end - 1, clipped below at t_begin.
+__device__ __forceinline__ void seg_ending_at(const GemmProblem* pp, int np, long long t_begin, long long t_end,
+                                              Seg& s) {
+    const long long t = t_end - 1;
+    const int pi = find_problem_by_tile(pp, np, t);
+    const GemmProblem& pr = pp[pi];
+    const int local = static_cast<int>(t - pr.tile_begin);  // < nt * kt < 2^31
+    const int rt = local / pr.kt;
+    const long long r0 = pr.tile_begin + static_cast<long long>(rt) * pr.kt;
+    const long long s0 = r0 > t_begin ? r0 : t_begin;
+    s.pi = pi;
+    s.rt = rt;
+    s.ka = static_cast<int>(s0 - r0);
+    s.kb = static_cast<int>(t_end - r0);
+    s.t0 = s0;
+}
+
+// The tiles of a CTA's range in processing order: segments from the range's
+// end to its start, k ascending inside each.
+struct ProcIter {
+    Seg s;
+    int k;
+    __device__ void init(const GemmProblem* pp, int np, long long t_begin, long long t_end) {
+        seg_ending_at(pp, np, t_begin, t_end, s);
+        k = s.ka;
     }
-    __device__ void next(const GemmProblem* pp) {
-        if (++kt == pp[pi].kt) {
-            kt = 0;
-            if (++rt == pp[pi].nt) {
-                rt = 0;
-                ++pi;
-            }
+    __device__ void next(const GemmProblem* pp, int np, long long t_begin) {
+        if (++k < s.kb) return;
+        if (s.t0 > t_begin) {
+            seg_ending_at(pp, np, t_begin, s.t0, s);
+            k = s.ka;
         }
     }
 };
 
-// Position of local tile i in the chunk ring and in the A buffers, advanced
-// one tile at a time (no division by the runtime ring size on the way to an
-// MMA issue or a barrier wait).
+// Position of local tile i (processing order) in the chunk ring and in the A
+// buffers, advanced one tile at a time (no division by the runtime ring size
+// on the way to an MMA issue or a barrier wait).
 struct RingPos {
     int cp;          // i % kChunk
     int q;           // (i / kChunk) % R: ring slot of the chunk
@@ -207,56 +245,43 @@ struct RingPos {
     __device__ int slot() const { return q * kChunk + cp; }  // tile slot in the ring
 };
 
-// Bulk-copy the weight tiles of tiles [first, first + count) of this CTA's
-// range into consecutive ring slots, one copy per run that is contiguous in
-// global memory (within one problem); all copies complete on `bar`.  Run by
-// a whole converged warp; only the lane with `on` set issues.
-__device__ void issue_weights(const GemmProblem* pp, int np, long long first, int count, uint8_t* dst, uint32_t bar,
-                              uint64_t pol, uint32_t on) {
+// Bulk-copy the weight tiles of the next `count` tiles of `it` (processing
+// order) into consecutive ring slots, one copy per run that is contiguous in
+// global memory (the k tiles of one segment); all copies complete on `bar`.
+// Run by a whole converged warp; only the lane with `on` set issues.
+__device__ void issue_weights(const GemmProblem* pp, int np, long long t_begin, ProcIter& it, int count,
+                              uint8_t* dst, uint32_t bar, uint64_t pol, uint32_t on) {
     mbar_arrive_expect_tx_if(on, bar, static_cast<uint32_t>(count * kTileBytes));
-    TileIter it;
-    it.init(pp, np, first);
-    const uint8_t* run_src = nullptr;
-    int run_len = 0, run_pi = -1;
-    uint8_t* run_dst = dst;
-    for (int k = 0; k < count; ++k) {
-        const GemmProblem& pr = pp[it.pi];
-        const uint8_t* src = pr.pk + (static_cast<size_t>(it.rt) * pr.kt + it.kt) * kTileBytes;
-        if (run_len == 0 || it.pi != run_pi) {
-            if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * kTileBytes, bar, pol);
-            run_dst = dst + k * kTileBytes;
-            run_src = src;
-            run_len = 0;
-            run_pi = it.pi;
-        }
-        ++run_len;
-        it.next(pp);
+    int k = 0;
+    while (k < count) {
+        const GemmProblem& pr = pp[it.s.pi];
+        const int run = min(count - k, it.s.kb - it.k);
+        if (run <= 0) break;  // never: count never exceeds the tiles left
+        const uint8_t* src = pr.pk + (static_cast<size_t>(it.s.rt) * pr.kt + it.k) * kTileBytes;
+        bulk_g2s_if(on, smem_u32(dst + static_cast<size_t>(k) * kTileBytes), src,
+                    static_cast<uint32_t>(run * kTileBytes), bar, pol);
+        k += run;
+        it.k += run - 1;
+        it.next(pp, np, t_begin);
     }
-    if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * kTileBytes, bar, pol);
 }
 
-// The same for the activation tiles (BT bytes each) of those tiles: a run
-// ends where the k index wraps to the next row tile or the problem changes.
-__device__ void issue_acts(const GemmProblem* pp, int np, long long first, int count, int BT, uint8_t* dst,
-                           uint32_t bar, uint64_t pol, uint32_t on) {
+// The same for the activation tiles (BT bytes each) of those tiles, from the
+// preparation kernel's operand in the workspace (one tile per k tile of the
+// problem): a run ends where the k index or the problem changes.
+__device__ void issue_acts(const GemmProblem* pp, int np, long long t_begin, ProcIter& it, int count, int BT,
+                           uint8_t* dst, uint32_t bar, uint64_t pol, uint32_t on) {
     mbar_arrive_expect_tx_if(on, bar, static_cast<uint32_t>(count * BT));
-    TileIter it;
-    it.init(pp, np, first);
-    const uint8_t* run_src = nullptr;
-    int run_len = 0;
-    uint8_t* run_dst = dst;
-    for (int k = 0; k < count; ++k) {
-        const uint8_t* src = pp[it.pi].actb + static_cast<size_t>(it.kt) * BT;
-        if (run_len == 0 || src != run_src + static_cast<size_t>(run_len) * BT) {
-            if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * BT, bar, pol);
-            run_dst = dst + k * BT;
-            run_src = src;
-            run_len = 0;
-        }
-        ++run_len;
-        it.next(pp);
+    int k = 0;
+    while (k < count) {
+        const int run = min(count - k, it.s.kb - it.k);
+        if (run <= 0) break;  // never: count never exceeds the tiles left
+        const uint8_t* src = pp[it.s.pi].actb + static_cast<size_t>(it.k) * BT;
+        bulk_g2s_if(on, smem_u32(dst + static_cast<size_t>(k) * BT), src, static_cast<uint32_t>(run * BT), bar, pol);
+        k += run;
+        it.k += run - 1;
+        it.next(pp, np, t_begin);
     }
-    if (run_len > 0) bulk_g2s_if(on, smem_u32(run_dst), run_src, run_len * BT, bar, pol);
 }
 
 // Element k of one activation row as fp32 (exact for all three kinds).
@@ -483,105 +508,92 @@ __device__ __forceinline__ void store_out(const GemmProblem& pr, int m, int n, i
     if (pr.acc) pr.acc[static_cast<long long>(m) * pr.lda + n] = acc;
 }
 
-// A split row tile this CTA contributed to, finished after the main loop.
-struct Pending {
-    int pi, rt, b_first, b_last;
-};
-
-// Accumulator of the split row tile whose last k tile CTA b holds: four groups
-// of four rows, one float4 per column in each, columns consecutive.  A warp's
-// vector atomics then cover 512 contiguous bytes, and a narrow block touches
-// only the groups its rows occupy.
-__device__ __forceinline__ float4* acc_slot(const GemmParams& P, int b, int g, int col) {
-    return reinterpret_cast<float4*>(P.slots) + (static_cast<size_t>(b) * 4 + g) * kTileN + col;
+// Partial-sum slot of CTA b: four groups of four rows, one int4 per column in
+// each, columns consecutive (a warp's stores and loads cover 512 contiguous
+// bytes; a narrow block touches only the groups its rows occupy).
+__device__ __forceinline__ int4* slot_ptr(const GemmParams& P, int b, int g, int col) {
+    return reinterpret_cast<int4*>(P.slots) + (static_cast<size_t>(b) * 4 + g) * kTileN + col;
 }
 
-// Finish one segment (k tiles [ka, kb) of row tile rt of problem pi).
-// acc[m] is the exact partial sum_k T*q for the thread's row.  A whole row
-// tile is written out at once; a split one is added (fp32 vector atomics of
-// integer values, no return value) into its accumulator in the workspace -- the one of the CTA
-// holding the row tile's last k tile -- and recorded in `pend`.  b_first and
-// b_last: the CTAs holding the row tile's first and last k tiles (used only
-// for a split tile).  kRows: the compute path's rows per tile, a compile-time
-// bound on M that keeps the unrolled row loops (and the code) short.
+// Bounded wait for another CTA's flag (acquire at GPU scope).
+__device__ __forceinline__ bool wait_flag(const unsigned* f, unsigned long long limit_ns) {
+    if (ld_acquire_gpu(f) != 0u) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (ld_acquire_gpu(f) != 0u) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Segment roles: the whole row tile, the tail that finishes a row tile begun
+// by earlier CTAs (owner), or a part that another CTA finishes (contributor).
+enum SegRole : int { kWhole = 0, kOwner = 1, kContrib = 2 };
+
+__device__ __forceinline__ int seg_role(const Seg& s, const GemmProblem& pr) {
+    if (s.kb < pr.kt) return kContrib;
+    return s.ka == 0 ? kWhole : kOwner;
+}
+
+// Finish one segment.  acc[m]: the exact sum_k T*q of the segment for the
+// thread's output column (row tile column tid) and block row m.  kRows: the
+// compute path's rows per tile, a compile-time bound on M that keeps the
+// unrolled row loops (and the code) short.  owner_first: the first CTA of the
+// owner segment's row tile.  Every consumer thread calls it with the same
+// segment (the named barriers below need all four warps).
 template <int kRows>
-__device__ void segment_epilogue(const GemmParams& P, const Ctrl* c, int p0, int pi, int rt, int ka, int kb,
-                                 int b_first, int b_last, const int (&acc)[16], int tid, bool alive,
-                                 Pending* pend, int& npend) {
-    const GemmProblem& pr = c->prob[pi];
+__device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int p_lo, const Seg& s, int owner_first,
+                                 int (&acc)[16], int tid, bool& alive) {
+    const GemmProblem& pr = c->prob[s.pi];
     const int M = pr.M;
-    const int n = rt * kTileN + tid;
-    if (ka == 0 && kb == pr.kt) {
-        if (alive && n < pr.N) {
+    const int n = s.rt * kTileN + tid;
+    const int role = seg_role(s, pr);
+    const int b = blockIdx.x;
+    constexpr int kGroups = (kRows + 3) / 4;
+    if (role == kContrib) {
+        // the partial sums of this CTA's slot; warp 4 publishes the flag
 #pragma unroll
-            for (int m = 0; m < kRows; ++m)
-                if (m < M) store_out(pr, m, n, acc[m], c->asc[pi - p0][m]);
-        }
+        for (int g = 0; g < kGroups; ++g)
+            if (alive && 4 * g < M)
+                *slot_ptr(P, b, g, tid) = make_int4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(smem_u32(&c->slot_done));
         return;
     }
-    Pending& pe = pend[npend++];
-    pe.pi = pi;
-    pe.rt = rt;
-    pe.b_first = b_first;
-    pe.b_last = b_last;
-    // column tid of the row tile: one vector atomic per group of four rows (the
-    // partial sums are integers below 2^24 in magnitude, so fp32 adds are
-    // exact in any order)
-#pragma unroll
-    for (int g = 0; g < (kRows + 3) / 4; ++g)
-        if (alive && 4 * g < M)
-            red_add_v4(acc_slot(P, pe.b_last, g, tid), make_float4(static_cast<float>(acc[4 * g]), static_cast<float>(acc[4 * g + 1]),
-                                           static_cast<float>(acc[4 * g + 2]), static_cast<float>(acc[4 * g + 3])));
-}
-
-// After the main loop: one fence, one counter increment per split row tile;
-// the last contributor of a tile reads the accumulated sum, writes the output
-// and leaves the accumulator and the counter at zero.  A split row tile is
-// identified by the CTA holding its last k tile (a CTA is the last k tile's
-// holder for at most one split row tile).  Warps 0-3.  kRows as for
-// segment_epilogue.
-template <int kRows>
-__device__ void finish_pending(const GemmParams& P, Ctrl* c, int p0, const Pending* pend, int npend, int tid,
-                               bool alive) {
-    if (npend == 0) return;  // uniform across the four warps
-    named_bar_sync(1, 128);  // every atomic add of this CTA is issued
-    if (tid == 0) {
-        __threadfence();     // ... and performed before the counters move
-        for (int k = 0; k < npend; ++k) {
-            const unsigned old = atomicAdd(P.counters + pend[k].b_last, 1u);
-            c->flag[k] = (old == static_cast<unsigned>(pend[k].b_last - pend[k].b_first)) ? 1 : 0;
+    if (role == kOwner) {
+        // thread i waits for contributor owner_first + i (all at once)
+        if (tid == 0) c->owner_ok = 1;
+        named_bar_sync(kBarEpi, 128);
+        for (int cc = owner_first + tid; cc < b; cc += 128) {
+            const bool ok = alive && wait_flag(P.flags + cc, P.wait_ns);
+            if (ok) {
+                P.flags[cc] = 0u;  // consumed (no CTA of this launch sets it again)
+            } else {
+                c->owner_ok = 0;
+                if (alive) fail(c, P.err, kErrWaitFlag);
+            }
         }
-        __threadfence();     // the last contributor then sees every addition
+        named_bar_sync(kBarEpi, 128);
+        alive = alive && c->owner_ok;
+        if (alive) {
+            for (int cc = owner_first; cc < b; ++cc) {
+#pragma unroll
+                for (int g = 0; g < kGroups; ++g) {
+                    if (4 * g < M) {
+                        const int4 v = __ldcg(slot_ptr(P, cc, g, tid));
+                        acc[4 * g] += v.x;
+                        acc[4 * g + 1] += v.y;
+                        acc[4 * g + 2] += v.z;
+                        acc[4 * g + 3] += v.w;
+                    }
+                }
+            }
+        }
     }
-    named_bar_sync(1, 128);
-    const int last0 = c->flag[0], last1 = npend > 1 ? c->flag[1] : 0;
-    constexpr int kGroups = (kRows + 3) / 4;
-    float4 tot[2][kGroups];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const bool mine = k < npend && (k == 0 ? last0 : last1);
-        const int M = mine ? c->prob[pend[k].pi].M : 0;
-        const int b = mine ? pend[k].b_last : 0;
-#pragma unroll
-        for (int g = 0; g < kGroups; ++g)
-            tot[k][g] = (4 * g < M) ? __ldcg(acc_slot(P, b, g, tid)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        if (!(k < npend && (k == 0 ? last0 : last1))) continue;
-        const GemmProblem& pr = c->prob[pend[k].pi];
-        const int M = pr.M;
-        const int n = pend[k].rt * kTileN + tid;
-        const float* t = reinterpret_cast<const float*>(&tot[k][0]);
+    if (alive && n < pr.N) {
 #pragma unroll
         for (int m = 0; m < kRows; ++m)
-            if (alive && m < M && n < pr.N) store_out(pr, m, n, __float2int_rn(t[m]), c->asc[pend[k].pi - p0][m]);
-#pragma unroll
-        for (int g = 0; g < kGroups; ++g)
-            if (4 * g < M) *acc_slot(P, pend[k].b_last, g, tid) = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (tid == 0) P.counters[pend[k].b_last] = 0u;
+            if (m < M) store_out(pr, m, n, acc[m], c->asc[s.pi - p_lo][m]);
     }
-    named_bar_sync(1, 128);
 }
 
 // The preparation kernel's prefix sums at k tiles ka and kb: lane m < 16
@@ -613,9 +625,9 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int b = blockIdx.x;
-    const long long T = P.total_tiles;
-    const long long t_begin = range_start(b, T, P.nctas);
-    const int nloc = static_cast<int>(range_start(b + 1, T, P.nctas) - t_begin);
+    const long long t_begin = range_start(b, P.tiles_q, P.tiles_r);
+    const long long t_end = range_start(b + 1, P.tiles_q, P.tiles_r);
+    const int nloc = static_cast<int>(t_end - t_begin);
     const int nchunks = (nloc + kChunk - 1) / kChunk;
     const int np = P.n_problems;
 
@@ -629,18 +641,20 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         for (int z = tid; z < words; z += kGemmThreads) dst[z] = src[z];
     }
     const GemmProblem* pp = c->prob;
-    if (tid == 0) {
-        for (int q = 0; q < R; ++q) {
-            mbar_init(smem_u32(&c->wfull[q]), 1);
-            mbar_init(smem_u32(&c->bfull[q]), 1);
-            mbar_init(smem_u32(&c->empty[q]), kTC ? 1 : 4);
-        }
-        for (int a = 0; a < kATiles; ++a) mbar_init(smem_u32(&c->a_full[a]), 4);
-        for (int a = 0; a < kBatchBars; ++a) mbar_init(smem_u32(&c->mma_done[a]), 1);
-        mbar_init(smem_u32(&c->dfull[0]), 1);
-        mbar_init(smem_u32(&c->dfull[1]), 1);
-        c->failed = 0;
+    // the mbarriers, one per thread (consecutive 8-byte words)
+    static_assert(offsetof(Ctrl, slot_done) == offsetof(Ctrl, wfull) + 8 * (3 * kMaxRing + kATiles + kBatchBars + 2),
+                  "mbarriers not consecutive");
+    if (tid < 3 * kMaxRing + kATiles + kBatchBars + 3) {
+        uint32_t count = 1;                                                          // wfull, bfull, mma_done, dfull
+        if (tid >= 2 * kMaxRing && tid < 3 * kMaxRing) count = kTC ? 1 : 4;          // empty
+        else if (tid >= 3 * kMaxRing && tid < 3 * kMaxRing + kATiles) count = 4;     // a_full
+        else if (tid == 3 * kMaxRing + kATiles + kBatchBars + 2) count = 4;          // slot_done
+        mbar_init(smem_u32(&c->wfull[0]) + 8 * tid, count);
         fence_mbar_init();
+    }
+    if (tid == 0) {
+        c->failed = 0;
+        c->owner_ok = 0;
     }
     if constexpr (kTC) {
         if (warp == 0) {
@@ -654,42 +668,72 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     const uint32_t tmem = kTC ? c->tmem_base : 0u;
     pdl_launch_dependents();
     const int p0 = find_problem_by_tile(pp, np, t_begin);
-    const int p1 = find_problem_by_tile(pp, np, t_begin + nloc - 1);
+    const int p1 = find_problem_by_tile(pp, np, t_end - 1);
 
     const int npre = nchunks < R ? nchunks : R;
-    int w_issued = 0, b_issued = 0;  // chunks whose copies were requested (warp 4)
+    int w_issued[kMaxRing], b_issued[kMaxRing];  // warp 4: chunk index + 1 of the last requests per slot
+#pragma unroll
+    for (int q = 0; q < kMaxRing; ++q) w_issued[q] = b_issued[q] = 0;
 
     // -------------------------------------------------------- main loop --
     if (warp == 4) {
-        // The whole warp runs the producer loop; the elected lane issues.
+        // The whole warp runs the producer loop; the elected lane issues.  A
+        // CTA whose range ends inside a row tile also publishes that
+        // segment's partial sums (processed first) once the consumer warps
+        // have stored them: checked between refills, else waited for at the
+        // end.
         const uint32_t leader = elect_one();
+        Seg sl;
+        seg_ending_at(pp, np, t_begin, t_end, sl);
+        bool pending = seg_role(sl, pp[sl.pi]) == kContrib;
+        auto publish = [&]() {
+            if (leader && !c->failed) {
+                __threadfence();  // the slot's stores before the flag
+                *reinterpret_cast<volatile unsigned*>(P.flags + b) = 1u;
+            }
+            pending = false;
+        };
         // weights first: they do not depend on the kernels before this one
         const uint64_t pol = policy_evict_first();
-        for (int j = 0; j < npre; ++j)
-            issue_weights(pp, np, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk),
-                          Wr + static_cast<size_t>(j) * kChunk * kTileBytes, smem_u32(&c->wfull[j]), pol, leader);
-        w_issued = npre;
+        ProcIter itw, ita;  // processing order
+        itw.init(pp, np, t_begin, t_end);
+        ita = itw;
+        for (int j = 0; j < npre; ++j) {
+            const bool withheld = P.withhold == j && b == 0;  // test only: never requested
+            issue_weights(pp, np, t_begin, itw, min(kChunk, nloc - j * kChunk),
+                          Wr + static_cast<size_t>(j) * kChunk * kTileBytes, smem_u32(&c->wfull[j]), pol,
+                          withheld ? 0u : leader);
+            if (!withheld) w_issued[j] = j + 1;
+        }
         pdl_wait();  // the activation tiles are written by the preparation kernel
         const uint64_t pol_b = policy_evict_last();
-        for (int j = 0; j < npre; ++j)
-            issue_acts(pp, np, t_begin + static_cast<long long>(j) * kChunk, min(kChunk, nloc - j * kChunk), BT,
+        for (int j = 0; j < npre; ++j) {
+            issue_acts(pp, np, t_begin, ita, min(kChunk, nloc - j * kChunk), BT,
                        Br + static_cast<size_t>(j) * kChunk * BT, smem_u32(&c->bfull[j]), pol_b, leader);
-        b_issued = npre;
+            b_issued[j] = j + 1;
+        }
         // refill ring slots as they are released
         for (int j = npre; j < nchunks; ++j) {
             const int q = j % R;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->empty[q]), ((j / R) - 1) & 1))) {
+            if (pending && mbar_test_wait(smem_u32(&c->slot_done), 0)) publish();
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->empty[q]), ((j / R) - 1) & 1, P.wait_ns))) {
                 if (leader) fail(c, P.err, kErrWaitEmpty);
                 break;
             }
-            const long long first = t_begin + static_cast<long long>(j) * kChunk;
             const int cnt = min(kChunk, nloc - j * kChunk);
-            issue_weights(pp, np, first, cnt, Wr + static_cast<size_t>(q) * kChunk * kTileBytes,
+            issue_weights(pp, np, t_begin, itw, cnt, Wr + static_cast<size_t>(q) * kChunk * kTileBytes,
                           smem_u32(&c->wfull[q]), pol, leader);
-            w_issued = j + 1;
-            issue_acts(pp, np, first, cnt, BT, Br + static_cast<size_t>(q) * kChunk * BT, smem_u32(&c->bfull[q]),
-                       pol_b, leader);
-            b_issued = j + 1;
+            w_issued[q] = j + 1;
+            issue_acts(pp, np, t_begin, ita, cnt, BT, Br + static_cast<size_t>(q) * kChunk * BT,
+                       smem_u32(&c->bfull[q]), pol_b, leader);
+            b_issued[q] = j + 1;
+        }
+        if (pending) {
+            if (__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->slot_done), 0, P.wait_ns))) {
+                publish();
+            } else if (leader) {
+                fail(c, P.err, kErrWaitSlot);
+            }
         }
         __syncwarp();
     } else if (warp == 5) {
@@ -706,14 +750,16 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             constexpr uint32_t kIdesc = idesc_f16_f32(128, kBR);
             constexpr uint32_t kUnit = kBR * 16;      // bytes of one 16-k unit
             const uint32_t bbase = smem_u32(Br);
-            TileIter it;
-            it.init(pp, np, t_begin);
             RingPos rp;
             rp.reset();
             int nbatch = 0, seg = 0;
             bool ok = true;
+            long long cur_end = t_end;
             while (rp.i < nloc && ok) {
-                const int len = min(pp[it.pi].kt - it.kt, nloc - rp.i);
+                Seg s;
+                seg_ending_at(pp, np, t_begin, cur_end, s);
+                cur_end = s.t0;
+                const int len = s.kb - s.ka;
                 const uint32_t dcol = tmem + kAccCol + (seg & 1) * 32;
                 for (int e = 0; e < len && ok;) {
                     const int nb = min(kMmaBatch, len - e);
@@ -728,13 +774,13 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
                     for (int t = 0; t < kMmaBatch; ++t)
                         if (ok && t < nb && r[t].cp == 0)
-                            ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[r[t].q]), r[t].qph));
+                            ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[r[t].q]), r[t].qph, P.wait_ns));
                     if (!ok) {
                         if (leader) fail(c, P.err, kErrWaitB);
                         break;
                     }
                     const RingPos& rl = r[nb - 1];
-                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->a_full[rl.ab]), rl.abph));
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->a_full[rl.ab]), rl.abph, P.wait_ns));
                     if (!ok) {
                         if (leader) fail(c, P.err, kErrWaitAFull);
                         break;
@@ -765,12 +811,6 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 if (!ok) break;
                 mma_commit_if(leader, smem_u32(&c->dfull[seg & 1]));
                 ++seg;
-                // next segment: k tile 0 of the next row tile
-                it.kt = 0;
-                if (++it.rt == pp[it.pi].nt) {
-                    it.rt = 0;
-                    ++it.pi;
-                }
             }
         }
         __syncwarp();
@@ -778,23 +818,14 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         // warps 0-3: one output row per thread, segment by segment.  A failed
         // (timed-out) wait only clears `alive`; every named barrier is still
         // executed by all four warps.
-        TileIter it;
-        it.init(pp, np, t_begin);
-        // Only a range's first and last segments can be split row tiles.  The
-        // CTAs holding their first and last k tiles take 64-bit divisions, so
-        // they are worked out here, while the preparation kernel still runs.
-        int own_f0, own_l0, own_f1, own_l1;
+        // The owner segment (processed last) needs its row tile's first CTA:
+        // worked out while the preparation kernel still runs.
+        int owner_first = b;
         {
-            const GemmProblem& pa = pp[it.pi];
-            const long long fa = pa.tile_begin + static_cast<long long>(it.rt) * pa.kt;
-            own_f0 = range_owner(fa, T, P.nctas);
-            own_l0 = range_owner(fa + pa.kt - 1, T, P.nctas);
-            TileIter z;
-            z.init(pp, np, t_begin + nloc - 1);
-            const GemmProblem& pz = pp[z.pi];
-            const long long fz = pz.tile_begin + static_cast<long long>(z.rt) * pz.kt;
-            own_f1 = range_owner(fz, T, P.nctas);
-            own_l1 = range_owner(fz + pz.kt - 1, T, P.nctas);
+            Seg s0;
+            seg_ending_at(pp, np, t_begin, t_begin + 1, s0);
+            const GemmProblem& pa = pp[s0.pi];
+            owner_first = range_owner(static_cast<int>(pa.tile_begin) + s0.rt * pa.kt, P.tiles_q, P.tiles_r);
         }
         pdl_wait();  // outputs and workspace: the preparation kernel has finished
         // dequant scales of problems p0..p1 (at most 8 x 16: one per thread),
@@ -805,8 +836,6 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             const GemmProblem& pr = pp[p0 + tid / 16];
             if (tid % 16 < pr.M) asc_reg = __ldcg(pr.asc + tid % 16);
         }
-        Pending pend[2];
-        int npend = 0;
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         bool alive = true;
         int seg_idx = 0;
@@ -824,18 +853,20 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         // of the next segment are written (the accumulator is double-buffered),
         // so the MMA pipeline does not drain at row-tile boundaries.
         bool dv = false;
-        int d_pi = 0, d_rt = 0, d_ka = 0, d_kb = 0, d_seg = 0;
-        int d_rq[16];
+        Seg ds;
+        ds.pi = ds.rt = ds.ka = ds.kb = 0;
+        ds.t0 = 0;
+        int d_seg = 0;
+        int d_rq[kOutRows];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) d_rq[m] = 0;
-        auto epilogue = [&](int e_pi, int e_rt, int e_ka, int e_kb, int e_seg, const int (&acc)[16]) {
+        for (int m = 0; m < kOutRows; ++m) d_rq[m] = 0;
+        auto epilogue = [&](const Seg& es, int (&acc)[16]) {
             if (first_epi) {  // publish the dequant scales once
                 if (asc_mine) c->asc[tid / 16][tid % 16] = asc_reg;
-                named_bar_sync(1, 128);
+                named_bar_sync(kBarEpi, 128);
                 first_epi = false;
             }
-            segment_epilogue<kOutRows>(P, c, p0, e_pi, e_rt, e_ka, e_kb, e_seg == 0 ? own_f0 : own_f1,
-                             e_seg == 0 ? own_l0 : own_l1, acc, tid, alive, pend, npend);
+            segment_epilogue<kOutRows>(P, c, p0, es, owner_first, acc, tid, alive);
         };
         auto finish_deferred = [&]() {
             int acc[16];
@@ -843,7 +874,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             for (int m = 0; m < 16; ++m) acc[m] = 0;
             if constexpr (kTC) {
                 if (alive) {
-                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->dfull[d_seg & 1]), (d_seg >> 1) & 1));
+                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->dfull[d_seg & 1]), (d_seg >> 1) & 1, P.wait_ns));
                     if (!alive && lane == 0) fail(c, P.err, kErrWaitD);
                 }
                 if (alive) {
@@ -863,13 +894,17 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                     }
                 }
             }
-            epilogue(d_pi, d_rt, d_ka, d_kb, d_seg, acc);
+            epilogue(ds, acc);
             dv = false;
         };
+        long long cur_end = t_end;
         while (rp.i < nloc) {
-            const GemmProblem& pr = pp[it.pi];
-            const int ka = it.kt;
-            const int len = min(pr.kt - ka, nloc - rp.i);
+            Seg sg;
+            seg_ending_at(pp, np, t_begin, cur_end, sg);
+            cur_end = sg.t0;
+            const GemmProblem& pr = pp[sg.pi];
+            const int ka = sg.ka;
+            const int len = sg.kb - sg.ka;
             const int rsl = load_code_sum_lane(pr, ka, ka + len, lane);
             int dacc[4][DPR];
 #pragma unroll
@@ -882,11 +917,11 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 }
                 const int s = rp.slot();
                 if (alive && rp.cp == 0) {
-                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[rp.q]), rp.qph));
+                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[rp.q]), rp.qph, P.wait_ns));
                     if (!alive && lane == 0) fail(c, P.err, kErrWaitW);
                     if constexpr (!kTC) {
                         if (alive) {
-                            alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[rp.q]), rp.qph));
+                            alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[rp.q]), rp.qph, P.wait_ns));
                             if (!alive && lane == 0) fail(c, P.err, kErrWaitB);
                         }
                     }
@@ -900,7 +935,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                     hist[kATiles - 1] = nbatch + e / kMmaBatch;
                     if (alive && rp.i >= kATiles) {
                         alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->mma_done[prev % kBatchBars]),
-                                                                          (prev / kBatchBars) & 1));
+                                                                          (prev / kBatchBars) & 1, P.wait_ns));
                         if (!alive && lane == 0) fail(c, P.err, kErrWaitAEmpty);
                         tc_fence_after();
                     }
@@ -950,10 +985,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             }
             if constexpr (kTC) {
                 if (dv) finish_deferred();  // the previous segment, if this one was short
-                d_pi = it.pi;
-                d_rt = it.rt;
-                d_ka = ka;
-                d_kb = ka + len;
+                ds = sg;
                 d_seg = seg_idx;
 #pragma unroll
                 for (int m = 0; m < kOutRows; ++m) d_rq[m] = code_sum(rsl, m);
@@ -965,19 +997,12 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
                 for (int m = 0; m < DPR; ++m)
                     acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) - code_sum(rsl, m);
-                epilogue(it.pi, it.rt, ka, ka + len, seg_idx, acc);
+                epilogue(sg, acc);
             }
             ++seg_idx;
             nbatch += (len + kMmaBatch - 1) / kMmaBatch;
-            // next segment: k tile 0 of the next row tile
-            it.kt = 0;
-            if (++it.rt == pr.nt) {
-                it.rt = 0;
-                ++it.pi;
-            }
         }
         if (dv) finish_deferred();
-        finish_pending<kOutRows>(P, c, p0, pend, npend, tid, alive);
     }
 
     // ------------------------------------------------------- tear-down --
@@ -986,10 +1011,10 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         // never release shared memory with a bulk copy still in flight: wait
         // (bounded) for the last requested phase of every slot
         for (int q = 0; q < R; ++q) {
-            if (q < w_issued)
-                (void)mbar_wait_bounded(smem_u32(&c->wfull[q]), ((w_issued - 1 - q) / R) & 1, 100000000ull);
-            if (q < b_issued)
-                (void)mbar_wait_bounded(smem_u32(&c->bfull[q]), ((b_issued - 1 - q) / R) & 1, 100000000ull);
+            if (w_issued[q] > 0)
+                (void)mbar_wait_bounded(smem_u32(&c->wfull[q]), ((w_issued[q] - 1) / R) & 1, 100000000ull);
+            if (b_issued[q] > 0)
+                (void)mbar_wait_bounded(smem_u32(&c->bfull[q]), ((b_issued[q] - 1) / R) & 1, 100000000ull);
         }
     }
     if constexpr (kTC) {
@@ -1012,15 +1037,18 @@ cudaLaunchAttribute pdl_attr() {
 template <int PATH, int DPR>
 cudaError_t launch_one(const GemmParams& prm, bool pdl, cudaStream_t stream) {
     auto kern = &w2a8_streamk_kernel<PATH, DPR>;
-    static bool configured[64] = {};
+    // the opt-in shared-memory size, once per device (first-use races only
+    // repeat the same call)
+    static std::atomic<unsigned long long> configured{0ull};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !configured[dev]) {
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (dev >= 64 || !(configured.load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(gemm_smem_bytes(PATH, DPR, kMaxRing)));
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        if (dev < 64) configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     cudaLaunchAttribute attr[1] = {pdl_attr()};
 

@@ -16,9 +16,9 @@ constexpr int kCtasPerSm = 2;     // persistent CTAs per SM
 // Compute paths.  The activation operand ("B tile", one per k tile) is laid
 // out for the path that consumes it.
 enum ComputePath : int {
-    kPathTC16 = 0,  // tcgen05, block width 9..16: B = 16 rows fp16, 4096 B
-    kPathTC8 = 1,   // tcgen05, block width 3..8:  B = 8 rows fp16, 2048 B
-    kPathDP = 2,    // dp4a, block width 1..4:     B = dp_rows rows int8, 128 B per row
+    kPathTC16 = 0,  // tcgen05, block width 9..16: B = 32 operand rows (h and l of 16 rows), 4096 B
+    kPathTC8 = 1,   // tcgen05, block width 5..8:  B = 16 operand rows, 2048 B
+    kPathDP = 2,    // dp4a, block width 1..4:     B = dp_rows rows of int8 codes, 128 B per row
 };
 
 struct GemmProblem {
@@ -33,6 +33,7 @@ struct GemmProblem {
     int nt, kt;               // row tiles, k tiles
     int act_kind;             // BITMTP_F32 / BITMTP_BF16 / BITMTP_Q8
     int out_dtype;            // BITMTP_F32 / BITMTP_BF16
+    int vec_ok;               // activation rows 16-byte aligned (base and row stride)
     long long tile_begin;     // first flattened (row tile, k tile) index of this problem
     // Activation operand in the workspace, written by the preparation kernel:
     uint8_t* actb;            // [kt] tiles in the compute path's layout
@@ -45,25 +46,31 @@ struct GemmParams {
     int n_problems;
     int stages;               // chunks in the shared-memory ring
     int nctas;
+    int withhold;             // test only: ring chunk CTA 0 never requests (-1: none)
+    int tiles_q, tiles_r;     // stream-K split: CTA b gets tiles_q tiles, plus one if b < tiles_r
     long long total_tiles;
-    unsigned* counters;       // [kMaxCtas] split-row-tile arrival counters (left at zero)
-    int* slots;               // [kMaxCtas][4][128][4] split-row-tile accumulators, fp32 (left at zero)
+    unsigned long long wait_ns;  // bound on every wait of the launch
+    unsigned* flags;          // [kMaxCtas] partial-sum-ready flags (left at zero)
+    int* slots;               // [kMaxCtas][4][128][4] int32 partial sums of split row tiles
     int* err;                 // device error word
 };
 
 constexpr int kMaxCtas = 320;         // persistent CTAs per launch (>= 2 per SM on GB300)
 constexpr int kMinTilesPerCta = 4;    // fewer CTAs on small problems: fewer split row tiles
 
-// Workspace: split-row-tile counters and accumulators at fixed offsets (both
-// must be zero when a launch starts; every launch leaves them at zero), then
-// one activation region per problem (sized by its k tiles).
+// Workspace: partial-sum-ready flags (must be zero when a launch starts; every
+// launch leaves them at zero), one partial-sum slot per CTA, then one
+// activation region per problem (sized by its k tiles).
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-constexpr size_t kWsCounters = 256;
-constexpr size_t kWsSlots = kWsCounters + align256(static_cast<size_t>(kMaxCtas) * 4);
+constexpr size_t kWsFlags = 256;
+constexpr size_t kWsSlots = kWsFlags + align256(static_cast<size_t>(kMaxCtas) * 4);
 constexpr size_t kWsAct = kWsSlots + static_cast<size_t>(kMaxCtas) * 16 * kTileN * 4;
 constexpr size_t act_tiles_bytes(int kt) { return align256(static_cast<size_t>(kt) * 4096); }
 constexpr size_t act_rsp_bytes(int kt) { return align256(static_cast<size_t>(16) * (kt + 1) * 4); }
 constexpr size_t act_region_bytes(int kt) { return act_tiles_bytes(kt) + act_rsp_bytes(kt) + 256; }
+
+constexpr unsigned long long kWaitNs = 2000000000ull;      // 2 s: every wait of a normal launch
+constexpr unsigned long long kTestWaitNs = 1000000ull;     // 1 ms: launches with BITMTP_FLAG_TEST_WITHHOLD
 
 size_t gemm_smem_bytes(int path, int dp_rows, int stages);
 int gemm_stages(int path, int dp_rows);

@@ -1,6 +1,6 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a used by the W2A8 kernels:
-// mbarriers, bulk (TMA) copies, thread-block-cluster shared memory, programmatic
-// dependent launch and the tcgen05 tensor-memory / MMA instructions.
+// mbarriers, bulk (TMA) copies, programmatic dependent launch and the tcgen05
+// tensor-memory / MMA instructions.
 #pragma once
 #include <cstdint>
 
@@ -13,7 +13,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // ---------------------------------------------------------------- timers --
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t) :: "memory");
     return t;
 }
 
@@ -33,10 +33,6 @@ __device__ __forceinline__ void mbar_arrive_if(uint32_t on, uint32_t bar) {
                  "@g mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
                  :: "r"(bar), "r"(on) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
-                 :: "r"(bar), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void mbar_arrive_expect_tx_if(uint32_t on, uint32_t bar, uint32_t bytes) {
     asm volatile("{\n\t.reg .b64 st;\n\t.reg .pred g;\n\tsetp.ne.b32 g, %2, 0;\n\t"
                  "@g mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
@@ -50,29 +46,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
                  : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
 // Bounded wait on an mbarrier phase.  Gives up after `limit_ns` of wall time
 // and returns false (the caller records an error and skips its work).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
+        if (it == 0) {
+            t0 = global_ns();
+        } else if ((it & 255u) == 0 && global_ns() - t0 > limit_ns) {
+            return false;
+        }
     }
 }
 
 // ----------------------------------------------------------- bulk copies --
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar` with
-// the byte count (cp.async.bulk, TMA engine).  16-byte aligned addresses and a
-// size that is a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar, uint64_t policy) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-                 " [%0], [%1], %2, [%3], %4;"
-                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
-}
-// The same, issued only where `on` is non-zero (guard predicate).
+// the byte count (cp.async.bulk, TMA engine), issued only where `on` is
+// non-zero (guard predicate).  16-byte aligned addresses and a size that is a
+// multiple of 16.
 __device__ __forceinline__ void bulk_g2s_if(uint32_t on, uint32_t dst, const void* src, uint32_t bytes,
                                             uint32_t bar, uint64_t policy) {
     asm volatile("{\n\t.reg .pred g;\n\tsetp.ne.b32 g, %5, 0;\n\t"
@@ -91,56 +92,21 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
-// Generic-proxy shared-memory writes -> visible to the async proxy (tensor core).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 // Generic-proxy global writes <-> async-proxy (bulk copy) reads of the same memory.
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ------------------------------------------------------ global / barriers --
+// Load with acquire order at GPU scope (another CTA's release store).
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-// Four fp32 additions to 16 consecutive, 16-byte aligned bytes of global
-// memory as one reduction (no value returned, so nothing waits for it).
-__device__ __forceinline__ void red_add_v4(float4* p, float4 v) {
-    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-                 :: "l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
-}
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
-}
-
-// --------------------------------------------------------------- cluster --
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
-    int v;
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
 }
 
 // ------------------------------------------- programmatic dependent launch --
@@ -201,25 +167,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr) : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]; kind::f16 (fp16 inputs, fp32 accumulate),
-// one CTA.  Issued by a single thread.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
-}
 // D[tmem] (+)= A[tmem] * B[smem]; kind::f8f6f4 (8-bit float inputs, fp32
-// accumulate, K = 32 per instruction), one CTA.  Issued by a single thread.
-__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
-                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
-}
-// The same, issued only where `on` is non-zero (a guard predicate, no branch).
+// accumulate, K = 32 per instruction), one CTA, issued only where `on` is
+// non-zero (a guard predicate, no branch).
 __device__ __forceinline__ void mma_f8_ts_if(uint32_t on, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate) {
     asm volatile("{\n\t.reg .pred p, g;\n\t"
@@ -244,12 +194,6 @@ __device__ __forceinline__ void mma_commit_if(uint32_t on, uint32_t bar) {
                  "@g tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
                  :: "r"(bar), "r"(on) : "memory");
 }
-// Arrive on an mbarrier once all previously issued tcgen05.mma of this thread complete.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 :: "r"(bar) : "memory");
-}
-
 // Shared-memory matrix descriptor, no swizzle, K-major canonical layout:
 // core matrices of 8 rows x 16 bytes; lbo = byte stride between core matrices
 // along K, sbo = byte stride between 8-row groups.

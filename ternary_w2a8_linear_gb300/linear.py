@@ -25,7 +25,7 @@ OK = 0
 ERR_INVALID, ERR_ALIGN, ERR_SHAPE, ERR_NOT_TERNARY, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE, ERR_NOT_FINITE = \
     range(-1, -9, -1)
 F32, BF16, Q8 = 0, 1, 2
-FLAG_PDL, FLAG_FORCE_TC, FLAG_FORCE_DP = 0x1, 0x2, 0x4
+FLAG_PDL, FLAG_FORCE_TC, FLAG_FORCE_DP, FLAG_TEST_WITHHOLD = 0x1, 0x2, 0x4, 0x100
 MAX_M, MAX_K, MAX_N, MAX_GROUP = 16, 32768, 16777216, 8
 NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 

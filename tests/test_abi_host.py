@@ -153,16 +153,18 @@ def test_grouped_validation(lib):
 def test_workspace_bytes(lib):
     wb = L.bitmtp_linear_workspace_bytes
     assert wb(0, 64, 4) == 0 and wb(64, 0, 4) == 0 and wb(64, 64, 0) == 0 and wb(64, 64, 17) == 0
-    small, big = wb(128, 128, 1), wb(32000, 2560, 16)
-    # split-row-tile slots and counters for the largest grid, plus one
-    # activation region (4 KiB per k tile, prefix sums, scales) per problem
-    assert small >= 320 * 16 * 128 * 4
-    assert big - small == 19 * 4096 + (16 * 21 * 4 + 255) // 256 * 256 - 256
-    assert wb(32000, 2560, 1) == big == wb(5, 2560, 16)   # depends on K only
+    a256 = lambda x: -(-x // 256) * 256
+    # a 256-byte header, one ready flag and one partial-sum slot (16 rows x 128
+    # columns of int32) per CTA of the largest grid, then one activation region
+    # per problem: 4 KiB per k tile, prefix sums of 16 rows, 16 scales
+    fixed = 256 + a256(320 * 4) + 320 * 16 * 128 * 4
+    region = lambda kt: a256(kt * 4096) + a256(16 * (kt + 1) * 4) + 256
+    assert wb(128, 128, 1) == fixed + region(1)
+    assert wb(32000, 2560, 16) == fixed + region(20)
+    assert wb(32000, 2560, 1) == wb(5, 2560, 16)   # depends on K only
     d = [L.GemmDesc(FAKE, 0.02, 2560, 2560, 8, _act(ldx=2560), _out(ldy=2560)),
-         L.GemmDesc(FAKE, 0.02, 640, 2560, 8, _act(ldx=2560), _out(ldy=640))]
-    one = wb(2560, 2560, 8)
-    assert L.bitmtp_linear_workspace_bytes_grouped(d) == 2 * one - (small - (4096 + 256 + 256))
+         L.GemmDesc(FAKE, 0.02, 640, 6912, 8, _act(ldx=6912), _out(ldy=640))]
+    assert L.bitmtp_linear_workspace_bytes_grouped(d) == fixed + region(20) + region(54)
     bad = [L.GemmDesc(FAKE, 0.02, 2560, 2560, 20, _act(ldx=2560), _out(ldy=2560))]
     assert L.bitmtp_linear_workspace_bytes_grouped(bad) == 0
 
