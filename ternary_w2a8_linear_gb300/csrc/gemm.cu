@@ -115,6 +115,7 @@ struct Ctrl {
     uint64_t mma_done[kBatchBars]; // MMA batch b complete: barrier b % kBatchBars
     uint64_t dfull[2];            // accumulator of segment s (D buffer s & 1) complete
     uint64_t slot_done;           // contributor partial sums stored (four consumer warps)
+    uint64_t drained;             // after a failed wait: every MMA this CTA issued is complete
     uint32_t tmem_base;
     int failed;
     int owner_ok;
@@ -644,7 +645,8 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     // the mbarriers, one per thread (consecutive 8-byte words)
     static_assert(offsetof(Ctrl, slot_done) == offsetof(Ctrl, wfull) + 8 * (3 * kMaxRing + kATiles + kBatchBars + 2),
                   "mbarriers not consecutive");
-    if (tid < 3 * kMaxRing + kATiles + kBatchBars + 3) {
+    static_assert(offsetof(Ctrl, drained) == offsetof(Ctrl, slot_done) + 8, "mbarriers not consecutive");
+    if (tid < 3 * kMaxRing + kATiles + kBatchBars + 4) {
         uint32_t count = 1;                                                          // wfull, bfull, mma_done, dfull
         if (tid >= 2 * kMaxRing && tid < 3 * kMaxRing) count = kTC ? 1 : 4;          // empty
         else if (tid >= 3 * kMaxRing && tid < 3 * kMaxRing + kATiles) count = 4;     // a_full
@@ -811,6 +813,12 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 if (!ok) break;
                 mma_commit_if(leader, smem_u32(&c->dfull[seg & 1]));
                 ++seg;
+            }
+            if (!ok) {
+                // tensor memory is freed at exit: first let every MMA this
+                // warp issued complete (bounded)
+                mma_commit_if(leader, smem_u32(&c->drained));
+                (void)mbar_wait_bounded(smem_u32(&c->drained), 0, 100000000ull);
             }
         }
         __syncwarp();

@@ -118,7 +118,35 @@ def test_noalloc_alternating_shapes():
         _assert_same(c, got, ref)
 
 
+def test_noalloc_pdl_side_stream_mixed_shapes():
+    """Back-to-back calls of mixed shapes with programmatic dependent launch on
+    a side stream (each call's weight prefetch overlaps the previous call)
+    share the array; each matches the workspace entry point bit for bit."""
+    probs = [(CASES[i], *_setup(CASES[i], 970 + i)) for i in (0, 1, 2, 3, 0, 2)]
+    refs = [_run_existing(c, pk, w, xd) for c, pk, w, xd in probs]
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    outs = []
+    with torch.cuda.stream(side):
+        for c, pk, w, xd in probs:
+            N, K, M = c[:3]
+            y, acc = _outputs(c)
+            st = L.bitmtp_linear_gemm_noalloc(L._ptr(pk), w, N, K, M, L.make_act(xd), L.make_out(y, acc),
+                                              L.FLAG_PDL, L._stream(side))
+            assert st == L.OK, L.status_string(st)
+            outs.append((y, acc))
+    side.synchronize()
+    for (c, *_), (y, acc), (y_ref, acc_ref) in zip(probs, outs, refs):
+        if acc is not None:
+            assert torch.equal(acc, acc_ref)
+        assert torch.equal(y, y_ref)
+    assert L.bitmtp_linear_device_error(side) == 0
+
+
 def test_noalloc_rejects_beyond_limits():
+    """The shape check: a width beyond BITMTP_MAX_M is rejected before anything
+    is enqueued.  (Every shape inside the library's limits fits the array, so
+    its size check cannot be reached through valid shapes.)"""
     case = CASES[0]
     pk, w, xd = _setup(case, 990)
     y, acc = _outputs(case)
