@@ -1,32 +1,48 @@
 """Benchmark of the W2A8 ternary linear on GB300.
 
-Default workload (one "step"): the BitNet-2B-shaped layer set -- projections
-q 2560->2560, k/v 2560->640, o 2560->2560, gate/up 2560->6912, down 6912->2560,
-ternary weights with P(0)=0.5, bf16 activations with 1% outliers x20 -- at
-block widths M = 1, 2, 4, 8.  One step runs, for each width, the seven
-projections: by default as one grouped call per width, otherwise one call per
-projection.  A call is two launches: the activation preparation (absmax
-quantisation of the raw bf16 rows into the operand tiles) and the GEMM (2-bit
-weight stream, exact integer product, dequant to bf16), which starts
-streaming weights while the first runs.  Weights rotate over enough distinct
-copies that no step finds its weights in L2.  Steps are replayed from CUDA
-graphs with programmatic dependent launch between consecutive launches.
-
 Metric: achieved HBM GB/s on algorithmic bytes (packed weights + activations),
-also as a fraction of the measured copy bandwidth, plus rows/s per width.
+as a fraction of the measured copy bandwidth, and rows/s, at block widths
+1-16, for the five synthetic workloads:
 
-The line also carries ``ternarize_pack``: the offline step before the path,
-device absmean ternarisation + pack of the layer set's seven projections from
-fp32 weights, in GB/s of algorithmic bytes (fp32 weights once + packed tiles),
-outside the timed steps (``--no-ternarize`` skips it).
+  1  a single 2560 -> 2560 linear, fp32 in and out, widths 1 and 4: one call
+     alone, and 128 calls back to back over distinct weights;
+  2  the BitNet-2B-shaped layer set (q/k/v/o 2560 -> 2560/640/640/2560,
+     gate/up 2560 -> 6912, down 6912 -> 2560; P(0) = 0.5; bf16 activations
+     with 1% outliers x20), every width 1-16, the seven projections as one
+     grouped call or as seven calls;
+  3  the 30-layer stack of that layer set at width 4 (0.521 GB packed): one
+     step is the 30 layers, one grouped call each (and one call per
+     projection);
+  4  the 36-layer stack of hidden 4096 / FFN 11008 (k/v 4096 -> 1024;
+     P(0) = 1/3; bf16 N(0, 1); 1.595 GB packed) at widths 8, 12 and 16 --
+     the headline: one step is the stack at the three widths, one grouped
+     call per layer;
+  5  the role-dependent grouped call at width 16 (rows 0-3 through a
+     2560 -> 32000 projection, rows 4-15 through a 2560 -> 2560 one, P(0)
+     0.2 / 0.5 / 0.8, activations quantised to int8 first).
 
-``--impl reference`` times the CPU oracle on a bounded sample of the same
-workload (its only use of the oracle besides the cpu_baseline field).
+A call is two launches: the activation preparation (absmax quantisation of
+the raw rows into the operand tiles) and the GEMM (2-bit weight stream, exact
+integer product, dequant), which starts streaming weights while the first
+runs.  Calls are replayed from CUDA graphs with programmatic dependent launch
+between consecutive launches; no step finds its weights in L2 (the stacks
+are larger than L2, the small workloads rotate over distinct weight copies).
+
+The line also carries ``e2e`` (the headline step through the C ABI with its
+activations copied from pinned host memory and its outputs read back every
+step), ``ternarize_pack`` (the offline step before the path: device absmean
+ternarisation + pack of the layer set from fp32 weights) and
+``cpu_baseline``: the CPU oracle on one host core and on every host core,
+timed on bounded samples of each workload, which also checks a sample of the
+headline step's outputs against the oracle.  ``--impl reference`` times the
+oracle alone on the headline workload.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
+import multiprocessing as mp
 import os
 import statistics
 import subprocess
@@ -42,47 +58,50 @@ if ROOT not in sys.path:
 
 from ternary_w2a8_linear_gb300 import inputs  # noqa: E402
 
-WIDTHS = (1, 2, 4, 8)
-# DRAM bytes (read + write) of one step's GEMM launches, summed over the four
-# widths, from the ncu capture summarised in profiles/; None while the kernel
-# differs from the one captured.
-STEP_DRAM_TRAFFIC = 17_799_936 + 17_818_624 + 17_869_312 + 18_531_328  # widths 1, 2, 4, 8
-FALLBACK_HBM_GBS = 6800.0
 METRIC = "W2A8 linear achieved HBM GB/s (% of roofline) and rows/s at widths 1-16"
+HEADLINE_WIDTHS = (8, 12, 16)
+FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes (read + write) of one headline step from an ncu capture, keyed by
+# the hash of the library sources it was taken with; reported only while the
+# sources are unchanged.
+CAPTURED_TRAFFIC: dict[str, int] = {}
+KERNEL_SOURCES = ("ternary_w2a8_linear_gb300/csrc/gemm.cu", "ternary_w2a8_linear_gb300/csrc/api.cu",
+                  "ternary_w2a8_linear_gb300/csrc/internal.h", "ternary_w2a8_linear_gb300/csrc/ptx.cuh",
+                  "ternary_w2a8_linear_gb300/csrc/quant.cuh", "include/bitmtp_linear.h")
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--steps", type=int, default=40)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--copies", type=int, default=16, help="distinct weight copies rotated per step")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--no-per-width", action="store_true")
+    p.add_argument("--no-per-config", action="store_true")
     p.add_argument("--no-ternarize", action="store_true",
                    help="skip the device ternarisation + pack figure (the offline step before the path)")
-    p.add_argument("--cpu-seconds", type=float, default=12.0)
-    p.add_argument("--e2e-steps", type=int, default=1000)
-    p.add_argument("--mode", choices=["grouped", "chained"], default="grouped",
-                   help="grouped: each width's seven projections in one launch; chained: one launch each")
-    return p.parse_args()
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--e2e-steps", type=int, default=10)
+    return p.parse_args(argv)
 
 
 # --------------------------------------------------------------------------
-def algorithmic_bytes(K, N, M, x_bytes=2):
-    """Packed weight bytes (tiles) + activation bytes of one linear."""
-    pk = -(-N // 128) * -(-K // 128) * 4096
-    return pk + M * K * x_bytes
+def packed_tile_bytes(N, K):
+    return -(-N // 128) * -(-K // 128) * 4096
 
 
-def step_bytes():
-    tot = 0
-    for M in WIDTHS:
-        for _, K, N in inputs.BITNET2B_PROJ:
-            tot += algorithmic_bytes(K, N, M)
-    return tot
+def call_bytes(K, N, M, x_bytes=2):
+    """Algorithmic bytes of one linear: packed weight tiles + activations."""
+    return packed_tile_bytes(N, K) + M * K * x_bytes
+
+
+def layer_set_bytes(proj, M, x_bytes=2):
+    return sum(call_bytes(K, N, M, x_bytes) for _, K, N in proj)
+
+
+def headline_step_bytes():
+    return sum(inputs.LARGE_LAYERS * layer_set_bytes(inputs.LARGE_PROJ, M) for M in HEADLINE_WIDTHS)
 
 
 def ternarize_bytes():
@@ -90,8 +109,16 @@ def ternarize_bytes():
     weights read once plus the packed tiles (and 16-byte trailers) written."""
     tot = 0
     for _, K, N in inputs.BITNET2B_PROJ:
-        tot += 4 * N * K + -(-N // 128) * -(-K // 128) * 4096 + 16
+        tot += 4 * N * K + packed_tile_bytes(N, K) + 16
     return tot
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_peaks():
@@ -160,6 +187,110 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------
+class Stack:
+    """Packed weights, activations and outputs of `nlayers` layer sets on the
+    device, with one grouped-call descriptor array per (layer, width).  Layer
+    0 is drawn with the numpy generators (the layer the oracle checks), the
+    others with the device generators."""
+
+    def __init__(self, L, torch, dev, proj, nlayers, numpy_layer0, device_seed, p_zero, outliers,
+                 out_dtype="bf16"):
+        self.L, self.proj, self.nlayers = L, proj, nlayers
+        self.pk, self.w, self.x, self.y = [], [], [], []
+        self.host = {}  # layer 0: (T, w, x bits) per projection, for the oracle
+        for layer in range(nlayers):
+            pks, ws, xs, ys = [], [], [], []
+            for p, (_, K, N) in enumerate(proj):
+                if layer == 0:
+                    T, w, xb = numpy_layer0(p)
+                    self.host[p] = (T, w, xb)
+                    Td = torch.from_numpy(T).to(dev)
+                    x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+                else:
+                    seed = device_seed + 10 * layer + p
+                    Td = inputs.device_ternary(seed, (N, K), p_zero, dev)
+                    w = float(np.random.default_rng(seed + 500_000).uniform(0.01, 0.05))
+                    x = inputs.device_normal_bf16(seed + 1_000_000, (inputs.MAX_ROWS, K), dev,
+                                                  0.01 if outliers else 0.0)
+                pks.append(L.pack(Td))
+                del Td
+                ws.append(float(w))
+                xs.append(x)
+                ys.append(torch.empty((inputs.MAX_ROWS, N), dtype=torch.bfloat16, device=dev))
+            self.pk.append(pks)
+            self.w.append(ws)
+            self.x.append(xs)
+            self.y.append(ys)
+        self.descs = {}
+        ws_need = 0
+        for layer in range(nlayers):
+            for M in range(1, inputs.MAX_ROWS + 1):
+                d = [L.GemmDesc(self.pk[layer][p].data_ptr(), self.w[layer][p], N, K, M,
+                                L.Act(L.BF16, self.x[layer][p].data_ptr(), K, None),
+                                L.Out(L.BF16, self.y[layer][p].data_ptr(), N, None, 0))
+                     for p, (_, K, N) in enumerate(proj)]
+                self.descs[(layer, M)] = ((L.GemmDesc * len(d))(*d), d)
+        for M in (inputs.MAX_ROWS,):
+            ws_need = max(ws_need, L.bitmtp_linear_workspace_bytes_grouped(self.descs[(0, M)][1]))
+        self.ws = torch.zeros(ws_need, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+    def grouped(self, layer, M, stream, flags):
+        arr, d = self.descs[(layer, M)]
+        lib = self.L.load()
+        st = lib.bitmtp_linear_gemm_grouped(arr, len(d), self.L.ctypes.c_void_p(self.ws.data_ptr()),
+                                            self.ws.numel(), flags, stream)
+        if st != self.L.OK:
+            raise self.L.BitmtpError(st, "gemm_grouped")
+        return 2
+
+    def chained(self, layer, M, stream, flags):
+        _, d = self.descs[(layer, M)]
+        lib = self.L.load()
+        n = 0
+        for x in d:
+            st = lib.bitmtp_linear_gemm(self.L.ctypes.c_void_p(x.pk), x.w_scale, x.N, x.K, x.M,
+                                        self.L.ctypes.byref(x.act), self.L.ctypes.byref(x.out),
+                                        self.L.ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(), flags, stream)
+            if st != self.L.OK:
+                raise self.L.BitmtpError(st, "gemm")
+            n += 2
+        return n
+
+
+def graph_of(torch, stream, enqueue):
+    """Capture enqueue() into a CUDA graph (after one warm call outside it)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        enqueue()
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            launches = enqueue()
+    return g, launches
+
+
+def time_graph(torch, stream, g, reps, warm=2):
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            g.replay()
+        stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / 1e3 / reps  # seconds per replay
+
+
+def entry(byt, sec, rows, peak):
+    gbs = byt / sec / 1e9
+    return {"us": round(sec * 1e6, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "rows_per_s": round(rows / sec, 1), "bytes": byt}
+
+
+# --------------------------------------------------------------------------
 def run_ours(args, rank, world):
     import torch
     import ternary_w2a8_linear_gb300.linear as L
@@ -171,91 +302,26 @@ def run_ours(args, rank, world):
     L.load()
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
-    R = max(4, args.copies)
+    cs = L.ctypes.c_void_p(stream.cuda_stream)
+    peak = load_peaks()[0]
 
-    # weights: R distinct copies of the layer set (different layer seeds)
-    weights = []   # weights[c][p] = (pk, w_scale, K, N)
-    with torch.cuda.stream(stream):
-        for c in range(R):
-            row = []
-            for p, (_, K, N) in enumerate(inputs.BITNET2B_PROJ):
-                T, w = inputs.bitnet2b_weights(p, layer=c)
-                pk = L.pack(torch.from_numpy(T).to(dev), stream=stream)
-                row.append((pk, float(w), K, N))
-            weights.append(row)
-        xs = [torch.from_numpy(inputs.bitnet2b_act(p, 16).view(np.int16)).to(dev).view(torch.bfloat16)
-              for p in range(len(inputs.BITNET2B_PROJ))]
-        ys = [torch.empty((16, N), dtype=torch.bfloat16, device=dev) for _, _, N in inputs.BITNET2B_PROJ]
-    torch.cuda.synchronize()
+    # ---------------------------------------------- headline: workload 4
+    large = Stack(L, torch, dev, inputs.LARGE_PROJ, inputs.LARGE_LAYERS,
+                  lambda p: (*inputs.large_weights(p, 0), inputs.large_act(p, inputs.MAX_ROWS, 0)),
+                  40_000, None, False)
 
-    cstream = L.ctypes.c_void_p(stream.cuda_stream)
-    # one caller-owned workspace, zero-filled once, shared by every launch on the stream
-    ws_need = 0
-    for M in WIDTHS:
-        for _, K, N in inputs.BITNET2B_PROJ:
-            ws_need = max(ws_need, L.bitmtp_linear_workspace_bytes(N, K, M))
-    probe = [L.GemmDesc(0, 0.0, N, K, max(WIDTHS), L.Act(L.BF16, 0, K, None), L.Out(L.BF16, 0, N, None, 0))
-             for _, K, N in inputs.BITNET2B_PROJ]
-    ws_need = max(ws_need, L.bitmtp_linear_workspace_bytes_grouped(probe))
-    ws = torch.zeros(ws_need, dtype=torch.uint8, device=dev)
-    torch.cuda.synchronize()
-    ws_ptr, ws_n = L.ctypes.c_void_p(ws.data_ptr()), ws.numel()
-    # per (copy, width): the seven problems as one grouped-launch descriptor array
-    group_desc = {}
-    for c in range(R):
-        for M in WIDTHS:
-            descs = []
-            for p, (pk, w, K, N) in enumerate(weights[c]):
-                descs.append(L.GemmDesc(pk.data_ptr(), w, N, K, M,
-                                        L.Act(L.BF16, xs[p].data_ptr(), K, None),
-                                        L.Out(L.BF16, ys[p].data_ptr(), N, None, 0)))
-            group_desc[(c, M)] = ((L.GemmDesc * len(descs))(*descs), len(descs))
-
-    def enqueue_step(s, widths=WIDTHS, mode=None, flags=L.FLAG_PDL):
-        mode = mode or args.mode
+    def step():
         n = 0
-        for M in widths:
-            c = (s * len(WIDTHS) + WIDTHS.index(M)) % R
-            if mode == "grouped":
-                arr, nd = group_desc[(c, M)]
-                st = L.load().bitmtp_linear_gemm_grouped(arr, nd, ws_ptr, ws_n, flags, cstream)
-                if st != L.OK:
-                    raise L.BitmtpError(st, "gemm_grouped")
-                n += 1
-                continue
-            for p, (pk, w, K, N) in enumerate(weights[c]):
-                act = L.Act(L.BF16, xs[p].data_ptr(), K, None)
-                out = L.Out(L.BF16, ys[p].data_ptr(), N, None, 0)
-                st = L.bitmtp_linear_gemm(pk.data_ptr(), w, N, K, M, act, out, ws_ptr, ws_n, flags, cstream)
-                if st != L.OK:
-                    raise L.BitmtpError(st, "gemm")
-                n += 1
+        for M in HEADLINE_WIDTHS:
+            for layer in range(inputs.LARGE_LAYERS):
+                n += large.grouped(layer, M, cs, L.FLAG_PDL)
         return n
 
-    def capture(nsteps, start, widths=WIDTHS, mode=None):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            enqueue_step(start, widths, mode)    # untimed warm call outside capture
-            stream.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                for s in range(nsteps):
-                    enqueue_step(start + s, widths, mode)
-        return g
-
-    G = 16  # steps per graph; weights cycle every R/len(WIDTHS) steps
-    g_full = capture(G, 0)
-    K = args.steps
-    reps, rem = divmod(K, G)
-    g_rem = capture(rem, 0) if rem else None
-    # two kernels per call: activation preparation + GEMM
-    launches_per_step = 2 * len(WIDTHS) * (1 if args.mode == "grouped" else len(inputs.BITNET2B_PROJ))
-
-    # warm-up
+    g_step, launches_per_step = graph_of(torch, stream, step)
     with torch.cuda.stream(stream):
-        for _ in range(max(1, -(-args.warmup // G))):
-            g_full.replay()
+        for _ in range(args.warmup):
+            g_step.replay()
     stream.synchronize()
-
     dist_barrier(world)
     torch.cuda.synchronize()
     sampler = ClockSampler(local) if rank == 0 else None
@@ -265,53 +331,180 @@ def run_ours(args, rank, world):
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(reps):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
+        for _ in range(args.steps):
+            g_step.replay()
         e1.record(stream)
     e1.synchronize()
     torch.cuda.synchronize()
     dist_barrier(world)
     clocks = sampler.stop() if sampler else None
-    ms = e0.elapsed_time(e1)
-    ms = dist_max(ms, world)
+    ms = dist_max(e0.elapsed_time(e1), world)
+    bytes_step = headline_step_bytes()
     sec = ms / 1e3
-    bytes_step = step_bytes()
-    value = bytes_step * K * world / sec / 1e9
-    ms_per_step = ms / K
-
-    # per-width breakdown, both execution modes (same weight rotation)
+    value = bytes_step * args.steps * world / sec / 1e9
+    ms_per_step = ms / args.steps
     per_width = {}
-    for mode in (() if args.no_per_width else ("grouped", "chained")):
-        per_width[mode] = {}
-        for M in WIDTHS:
-            g = capture(G, 0, (M,), mode)
-            with torch.cuda.stream(stream):
-                g.replay()
-                stream.synchronize()
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                n_rep = 20
-                a.record(stream)
-                for _ in range(n_rep):
-                    g.replay()
-                b.record(stream)
-            b.synchronize()
-            t = a.elapsed_time(b) / 1e3 / (n_rep * G)  # seconds per width-pass (7 linears)
-            byt = sum(algorithmic_bytes(Kp, Np, M) for _, Kp, Np in inputs.BITNET2B_PROJ)
-            per_width[mode][str(M)] = {"gbs": round(byt / t / 1e9, 1), "us_per_layer_set": round(t * 1e6, 2),
-                                       "rows_per_s": round(M / t, 1),
-                                       "frac": round(byt / t / 1e9 / load_peaks()[0], 4)}
-            del g
+    for M in HEADLINE_WIDTHS:
+        g, _ = graph_of(torch, stream, lambda M=M: sum(large.grouped(l, M, cs, L.FLAG_PDL)
+                                                       for l in range(inputs.LARGE_LAYERS)))
+        t = time_graph(torch, stream, g, 5)
+        per_width[str(M)] = entry(inputs.LARGE_LAYERS * layer_set_bytes(inputs.LARGE_PROJ, M), t, M, peak)
+        per_width[str(M)]["us_per_layer"] = round(t * 1e6 / inputs.LARGE_LAYERS, 2)
+        del g
 
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(args, L, torch, dev, stream, weights, rank, world)
+    # the headline's layer 0 outputs at each width, for the oracle check
+    check_outputs = {}
+    for M in HEADLINE_WIDTHS:
+        with torch.cuda.stream(stream):
+            large.grouped(0, M, cs, 0)
+        stream.synchronize()
+        check_outputs[M] = [large.y[0][p][:M].clone() for p in range(len(inputs.LARGE_PROJ))]
+
+    e2e = None if args.no_e2e else run_e2e(args, L, torch, dev, stream, large, world)
+    per_config = None if args.no_per_config else run_configs(L, torch, dev, stream, peak)
     tern = None if args.no_ternarize else run_ternarize(L, torch, dev, stream)
+    err = L.bitmtp_linear_device_error(stream)
+    if err != 0:
+        raise RuntimeError(f"device error word set: {err:#x}")
+    host_check = {"layer0": {p: large.host[p] for p in range(len(inputs.LARGE_PROJ))},
+                  "outputs": {M: [bits_of(torch, y) for y in ys] for M, ys in check_outputs.items()}}
+    return dict(value=value, ms_per_step=ms_per_step, clocks=clocks, per_width=per_width, e2e=e2e,
+                per_config=per_config, tern=tern, gpu_launches=args.steps * launches_per_step,
+                launches_per_step=launches_per_step, host_check=host_check)
 
-    return dict(value=value, ms_per_step=ms_per_step, clocks=clocks, per_width=per_width, e2e=e2e, tern=tern,
-                gpu_launches=K * launches_per_step, copies=R, graph_steps=G)
+
+def bits_of(torch, y):
+    return y.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_configs(L, torch, dev, stream, peak):
+    """Workloads 1, 2, 3 and 5 (and nothing else is timed while they run)."""
+    cs = L.ctypes.c_void_p(stream.cuda_stream)
+    out = {}
+
+    # ---- workload 2: the layer set at every width, grouped and chained
+    copies = 16  # 16 x 17.4 MB rotating: no call finds its weights in L2
+    ls = Stack(L, torch, dev, inputs.BITNET2B_PROJ, copies,
+               lambda p: (*inputs.bitnet2b_weights(p), inputs.bitnet2b_act(p, inputs.MAX_ROWS)),
+               20_000, 0.5, True)
+    w2 = {"grouped": {}, "chained": {}}
+    G = 32
+    for mode in ("grouped", "chained"):
+        for M in range(1, inputs.MAX_ROWS + 1):
+            fn = ls.grouped if mode == "grouped" else ls.chained
+            g, _ = graph_of(torch, stream, lambda M=M, fn=fn: sum(fn(c % copies, M, cs, L.FLAG_PDL) for c in range(G)))
+            t = time_graph(torch, stream, g, 10) / G
+            w2[mode][str(M)] = entry(layer_set_bytes(inputs.BITNET2B_PROJ, M), t, M, peak)
+            del g
+    out["2_bitnet2b_layer_set"] = {"unit": "per layer set (7 projections)", **w2}
+    del ls
+
+    # ---- workload 3: the 30-layer stack at width 4
+    st = Stack(L, torch, dev, inputs.BITNET2B_PROJ, inputs.BITNET2B_LAYERS,
+               lambda p: (*inputs.bitnet2b_weights(p, layer=0), inputs.bitnet2b_act(p, inputs.MAX_ROWS, layer=0)),
+               30_000, 0.5, True)
+    w3 = {}
+    for mode in ("grouped", "chained"):
+        fn = st.grouped if mode == "grouped" else st.chained
+        g, _ = graph_of(torch, stream, lambda fn=fn: sum(fn(l, 4, cs, L.FLAG_PDL) for l in range(inputs.BITNET2B_LAYERS)))
+        t = time_graph(torch, stream, g, 10)
+        w3[mode] = entry(inputs.BITNET2B_LAYERS * layer_set_bytes(inputs.BITNET2B_PROJ, 4), t, 4, peak)
+        w3[mode]["us_per_step"] = w3[mode].pop("us")
+        del g
+    out["3_bitnet2b_30_layers_M4"] = w3
+    del st
+
+    # ---- workload 1: single 2560 -> 2560 linear, fp32, widths 1 and 4
+    ncopy = 128  # 128 x 1.64 MB: back to back over distinct weights, larger than L2
+    T0, w0, _ = inputs.single_linear(1)
+    pks = [L.pack(torch.from_numpy(T0).to(dev))]
+    for c in range(1, ncopy):
+        pks.append(L.pack(inputs.device_ternary(10_000 + c, (2560, 2560), None, dev)))
+    w1 = {}
+    ws = torch.zeros(L.bitmtp_linear_workspace_bytes(2560, 2560, 16), dtype=torch.uint8, device=dev)
+    for M in (1, 4):
+        _, _, xh = inputs.single_linear(M)
+        x = torch.from_numpy(xh).to(dev)
+        y = torch.empty((M, 2560), dtype=torch.float32, device=dev)
+        act = L.Act(L.F32, x.data_ptr(), 2560, None)
+        o = L.Out(L.F32, y.data_ptr(), 2560, None, 0)
+        lib = L.load()
+
+        def call(c, flags):
+            st_ = lib.bitmtp_linear_gemm(L.ctypes.c_void_p(pks[c].data_ptr()), float(w0), 2560, 2560, M,
+                                         L.ctypes.byref(act), L.ctypes.byref(o), L.ctypes.c_void_p(ws.data_ptr()),
+                                         ws.numel(), flags, cs)
+            if st_ != L.OK:
+                raise L.BitmtpError(st_, "gemm")
+            return 2
+        g, _ = graph_of(torch, stream, lambda: sum(call(c, L.FLAG_PDL) for c in range(ncopy)))
+        t = time_graph(torch, stream, g, 10) / ncopy
+        back = entry(call_bytes(2560, 2560, M, 4), t, M, peak)
+        del g
+        # one call alone: its own graph, replayed with a sync between calls
+        times = []
+        for c in range(40):
+            g1, _ = graph_of(torch, stream, lambda c=c: call(c % ncopy, 0))
+            torch.cuda.synchronize()
+            times.append(time_graph(torch, stream, g1, 1, warm=0))
+            del g1
+        alone = entry(call_bytes(2560, 2560, M, 4), statistics.median(times), M, peak)
+        w1[str(M)] = {"alone": alone, "back_to_back_128_copies": back}
+    out["1_single_2560"] = w1
+    del pks
+
+    # ---- workload 5: the role-dependent grouped call at width 16
+    w5 = {}
+    ncopy5 = 6  # 6 x 22.1 MB rotating
+    for s in range(len(inputs.ROLE_SPARSITY)):
+        x = torch.from_numpy(inputs.role_act(s)).to(dev)
+        q = torch.empty((16, 2560), dtype=torch.int8, device=dev)
+        a = torch.empty(16, dtype=torch.float32, device=dev)
+        groups = []
+        for c in range(ncopy5):
+            descs = []
+            for gi, (_, row0, rows, K, N) in enumerate(inputs.ROLE_GROUPS):
+                if c == 0:
+                    T, w = inputs.role_weights(s, gi)
+                    pk = L.pack(torch.from_numpy(T).to(dev))
+                else:
+                    pk = L.pack(inputs.device_ternary(50_000 + 100 * s + 10 * c + gi, (N, K),
+                                                      inputs.ROLE_SPARSITY[s], dev))
+                    w = 0.02
+                y = torch.empty((rows, N), dtype=torch.float32, device=dev)
+                descs.append((pk, float(w), N, K, rows, row0, y))
+            groups.append(descs)
+        nb = 0
+        arrs = []
+        for descs in groups:
+            d = [L.GemmDesc(pk.data_ptr(), w, N, K, rows,
+                            L.Act(L.Q8, q.data_ptr() + row0 * 2560, 2560, a.data_ptr() + 4 * row0),
+                            L.Out(L.F32, y.data_ptr(), N, None, 0)) for pk, w, N, K, rows, row0, y in descs]
+            arrs.append(((L.GemmDesc * len(d))(*d), d))
+            nb = max(nb, L.bitmtp_linear_workspace_bytes_grouped(d))
+        ws5 = torch.zeros(nb, dtype=torch.uint8, device=dev)
+        lib = L.load()
+
+        def call5(c):
+            st_ = lib.bitmtp_linear_quant_act(L.ctypes.c_void_p(x.data_ptr()), L.F32, 16, 2560, 2560,
+                                              L.ctypes.c_void_p(q.data_ptr()), 2560, L.ctypes.c_void_p(a.data_ptr()),
+                                              None, cs)
+            if st_ != L.OK:
+                raise L.BitmtpError(st_, "quant_act")
+            arr, d = arrs[c % ncopy5]
+            st_ = lib.bitmtp_linear_gemm_grouped(arr, len(d), L.ctypes.c_void_p(ws5.data_ptr()), ws5.numel(),
+                                                 L.FLAG_PDL, cs)
+            if st_ != L.OK:
+                raise L.BitmtpError(st_, "gemm_grouped")
+            return 3
+        g, _ = graph_of(torch, stream, lambda: sum(call5(c) for c in range(24)))
+        t = time_graph(torch, stream, g, 10) / 24
+        byt = sum(packed_tile_bytes(N, K) for _, _, _, K, N in inputs.ROLE_GROUPS) + 16 * 2560 * 4
+        w5[str(inputs.ROLE_SPARSITY[s])] = entry(byt, t, 16, peak)
+        del g, groups, arrs
+    out["5_role_grouped_M16"] = {"unit": "per call (quant_act + grouped GEMM)", **w5}
+    torch.cuda.synchronize()
+    return out
 
 
 def run_ternarize(L, torch, dev, stream):
@@ -355,140 +548,223 @@ def run_ternarize(L, torch, dev, stream):
             "what": "bitmtp_linear_ternarize_pack of the 7 projections from fp32 N(0, 0.02^2) weights"}
 
 
-def run_e2e(args, L, torch, dev, stream, weights, rank, world):
-    """Same workload through the library's C ABI with host buffers: every step
-    copies its activations host->device from pinned memory (one copy of the
-    16 rows of every projection; each width reads its first M rows), runs the
-    four grouped calls and reads every output back device->host (one copy),
-    then synchronises."""
-    R = len(weights)
-    proj = inputs.BITNET2B_PROJ
-    kofs, off = [], 0
-    for _, K, _ in proj:
-        kofs.append(off)
-        off += 16 * K
+def run_e2e(args, L, torch, dev, stream, large, world):
+    """The headline step through the library's C ABI with host buffers: every
+    step copies the activations of every layer host->device from pinned
+    memory (one copy), makes the 108 grouped calls and reads every output
+    back device->host (one copy), then synchronises."""
+    nl, proj = inputs.LARGE_LAYERS, inputs.LARGE_PROJ
+    kofs, off = {}, 0
+    for layer in range(nl):
+        for p, (_, K, _) in enumerate(proj):
+            kofs[(layer, p)] = off
+            off += inputs.MAX_ROWS * K
     x_host = torch.empty(off, dtype=torch.int16).pin_memory()
-    for p in range(len(proj)):
-        _, K, _ = proj[p]
-        x_host[kofs[p]:kofs[p] + 16 * K] = torch.from_numpy(inputs.bitnet2b_act(p, 16).view(np.int16).reshape(-1))
+    for layer in range(nl):
+        for p in range(len(proj)):
+            o = kofs[(layer, p)]
+            x_host[o:o + large.x[layer][p].numel()] = large.x[layer][p].reshape(-1).view(torch.int16).cpu()
     x_dev = torch.empty_like(x_host, device=dev)
     yofs, off = {}, 0
-    for M in WIDTHS:
+    for layer in range(nl):
         for p, (_, _, N) in enumerate(proj):
-            yofs[(M, p)] = off
-            off += M * N
+            yofs[(layer, p)] = off
+            off += inputs.MAX_ROWS * N
     y_dev = torch.empty(off, dtype=torch.int16, device=dev)
     y_host = torch.empty(off, dtype=torch.int16).pin_memory()
     descs = {}
-    for c in range(R):
-        for M in WIDTHS:
-            d = [L.GemmDesc(pk.data_ptr(), w, N, K, M,
-                            L.Act(L.BF16, x_dev.data_ptr() + 2 * kofs[p], K, None),
-                            L.Out(L.BF16, y_dev.data_ptr() + 2 * yofs[(M, p)], N, None, 0))
-                 for p, (pk, w, K, N) in enumerate(weights[c])]
-            descs[(c, M)] = ((L.GemmDesc * len(d))(*d), len(d))
-    nb = L.bitmtp_linear_workspace_bytes_grouped(list(descs[(0, max(WIDTHS))][0]))
-    ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
-    torch.cuda.synchronize()
+    for layer in range(nl):
+        for M in HEADLINE_WIDTHS:
+            d = [L.GemmDesc(large.pk[layer][p].data_ptr(), large.w[layer][p], N, K, M,
+                            L.Act(L.BF16, x_dev.data_ptr() + 2 * kofs[(layer, p)], K, None),
+                            L.Out(L.BF16, y_dev.data_ptr() + 2 * yofs[(layer, p)], N, None, 0))
+                 for p, (_, K, N) in enumerate(proj)]
+            descs[(layer, M)] = ((L.GemmDesc * len(d))(*d), len(d))
     lib = L.load()
     cs = L.ctypes.c_void_p(stream.cuda_stream)
-    wsp = L.ctypes.c_void_p(ws.data_ptr())
-    steps = args.e2e_steps
+    wsp = L.ctypes.c_void_p(large.ws.data_ptr())
+    nb = large.ws.numel()
 
-    def one(s):
+    def one():
         x_dev.copy_(x_host, non_blocking=True)
-        for M in WIDTHS:
-            arr, n = descs[((s * len(WIDTHS) + WIDTHS.index(M)) % R, M)]
-            st = lib.bitmtp_linear_gemm_grouped(arr, n, wsp, nb, L.FLAG_PDL, cs)
-            if st != L.OK:
-                raise L.BitmtpError(st, "gemm_grouped")
+        for M in HEADLINE_WIDTHS:
+            for layer in range(nl):
+                arr, n = descs[(layer, M)]
+                st = lib.bitmtp_linear_gemm_grouped(arr, n, wsp, nb, L.FLAG_PDL, cs)
+                if st != L.OK:
+                    raise L.BitmtpError(st, "gemm_grouped")
         y_host.copy_(y_dev, non_blocking=True)
         stream.synchronize()
 
     with torch.cuda.stream(stream):
-        for s in range(3):
-            one(s)
+        for _ in range(2):
+            one()
         dist_barrier(world)
         t0 = time.perf_counter()
-        for s in range(steps):
-            one(s)
+        for _ in range(args.e2e_steps):
+            one()
         t1 = time.perf_counter()
     sec = dist_max(t1 - t0, world)
-    return {"value": round(step_bytes() * steps * world / sec / 1e9, 2), "unit": "GB/s",
+    return {"value": round(headline_step_bytes() * args.e2e_steps * world / sec / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
-            "steps": steps, "ms_per_step": round(sec * 1e3 / steps, 4)}
+            "steps": args.e2e_steps, "ms_per_step": round(sec * 1e3 / args.e2e_steps, 4)}
 
 
-# --------------------------------------------------------------------------
-def oracle_sample(seconds):
-    """Time the CPU oracle on the workload's linears, cycling (width, projection)
-    pairs until about `seconds` of work.  Returns (GB/s, description)."""
+# -------------------------------------------------------------- CPU oracle --
+_SAMPLE_W: dict = {}
+_SAMPLE_X: dict = {}
+
+
+def _oracle_sample(kind, i):
+    """The i-th linear of a workload's oracle sample: (T, w, x, x_is_bf16).
+    Weights are drawn once per projection and kept; activations per width."""
+    if kind == "4":
+        M, p = HEADLINE_WIDTHS[i % 3], (i // 3) % len(inputs.LARGE_PROJ)
+        wk, xk = (kind, p), (kind, p, M)
+        if wk not in _SAMPLE_W:
+            _SAMPLE_W[wk] = inputs.large_weights(p, 0)
+        if xk not in _SAMPLE_X:
+            _SAMPLE_X[xk] = (inputs.large_act(p, M, 0), True)
+    elif kind == "2":
+        M, p = 1 + i % 16, (i // 16) % len(inputs.BITNET2B_PROJ)
+        wk, xk = (kind, p), (kind, p, M)
+        if wk not in _SAMPLE_W:
+            _SAMPLE_W[wk] = inputs.bitnet2b_weights(p)
+        if xk not in _SAMPLE_X:
+            _SAMPLE_X[xk] = (inputs.bitnet2b_act(p, M), True)
+    elif kind == "3":
+        p = i % len(inputs.BITNET2B_PROJ)
+        wk, xk = (kind, p), (kind, p, 4)
+        if wk not in _SAMPLE_W:
+            _SAMPLE_W[wk] = inputs.bitnet2b_weights(p, layer=0)
+        if xk not in _SAMPLE_X:
+            _SAMPLE_X[xk] = (inputs.bitnet2b_act(p, 4, layer=0), True)
+    elif kind == "1":
+        M = (1, 4)[i % 2]
+        wk, xk = (kind,), (kind, M)
+        if wk not in _SAMPLE_W:
+            T, w, _ = inputs.single_linear(1)
+            _SAMPLE_W[wk] = (T, w)
+        if xk not in _SAMPLE_X:
+            _SAMPLE_X[xk] = (inputs.single_linear(M)[2], False)
+    elif kind == "5":
+        s, g = i % 3, (i // 3) % 2
+        wk, xk = (kind, s, g), (kind, s, g)
+        if wk not in _SAMPLE_W:
+            _SAMPLE_W[wk] = inputs.role_weights(s, g)
+        if xk not in _SAMPLE_X:
+            _, row0, rows, _, _ = inputs.ROLE_GROUPS[g]
+            _SAMPLE_X[xk] = (inputs.role_act(s)[row0:row0 + rows], False)
+    else:
+        raise ValueError(kind)
+    T, w = _SAMPLE_W[wk]
+    x, is_bf16 = _SAMPLE_X[xk]
+    return T, w, x, is_bf16
+
+
+def _oracle_worker(task):
+    """Run oracle linears of one workload for about `seconds` of oracle time
+    (inputs drawn outside the timed calls); returns (algorithmic bytes,
+    seconds, linears).  Module-level for the spawn pool."""
+    kind, seconds, start = task
     import oracle
-    pairs = [(M, p) for M in WIDTHS for p in range(len(inputs.BITNET2B_PROJ))]
-    data = {}
-    done_bytes, done_sec, n = 0, 0.0, 0
-    while done_sec < seconds:
-        M, p = pairs[n % len(pairs)]
-        if p not in data:
-            T, w = inputs.bitnet2b_weights(p, layer=0)
-            data[p] = (T, w, inputs.bitnet2b_act(p, 16))
-        T, w, x = data[p]
-        _, K, N = inputs.BITNET2B_PROJ[p]
+    done_b, done_s, n = 0, 0.0, 0
+    i = start
+    while done_s < seconds or n == 0:
+        T, w, x, is_bf16 = _oracle_sample(kind, i)
         t0 = time.perf_counter()
-        oracle.w2a8_linear(T, w, x[:M], "bf16", x_is_bf16=True)
-        done_sec += time.perf_counter() - t0
-        done_bytes += algorithmic_bytes(K, N, M)
+        oracle.w2a8_linear(T, w, x, "bf16" if is_bf16 else "f32", x_is_bf16=is_bf16)
+        done_s += time.perf_counter() - t0
+        N, K = T.shape
+        done_b += call_bytes(K, N, x.shape[0], 2 if is_bf16 else 4)
         n += 1
-    return done_bytes / done_sec / 1e9, f"{n} linears of the layer set cycling widths {list(WIDTHS)}", n
+        i += 1
+    return done_b, done_s, n
+
+
+def cpu_baseline(seconds, host_check):
+    """The oracle on one host core and on every host core (a spawn process
+    pool, one sample stream per core), on the headline workload, plus one
+    core on bounded samples of the other workloads; and the parity check of
+    a sample of the headline step's outputs."""
+    import oracle
+    cores = os.cpu_count() or 1
+    b, s, n = _oracle_worker(("4", seconds, 0))
+    one = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"{n} linears of the 36-layer stack's first layer, widths 8/12/16, "
+                     "cycling the seven projections"}
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        res = pool.map(_oracle_worker, [("4", seconds, 7 * k) for k in range(cores)])
+    # every core runs at once: aggregate rate = all bytes / the longest core's oracle time
+    tb = sum(r[0] for r in res)
+    tn = sum(r[2] for r in res)
+    slowest = max(r[1] for r in res)
+    allc = {"value": round(tb / slowest / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{tn} linears of the same sample, one stream per core in a process pool, "
+                      "all cores computing at once (inputs drawn outside the timed calls)"}
+    per = {}
+    for kind in ("1", "2", "3", "5"):
+        b, s, n = _oracle_worker((kind, max(1.0, seconds / 5), 0))
+        per[kind] = {"gbs_1core": round(b / s / 1e9, 4), "linears": n, "seconds": round(s, 2)}
+    # parity: 64 sampled output features of every projection of layer 0 at each width
+    rng = np.random.default_rng(77)
+    checked, bad = 0, 0
+    for M, ys in host_check["outputs"].items():
+        for p, y_bits in enumerate(ys):
+            T, w, xb = host_check["layer0"][p]
+            cols = np.sort(rng.choice(T.shape[0], 64, replace=False))
+            q, a, _ = oracle.quant_act_bf16(xb[:M])
+            acc = oracle.gemm_acc(T[cols], q)
+            ref = oracle.dequant(acc, a, w, "bf16").astype(np.int32)
+            got = y_bits[:, cols].astype(np.int32)
+            o = lambda v: np.where(v & 0x8000, 0x8000 - v, v)
+            bad += int(np.count_nonzero(np.abs(o(got) - o(ref)) > 1))
+            checked += ref.size
+    one["all_cores"] = allc
+    one["per_workload_1core"] = per
+    one["parity_check"] = {"outputs_checked": checked, "beyond_1_bf16_ulp": bad,
+                           "what": "headline layer 0, widths 8/12/16, 64 sampled features per projection"}
+    return one
 
 
 def run_reference(args, rank, world):
+    """The oracle alone on the headline workload: each step is one linear of
+    the stack's first layer (cycling widths 8/12/16 and the projections)."""
     if rank != 0:
         return None
-    per = []
-    tot_b, tot_s = 0, 0.0
     import oracle
-    pairs = [(M, p) for M in WIDTHS for p in range(len(inputs.BITNET2B_PROJ))]
-    cache = {}
-
-    def step(i):
-        M, p = pairs[i % len(pairs)]
-        if p not in cache:
-            T, w = inputs.bitnet2b_weights(p, layer=0)
-            cache[p] = (T, w, inputs.bitnet2b_act(p, 16))
-        T, w, x = cache[p]
-        _, K, N = inputs.BITNET2B_PROJ[p]
+    tot_b, tot_s = 0, 0.0
+    for i in range(args.warmup + args.steps):
+        T, w, x, _ = _oracle_sample("4", i)
         t0 = time.perf_counter()
-        oracle.w2a8_linear(T, w, x[:M], "bf16", x_is_bf16=True)
-        return algorithmic_bytes(K, N, M), time.perf_counter() - t0
-
-    for i in range(args.warmup):
-        step(i)
-    for i in range(args.steps):
-        b, s = step(args.warmup + i)
-        tot_b += b
-        tot_s += s
-        per.append(s)
+        oracle.w2a8_linear(T, w, x, "bf16", x_is_bf16=True)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            tot_s += dt
+            tot_b += call_bytes(T.shape[1], T.shape[0], x.shape[0])
     v = tot_b / tot_s / 1e9
     line = {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "w2a8-int32",
-            "data": "synthetic", "impl": "reference",
-            "config": workload_config(args),
+            "data": "synthetic", "impl": "reference", "config": workload_config(args),
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": "each step is one (width, projection) linear of the layer set, "
-                                       "cycling widths 1,2,4,8 and the 7 projections"},
+                             "sample": "each step is one linear of the 36-layer stack's first layer, cycling "
+                                       "widths 8/12/16 and the seven projections"},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return line
 
 
 def workload_config(args, extra=None):
-    cfg = {"workload": "bitnet2b_layer_set", "projections": "q,k,v,o 2560->2560/640/640/2560; gate,up 2560->6912; "
-                                                       "down 6912->2560",
-           "widths": list(WIDTHS), "weights": "ternary P(0)=0.5, per-tensor scale U[0.01,0.05]",
-           "activations": "bf16 N(0,1), 1% x20 outliers, quantised per row in-kernel",
-           "output": "bf16", "parallelism": f"replicas{args.gpus}"}
+    cfg = {"workload": "large36_stack_M8_12_16",
+           "layers": inputs.LARGE_LAYERS,
+           "projections": "q,o 4096->4096; k,v 4096->1024; gate,up 4096->11008; down 11008->4096",
+           "widths": list(HEADLINE_WIDTHS), "weights": "ternary uniform (P(0)=1/3), per-tensor scale U[0.01,0.05]",
+           "activations": "bf16 N(0,1), quantised per row in the preparation kernel",
+           "output": "bf16", "parallelism": f"replicas{args.gpus}",
+           "l2": "inputs larger than L2 (1.595 GB of packed weights per width pass)",
+           "launch": "one grouped call (7 projections) per layer, 2 launches each; CUDA graph + PDL"}
     if extra:
         cfg.update(extra)
     return cfg
@@ -535,33 +811,28 @@ def main():
     if rank != 0:
         return
     peak, peak_kind = load_peaks()
-    cpu = None
-    if not args.no_cpu_baseline:
-        v, desc, n = oracle_sample(args.cpu_seconds)
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
+    cpu = None if args.no_cpu_baseline else cpu_baseline(args.cpu_seconds, res["host_check"])
     value = res["value"]
     per_gpu = value / world
+    traffic = CAPTURED_TRAFFIC.get(kernel_sources_hash())
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "w2a8-int32",
         "data": "synthetic (seeded ternary weights, bf16 activations)",
-        "config": workload_config(args, {"weight_copies": res["copies"],
-                                         "l2": f"weights rotate over {res['copies']} distinct copies "
-                                               f"({res['copies']} x 17.4 MB > L2)",
-                                         "graph_steps": res["graph_steps"],
-                                         "launch": f"{args.mode}; CUDA graph + PDL"}),
+        "config": workload_config(args),
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(per_gpu / peak, 4), "peak_kind": peak_kind,
-                     "traffic": STEP_DRAM_TRAFFIC,
-                     "kernel": "act_prep_kernel + w2a8_streamk_kernel: the two launches of each grouped call, "
-                               "4 calls per step; achieved = algorithmic bytes per step / mean step time"},
+                     "frac": round(per_gpu / peak, 4), "peak_kind": peak_kind, "traffic": traffic,
+                     "kernel": "act_prep_kernel + w2a8_streamk_kernel (both launches of every grouped call; "
+                               "108 calls per step); achieved = algorithmic bytes per step / mean step time"},
         "per_width": res["per_width"],
+        "per_config": res["per_config"],
         "e2e": res["e2e"],
         "ternarize_pack": res["tern"],
         "gpu_launches": res["gpu_launches"],
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
+        "kernel_sources": kernel_sources_hash(),
     }
     print(json.dumps(line), flush=True)
 

@@ -1,8 +1,9 @@
 """Seeded synthetic inputs for the W2A8 ternary linear.
 
-This module only draws random data (numpy PCG64, fixed seeds); it holds none of
-the linear's arithmetic.  Tests and the benchmark feed the same arrays to the
-CUDA path and to the CPU oracle.
+This module only draws random data (numpy PCG64 with fixed seeds, and torch's
+seeded generator on the device for the benchmark's large stacks); it holds
+none of the linear's arithmetic.  Tests and the benchmark feed the same
+arrays to the CUDA path and to the CPU oracle.
 
 The pages measure only end-to-end decoding of trained models on task suites;
 none of that is available here, so every workload below is synthetic, shaped
@@ -158,3 +159,38 @@ def random_problem(seed: int, M: int, N: int, K: int, p_zero=None, x_kind: str =
     if x_kind == "bf16":
         return T, w_scale, to_bf16_bits(x)
     return T, w_scale, x
+
+
+# ---------------------------------------------------------------------------
+# Device-side generators for the benchmark's large stacks (hundreds of
+# millions of weights per layer set), drawn with torch's seeded generator on
+# the GPU.  Same distributions as above; different streams from the numpy
+# ones, so the benchmark draws the layers it checks against the oracle with
+# the numpy generators and the rest with these.
+# ---------------------------------------------------------------------------
+def device_ternary(seed: int, shape, p_zero: float | None, device):
+    """Ternary int8 tensor on `device`.  p_zero None: uniform over {-1, 0, +1};
+    otherwise P(0) = p_zero (to 2^-16) and P(+1) = P(-1)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    if p_zero is None:
+        return (torch.randint(0, 3, shape, generator=g, device=device, dtype=torch.int8) - 1).contiguous()
+    z = int(round(p_zero * 65536))
+    h = z + (65536 - z) // 2
+    r = torch.randint(0, 65536, shape, generator=g, device=device, dtype=torch.int32)
+    t = torch.where(r < z, 0, torch.where(r < h, 1, -1))
+    return t.to(torch.int8).contiguous()
+
+
+def device_normal_bf16(seed: int, shape, device, outlier_frac: float = 0.0, mult: float = 20.0):
+    """bf16 N(0, 1) tensor on `device`; each element multiplied by `mult`
+    with probability `outlier_frac`."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if outlier_frac > 0:
+        hit = torch.rand(shape, generator=g, device=device) < outlier_frac
+        x = torch.where(hit, x * mult, x)
+    return x.to(torch.bfloat16).contiguous()

@@ -17,16 +17,34 @@ import bench  # noqa: E402
 from ternary_w2a8_linear_gb300 import inputs  # noqa: E402
 
 
-def test_step_bytes():
-    pk = 0
-    act = 0
-    for M in (1, 2, 4, 8):
-        for _, K, N in inputs.BITNET2B_PROJ:
-            pk += (N // 128) * (K // 128) * 4096
-            act += M * K * 2
-    assert bench.step_bytes() == pk + act
-    # 17.37 MB of packed weights per layer set, four widths per step
-    assert pk == 4 * 17_367_040
+def test_headline_step_bytes():
+    # the 36-layer stack at widths 8, 12, 16: packed tiles of the layer set
+    # (44,302,336 bytes) per layer and width, plus bf16 activation rows
+    pk = sum((-(-N // 128)) * (-(-K // 128)) * 4096 for _, K, N in inputs.LARGE_PROJ)
+    assert pk == 44_302_336
+    act_k = sum(K for _, K, _ in inputs.LARGE_PROJ)
+    want = sum(36 * (pk + M * act_k * 2) for M in (8, 12, 16))
+    assert bench.headline_step_bytes() == want
+    # 36 layer sets of packed weights = the 1.595 GB stack
+    assert 36 * pk == 1_594_884_096
+
+
+def test_layer_set_bytes():
+    pk = sum((N // 128) * (K // 128) * 4096 for _, K, N in inputs.BITNET2B_PROJ)
+    assert pk == 17_367_040
+    for M in (1, 2, 4, 8, 16):
+        assert bench.layer_set_bytes(inputs.BITNET2B_PROJ, M) == pk + M * 2 * (6 * 2560 + 6912)
+
+
+def test_oracle_samples_cycle_the_workloads():
+    seen = set()
+    for i in range(21):
+        T, w, x, is_bf16 = bench._oracle_sample("4", i)
+        assert is_bf16 and x.shape[1] == T.shape[1] and x.shape[0] in (8, 12, 16)
+        seen.add((x.shape[0], T.shape))
+    assert len(seen) == 3 * 4  # widths x the layer set's four distinct (N, K) shapes
+    T, w, x, is_bf16 = bench._oracle_sample("5", 3)  # sparsity 0, the draft group
+    assert not is_bf16 and x.shape == (12, 2560) and T.shape == (2560, 2560)
 
 
 def test_ternarize_bytes():
