@@ -110,12 +110,12 @@ enum : int {
 struct Ctrl {
     uint64_t wfull[kMaxRing];     // weight tiles of the chunk landed
     uint64_t bfull[kMaxRing];     // activation tiles of the chunk landed
-    uint64_t empty[kMaxRing];     // chunk slot free again (MMA commit / dp4a consumers)
+    uint64_t empty[kMaxRing];     // chunk slot free again (both MMA warps' commits / dp4a consumers)
     uint64_t a_full[kATiles];     // A buffer written (four consumer warps)
     uint64_t mma_done[kBatchBars]; // MMA batch b complete: barrier b % kBatchBars
-    uint64_t dfull[2];            // accumulator of segment s (D buffer s & 1) complete
+    uint64_t dfull[2][4];         // MMA warp 5 + i finished segment s: dfull[i][s & 3]
     uint64_t slot_done;           // contributor partial sums stored (four consumer warps)
-    uint64_t drained;             // after a failed wait: every MMA this CTA issued is complete
+    uint64_t drained[2];          // after a failed wait: every MMA MMA warp 5 + i issued is complete
     uint32_t tmem_base;
     int failed;
     int owner_ok;
@@ -611,7 +611,7 @@ __device__ __forceinline__ int code_sum(int v, int m) {
 }
 
 template <int PATH, int DPR>
-__global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
+__global__ void __launch_bounds__(gemm_threads(PATH), kCtasPerSm)
 w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr bool kTC = PATH != kPathDP;
@@ -639,18 +639,18 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         const uint32_t* src = reinterpret_cast<const uint32_t*>(&P.p[0]);
         uint32_t* dst = reinterpret_cast<uint32_t*>(&c->prob[0]);
         const int words = np * static_cast<int>(sizeof(GemmProblem) / 4);
-        for (int z = tid; z < words; z += kGemmThreads) dst[z] = src[z];
+        for (int z = tid; z < words; z += gemm_threads(PATH)) dst[z] = src[z];
     }
     const GemmProblem* pp = c->prob;
     // the mbarriers, one per thread (consecutive 8-byte words)
-    static_assert(offsetof(Ctrl, slot_done) == offsetof(Ctrl, wfull) + 8 * (3 * kMaxRing + kATiles + kBatchBars + 2),
+    static_assert(offsetof(Ctrl, slot_done) == offsetof(Ctrl, wfull) + 8 * (3 * kMaxRing + kATiles + kBatchBars + 8),
                   "mbarriers not consecutive");
     static_assert(offsetof(Ctrl, drained) == offsetof(Ctrl, slot_done) + 8, "mbarriers not consecutive");
-    if (tid < 3 * kMaxRing + kATiles + kBatchBars + 4) {
-        uint32_t count = 1;                                                          // wfull, bfull, mma_done, dfull
-        if (tid >= 2 * kMaxRing && tid < 3 * kMaxRing) count = kTC ? 1 : 4;          // empty
+    if (tid < 3 * kMaxRing + kATiles + kBatchBars + 11) {
+        uint32_t count = 1;                                                          // wfull, bfull, mma_done, dfull, drained
+        if (tid >= 2 * kMaxRing && tid < 3 * kMaxRing) count = kTC ? 2 : 4;          // empty
         else if (tid >= 3 * kMaxRing && tid < 3 * kMaxRing + kATiles) count = 4;     // a_full
-        else if (tid == 3 * kMaxRing + kATiles + kBatchBars + 2) count = 4;          // slot_done
+        else if (tid == 3 * kMaxRing + kATiles + kBatchBars + 8) count = 4;          // slot_done
         mbar_init(smem_u32(&c->wfull[0]) + 8 * tid, count);
         fence_mbar_init();
     }
@@ -738,87 +738,103 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp >= 5) {
+        // Tensor paths (the dp4a block's warp 5 idles).  Two MMA
+        // warps: warp 5 issues the even MMA batches, warp 6 the odd ones (one
+        // issuing warp cannot keep up: each tcgen05.mma holds it for tens of
+        // ns).  Both accumulate into the segment's D buffer, which the consumer
+        // warps zero before the segment's first A tile, so every MMA adds
+        // (the order does not matter: every partial sum is a multiple of
+        // 2^-9 below 2^15 in magnitude, so fp32 holds it exactly).  A batch is up to kMmaBatch tiles of one
+        // segment; its issuer waits for the activation tiles of every chunk it
+        // is the first to touch, then for the batch's last A buffer (the
+        // consumer warps fill buffers in order), issues the batch's MMAs as
+        // straight-line code and commits mma_done.  Chunk slots and finished
+        // segments need both warps: each commits `empty` at every chunk end
+        // and its own dfull[.][s & 3] at every segment end s it passes (a
+        // commit tracks only the committing thread's own MMAs).  A warp with
+        // no batch in a short segment passes it at once, so it can run up to
+        // two segments ahead of the epilogue's wait: four barriers per warp
+        // keep its phases apart.  The whole warp runs the loop; the
+        // elected lane issues through guard predicates.
         if constexpr (kTC) {
-            // The whole warp runs the loop (uniform control flow, waits by every
-            // lane); the elected lane issues the MMAs and commits through guard
-            // predicates, so the warp never diverges around a tcgen05 issue.
-            // Segment by segment (k tiles of one row tile) in batches of up to
-            // kMmaBatch tiles: one wait (the batch's last A buffer: the consumer
-            // warps fill buffers in order), the batch's MMAs as straight-line
-            // code, one commit for the batch.
+            static_assert(kMmaBatch == 2, "the issue loop below handles batches of one or two tiles");
+            const int par = warp - 5;
             const uint32_t leader = elect_one();
             constexpr int kBR = btile_brows(PATH, DPR);
             constexpr uint32_t kIdesc = idesc_f16_f32(128, kBR);
-            constexpr uint32_t kUnit = kBR * 16;      // bytes of one 16-k unit
-            const uint32_t bbase = smem_u32(Br);
+            constexpr uint32_t kUnit = kBR * 16;                  // bytes of one 16-k unit
+            const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(Br), kUnit, 128);
+            constexpr uint64_t kStepDesc = (2 * kUnit) >> 4;      // 32 k further, in descriptor units
+            constexpr uint64_t kTileDesc = static_cast<uint64_t>(BT) >> 4;
             RingPos rp;
             rp.reset();
-            int nbatch = 0, seg = 0;
+            int nbatch = 0, seg = 0, my_chunk = -1;
             bool ok = true;
             long long cur_end = t_end;
             while (rp.i < nloc && ok) {
-                Seg s;
-                seg_ending_at(pp, np, t_begin, cur_end, s);
-                cur_end = s.t0;
-                const int len = s.kb - s.ka;
+                Seg sg;
+                seg_ending_at(pp, np, t_begin, cur_end, sg);
+                cur_end = sg.t0;
+                const int len = sg.kb - sg.ka;
                 const uint32_t dcol = tmem + kAccCol + (seg & 1) * 32;
                 for (int e = 0; e < len && ok;) {
                     const int nb = min(kMmaBatch, len - e);
-                    RingPos r[kMmaBatch];
-                    r[0] = rp;
-#pragma unroll
-                    for (int t = 1; t < kMmaBatch; ++t) {
-                        r[t] = r[t - 1];
-                        if (t < nb) r[t].next(R);
+                    RingPos r1 = rp;  // the batch's last tile
+                    if (nb > 1) r1.next(R);
+                    if ((nbatch & 1) == par) {
+                        const int c0 = rp.i / kChunk, c1 = r1.i / kChunk;
+                        if (c0 > my_chunk) {
+                            ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[rp.q]), rp.qph, P.wait_ns));
+                            my_chunk = c0;
+                        }
+                        if (ok && c1 > my_chunk) {
+                            ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[r1.q]), r1.qph, P.wait_ns));
+                            my_chunk = c1;
+                        }
+                        if (!ok) {
+                            if (leader) fail(c, P.err, kErrWaitB);
+                            break;
+                        }
+                        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->a_full[r1.ab]), r1.abph, P.wait_ns));
+                        if (!ok) {
+                            if (leader) fail(c, P.err, kErrWaitAFull);
+                            break;
+                        }
+                        tc_fence_after();
+                        // k step j of a tile: A columns 8j, B units 2j and 2j + 1
+                        const uint64_t b0 = bdesc0 + static_cast<uint64_t>(rp.slot()) * kTileDesc;
+                        const uint32_t a0 = tmem + kACol + rp.ab * kATileCols;
+                        mma_f8_ts_acc_if(leader, dcol, a0, b0, kIdesc);
+                        mma_f8_ts_acc_if(leader, dcol, a0 + 8, b0 + kStepDesc, kIdesc);
+                        mma_f8_ts_acc_if(leader, dcol, a0 + 16, b0 + 2 * kStepDesc, kIdesc);
+                        mma_f8_ts_acc_if(leader, dcol, a0 + 24, b0 + 3 * kStepDesc, kIdesc);
+                        const uint32_t on1 = nb > 1 ? leader : 0u;
+                        const uint64_t b1 = bdesc0 + static_cast<uint64_t>(r1.slot()) * kTileDesc;
+                        const uint32_t a1 = tmem + kACol + r1.ab * kATileCols;
+                        mma_f8_ts_acc_if(on1, dcol, a1, b1, kIdesc);
+                        mma_f8_ts_acc_if(on1, dcol, a1 + 8, b1 + kStepDesc, kIdesc);
+                        mma_f8_ts_acc_if(on1, dcol, a1 + 16, b1 + 2 * kStepDesc, kIdesc);
+                        mma_f8_ts_acc_if(on1, dcol, a1 + 24, b1 + 3 * kStepDesc, kIdesc);
+                        mma_commit_if(leader, smem_u32(&c->mma_done[nbatch % kBatchBars]));
                     }
-                    // activation tiles of every chunk the batch enters
-#pragma unroll
-                    for (int t = 0; t < kMmaBatch; ++t)
-                        if (ok && t < nb && r[t].cp == 0)
-                            ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[r[t].q]), r[t].qph, P.wait_ns));
-                    if (!ok) {
-                        if (leader) fail(c, P.err, kErrWaitB);
-                        break;
-                    }
-                    const RingPos& rl = r[nb - 1];
-                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->a_full[rl.ab]), rl.abph, P.wait_ns));
-                    if (!ok) {
-                        if (leader) fail(c, P.err, kErrWaitAFull);
-                        break;
-                    }
-                    tc_fence_after();
-                    // chunk cc of 32 k of tile t: A columns 8*cc, B units 2cc and 2cc+1
-#pragma unroll
-                    for (int t = 0; t < kMmaBatch; ++t) {
-                        const uint32_t on = (t < nb) ? leader : 0u;
-                        const uint64_t bd = smem_desc_noswizzle(bbase + r[t].slot() * BT, kUnit, 128);
-                        const uint32_t at = tmem + kACol + r[t].ab * kATileCols;
-                        mma_f8_ts_if(on, dcol, at, bd, kIdesc, (t == 0 && e == 0) ? 0u : 1u);
-                        mma_f8_ts_if(on, dcol, at + 8, bd + ((2 * kUnit) >> 4), kIdesc, 1u);
-                        mma_f8_ts_if(on, dcol, at + 16, bd + ((4 * kUnit) >> 4), kIdesc, 1u);
-                        mma_f8_ts_if(on, dcol, at + 24, bd + ((6 * kUnit) >> 4), kIdesc, 1u);
-                    }
-                    mma_commit_if(leader, smem_u32(&c->mma_done[nbatch % kBatchBars]));
-#pragma unroll
-                    for (int t = 0; t < kMmaBatch; ++t) {
-                        const bool chunk_end = t < nb && (r[t].cp == kChunk - 1 || r[t].i == nloc - 1);
-                        mma_commit_if(chunk_end ? leader : 0u, smem_u32(&c->empty[r[t].q]));
-                    }
+                    // chunk ends inside the batch: this warp's MMAs so far read them
+                    if (rp.cp == kChunk - 1 || rp.i == nloc - 1) mma_commit_if(leader, smem_u32(&c->empty[rp.q]));
+                    if (nb > 1 && (r1.cp == kChunk - 1 || r1.i == nloc - 1)) mma_commit_if(leader, smem_u32(&c->empty[r1.q]));
                     ++nbatch;
-                    rp = rl;
+                    rp = r1;
                     rp.next(R);
                     e += nb;
                 }
                 if (!ok) break;
-                mma_commit_if(leader, smem_u32(&c->dfull[seg & 1]));
+                mma_commit_if(leader, smem_u32(&c->dfull[par][seg & 3]));
                 ++seg;
             }
             if (!ok) {
-                // tensor memory is freed at exit: first let every MMA this
-                // warp issued complete (bounded)
-                mma_commit_if(leader, smem_u32(&c->drained));
-                (void)mbar_wait_bounded(smem_u32(&c->drained), 0, 100000000ull);
+                // tensor memory is freed at exit: first let every MMA this warp
+                // issued complete (bounded)
+                mma_commit_if(leader, smem_u32(&c->drained[par]));
+                (void)mbar_wait_bounded(smem_u32(&c->drained[par]), 0, 100000000ull);
             }
         }
         __syncwarp();
@@ -856,6 +872,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
         for (int k = 0; k < kATiles; ++k) hist[k] = 0;
         int nbatch = 0;
+        int prev_ab = 0;  // A buffer of the batch's first tile
         bool first_epi = true;
         // Tensor paths: a segment's epilogue is deferred until kDeferTiles tiles
         // of the next segment are written (the accumulator is double-buffered),
@@ -881,9 +898,14 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
             for (int m = 0; m < 16; ++m) acc[m] = 0;
             if constexpr (kTC) {
-                if (alive) {
-                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->dfull[d_seg & 1]), (d_seg >> 1) & 1, P.wait_ns));
-                    if (!alive && lane == 0) fail(c, P.err, kErrWaitD);
+                // both MMA warps have finished the segment
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    if (alive) {
+                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->dfull[w][d_seg & 3]),
+                                                                          (d_seg >> 2) & 1, P.wait_ns));
+                        if (!alive && lane == 0) fail(c, P.err, kErrWaitD);
+                    }
                 }
                 if (alive) {
                     // D column m: high parts of row m; column m + kRows: low parts
@@ -948,6 +970,10 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         tc_fence_after();
                     }
                     if (alive) {
+                        // the segment's accumulator starts at zero (both MMA
+                        // warps only add); its previous use was read out by
+                        // the epilogue of the segment two back
+                        if (e == 0) tmem_st32_fill(tmem + lane_base + kAccCol + (seg_idx & 1) * 32, 0u);
                         const uint4 w0 = *reinterpret_cast<const uint4*>(wst + tid * 16);
                         const uint4 w1 = *reinterpret_cast<const uint4*>(wst + 2048 + tid * 16);
                         uint32_t r[32];  // A columns 4w + s: word w (16 k), register s
@@ -960,10 +986,16 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         unpack_word_e4m3(w1.z, r + 24);
                         unpack_word_e4m3(w1.w, r + 28);
                         tmem_st32(tmem + lane_base + kACol + ab * kATileCols, r);
-                        tc_wait_st();
-                        tc_fence_before();
-                        __syncwarp();
-                        mbar_arrive_if(lane == 0, smem_u32(&c->a_full[ab]));
+                        // one wait for the batch's stores, then both of its A
+                        // buffers are announced (the issuer waits for the last)
+                        if (e % kMmaBatch == kMmaBatch - 1 || e == len - 1) {
+                            tc_wait_st();
+                            tc_fence_before();
+                            __syncwarp();
+                            if (e % kMmaBatch != 0) mbar_arrive_if(lane == 0, smem_u32(&c->a_full[prev_ab]));
+                            mbar_arrive_if(lane == 0, smem_u32(&c->a_full[ab]));
+                        }
+                        prev_ab = ab;
                     }
                 } else {
                     if (alive) {
@@ -1072,7 +1104,7 @@ cudaError_t launch_one(const GemmParams& prm, bool pdl, cudaStream_t stream) {
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(prm.nctas), 1, 1);
-    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.blockDim = dim3(gemm_threads(PATH), 1, 1);
     cfg.dynamicSmemBytes = gemm_smem_bytes(PATH, DPR, prm.stages);
     cfg.stream = stream;
     cfg.attrs = attr;

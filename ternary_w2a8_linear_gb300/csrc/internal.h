@@ -10,7 +10,6 @@ namespace bitmtp {
 constexpr int kTileN = 128;       // out-features per row tile (= TMEM lanes)
 constexpr int kTileK = 128;       // in-features per k tile
 constexpr int kTileBytes = 4096;  // packed bytes per (row tile, k tile)
-constexpr int kGemmThreads = 192; // warps 0-3 compute + epilogue, 4 bulk copies, 5 MMA issue
 constexpr int kCtasPerSm = 2;     // persistent CTAs per SM
 
 // Compute paths.  The activation operand ("B tile", one per k tile) is laid
@@ -20,6 +19,10 @@ enum ComputePath : int {
     kPathTC8 = 1,   // tcgen05, block width 5..8:  B = 16 operand rows, 2048 B
     kPathDP = 2,    // dp4a, block width 1..4:     B = dp_rows rows of int8 codes, 128 B per row
 };
+
+// GEMM block: warps 0-3 compute + epilogue, 4 bulk copies; the tensor paths
+// add warps 5 and 6, which issue the MMAs of alternate batches.
+__host__ __device__ constexpr int gemm_threads(int path) { return path == kPathDP ? 192 : 224; }
 
 struct GemmProblem {
     const uint8_t* pk;

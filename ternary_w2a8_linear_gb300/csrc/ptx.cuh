@@ -157,6 +157,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// Store the value v into 32 consecutive 32-bit columns for this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st32_fill(uint32_t taddr, uint32_t v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"
+        :: "r"(taddr), "r"(v) : "memory");
+}
+
 // Load 16 consecutive 32-bit columns for this warp's 32 lanes.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -177,6 +185,14 @@ __device__ __forceinline__ void mma_f8_ts_if(uint32_t on, uint32_t d_tmem, uint3
                  "setp.ne.b32 g, %5, 0;\n\t"
                  "@g tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
                  :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(on) : "memory");
+}
+// The same, always accumulating into D (the caller zeroed it).
+__device__ __forceinline__ void mma_f8_ts_acc_if(uint32_t on, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc) {
+    asm volatile("{\n\t.reg .pred g;\n\t"
+                 "setp.ne.b32 g, %4, 0;\n\t"
+                 "@g tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, 1;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(on) : "memory");
 }
 // One lane of a converged warp: 1 in the elected lane, 0 elsewhere.  Single-lane
 // tcgen05 work issued from a converged warp under this predicate (no branch)

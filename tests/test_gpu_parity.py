@@ -139,6 +139,18 @@ def test_gemm_tensor_path_widths(N, K, M):
     check_gemm(T, w, x, False, "f32", PATHS["tc"])
 
 
+@pytest.mark.parametrize("K", [128, 256, 384])
+@pytest.mark.parametrize("M", [8, 16])
+def test_tensor_path_many_short_segments(K, M):
+    """One to three k tiles per row tile and several row tiles per CTA: every
+    CTA runs a run of short segments, most of them a single MMA batch, so the
+    two MMA-issuing warps take turns segment by segment and one of them passes
+    whole segments without issuing.  Exact accumulators against the oracle."""
+    N = 128 * 700 + 37
+    T, w, x = inputs.random_problem(7000 + K + M, M, N, K, p_zero=0.3, outliers=True)
+    check_gemm(T, w, x, False, "f32", PATHS["tc"])
+
+
 @pytest.mark.parametrize("path", ["tc", "dp"])
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
 def test_gemm_bf16_activations(path, out_dtype):
