@@ -347,9 +347,10 @@ __device__ __forceinline__ const char* act_row(const GemmProblem& pr, int m) {
 // sums rsp[m][0..kt] of the row's codes over k tiles, and asc[m].  Each
 // thread owns whole 16-k units; rows of up to kPass units (K <= 8192) stay in
 // registers between the absmax and the quantisation, longer rows are read
-// twice.
+// twice.  A CTA (256 threads, at most 64 registers each) fits in the
+// registers that two GEMM CTAs leave free (the GEMM's register cap).
 template <int PATH, int DPR>
-__global__ void __launch_bounds__(kPrepThreads, 4)
+__global__ void __launch_bounds__(kPrepThreads, 4)  // <= 64 registers: 16 K registers a CTA
 act_prep_kernel(const __grid_constant__ GemmParams P) {
     constexpr int kRows = btile_rows(PATH, DPR);
     constexpr int kBRows = btile_brows(PATH, DPR);
@@ -376,13 +377,14 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
 
     float v[kPrepUnits][16];
     float amax = 0.f, s = 0.f;
-    // Passes 0..npass-1 find the row's absmax, passes npass..2*npass-1
-    // quantise it (reading the row again only when it spans several passes).
-    // One loop, so that the loads are compiled once.
+    // Passes 0..npass-1 find the row's absmax; the quantisation then takes
+    // the last pass first, from the values still in registers, and reads the
+    // row again only for the earlier ones.  One loop, so that the loads are
+    // compiled once.
     for (int it = 0; it < 2 * npass; ++it) {
         const bool quant = it >= npass;
-        const int ps = quant ? it - npass : it;
-        if (!quant || npass > 1) {
+        const int ps = !quant ? it : (it == npass ? npass - 1 : it - npass - 1);
+        if (!quant || ps != npass - 1) {
 #pragma unroll
             for (int j = 0; j < kPrepUnits; ++j) {
                 const int u = ps * kPass + j * kPrepThreads + tid;
@@ -611,7 +613,7 @@ __device__ __forceinline__ int code_sum(int v, int m) {
 }
 
 template <int PATH, int DPR>
-__global__ void __launch_bounds__(gemm_threads(PATH), kCtasPerSm)
+__global__ void __maxnreg__(gemm_max_regs(PATH))
 w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr bool kTC = PATH != kPathDP;
