@@ -9,6 +9,7 @@
 
 #include "internal.h"
 #include "quant.cuh"
+#include "ptx.cuh"
 
 namespace bitmtp {
 
@@ -42,10 +43,23 @@ struct Int8Source {
     }
 };
 
-// fp32 W under the absmean scale *g: clamp(round_half_even(w / g), -1, 1)
-// with one IEEE fp32 division.
-__device__ __forceinline__ int ternary_code(float w, float g) {
-    return static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(w, g)), -1.f), 1.f));
+// fp32 W under the absmean scale g: clamp(round_half_even(RN(w / g)), -1, 1),
+// computed without the division.  With g >= 1e-5 (a normal number) h = g / 2
+// is exact, and the code is +1 exactly when w > h: for w = h the quotient is
+// 0.5, which rounds (half to even) to 0; the next float above h, h + ulp(h),
+// gives w / g = 0.5 + 2^-24 / m with m in [1, 2) the significand of h, which
+// is above the rounding midpoint 0.5 + 2^-25 and so rounds to a float above
+// 0.5, whose rint is at least 1; larger w only raise the quotient.  The
+// negative side is the mirror image.
+__device__ __forceinline__ int ternary_code(float w, float h) {
+    return (w > h ? 1 : 0) - (w < -h ? 1 : 0);
+}
+// 16-byte load with an L2 eviction-priority hint.
+__device__ __forceinline__ float4 ld_f4_hint(const float4* p, uint64_t pol) {
+    float4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p), "l"(pol));
+    return v;
 }
 struct F32Source {
     const float* W;
@@ -53,13 +67,15 @@ struct F32Source {
     const float* g;  // device scalar written by absmean_finish_kernel
     bool vec;        // W 16-byte aligned and ld a multiple of 4: float4 loads
     __device__ void load16(int n, int k0, int N, int K, int (&t)[16], int&) const {
-        const float gs = *g;
+        const float gs = 0.5f * *g;  // exact: g is normal
         const float* row = W + static_cast<long long>(n) * ld;
         if (n < N && vec && k0 + 16 <= K) {
+            // the second and last read of W (the absmean pass left it in L2)
+            const uint64_t pol = policy_evict_first();
             const float4* p = reinterpret_cast<const float4*>(row + k0);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float4 v = p[i];
+                const float4 v = ld_f4_hint(p + i, pol);
                 t[4 * i] = ternary_code(v.x, gs);
                 t[4 * i + 1] = ternary_code(v.y, gs);
                 t[4 * i + 2] = ternary_code(v.z, gs);
@@ -117,14 +133,26 @@ pack_kernel(Src src, int N, int K, int KT, uint32_t* __restrict__ pk, uint32_t* 
 constexpr int kHistBins = 512;
 constexpr int kBinOff = 128;
 constexpr int kNonFiniteBin = 511;
-constexpr int kHistMaxBlocks = 512;
+constexpr int kHistBlocksPerSm = 8;  // 8 x 256 threads: a full SM
 
-int hist_blocks(int64_t N) { return static_cast<int>(std::min<int64_t>(N, kHistMaxBlocks)); }
+// Blocks of the absmean pass: enough to fill every SM (flat walk) or one per
+// row up to that (row walk), and never fewer than keep a thread at or below
+// 2^22 entries (the accumulator bound above).
+int hist_blocks(int64_t N, int64_t K, bool flat, int sms) {
+    const int64_t full = static_cast<int64_t>(kHistBlocksPerSm) * std::max(sms, 1);
+    const int64_t per_thread_max = static_cast<int64_t>(256) << 22;
+    const int64_t min_blocks = (N * K + per_thread_max - 1) / per_thread_max;
+    const int64_t g = flat ? std::min<int64_t>(full, (N * K + 1023) / 1024) : std::min<int64_t>(N, full);
+    return static_cast<int>(std::max<int64_t>(g, min_blocks));
+}
 
-// Grid-stride over rows; vec: rows 16-byte aligned (W aligned, ldw % 4 == 0),
-// read as float4 with the row's last K % 4 entries one by one.
+// flat: W contiguous (ldw == K) and 16-byte aligned: a grid-stride walk over
+// the whole matrix as float4, the last (N * K) % 4 entries one by one.
+// Otherwise a grid-stride over rows; vec: rows 16-byte aligned (W aligned,
+// ldw % 4 == 0), read as float4 with the row's last K % 4 entries one by
+// one.  The loads ask L2 to keep W for the pack pass that reads it next.
 __global__ void __launch_bounds__(256)
-absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, bool vec,
+absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, bool flat, bool vec,
                     unsigned long long* __restrict__ gbins) {
     __shared__ unsigned long long h[kHistBins];
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = 0ull;
@@ -156,19 +184,37 @@ absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, bo
             atomicAdd(&h[e + kBinOff], m);
         }
     };
-    const int K4 = vec ? K / 4 : 0;
-    for (int n = blockIdx.x; n < N; n += gridDim.x) {
-        const float* row = W + static_cast<long long>(n) * ldw;
-        const float4* row4 = reinterpret_cast<const float4*>(row);
+    const uint64_t pol = policy_evict_last();
+    if (flat) {
+        const long long total = static_cast<long long>(N) * K;
+        const long long n4 = total / 4;
+        const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+        const long long first = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+        const float4* W4 = reinterpret_cast<const float4*>(W);
 #pragma unroll 4
-        for (int k4 = threadIdx.x; k4 < K4; k4 += blockDim.x) {
-            const float4 v = row4[k4];
+        for (long long i = first; i < n4; i += stride) {
+            const float4 v = ld_f4_hint(W4 + i, pol);
             add(v.x);
             add(v.y);
             add(v.z);
             add(v.w);
         }
-        for (int k = 4 * K4 + threadIdx.x; k < K; k += blockDim.x) add(row[k]);
+        for (long long i = 4 * n4 + first; i < total; i += stride) add(W[i]);
+    } else {
+        const int K4 = vec ? K / 4 : 0;
+        for (int n = blockIdx.x; n < N; n += gridDim.x) {
+            const float* row = W + static_cast<long long>(n) * ldw;
+            const float4* row4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 4
+            for (int k4 = threadIdx.x; k4 < K4; k4 += blockDim.x) {
+                const float4 v = ld_f4_hint(row4 + k4, pol);
+                add(v.x);
+                add(v.y);
+                add(v.z);
+                add(v.w);
+            }
+            for (int k = 4 * K4 + threadIdx.x; k < K; k += blockDim.x) add(row[k]);
+        }
     }
     if (have_base) {
         const unsigned long long piece[4] = {acc_lo & 0xFFFFFFFFull, acc_lo >> 32, acc_hi & 0xFFFFFFFFull, acc_hi >> 32};
@@ -187,45 +233,57 @@ absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, bo
 constexpr int kLimbs = 8;
 constexpr int kUnitExp = -213;
 
-__device__ void wide_add_shifted(unsigned long long (&L)[kLimbs], unsigned long long v, int sh) {
+// The limbs stay in registers: every limb index below is a compile-time
+// constant (unrolled loops with predicates; a runtime index would move the
+// array to local memory and make the one-thread sum ~10x slower).
+__device__ __forceinline__ void wide_add_shifted(unsigned long long (&L)[kLimbs], unsigned long long v, int sh) {
     const int i = sh >> 6, o = sh & 63;  // sh <= 445: i + 1 < kLimbs
     const unsigned long long lo = v << o;
     const unsigned long long hi = o ? (v >> (64 - o)) : 0ull;
-    unsigned long long s = L[i] + lo;
-    unsigned long long c = s < lo;
-    L[i] = s;
-    s = L[i + 1] + hi;
-    unsigned long long c1 = s < hi;
-    s += c;
-    c1 |= (s < c);
-    L[i + 1] = s;
-    for (int j = i + 2; c1 && j < kLimbs; ++j) {
-        L[j] += 1ull;
-        c1 = (L[j] == 0ull);
+    unsigned long long carry = 0ull;
+#pragma unroll
+    for (int j = 0; j < kLimbs; ++j) {
+        const unsigned long long add = (j == i) ? lo : (j == i + 1) ? hi : 0ull;
+        const unsigned long long s1 = L[j] + add;
+        const unsigned long long c1 = s1 < add ? 1ull : 0ull;
+        const unsigned long long s2 = s1 + carry;
+        const unsigned long long c2 = s2 < carry ? 1ull : 0ull;
+        L[j] = (j >= i) ? s2 : L[j];
+        carry = (j >= i) ? (c1 | c2) : 0ull;
     }
 }
 
-__device__ unsigned long long wide_bits(const unsigned long long (&L)[kLimbs], int pos) {  // 64 bits from pos
+// 64 bits of L from bit pos (bits past the top read as 0).
+__device__ __forceinline__ unsigned long long wide_bits(const unsigned long long (&L)[kLimbs], int pos) {
     const int i = pos >> 6, o = pos & 63;
-    unsigned long long v = L[i] >> o;
-    if (o && i + 1 < kLimbs) v |= L[i + 1] << (64 - o);
+    unsigned long long v = 0ull;
+#pragma unroll
+    for (int j = 0; j < kLimbs; ++j) {
+        if (j == i) v |= L[j] >> o;
+        if (j == i + 1 && o) v |= L[j] << (64 - o);
+    }
     return v;
 }
 
 // L * 2^kUnitExp rounded to the nearest fp64, ties to even.
-__device__ double wide_to_double(const unsigned long long (&L)[kLimbs]) {
+__device__ __forceinline__ double wide_to_double(const unsigned long long (&L)[kLimbs]) {
     int top = -1;
-    for (int j = kLimbs - 1; j >= 0 && top < 0; --j)
+#pragma unroll
+    for (int j = 0; j < kLimbs; ++j)
         if (L[j]) top = 64 * j + 63 - __clzll(static_cast<long long>(L[j]));
     if (top < 0) return 0.0;
-    if (top < 53) return ldexp(static_cast<double>(L[0]), kUnitExp);  // exact
+    if (top < 53) return __dmul_rn(static_cast<double>(L[0]), 0x1p-213);  // exact (kUnitExp = -213)
     int lo = top - 52;  // the 53 bits [lo, top]
     unsigned long long mant = wide_bits(L, lo) & ((1ull << 53) - 1ull);
-    const unsigned long long round = (L[(lo - 1) >> 6] >> ((lo - 1) & 63)) & 1ull;
+    const unsigned long long round = wide_bits(L, lo - 1) & 1ull;
     bool sticky = false;
     const int sb = lo - 1;  // bits [0, sb) below the round bit
-    for (int j = 0; j < (sb >> 6); ++j) sticky = sticky || L[j] != 0ull;
-    if (sb & 63) sticky = sticky || (L[sb >> 6] & ((1ull << (sb & 63)) - 1ull)) != 0ull;
+#pragma unroll
+    for (int j = 0; j < kLimbs; ++j) {
+        const int b0 = 64 * j;
+        if (b0 + 64 <= sb) sticky = sticky || L[j] != 0ull;
+        else if (b0 < sb) sticky = sticky || (L[j] & ((1ull << (sb - b0)) - 1ull)) != 0ull;
+    }
     if (round && (sticky || (mant & 1ull))) {
         ++mant;
         if (mant == (1ull << 53)) {
@@ -233,7 +291,11 @@ __device__ double wide_to_double(const unsigned long long (&L)[kLimbs]) {
             ++lo;
         }
     }
-    return ldexp(static_cast<double>(mant), lo + kUnitExp);  // exact: a normal fp64
+    // mant * 2^(lo + kUnitExp), a normal fp64 (mant has its top bit at 52):
+    // biased exponent lo + kUnitExp + 52 + 1023, fraction the low 52 bits
+    const long long bexp = static_cast<long long>(lo + kUnitExp + 52 + 1023);
+    return __longlong_as_double(static_cast<long long>((static_cast<unsigned long long>(bexp) << 52) |
+                                                       (mant & ((1ull << 52) - 1ull))));
 }
 
 // One block of kHistBins threads: the exact sum from the global bins,
@@ -562,14 +624,15 @@ int bitmtp_linear_ternarize_pack(const float* W, int64_t N, int64_t K, int64_t l
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int NT = static_cast<int>(ceil_div(N, kTileN));
     const int KT = static_cast<int>(ceil_div(K, kTileK));
-    const int G = hist_blocks(N);
+    const bool vec = aligned16(W) && (ldw % 4) == 0;
+    const bool flat = aligned16(W) && ldw == K;
+    const int G = hist_blocks(N, K, flat, dev->sms);
     unsigned long long* gbins = static_cast<unsigned long long*>(workspace);
     uint32_t* nonfinite = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) +
                                                       kHistBins * sizeof(unsigned long long));
-    const bool vec = aligned16(W) && (ldw % 4) == 0;
     st = cuda_status(cudaMemsetAsync(gbins, 0, kHistBins * sizeof(unsigned long long), s));
     if (st != BITMTP_OK) return st;
-    absmean_hist_kernel<<<G, 256, 0, s>>>(W, ldw, static_cast<int>(N), static_cast<int>(K), vec, gbins);
+    absmean_hist_kernel<<<G, 256, 0, s>>>(W, ldw, static_cast<int>(N), static_cast<int>(K), flat, vec, gbins);
     st = cuda_status(cudaGetLastError());
     if (st != BITMTP_OK) return st;
     uint8_t* base = static_cast<uint8_t*>(pk);

@@ -70,6 +70,50 @@ def test_ties_and_epsilon():
     _check(np.full((2, 2), 1e-7, dtype=np.float32))
 
 
+def _plant_boundaries(W: np.ndarray, g: np.float32) -> np.ndarray:
+    """Copy of W (all entries positive in the planting region) with entries at
+    and next to the code boundaries +-g/2 and +-3g/2, placed in pairs whose
+    exact sum of magnitudes is unchanged, so that mean|W| -- and g -- stay the
+    same.  Partner values are chosen so that the pair sum stays exact."""
+    W = W.copy()
+    h = np.float32(g * np.float32(0.5))
+    up, dn = np.float32(np.inf), np.float32(0.0)
+    targets = [h, np.nextafter(h, up), np.nextafter(h, dn), np.float32(3 * h),
+               np.nextafter(np.float32(3 * h), up), np.nextafter(np.float32(3 * h), dn)]
+    flat = W.reshape(-1)
+    i = 0
+    placed = 0
+    for t in targets:
+        for sign in (1, -1):
+            while True:
+                a, b = flat[i], flat[i + 1]
+                i += 2
+                tot = np.float64(abs(a)) + np.float64(abs(b))
+                rest = np.float32(tot - np.float64(t))
+                if rest > 0 and np.float64(rest) + np.float64(t) == tot:
+                    flat[i - 2] = np.float32(sign * t)
+                    flat[i - 1] = np.float32(np.sign(b) * rest) if b != 0 else rest
+                    placed += 1
+                    break
+    assert placed == 2 * len(targets)
+    return W
+
+
+def test_code_boundaries_exact():
+    """Weights exactly at +-g/2 (code 0), one ulp beyond (code +-1), one ulp
+    inside (code 0), and the same around +-3g/2 (code +-1): the packed codes
+    match the oracle's division and round-half-even byte for byte."""
+    W0 = (np.abs(np.random.default_rng(91).standard_normal((256, 512))) * 0.02 + 0.001).astype(np.float32)
+    _, g = oracle.ternarize_absmean(W0)
+    W = _plant_boundaries(W0, g)
+    T, g2 = oracle.ternarize_absmean(W)
+    assert _bits(g2) == _bits(g)
+    h = np.float32(g * np.float32(0.5))
+    assert (W == h).sum() == 1 and (W == -h).sum() == 1  # the boundaries are really there
+    assert T[W == h].tolist() == [0] and T[W == np.nextafter(h, np.float32(np.inf))].tolist() == [1]
+    _check(W)
+
+
 def test_strided_and_unaligned_rows():
     rng = np.random.default_rng(8)
     W = (rng.standard_normal((150, 300)) * 0.05).astype(np.float32)

@@ -332,3 +332,33 @@ def test_unpack_rejects_code_three():
     pk[0] = 0xFF
     with pytest.raises(ValueError):
         oracle.unpack_tiles(pk, 1, 16)
+
+
+def test_ternary_code_without_division():
+    """The device pack computes the ternary code of w under scale g (a normal
+    fp32 >= 1e-5) as (w > g/2) - (w < -g/2) instead of clamp(rint(w / g)).
+    This checks that identity against the oracle's definition (fp32 IEEE
+    division, round half to even, clamp) on random weights and on every float
+    next to the boundaries +-g/2 and +-3g/2, for many g."""
+    rng = np.random.default_rng(2024)
+    gs = np.concatenate([np.float32([1e-5, 2.0 ** -17, 1.0, 0.75, 3.0, 1e30]),
+                         (np.exp2(rng.uniform(-16, 20, 400))).astype(np.float32)])
+    for g in gs:
+        g = np.float32(g)
+        h = np.float32(g * np.float32(0.5))
+        assert np.float64(h) * 2 == np.float64(g)  # g / 2 is exact
+        pts = []
+        for c in (h, np.float32(3 * h), np.float32(g)):
+            v = c
+            lo = c
+            for _ in range(3):
+                v = np.nextafter(v, np.float32(np.inf))
+                lo = np.nextafter(lo, np.float32(0))
+                pts += [v, lo]
+            pts.append(c)
+        w = np.array(pts + [np.float32(0), np.float32(1e-45), np.float32(3e38)], dtype=np.float32)
+        w = np.concatenate([w, -w, (rng.standard_normal(2000) * g).astype(np.float32)])
+        with np.errstate(over="ignore"):
+            ref = np.clip(np.rint((w / g).astype(np.float32)), -1, 1).astype(np.int8)
+        got = (w > h).astype(np.int8) - (w < -h).astype(np.int8)
+        assert np.array_equal(got, ref), (g, w[got != ref][:4])
