@@ -510,43 +510,57 @@ def run_configs(L, torch, dev, stream, peak):
 
 def run_ternarize(L, torch, dev, stream):
     """Device absmean ternarisation + pack of the layer set's seven projections
-    from fp32 weights, through the C ABI on preallocated buffers (each call is
-    three launches and ends in a stream sync).  Algorithmic bytes: the fp32
-    weights read once plus the packed tiles written (278 MB + 17.4 MB, larger
-    than L2, so one pass over the set flushes the previous one)."""
+    from fp32 weights, through the C ABI on preallocated buffers: one grouped
+    call for the seven (four launches, one stream sync), and for comparison
+    seven single calls (each four launches and a sync).  Algorithmic bytes:
+    the fp32 weights read once plus the packed tiles written (278 MB + 17.4
+    MB, larger than L2, so one pass over the set flushes the previous one)."""
     projs = []
     for p, (_, K, N) in enumerate(inputs.BITNET2B_PROJ):
         W = torch.from_numpy(inputs.bitnet2b_dense_weights(p)).to(dev)
         nb = L.packed_bytes(N, K)
-        wb = L.bitmtp_linear_ternarize_workspace_bytes(N, K)
         projs.append((W, N, K, torch.empty(nb, dtype=torch.uint8, device=dev), nb,
-                      torch.empty(1, dtype=torch.float32, device=dev),
-                      torch.empty(wb, dtype=torch.uint8, device=dev), wb))
+                      torch.empty(1, dtype=torch.float32, device=dev)))
+    n = len(projs)
+    wb = L.bitmtp_linear_ternarize_workspace_bytes_grouped(n)
+    ws = torch.empty(wb, dtype=torch.uint8, device=dev)
+    descs = (L.TernDesc * n)(*[L.TernDesc(L._ptr(W), N, K, K, L._ptr(pk), nb, L._ptr(g))
+                                for W, N, K, pk, nb, g in projs])
+    wb1 = max(L.bitmtp_linear_ternarize_workspace_bytes(N, K) for _, N, K, _, _, _ in projs)
     torch.cuda.synchronize()
     cs = L.ctypes.c_void_p(stream.cuda_stream)
 
-    def one_pass():
-        for W, N, K, pk, nb, g, ws, wb in projs:
-            st = L.bitmtp_linear_ternarize_pack(L._ptr(W), N, K, K, L._ptr(pk), nb, L._ptr(g), L._ptr(ws), wb, cs)
+    def grouped():
+        st = L.bitmtp_linear_ternarize_pack_grouped(descs, n, L._ptr(ws), wb, cs)
+        if st != L.OK:
+            raise RuntimeError(L.status_string(st))
+
+    def singles():
+        for W, N, K, pk, nb, g in projs:
+            st = L.bitmtp_linear_ternarize_pack(L._ptr(W), N, K, K, L._ptr(pk), nb, L._ptr(g), L._ptr(ws), wb1, cs)
             if st != L.OK:
                 raise RuntimeError(L.status_string(st))
 
-    one_pass()
-    n_rep = 5
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(n_rep):
-        one_pass()
-    b.record(stream)
-    b.synchronize()
-    t = a.elapsed_time(b) / 1e3 / n_rep
     byt = ternarize_bytes()
     peak = load_peaks()[0]
-    return {"gbs": round(byt / t / 1e9, 1), "frac": round(byt / t / 1e9 / peak, 4),
-            "ms_per_layer_set": round(t * 1e3, 3), "bytes_per_layer_set": byt,
-            "gpu_launches_per_projection": 3,
-            "what": "bitmtp_linear_ternarize_pack of the 7 projections from fp32 N(0, 0.02^2) weights"}
+    res = {}
+    for name, fn in (("grouped", grouped), ("per_matrix", singles)):
+        fn()
+        n_rep = 5
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_rep):
+            fn()
+        b.record(stream)
+        b.synchronize()
+        t = a.elapsed_time(b) / 1e3 / n_rep
+        res[name] = {"gbs": round(byt / t / 1e9, 1), "frac": round(byt / t / 1e9 / peak, 4),
+                     "ms_per_layer_set": round(t * 1e3, 3)}
+    return {**res["grouped"], "per_matrix_calls": res["per_matrix"], "bytes_per_layer_set": byt,
+            "gpu_launches_per_layer_set": 3,
+            "what": "bitmtp_linear_ternarize_pack_grouped of the 7 projections from fp32 N(0, 0.02^2) weights "
+                    "(one call, one sync)"}
 
 
 def run_e2e(args, L, torch, dev, stream, large, world):

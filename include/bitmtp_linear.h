@@ -146,6 +146,34 @@ int bitmtp_linear_ternarize_pack(const float* W, int64_t N, int64_t K, int64_t l
                                  void* pk, size_t pk_bytes, float* w_scale,
                                  void* workspace, size_t ws_bytes, void* stream);
 
+/* One matrix of a grouped ternarisation (same meaning as the arguments of
+ * bitmtp_linear_ternarize_pack). */
+typedef struct bitmtp_ternarize_desc {
+    const float* W;        /* device fp32 [N][ldw], ldw >= K                        */
+    int64_t N, K, ldw;
+    void* pk;              /* device, pk_bytes >= bitmtp_linear_packed_bytes(N, K),
+                              16-byte aligned                                       */
+    size_t pk_bytes;
+    float* w_scale;        /* device float: receives gamma                          */
+} bitmtp_ternarize_desc;
+
+/* Workspace bytes for a grouped ternarisation of n_desc matrices (0 if
+ * n_desc is outside 1..BITMTP_MAX_GROUP). */
+size_t bitmtp_linear_ternarize_workspace_bytes_grouped(int n_desc);
+
+/* bitmtp_linear_ternarize_pack for up to BITMTP_MAX_GROUP matrices at once
+ * (e.g. the projections of a layer): four launches for the whole group (a
+ * memset, the absmean pass over every matrix, one scale per matrix, the pack
+ * of every tile) and one stream sync at the end.  Results are identical to
+ * calling bitmtp_linear_ternarize_pack on each matrix.  `d` is a HOST array
+ * (copied by value into the launches); the packed buffers must not overlap.
+ *   workspace  device scratch of ws_bytes >= the query above, 16-byte
+ *              aligned, need not be zeroed, left dirty
+ * Returns BITMTP_ERR_NOT_FINITE if any matrix holds a NaN or an infinity (pk
+ * and *w_scale of that matrix are then unspecified; the others are valid). */
+int bitmtp_linear_ternarize_pack_grouped(const bitmtp_ternarize_desc* d, int n_desc,
+                                         void* workspace, size_t ws_bytes, void* stream);
+
 /* Quantise a block of activation rows to int8 codes with per-row scales
  * (the quantiser defined at the top of this file).
  *   x        device [M][ldx], element kind x_kind = BITMTP_F32 or BITMTP_BF16,

@@ -89,12 +89,10 @@ struct F32Source {
     }
 };
 
-// Grid (KT, NT); each block writes one 4 KiB tile, each thread four words.
+// One 4 KiB tile (row tile rt, k tile kt) by one block, four words a thread.
 template <class Src>
-__global__ void __launch_bounds__(256)
-pack_kernel(Src src, int N, int K, int KT, uint32_t* __restrict__ pk, uint32_t* __restrict__ invalid) {
-    const int kt = blockIdx.x;
-    const int rt = blockIdx.y;
+__device__ __forceinline__ void pack_tile(const Src& src, int N, int K, int KT, int rt, int kt,
+                                          uint32_t* __restrict__ pk, uint32_t* __restrict__ invalid) {
     uint32_t* tile = pk + (static_cast<size_t>(rt) * KT + kt) * (kTileBytes / 4);
     int bad = 0;
     for (int widx = threadIdx.x; widx < kTileBytes / 4; widx += blockDim.x) {
@@ -113,6 +111,33 @@ pack_kernel(Src src, int N, int K, int KT, uint32_t* __restrict__ pk, uint32_t* 
     for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
     if ((threadIdx.x & 31) == 0 && bad) atomicAdd(invalid, static_cast<uint32_t>(bad));
 }
+
+// Grid (KT, NT): the int8 pack.
+template <class Src>
+__global__ void __launch_bounds__(256)
+pack_kernel(Src src, int N, int K, int KT, uint32_t* __restrict__ pk, uint32_t* __restrict__ invalid) {
+    pack_tile(src, N, K, KT, static_cast<int>(blockIdx.y), static_cast<int>(blockIdx.x), pk, invalid);
+}
+
+// A group of fp32 matrices to ternarise: per matrix its absmean blocks and
+// pack tiles occupy consecutive ranges of the two grids.
+struct TernMat {
+    const float* W;
+    long long ldw;
+    int N, K, KT;
+    int flat, vec;
+    int blk_begin, blocks;  // absmean pass
+    int tile_begin;         // pack pass: tiles tile_begin .. + NT * KT - 1
+    uint32_t* pk;
+    uint32_t* trailer;      // the packed buffer's last 16 bytes
+    float* w_scale;
+};
+struct TernParams {
+    TernMat m[BITMTP_MAX_GROUP];
+    int n;
+    unsigned long long* bins;  // [n][kHistBins]
+    uint32_t* nonfinite;       // [n]
+};
 
 // --------------------------------------------------- absmean ternarisation --
 // mean|W| is the exact sum of |W| rounded once to fp64, divided by the count
@@ -135,15 +160,21 @@ constexpr int kBinOff = 128;
 constexpr int kNonFiniteBin = 511;
 constexpr int kHistBlocksPerSm = 8;  // 8 x 256 threads: a full SM
 
-// Blocks of the absmean pass: enough to fill every SM (flat walk) or one per
-// row up to that (row walk), and never fewer than keep a thread at or below
-// 2^22 entries (the accumulator bound above).
-int hist_blocks(int64_t N, int64_t K, bool flat, int sms) {
+// Blocks of the absmean pass for a matrix of N x K entries out of `total`
+// entries in the group: the larger of its share of one full wave
+// (kHistBlocksPerSm blocks on every SM) and one block per 64 K entries up to
+// a full wave; at least one, at most one per row on the row walk, and never
+// fewer than keep a thread at or below 2^22 entries (the accumulator bound
+// above).
+int hist_blocks(int64_t N, int64_t K, int64_t total, bool flat, int sms) {
     const int64_t full = static_cast<int64_t>(kHistBlocksPerSm) * std::max(sms, 1);
     const int64_t per_thread_max = static_cast<int64_t>(256) << 22;
     const int64_t min_blocks = (N * K + per_thread_max - 1) / per_thread_max;
-    const int64_t g = flat ? std::min<int64_t>(full, (N * K + 1023) / 1024) : std::min<int64_t>(N, full);
-    return static_cast<int>(std::max<int64_t>(g, min_blocks));
+    const int64_t share = (full * N * K + total - 1) / total;
+    int64_t g = std::max<int64_t>(std::max<int64_t>(share, std::min<int64_t>(full, (N * K + 65535) / 65536)), 1);
+    g = std::min<int64_t>(g, (N * K + 1023) / 1024);  // at least 4 entries a thread
+    if (!flat) g = std::min<int64_t>(g, N);
+    return static_cast<int>(std::max<int64_t>(std::max<int64_t>(g, min_blocks), 1));
 }
 
 // flat: W contiguous (ldw == K) and 16-byte aligned: a grid-stride walk over
@@ -152,8 +183,19 @@ int hist_blocks(int64_t N, int64_t K, bool flat, int sms) {
 // ldw % 4 == 0), read as float4 with the row's last K % 4 entries one by
 // one.  The loads ask L2 to keep W for the pack pass that reads it next.
 __global__ void __launch_bounds__(256)
-absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, bool flat, bool vec,
-                    unsigned long long* __restrict__ gbins) {
+absmean_hist_kernel(const __grid_constant__ TernParams P) {
+    int mi = 0;
+#pragma unroll 1
+    for (int i = 1; i < P.n; ++i)
+        if (static_cast<int>(blockIdx.x) >= P.m[i].blk_begin) mi = i;
+    const TernMat& mt = P.m[mi];
+    const float* __restrict__ W = mt.W;
+    const long long ldw = mt.ldw;
+    const int N = mt.N, K = mt.K;
+    const bool flat = mt.flat != 0, vec = mt.vec != 0;
+    const int blk = static_cast<int>(blockIdx.x) - mt.blk_begin;  // block within the matrix
+    const int nblk = mt.blocks;
+    unsigned long long* __restrict__ gbins = P.bins + static_cast<size_t>(mi) * kHistBins;
     __shared__ unsigned long long h[kHistBins];
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = 0ull;
     __syncthreads();
@@ -188,8 +230,8 @@ absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, bo
     if (flat) {
         const long long total = static_cast<long long>(N) * K;
         const long long n4 = total / 4;
-        const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-        const long long first = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+        const long long stride = static_cast<long long>(nblk) * blockDim.x;
+        const long long first = static_cast<long long>(blk) * blockDim.x + threadIdx.x;
         const float4* W4 = reinterpret_cast<const float4*>(W);
 #pragma unroll 4
         for (long long i = first; i < n4; i += stride) {
@@ -202,7 +244,7 @@ absmean_hist_kernel(const float* __restrict__ W, long long ldw, int N, int K, bo
         for (long long i = 4 * n4 + first; i < total; i += stride) add(W[i]);
     } else {
         const int K4 = vec ? K / 4 : 0;
-        for (int n = blockIdx.x; n < N; n += gridDim.x) {
+        for (int n = blk; n < N; n += nblk) {
             const float* row = W + static_cast<long long>(n) * ldw;
             const float4* row4 = reinterpret_cast<const float4*>(row);
 #pragma unroll 4
@@ -302,11 +344,14 @@ __device__ __forceinline__ double wide_to_double(const unsigned long long (&L)[k
 // gamma = max(RN32(RN64(sum) / count), 1e-5) into *w_scale, the non-finite
 // flag, and the packed buffer's trailer {magic, N, K, 0}.
 __global__ void __launch_bounds__(kHistBins)
-absmean_finish_kernel(const unsigned long long* __restrict__ gbins, int N, int K, float* __restrict__ w_scale,
-                      uint32_t* __restrict__ nonfinite, uint32_t* __restrict__ trailer) {
+absmean_finish_kernel(const __grid_constant__ TernParams P) {
+    const int mi = static_cast<int>(blockIdx.x);
+    const TernMat& mt = P.m[mi];
+    const int N = mt.N, K = mt.K;
+    uint32_t* __restrict__ trailer = mt.trailer;
     __shared__ unsigned long long H[kHistBins];
     const int e = threadIdx.x;
-    H[e] = gbins[e];
+    H[e] = P.bins[static_cast<size_t>(mi) * kHistBins + e];
     __syncthreads();
     if (e == 0) {
         unsigned long long L[kLimbs] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
@@ -314,13 +359,27 @@ absmean_finish_kernel(const unsigned long long* __restrict__ gbins, int N, int K
             if (H[j]) wide_add_shifted(L, H[j], j - 65);
         const long long count = static_cast<long long>(N) * K;
         const double mean = __ddiv_rn(wide_to_double(L), static_cast<double>(count));
-        *w_scale = fmaxf(__double2float_rn(mean), 1e-5f);
-        *nonfinite = H[kNonFiniteBin] ? 1u : 0u;
+        *mt.w_scale = fmaxf(__double2float_rn(mean), 1e-5f);
+        P.nonfinite[mi] = H[kNonFiniteBin] ? 1u : 0u;
         trailer[0] = kTrailerMagic;
         trailer[1] = static_cast<uint32_t>(N);
         trailer[2] = static_cast<uint32_t>(K);
         trailer[3] = 0u;
     }
+}
+
+// The fp32 pack of every tile of the group: block b is tile b - tile_begin of
+// the matrix holding it.
+__global__ void __launch_bounds__(256)
+tern_pack_kernel(const __grid_constant__ TernParams P) {
+    int mi = 0;
+#pragma unroll 1
+    for (int i = 1; i < P.n; ++i)
+        if (static_cast<int>(blockIdx.x) >= P.m[i].tile_begin) mi = i;
+    const TernMat& mt = P.m[mi];
+    const int t = static_cast<int>(blockIdx.x) - mt.tile_begin;
+    pack_tile(F32Source{mt.W, mt.ldw, mt.w_scale, mt.vec != 0}, mt.N, mt.K, mt.KT, t / mt.KT, t % mt.KT, mt.pk,
+              mt.trailer + 3);
 }
 
 // ------------------------------------------------------------ quant_act --
@@ -608,7 +667,80 @@ int bitmtp_linear_pack(const int8_t* T, int64_t N, int64_t K, int64_t ldt, void*
 
 size_t bitmtp_linear_ternarize_workspace_bytes(int64_t N, int64_t K) {
     if (N < 1 || K < 1 || N > BITMTP_MAX_N || K > BITMTP_MAX_K) return 0;
-    return kHistBins * sizeof(unsigned long long) + 256;  // the bins, then the non-finite flag
+    return bitmtp_linear_ternarize_workspace_bytes_grouped(1);
+}
+
+size_t bitmtp_linear_ternarize_workspace_bytes_grouped(int n_desc) {
+    if (n_desc < 1 || n_desc > BITMTP_MAX_GROUP) return 0;
+    // the bins of each matrix, then one non-finite flag per matrix
+    return static_cast<size_t>(n_desc) * kHistBins * sizeof(unsigned long long) + 256;
+}
+
+int bitmtp_linear_ternarize_pack_grouped(const bitmtp_ternarize_desc* d, int n_desc, void* workspace,
+                                         size_t ws_bytes, void* stream) {
+    if (!d || n_desc < 1 || n_desc > BITMTP_MAX_GROUP) return BITMTP_ERR_INVALID;
+    if (!workspace) return BITMTP_ERR_INVALID;
+    if (!aligned16(workspace)) return BITMTP_ERR_ALIGN;
+    if (ws_bytes < bitmtp_linear_ternarize_workspace_bytes_grouped(n_desc)) return BITMTP_ERR_SHAPE;
+    for (int i = 0; i < n_desc; ++i) {  // every argument check before any CUDA call
+        const bitmtp_ternarize_desc& g = d[i];
+        if (g.N < 1 || g.K < 1 || g.N > BITMTP_MAX_N || g.K > BITMTP_MAX_K) return BITMTP_ERR_SHAPE;
+        if (!g.W || !g.pk || !g.w_scale || g.ldw < g.K) return BITMTP_ERR_INVALID;
+        if (!aligned16(g.pk)) return BITMTP_ERR_ALIGN;
+        if (g.pk_bytes < bitmtp_linear_packed_bytes(g.N, g.K)) return BITMTP_ERR_SHAPE;
+    }
+    DevInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != BITMTP_OK) return st;
+    TernParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.n = n_desc;
+    P.bins = static_cast<unsigned long long*>(workspace);
+    P.nonfinite = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) +
+                                              static_cast<size_t>(n_desc) * kHistBins * sizeof(unsigned long long));
+    long long blocks = 0, tiles = 0, total = 0;
+    for (int i = 0; i < n_desc; ++i) total += d[i].N * d[i].K;
+    for (int i = 0; i < n_desc; ++i) {
+        const bitmtp_ternarize_desc& g = d[i];
+        const size_t need = bitmtp_linear_packed_bytes(g.N, g.K);
+        TernMat& m = P.m[i];
+        m.W = g.W;
+        m.ldw = g.ldw;
+        m.N = static_cast<int>(g.N);
+        m.K = static_cast<int>(g.K);
+        m.KT = static_cast<int>(ceil_div(g.K, kTileK));
+        m.vec = aligned16(g.W) && (g.ldw % 4) == 0;
+        m.flat = aligned16(g.W) && g.ldw == g.K;
+        m.blk_begin = static_cast<int>(blocks);
+        m.blocks = hist_blocks(g.N, g.K, total, m.flat != 0, dev->sms);
+        m.tile_begin = static_cast<int>(tiles);
+        m.pk = static_cast<uint32_t*>(g.pk);
+        m.trailer = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(g.pk) + need - 16);
+        m.w_scale = g.w_scale;
+        blocks += m.blocks;
+        tiles += ceil_div(g.N, kTileN) * m.KT;
+        if (blocks > INT32_MAX || tiles > INT32_MAX) return BITMTP_ERR_SHAPE;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = cuda_status(cudaMemsetAsync(workspace, 0, bitmtp_linear_ternarize_workspace_bytes_grouped(n_desc), s));
+    if (st != BITMTP_OK) return st;
+    absmean_hist_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(P);
+    st = cuda_status(cudaGetLastError());
+    if (st != BITMTP_OK) return st;
+    absmean_finish_kernel<<<n_desc, kHistBins, 0, s>>>(P);
+    st = cuda_status(cudaGetLastError());
+    if (st != BITMTP_OK) return st;
+    tern_pack_kernel<<<static_cast<unsigned>(tiles), 256, 0, s>>>(P);
+    st = cuda_status(cudaGetLastError());
+    if (st != BITMTP_OK) return st;
+    uint32_t bad[BITMTP_MAX_GROUP] = {0};
+    st = cuda_status(cudaMemcpyAsync(bad, P.nonfinite, sizeof(uint32_t) * n_desc, cudaMemcpyDeviceToHost, s));
+    if (st != BITMTP_OK) return st;
+    st = cuda_status(cudaStreamSynchronize(s));
+    if (st != BITMTP_OK) return st;
+    for (int i = 0; i < n_desc; ++i)
+        if (bad[i]) return BITMTP_ERR_NOT_FINITE;
+    return BITMTP_OK;
 }
 
 int bitmtp_linear_ternarize_pack(const float* W, int64_t N, int64_t K, int64_t ldw, void* pk, size_t pk_bytes,
@@ -616,42 +748,10 @@ int bitmtp_linear_ternarize_pack(const float* W, int64_t N, int64_t K, int64_t l
     if (N < 1 || K < 1 || N > BITMTP_MAX_N || K > BITMTP_MAX_K) return BITMTP_ERR_SHAPE;
     if (!W || !pk || !w_scale || !workspace || ldw < K) return BITMTP_ERR_INVALID;
     if (!aligned16(pk) || !aligned16(workspace)) return BITMTP_ERR_ALIGN;
-    const size_t need = bitmtp_linear_packed_bytes(N, K);
-    if (pk_bytes < need || ws_bytes < bitmtp_linear_ternarize_workspace_bytes(N, K)) return BITMTP_ERR_SHAPE;
-    DevInfo* dev = nullptr;
-    int st = current_device(&dev);
-    if (st != BITMTP_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int NT = static_cast<int>(ceil_div(N, kTileN));
-    const int KT = static_cast<int>(ceil_div(K, kTileK));
-    const bool vec = aligned16(W) && (ldw % 4) == 0;
-    const bool flat = aligned16(W) && ldw == K;
-    const int G = hist_blocks(N, K, flat, dev->sms);
-    unsigned long long* gbins = static_cast<unsigned long long*>(workspace);
-    uint32_t* nonfinite = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) +
-                                                      kHistBins * sizeof(unsigned long long));
-    st = cuda_status(cudaMemsetAsync(gbins, 0, kHistBins * sizeof(unsigned long long), s));
-    if (st != BITMTP_OK) return st;
-    absmean_hist_kernel<<<G, 256, 0, s>>>(W, ldw, static_cast<int>(N), static_cast<int>(K), flat, vec, gbins);
-    st = cuda_status(cudaGetLastError());
-    if (st != BITMTP_OK) return st;
-    uint8_t* base = static_cast<uint8_t*>(pk);
-    uint32_t* trailer = reinterpret_cast<uint32_t*>(base + need - 16);
-    absmean_finish_kernel<<<1, kHistBins, 0, s>>>(gbins, static_cast<int>(N), static_cast<int>(K), w_scale,
-                                                  nonfinite, trailer);
-    st = cuda_status(cudaGetLastError());
-    if (st != BITMTP_OK) return st;
-    pack_kernel<F32Source><<<dim3(KT, NT), 256, 0, s>>>(F32Source{W, ldw, w_scale, vec}, static_cast<int>(N),
-                                                        static_cast<int>(K), KT,
-                                                        reinterpret_cast<uint32_t*>(base), trailer + 3);
-    st = cuda_status(cudaGetLastError());
-    if (st != BITMTP_OK) return st;
-    uint32_t bad = 0;
-    st = cuda_status(cudaMemcpyAsync(&bad, nonfinite, 4, cudaMemcpyDeviceToHost, s));
-    if (st != BITMTP_OK) return st;
-    st = cuda_status(cudaStreamSynchronize(s));
-    if (st != BITMTP_OK) return st;
-    return bad ? BITMTP_ERR_NOT_FINITE : BITMTP_OK;
+    if (pk_bytes < bitmtp_linear_packed_bytes(N, K) || ws_bytes < bitmtp_linear_ternarize_workspace_bytes(N, K))
+        return BITMTP_ERR_SHAPE;
+    const bitmtp_ternarize_desc d = {W, N, K, ldw, pk, pk_bytes, w_scale};
+    return bitmtp_linear_ternarize_pack_grouped(&d, 1, workspace, ws_bytes, stream);
 }
 
 int bitmtp_linear_quant_act(const void* x, int x_kind, int64_t M, int64_t K, int64_t ldx, int8_t* q,

@@ -46,6 +46,11 @@ class Out(ctypes.Structure):
                 ("acc", ctypes.c_void_p), ("lda", ctypes.c_int64)]
 
 
+class TernDesc(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("ldw", ctypes.c_int64),
+                ("pk", ctypes.c_void_p), ("pk_bytes", ctypes.c_size_t), ("w_scale", ctypes.c_void_p)]
+
+
 class GemmDesc(ctypes.Structure):
     _fields_ = [("pk", ctypes.c_void_p), ("w_scale", ctypes.c_float), ("N", ctypes.c_int64),
                 ("K", ctypes.c_int64), ("M", ctypes.c_int64), ("act", Act), ("out", Out)]
@@ -72,6 +77,9 @@ def load() -> ctypes.CDLL:
         "bitmtp_linear_ternarize_pack": (c.c_int, [c.c_void_p, c.c_int64, c.c_int64, c.c_int64, c.c_void_p,
                                                    c.c_size_t, c.c_void_p, c.c_void_p, c.c_size_t,
                                                    c.c_void_p]),
+        "bitmtp_linear_ternarize_workspace_bytes_grouped": (c.c_size_t, [c.c_int]),
+        "bitmtp_linear_ternarize_pack_grouped": (c.c_int, [c.POINTER(TernDesc), c.c_int, c.c_void_p, c.c_size_t,
+                                                           c.c_void_p]),
         "bitmtp_linear_quant_act": (c.c_int, [c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_int64,
                                               c.c_void_p, c.c_int64, c.c_void_p, c.c_void_p, c.c_void_p]),
         "bitmtp_linear_workspace_bytes": (c.c_size_t, [c.c_int64, c.c_int64, c.c_int64]),
@@ -254,6 +262,40 @@ def ternarize_pack(W: torch.Tensor, stream=None):
     _check(bitmtp_linear_ternarize_pack(_ptr(W), N, K, ldw, _ptr(pk), nb, _ptr(g), _ptr(ws), wb, _stream(stream)),
            "ternarize_pack")
     return pk, float(g.item())
+
+
+def bitmtp_linear_ternarize_workspace_bytes_grouped(n_desc: int) -> int:
+    return int(load().bitmtp_linear_ternarize_workspace_bytes_grouped(n_desc))
+
+
+def bitmtp_linear_ternarize_pack_grouped(descs, n_desc, ws_ptr, ws_bytes, stream) -> int:
+    return load().bitmtp_linear_ternarize_pack_grouped(descs, n_desc, ws_ptr, ws_bytes, stream)
+
+
+def ternarize_pack_grouped(Ws, stream=None):
+    """ternarize_pack of several fp32 weight matrices in one grouped call
+    (four launches, one sync) -> list of (packed uint8 buffer, w_scale)."""
+    n = len(Ws)
+    wb = bitmtp_linear_ternarize_workspace_bytes_grouped(n)
+    if wb == 0:
+        raise BitmtpError(ERR_INVALID, "ternarize_pack_grouped")
+    outs, descs = [], []
+    for W in Ws:
+        if W.dtype != torch.float32 or not W.is_cuda:
+            raise TypeError("W must be a CUDA float32 tensor")
+        N, K = W.shape
+        ldw = _rowmajor(W, "W")
+        nb = packed_bytes(N, K)
+        if nb == 0:
+            raise BitmtpError(ERR_SHAPE, "ternarize_pack_grouped")
+        pk = torch.empty(nb, dtype=torch.uint8, device=W.device)
+        g = torch.empty(1, dtype=torch.float32, device=W.device)
+        outs.append((pk, g))
+        descs.append(TernDesc(_ptr(W), N, K, ldw, _ptr(pk), nb, _ptr(g)))
+    ws = torch.empty(wb, dtype=torch.uint8, device=Ws[0].device)
+    arr = (TernDesc * n)(*descs)
+    _check(bitmtp_linear_ternarize_pack_grouped(arr, n, _ptr(ws), wb, _stream(stream)), "ternarize_pack_grouped")
+    return [(pk, float(g.item())) for pk, g in outs]
 
 
 def quant_act(x: torch.Tensor, stream=None):

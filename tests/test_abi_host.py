@@ -28,6 +28,7 @@ def test_exports_every_header_symbol(lib):
         "bitmtp_linear_status_string", "bitmtp_linear_version", "bitmtp_linear_workspace_bytes",
         "bitmtp_linear_workspace_bytes_grouped", "bitmtp_linear_gemm_noalloc",
         "bitmtp_linear_ternarize_workspace_bytes", "bitmtp_linear_ternarize_pack",
+        "bitmtp_linear_ternarize_workspace_bytes_grouped", "bitmtp_linear_ternarize_pack_grouped",
     }
     for s in syms:
         assert hasattr(lib, s), s
@@ -83,6 +84,37 @@ def test_ternarize_validation(lib):
     assert call(pk_bytes=nb - 1) == L.ERR_SHAPE
     assert call(ws_bytes=wb(64, 64) - 1) == L.ERR_SHAPE
     assert "NaN" in L.status_string(L.ERR_NOT_FINITE)
+
+
+def test_ternarize_grouped_validation(lib):
+    """Argument checks of the grouped ternarisation, all before any CUDA call."""
+    wbg = L.bitmtp_linear_ternarize_workspace_bytes_grouped
+    assert wbg(0) == 0 and wbg(L.MAX_GROUP + 1) == 0
+    assert wbg(1) == L.bitmtp_linear_ternarize_workspace_bytes(64, 64)
+    assert wbg(7) == 7 * 512 * 8 + 256
+    nb = L.packed_bytes(64, 64)
+
+    def call(n=2, ws=FAKE, ws_bytes=None, **kw):
+        base = dict(W=FAKE, N=64, K=64, ldw=64, pk=FAKE, pk_bytes=nb, w_scale=FAKE)
+        descs = [L.TernDesc(**base) for _ in range(n)]
+        for k, v in kw.items():
+            setattr(descs[-1], k, v)
+        arr = (L.TernDesc * max(n, 1))(*descs) if n else None
+        return L.bitmtp_linear_ternarize_pack_grouped(arr, n, ws, wbg(max(n, 1)) if ws_bytes is None else ws_bytes,
+                                                      None)
+
+    assert call(n=0) == L.ERR_INVALID
+    assert call(n=L.MAX_GROUP + 1) == L.ERR_INVALID
+    assert call(ws=None) == L.ERR_INVALID
+    assert call(ws=FAKE + 4) == L.ERR_ALIGN
+    assert call(ws_bytes=wbg(2) - 1) == L.ERR_SHAPE
+    assert call(N=0) == L.ERR_SHAPE
+    assert call(K=L.MAX_K + 1) == L.ERR_SHAPE
+    assert call(W=None) == L.ERR_INVALID
+    assert call(w_scale=None) == L.ERR_INVALID
+    assert call(ldw=63) == L.ERR_INVALID
+    assert call(pk=FAKE + 8) == L.ERR_ALIGN
+    assert call(pk_bytes=nb - 1) == L.ERR_SHAPE
 
 
 def test_packed_bytes_rejects(lib):

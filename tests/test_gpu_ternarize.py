@@ -114,6 +114,55 @@ def test_code_boundaries_exact():
     _check(W)
 
 
+def test_grouped_matches_oracle_per_matrix():
+    """One grouped call over matrices of different shapes and layouts (flat,
+    strided, unaligned rows, ragged tiles) gives every matrix's oracle scale and
+    packing."""
+    rng = np.random.default_rng(31)
+    shapes = [(640, 2560), (130, 129), (300, 1000), (257, 4097), (1, 1), (64, 128), (1000, 300)]
+    Ws, devs = [], []
+    for i, (N, K) in enumerate(shapes):
+        W = (rng.standard_normal((N, K)) * (0.01 + 0.01 * i)).astype(np.float32)
+        Ws.append(W)
+        if i == 2:  # strided rows, 16-byte aligned
+            big = dev_tensor(np.zeros((N, K + 4), dtype=np.float32))
+            big[:, :K] = dev_tensor(W)
+            devs.append(big[:, :K])
+        elif i == 3:  # odd row pitch
+            big = dev_tensor(np.zeros((N, K + 1), dtype=np.float32))
+            big[:, :K] = dev_tensor(W)
+            devs.append(big[:, :K])
+        else:
+            devs.append(dev_tensor(W))
+    out = L.ternarize_pack_grouped(devs)
+    for W, (pk, g) in zip(Ws, out):
+        T_ref, g_ref = oracle.ternarize_absmean(W)
+        assert _bits(g) == _bits(g_ref)
+        assert np.array_equal(pk.cpu().numpy(), oracle.pack_tiles(T_ref))
+
+
+def test_grouped_non_finite_in_one_matrix():
+    """A NaN in one matrix of the group is reported; the other matrices are
+    still packed exactly."""
+    rng = np.random.default_rng(32)
+    Ws = [(rng.standard_normal((200, 333)) * 0.02).astype(np.float32) for _ in range(3)]
+    Ws[1][17, 5] = np.nan
+    devs = [dev_tensor(W) for W in Ws]
+    N, K = Ws[0].shape
+    nb = L.packed_bytes(N, K)
+    outs = [(torch.empty(nb, dtype=torch.uint8, device="cuda"), torch.empty(1, dtype=torch.float32, device="cuda"))
+            for _ in Ws]
+    descs = [L.TernDesc(L._ptr(W), N, K, K, L._ptr(pk), nb, L._ptr(g)) for W, (pk, g) in zip(devs, outs)]
+    wb = L.bitmtp_linear_ternarize_workspace_bytes_grouped(3)
+    ws = torch.empty(wb, dtype=torch.uint8, device="cuda")
+    st = L.bitmtp_linear_ternarize_pack_grouped((L.TernDesc * 3)(*descs), 3, L._ptr(ws), wb, L._stream(None))
+    assert st == L.ERR_NOT_FINITE
+    for i in (0, 2):
+        T_ref, g_ref = oracle.ternarize_absmean(Ws[i])
+        assert _bits(outs[i][1].item()) == _bits(g_ref)
+        assert np.array_equal(outs[i][0].cpu().numpy(), oracle.pack_tiles(T_ref))
+
+
 def test_strided_and_unaligned_rows():
     rng = np.random.default_rng(8)
     W = (rng.standard_normal((150, 300)) * 0.05).astype(np.float32)
