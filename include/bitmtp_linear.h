@@ -195,6 +195,11 @@ typedef struct bitmtp_act {
     const void* x;         /* [M][ldx] elements of `kind` (int8 for BITMTP_Q8)        */
     int64_t ldx;           /* >= K                                                   */
     const float* a_scale;  /* BITMTP_Q8 only: [M] per-row scales; ignored otherwise   */
+    const float* amax;     /* optional, BITMTP_F32/BF16 only (NULL otherwise): device
+                              [M] = max_k |x[m][k]| of exactly these rows, e.g. the
+                              amax output of the GEMM that wrote x (a layer chain);
+                              the preparation then skips its own absmax pass.  Any
+                              other value gives wrong codes.                        */
 } bitmtp_act;
 
 /* Output of a GEMM. */
@@ -204,6 +209,13 @@ typedef struct bitmtp_out {
     int64_t ldy;           /* >= N                                                  */
     int32_t* acc;          /* optional int32 [M][lda] accumulators, may be NULL     */
     int64_t lda;           /* >= N when acc != NULL                                  */
+    float* amax;           /* optional device [M]: receives max_n |y[m][n]| of the
+                              values stored (after the bf16 rounding for BITMTP_BF16),
+                              ready to be the next call's act.amax; the call's first
+                              launch zeroes it, its epilogues combine per-CTA maxima
+                              with atomics (the first phase of a two-phase row
+                              absmax, the next call's preparation the second).  Must
+                              not overlap y, acc or this call's act.amax.           */
 } bitmtp_out;
 
 /* Workspace of a GEMM call: a device buffer the caller allocates once,

@@ -36,7 +36,8 @@ own internal layout, not the pages'; it is restated here from its written
 definition so that the device pack kernel can be checked byte for byte.
 
 Precision: the quantiser is fp32 (the specification fixes it); accumulation is
-exact int64; dequant is fp64 then rounded to fp32.
+exact int64; dequant is fp64 then rounded to fp32 (``dequant``), or, inside a
+layer chain, two fp32 roundings in a fixed order (``dequant_chain``).
 """
 from __future__ import annotations
 
@@ -171,6 +172,49 @@ def w2a8_linear(T, w_scale, x, out: str = "f32", x_is_bf16: bool = False):
     q, a_scale, rowsum = quant_act_bf16(x) if x_is_bf16 else quant_act(x)
     acc = gemm_acc(T, q)
     return dequant(acc, a_scale, w_scale, out), acc, q, a_scale, rowsum
+
+
+# ---------------------------------------------------------------------------
+# Layer chain: the output of one linear is the input of the next.  The next
+# layer's codes are decided on the stored output values, so a chain needs one
+# fixed dequant order on both sides; the pages fix none.  Reading taken:
+# y = RN32(RN32(acc * a_scale) * w_scale), then RN to bf16 for bf16 output
+# (the single fp64 rounding of ``dequant`` can differ from this by one fp32
+# ulp, which can move a code of the next layer).  The stored output's row
+# absmax is the next layer's amax.
+# ---------------------------------------------------------------------------
+def dequant_chain(acc: np.ndarray, a_scale: np.ndarray, w_scale, out: str = "f32") -> np.ndarray:
+    """y[m, n] = RN32(RN32(acc[m, n] * a_scale[m]) * w_scale) (fp32 IEEE
+    products; acc is exact in fp32); ``out="bf16"`` rounds that to bf16 and
+    returns uint16 bit patterns."""
+    acc = np.asarray(acc, dtype=np.int64)
+    if acc.size and np.abs(acc).max() >= 2 ** 24:
+        raise OverflowError("accumulator not exact in fp32")
+    t = (acc.astype(F32) * np.asarray(a_scale, dtype=F32)[:, None]).astype(F32)
+    y32 = (t * F32(w_scale)).astype(F32)
+    if out == "f32":
+        return y32
+    if out == "bf16":
+        return f32_to_bf16_bits(y32)
+    raise ValueError(f"unknown output dtype {out!r}")
+
+
+def linear_chain(layers, x0: np.ndarray, out: str = "f32", x0_is_bf16: bool = False):
+    """Run the linears (T, w_scale) of ``layers`` one after another, each on
+    the previous one's stored output (fp32, or bf16 bit patterns for
+    ``out="bf16"``).  Returns one dict per layer: y (as stored), acc, q,
+    a_scale and amax (max_n |y[m, n]| of the stored values, fp32)."""
+    x, is_bf16 = x0, x0_is_bf16
+    res = []
+    for T, w_scale in layers:
+        q, a_scale, _ = quant_act_bf16(x) if is_bf16 else quant_act(x)
+        acc = gemm_acc(T, q)
+        y = dequant_chain(acc, a_scale, w_scale, out)
+        yf = bf16_bits_to_f32(y) if out == "bf16" else y
+        amax = np.max(np.abs(yf), axis=1).astype(F32) if yf.shape[1] else np.zeros(yf.shape[0], F32)
+        res.append(dict(y=y, acc=acc, q=q, a_scale=a_scale, amax=amax))
+        x, is_bf16 = y, out == "bf16"
+    return res
 
 
 # ---------------------------------------------------------------------------

@@ -513,6 +513,8 @@ int check_problem(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M
     g->kt = static_cast<int>(ceil_div(K, kTileK));
     g->act_kind = act->kind;
     g->out_dtype = out->dtype;
+    g->amax_in = act->kind == BITMTP_Q8 ? nullptr : act->amax;
+    g->amax_out = out->amax;
     const int64_t esize = act->kind == BITMTP_F32 ? 4 : (act->kind == BITMTP_BF16 ? 2 : 1);
     g->vec_ok = (aligned16(act->x) && (act->ldx * esize) % 16 == 0) ? 1 : 0;
     return BITMTP_OK;

@@ -82,7 +82,7 @@ namespace {
 
 constexpr int kChunk = 4;            // k tiles per ring chunk (16 KiB of weights)
 constexpr int kMaxRing = 6;          // chunks in the ring (upper bound)
-constexpr int kCtrlBytes = 2048;
+constexpr int kCtrlBytes = 2304;
 constexpr int kBarEpi = 1;           // named barrier: the four consumer warps
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kAccCol = 0;      // D: two accumulators (alternate segments) of 32 fp32 columns
@@ -92,7 +92,7 @@ constexpr int kATiles = 6;
 constexpr int kDeferTiles = 5;       // a segment's epilogue runs this many tiles into the next one
 constexpr int kMmaBatch = 2;         // k tiles per MMA-issuer wait
 constexpr int kBatchBars = 8;        // MMA batch completion barriers (> kATiles)
-constexpr int kSmemTarget = 101 * 1024;
+constexpr int kSmemTarget = 102 * 1024;
 constexpr int kPrepThreads = 256;
 constexpr int kPrepUnits = 2;      // 16-element units of one row per thread and pass
 
@@ -374,17 +374,25 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     // The activations may come from the previous kernel on the stream, and the
     // previous GEMM on this workspace may still be reading it.
     pdl_wait();
+    // this call's epilogues combine the output rows' absmax into amax_out
+    if (tid == 0 && pr.amax_out && m < pr.M) pr.amax_out[m] = 0.f;
+    // a layer chain hands over the rows' absmax: no absmax pass
+    const bool have_amax = raw && pr.amax_in != nullptr;
 
     float v[kPrepUnits][16];
     float amax = 0.f, s = 0.f;
+    if (have_amax) {
+        amax = live ? __ldcg(pr.amax_in + m) : 0.f;
+        s = quant_scale(amax);
+    }
     // Passes 0..npass-1 find the row's absmax; the quantisation then takes
     // the last pass first, from the values still in registers, and reads the
     // row again only for the earlier ones.  One loop, so that the loads are
     // compiled once.
-    for (int it = 0; it < 2 * npass; ++it) {
+    for (int it = have_amax ? npass : 0; it < 2 * npass; ++it) {
         const bool quant = it >= npass;
         const int ps = !quant ? it : (it == npass ? npass - 1 : it - npass - 1);
-        if (!quant || ps != npass - 1) {
+        if (!quant || ps != npass - 1 || have_amax) {
 #pragma unroll
             for (int j = 0; j < kPrepUnits; ++j) {
                 const int u = ps * kPass + j * kPrepThreads + tid;
@@ -500,15 +508,20 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
 }
 
 // ------------------------------------------------------------ epilogue --
-__device__ __forceinline__ void store_out(const GemmProblem& pr, int m, int n, int acc, float a_scale) {
+// Store y[m][n] (and acc); returns |y[m][n]| as stored.
+__device__ __forceinline__ float store_out(const GemmProblem& pr, int m, int n, int acc, float a_scale) {
     const float v = __fmul_rn(__fmul_rn(static_cast<float>(acc), a_scale), pr.w_scale);
     const long long o = static_cast<long long>(m) * pr.ldy + n;
+    float stored = v;
     if (pr.out_dtype == BITMTP_F32) {
         static_cast<float*>(pr.y)[o] = v;
     } else {
-        static_cast<__nv_bfloat16*>(pr.y)[o] = __float2bfloat16_rn(v);
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        static_cast<__nv_bfloat16*>(pr.y)[o] = h;
+        stored = __bfloat162float(h);
     }
     if (pr.acc) pr.acc[static_cast<long long>(m) * pr.lda + n] = acc;
+    return fabsf(stored);
 }
 
 // Partial-sum slot of CTA b: four groups of four rows, one int4 per column in
@@ -592,10 +605,27 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int p_lo, const S
             }
         }
     }
+    float am[kRows];
+#pragma unroll
+    for (int m = 0; m < kRows; ++m) am[m] = 0.f;
     if (alive && n < pr.N) {
 #pragma unroll
         for (int m = 0; m < kRows; ++m)
-            if (m < M) store_out(pr, m, n, acc[m], c->asc[s.pi - p_lo][m]);
+            if (m < M) am[m] = store_out(pr, m, n, acc[m], c->asc[s.pi - p_lo][m]);
+    }
+    if (pr.amax_out) {
+        // first phase of the output rows' absmax: this warp's 32 columns, one
+        // atomic per row (non-negative floats order like their bit patterns)
+#pragma unroll
+        for (int m = 0; m < kRows; ++m) {
+            if (m < M) {
+                float v = am[m];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                if ((tid & 31) == 0 && v > 0.f)
+                    atomicMax(reinterpret_cast<unsigned*>(pr.amax_out + m), __float_as_uint(v));
+            }
+        }
     }
 }
 

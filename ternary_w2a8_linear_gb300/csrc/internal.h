@@ -47,6 +47,8 @@ struct GemmProblem {
     uint8_t* actb;            // [kt] tiles in the compute path's layout
     int* rsp;                 // [16][kt + 1] prefix sums over k tiles of each row's codes
     float* asc;               // [16] per-row dequant scales (amax / 127)
+    const float* amax_in;     // optional [M]: the rows' absmax, precomputed (layer chain)
+    float* amax_out;          // optional [M]: receives max_n |y[m][n]| (zeroed by the preparation)
 };
 
 struct GemmParams {

@@ -38,12 +38,12 @@ class BitmtpError(RuntimeError):
 
 class Act(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("x", ctypes.c_void_p), ("ldx", ctypes.c_int64),
-                ("a_scale", ctypes.c_void_p)]
+                ("a_scale", ctypes.c_void_p), ("amax", ctypes.c_void_p)]
 
 
 class Out(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("y", ctypes.c_void_p), ("ldy", ctypes.c_int64),
-                ("acc", ctypes.c_void_p), ("lda", ctypes.c_int64)]
+                ("acc", ctypes.c_void_p), ("lda", ctypes.c_int64), ("amax", ctypes.c_void_p)]
 
 
 class TernDesc(ctypes.Structure):
@@ -313,20 +313,22 @@ def quant_act(x: torch.Tensor, stream=None):
     return q, a_scale, rowsum
 
 
-def make_act(x: torch.Tensor, a_scale: torch.Tensor | None = None) -> Act:
+def make_act(x: torch.Tensor, a_scale: torch.Tensor | None = None, amax: torch.Tensor | None = None) -> Act:
     kind = _act_kind(x)
     if kind == Q8 and a_scale is None:
         raise ValueError("int8 activations need a_scale")
-    return Act(kind, x.data_ptr(), _rowmajor(x, "x"), a_scale.data_ptr() if kind == Q8 else None)
+    return Act(kind, x.data_ptr(), _rowmajor(x, "x"), a_scale.data_ptr() if kind == Q8 else None,
+               amax.data_ptr() if amax is not None else None)
 
 
-def make_out(y: torch.Tensor, acc: torch.Tensor | None = None) -> Out:
+def make_out(y: torch.Tensor, acc: torch.Tensor | None = None, amax: torch.Tensor | None = None) -> Out:
     dt = F32 if y.dtype == torch.float32 else BF16 if y.dtype == torch.bfloat16 else None
     if dt is None:
         raise TypeError("y must be float32 or bfloat16")
     return Out(dt, y.data_ptr(), _rowmajor(y, "y"),
                acc.data_ptr() if acc is not None else None,
-               _rowmajor(acc, "acc") if acc is not None else 0)
+               _rowmajor(acc, "acc") if acc is not None else 0,
+               amax.data_ptr() if amax is not None else None)
 
 
 def gemm(pk: torch.Tensor, w_scale: float, N: int, K: int, x: torch.Tensor,

@@ -362,3 +362,70 @@ def test_ternary_code_without_division():
             ref = np.clip(np.rint((w / g).astype(np.float32)), -1, 1).astype(np.int8)
         got = (w > h).astype(np.int8) - (w < -h).astype(np.int8)
         assert np.array_equal(got, ref), (g, w[got != ref][:4])
+
+
+def _rn32(r: Fraction) -> Fraction:
+    """Round a rational to the nearest fp32 value (ties to even), exactly;
+    written from the format definition (24-bit significand), normal range."""
+    if r == 0:
+        return Fraction(0)
+    sign = -1 if r < 0 else 1
+    a = abs(r)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** (e - 23)
+    n, rem = divmod(a, ulp)
+    if rem > ulp / 2 or (rem == ulp / 2 and n % 2 == 1):
+        n += 1
+    return sign * n * ulp
+
+
+def test_chain_dequant_order():
+    """dequant_chain is RN32(RN32(acc * a_scale) * w_scale), checked with exact
+    rationals; on these samples that order differs from the single fp64
+    rounding of dequant at least once, so the order is really pinned."""
+    rng = np.random.default_rng(606)
+    M = 400
+    acc = rng.integers(-2 ** 20, 2 ** 20, size=(M, 1))
+    a = (rng.uniform(1e-4, 1e-1, M)).astype(np.float32)
+    w = np.float32(0.0137)
+    got = oracle.dequant_chain(acc, a, w)
+    single = oracle.dequant(acc, a, w)
+    differs = 0
+    for m in range(M):
+        t = _rn32(Fraction(int(acc[m, 0])) * Fraction(float(a[m])))
+        ref = _rn32(t * Fraction(float(w)))
+        assert Fraction(float(got[m, 0])) == ref, m
+        differs += got[m, 0] != single[m, 0]
+    assert differs > 0
+
+
+def test_chain_identity_is_a_fixed_point():
+    """T = I, w_scale = 1: the first layer re-scales the codes (y = q * a_scale,
+    whose absmax is 127 * a_scale), so every later layer quantises back to the
+    same codes and acc == q; the recorded amax is the output's row absmax."""
+    K = 300
+    x = np.random.default_rng(607).standard_normal((5, K)).astype(np.float32)
+    I = np.eye(K, dtype=np.int8)
+    res = oracle.linear_chain([(I, np.float32(1.0))] * 4, x)
+    for l, r in enumerate(res):
+        assert np.array_equal(r["acc"], r["q"].astype(np.int64))
+        assert np.array_equal(r["amax"], np.max(np.abs(r["y"]), axis=1))
+        if l:
+            assert np.array_equal(r["q"], res[0]["q"])
+
+
+def test_chain_negation_alternates_sign():
+    """T = -I, w_scale = 1/2, fp32 outputs: y = -q * a_scale / 2 (the halving
+    is exact), so each layer's codes are the negation of the previous layer's.
+    (With bf16 outputs the rounding of q * a_scale to 8 bits can move a code by
+    one, so no such identity holds there.)"""
+    K = 257
+    x = np.random.default_rng(608).standard_normal((3, K)).astype(np.float32)
+    negI = -np.eye(K, dtype=np.int8)
+    res = oracle.linear_chain([(negI, np.float32(0.5))] * 5, x, out="f32")
+    for l in range(1, 5):
+        assert np.array_equal(res[l]["q"], -res[l - 1]["q"]), l
