@@ -63,9 +63,9 @@ HEADLINE_WIDTHS = (8, 12, 16)
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one headline step from an ncu capture, keyed by
 # the hash of the library sources it was taken with; reported only while the
-# sources are unchanged.  4d9d9ee968144cfd: the 216 launches of one step
+# sources are unchanged.  24beaa7b579ebcb9: the 216 launches of one step
 # (108 preparation + 108 GEMM), profiles/w2a8_streamk_large36_stack.md.
-CAPTURED_TRAFFIC: dict[str, int] = {"4d9d9ee968144cfd": 4_994_399_744}
+CAPTURED_TRAFFIC: dict[str, int] = {"24beaa7b579ebcb9": 4_995_407_104}
 KERNEL_SOURCES = ("ternary_w2a8_linear_gb300/csrc/gemm.cu", "ternary_w2a8_linear_gb300/csrc/api.cu",
                   "ternary_w2a8_linear_gb300/csrc/internal.h", "ternary_w2a8_linear_gb300/csrc/ptx.cuh",
                   "ternary_w2a8_linear_gb300/csrc/quant.cuh", "include/bitmtp_linear.h")
@@ -412,6 +412,46 @@ def run_configs(L, torch, dev, stream, peak):
         w3[mode] = entry(inputs.BITNET2B_LAYERS * layer_set_bytes(inputs.BITNET2B_PROJ, 4), t, 4, peak)
         w3[mode]["us_per_step"] = w3[mode].pop("us")
         del g
+    # the layer-chained step: per layer q -> o -> up -> down, each call's bf16
+    # output the next call's input (a real data dependency, 120 calls), with
+    # and without handing the output rows' absmax to the next call
+    chain = (0, 3, 5, 6)
+    M3 = 4
+    lib = L.load()
+    cbuf = [[(torch.empty((M3, inputs.BITNET2B_PROJ[p][2]), dtype=torch.bfloat16, device=dev),
+              torch.zeros(M3, dtype=torch.float32, device=dev)) for p in chain]
+            for _ in range(inputs.BITNET2B_LAYERS)]
+    cws = L.workspace(L.bitmtp_linear_workspace_bytes(6912, 6912, M3), dev, stream)
+
+    def run_chain(handoff):
+        x, xa = st.x[0][chain[0]], None
+        for layer in range(inputs.BITNET2B_LAYERS):
+            for j, p in enumerate(chain):
+                _, K, N = inputs.BITNET2B_PROJ[p]
+                y, am = cbuf[layer][j]
+                act = L.Act(L.BF16, x.data_ptr(), K, None, xa.data_ptr() if (handoff and xa is not None) else None)
+                o = L.Out(L.BF16, y.data_ptr(), N, None, 0, am.data_ptr())
+                r = lib.bitmtp_linear_gemm(L.ctypes.c_void_p(st.pk[layer][p].data_ptr()), st.w[layer][p], N, K, M3,
+                                           L.ctypes.byref(act), L.ctypes.byref(o), L.ctypes.c_void_p(cws.data_ptr()),
+                                           cws.numel(), L.FLAG_PDL, cs)
+                if r != L.OK:
+                    raise L.BitmtpError(r, "gemm")
+                x, xa = y, am
+        return 2 * inputs.BITNET2B_LAYERS * len(chain)
+
+    chain_bytes = inputs.BITNET2B_LAYERS * sum(L.packed_bytes(N, K) + M3 * K * 2
+                                               for _, K, N in (inputs.BITNET2B_PROJ[p] for p in chain))
+    for handoff in (True, False):
+        g, _ = graph_of(torch, stream, lambda h=handoff: run_chain(h))
+        t = time_graph(torch, stream, g, 10)
+        key = "layer_chain_amax_handoff" if handoff else "layer_chain_own_absmax"
+        w3[key] = entry(chain_bytes, t, M3, peak)
+        w3[key]["us_per_step"] = w3[key].pop("us")
+        w3[key]["calls"] = inputs.BITNET2B_LAYERS * len(chain)
+        del g
+    w3["layer_chain_what"] = ("per layer q -> o -> up -> down, each output (bf16) the next call's input, "
+                              "30 layers, width 4, one CUDA graph with PDL; amax_handoff: each call's "
+                              "epilogues reduce its output rows' absmax for the next call")
     out["3_bitnet2b_30_layers_M4"] = w3
     del st
 
