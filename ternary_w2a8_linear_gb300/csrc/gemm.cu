@@ -93,7 +93,7 @@ constexpr int kDeferTiles = 5;       // a segment's epilogue runs this many tile
 constexpr int kMmaBatch = 2;         // k tiles per MMA-issuer wait
 constexpr int kBatchBars = 8;        // MMA batch completion barriers (> kATiles)
 constexpr int kSmemTarget = 102 * 1024;
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 512;
 constexpr int kPrepUnits = 2;      // 16-element units of one row per thread and pass
 
 enum : int {
@@ -345,12 +345,11 @@ __device__ __forceinline__ const char* act_row(const GemmProblem& pr, int m) {
 // One CTA per (problem, row m < btile_rows).  Writes row m of every
 // activation tile of the problem (zeros for m >= M and beyond K), the prefix
 // sums rsp[m][0..kt] of the row's codes over k tiles, and asc[m].  Each
-// thread owns whole 16-k units; rows of up to kPass units (K <= 8192) stay in
-// registers between the absmax and the quantisation, longer rows are read
-// twice.  A CTA (256 threads, at most 64 registers each) fits in the
-// registers that two GEMM CTAs leave free (the GEMM's register cap).
+// thread owns whole 16-k units; rows of up to kPass units (K <= 16384) stay in
+// registers between the absmax and the quantisation (one pass over the row),
+// longer rows are read twice.  512 threads, at most 64 registers each.
 template <int PATH, int DPR>
-__global__ void __launch_bounds__(kPrepThreads, 4)  // <= 64 registers: 16 K registers a CTA
+__global__ void __launch_bounds__(kPrepThreads, 2)  // <= 64 registers
 act_prep_kernel(const __grid_constant__ GemmParams P) {
     constexpr int kRows = btile_rows(PATH, DPR);
     constexpr int kBRows = btile_brows(PATH, DPR);

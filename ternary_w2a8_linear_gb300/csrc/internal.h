@@ -23,10 +23,9 @@ enum ComputePath : int {
 // GEMM block: warps 0-3 compute + epilogue, 4 bulk copies; the tensor paths
 // add warps 5 and 6, which issue the MMAs of alternate batches.
 __host__ __device__ constexpr int gemm_threads(int path) { return path == kPathDP ? 192 : 224; }
-// Register cap of a GEMM thread: two GEMM CTAs leave room in an SM's 65,536
-// registers for one preparation CTA of the next call (256 threads x 64
-// registers): 2 x 224 x 104 + 16,384 = 62,976; 2 x 192 x 120 + 16,384 =
-// 62,464.
+// Register cap of a GEMM thread (no spills at these caps): two GEMM CTAs take
+// 2 x 224 x 104 = 46,592 (tensor paths) or 2 x 192 x 120 = 46,080 (dp4a) of
+// an SM's 65,536 registers.
 __host__ __device__ constexpr int gemm_max_regs(int path) { return path == kPathDP ? 120 : 104; }
 
 struct GemmProblem {
