@@ -904,6 +904,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         for (int k = 0; k < kATiles; ++k) hist[k] = 0;
         int nbatch = 0;
         int prev_ab = 0;  // A buffer of the batch's first tile
+        int waited = -1;  // the last MMA batch waited for
         bool first_epi = true;
         // Tensor paths: a segment's epilogue is deferred until kDeferTiles tiles
         // of the next segment are written (the accumulator is double-buffered),
@@ -994,11 +995,14 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
                     for (int k = 0; k + 1 < kATiles; ++k) hist[k] = hist[k + 1];
                     hist[kATiles - 1] = nbatch + e / kMmaBatch;
-                    if (alive && rp.i >= kATiles) {
+                    // (the second tile of a batch usually reuses a buffer of the
+                    // batch the first one already waited for)
+                    if (alive && rp.i >= kATiles && prev != waited) {
                         alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->mma_done[prev % kBatchBars]),
                                                                           (prev / kBatchBars) & 1, P.wait_ns));
                         if (!alive && lane == 0) fail(c, P.err, kErrWaitAEmpty);
                         tc_fence_after();
+                        waited = prev;
                     }
                     if (alive) {
                         // the segment's accumulator starts at zero (both MMA
