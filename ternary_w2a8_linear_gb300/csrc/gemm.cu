@@ -111,7 +111,7 @@ struct Ctrl {
     uint64_t wfull[kMaxRing];     // weight tiles of the chunk landed
     uint64_t bfull[kMaxRing];     // activation tiles of the chunk landed
     uint64_t empty[kMaxRing];     // chunk slot free again (both MMA warps' commits / dp4a consumers)
-    uint64_t a_full[kATiles];     // A buffer written (four consumer warps)
+    uint64_t a_full[kBatchBars];  // A tiles of MMA batch b written: a_full[b % kBatchBars] (four writer warps)
     uint64_t mma_done[kBatchBars]; // MMA batch b complete: barrier b % kBatchBars
     uint64_t dfull[2][4];         // MMA warp 5 + i finished segment s: dfull[i][s & 3]
     uint64_t slot_done;           // contributor partial sums stored (four consumer warps)
@@ -674,14 +674,14 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     }
     const GemmProblem* pp = c->prob;
     // the mbarriers, one per thread (consecutive 8-byte words)
-    static_assert(offsetof(Ctrl, slot_done) == offsetof(Ctrl, wfull) + 8 * (3 * kMaxRing + kATiles + kBatchBars + 8),
+    static_assert(offsetof(Ctrl, slot_done) == offsetof(Ctrl, wfull) + 8 * (3 * kMaxRing + kBatchBars + kBatchBars + 8),
                   "mbarriers not consecutive");
     static_assert(offsetof(Ctrl, drained) == offsetof(Ctrl, slot_done) + 8, "mbarriers not consecutive");
-    if (tid < 3 * kMaxRing + kATiles + kBatchBars + 11) {
+    if (tid < 3 * kMaxRing + kBatchBars + kBatchBars + 11) {
         uint32_t count = 1;                                                          // wfull, bfull, mma_done, dfull, drained
         if (tid >= 2 * kMaxRing && tid < 3 * kMaxRing) count = kTC ? 2 : 4;          // empty
-        else if (tid >= 3 * kMaxRing && tid < 3 * kMaxRing + kATiles) count = 4;     // a_full
-        else if (tid == 3 * kMaxRing + kATiles + kBatchBars + 8) count = 4;          // slot_done
+        else if (tid >= 3 * kMaxRing && tid < 3 * kMaxRing + kBatchBars) count = 4;  // a_full
+        else if (tid == 3 * kMaxRing + kBatchBars + kBatchBars + 8) count = 4;          // slot_done
         mbar_init(smem_u32(&c->wfull[0]) + 8 * tid, count);
         fence_mbar_init();
     }
@@ -776,10 +776,10 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         // ns).  Both accumulate into the segment's D buffer, which the consumer
         // warps zero before the segment's first A tile, so every MMA adds
         // (the order does not matter: every partial sum is a multiple of
-        // 2^-9 below 2^15 in magnitude, so fp32 holds it exactly).  A batch is up to kMmaBatch tiles of one
-        // segment; its issuer waits for the activation tiles of every chunk it
-        // is the first to touch, then for the batch's last A buffer (the
-        // consumer warps fill buffers in order), issues the batch's MMAs as
+        // 2^-9 below 2^15 in magnitude, so fp32 holds it exactly).  A batch
+        // is up to kMmaBatch tiles of one segment; its issuer waits for the
+        // activation tiles of every chunk it is the first to touch, then for
+        // the batch's A tiles (a_full of the batch), issues the batch's MMAs as
         // straight-line code and commits mma_done.  Chunk slots and finished
         // segments need both warps: each commits `empty` at every chunk end
         // and its own dfull[.][s & 3] at every segment end s it passes (a
@@ -827,7 +827,8 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                             if (leader) fail(c, P.err, kErrWaitB);
                             break;
                         }
-                        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->a_full[r1.ab]), r1.abph, P.wait_ns));
+                        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->a_full[nbatch % kBatchBars]),
+                                                                       (nbatch / kBatchBars) & 1, P.wait_ns));
                         if (!ok) {
                             if (leader) fail(c, P.err, kErrWaitAFull);
                             break;
@@ -903,7 +904,6 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
         for (int k = 0; k < kATiles; ++k) hist[k] = 0;
         int nbatch = 0;
-        int prev_ab = 0;  // A buffer of the batch's first tile
         int waited = -1;  // the last MMA batch waited for
         bool first_epi = true;
         // Tensor paths: a segment's epilogue is deferred until kDeferTiles tiles
@@ -1021,16 +1021,14 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         unpack_word_e4m3(w1.z, r + 24);
                         unpack_word_e4m3(w1.w, r + 28);
                         tmem_st32(tmem + lane_base + kACol + ab * kATileCols, r);
-                        // one wait for the batch's stores, then both of its A
-                        // buffers are announced (the issuer waits for the last)
+                        // one wait for the batch's stores, then one arrival
+                        // announces the batch's A tiles
                         if (e % kMmaBatch == kMmaBatch - 1 || e == len - 1) {
                             tc_wait_st();
                             tc_fence_before();
                             __syncwarp();
-                            if (e % kMmaBatch != 0) mbar_arrive_if(lane == 0, smem_u32(&c->a_full[prev_ab]));
-                            mbar_arrive_if(lane == 0, smem_u32(&c->a_full[ab]));
+                            mbar_arrive_if(lane == 0, smem_u32(&c->a_full[(nbatch + e / kMmaBatch) % kBatchBars]));
                         }
-                        prev_ab = ab;
                     }
                 } else {
                     if (alive) {
