@@ -973,65 +973,109 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             for (int s4 = 0; s4 < 4; ++s4)
 #pragma unroll
                 for (int m = 0; m < DPR; ++m) dacc[s4][m] = 0;
-            for (int e = 0; e < len; ++e, rp.next(R)) {
-                if constexpr (kTC) {
-                    if (dv && e == kDeferTiles) finish_deferred();
-                }
-                const int s = rp.slot();
-                if (alive && rp.cp == 0) {
-                    alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[rp.q]), rp.qph, P.wait_ns));
-                    if (!alive && lane == 0) fail(c, P.err, kErrWaitW);
-                    if constexpr (!kTC) {
-                        if (alive) {
-                            alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[rp.q]), rp.qph, P.wait_ns));
-                            if (!alive && lane == 0) fail(c, P.err, kErrWaitB);
-                        }
+            if constexpr (kTC) {
+                // one MMA batch (up to two tiles) per iteration: both tiles'
+                // shared loads in flight together, one wait for the stores,
+                // one arrival for the batch
+                static_assert(kMmaBatch == 2, "the writer loop below handles batches of one or two tiles");
+                for (int e = 0; e < len;) {
+                    const int nb = min(kMmaBatch, len - e);
+                    if (dv && e <= kDeferTiles && kDeferTiles < e + nb) finish_deferred();
+                    RingPos r1 = rp;  // the batch's last tile
+                    if (nb > 1) r1.next(R);
+                    if (alive && rp.cp == 0) {
+                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[rp.q]), rp.qph, P.wait_ns));
+                        if (!alive && lane == 0) fail(c, P.err, kErrWaitW);
                     }
-                }
-                const uint8_t* wst = Wr + static_cast<size_t>(s) * kTileBytes;
-                if constexpr (kTC) {
-                    const int ab = rp.ab;
-                    const int prev = hist[0];  // batch that read the tile kATiles back
+                    if (alive && nb > 1 && r1.cp == 0) {
+                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[r1.q]), r1.qph, P.wait_ns));
+                        if (!alive && lane == 0) fail(c, P.err, kErrWaitW);
+                    }
+                    // the batches that last read the two A buffers (kATiles
+                    // tiles back); the second usually equals the first
+                    const int bn = nbatch + e / kMmaBatch;
+                    const int prev0 = hist[0];
 #pragma unroll
                     for (int k = 0; k + 1 < kATiles; ++k) hist[k] = hist[k + 1];
-                    hist[kATiles - 1] = nbatch + e / kMmaBatch;
-                    // (the second tile of a batch usually reuses a buffer of the
-                    // batch the first one already waited for)
-                    if (alive && rp.i >= kATiles && prev != waited) {
-                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->mma_done[prev % kBatchBars]),
-                                                                          (prev / kBatchBars) & 1, P.wait_ns));
+                    hist[kATiles - 1] = bn;
+                    int prev1 = prev0;
+                    if (nb > 1) {
+                        prev1 = hist[0];
+#pragma unroll
+                        for (int k = 0; k + 1 < kATiles; ++k) hist[k] = hist[k + 1];
+                        hist[kATiles - 1] = bn;
+                    }
+                    if (alive && rp.i >= kATiles && prev0 != waited) {
+                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->mma_done[prev0 % kBatchBars]),
+                                                                          (prev0 / kBatchBars) & 1, P.wait_ns));
                         if (!alive && lane == 0) fail(c, P.err, kErrWaitAEmpty);
                         tc_fence_after();
-                        waited = prev;
+                        waited = prev0;
+                    }
+                    if (alive && nb > 1 && r1.i >= kATiles && prev1 != waited) {
+                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->mma_done[prev1 % kBatchBars]),
+                                                                          (prev1 / kBatchBars) & 1, P.wait_ns));
+                        if (!alive && lane == 0) fail(c, P.err, kErrWaitAEmpty);
+                        tc_fence_after();
+                        waited = prev1;
                     }
                     if (alive) {
                         // the segment's accumulator starts at zero (both MMA
                         // warps only add); its previous use was read out by
                         // the epilogue of the segment two back
                         if (e == 0) tmem_st32_fill(tmem + lane_base + kAccCol + (seg_idx & 1) * 32, 0u);
-                        const uint4 w0 = *reinterpret_cast<const uint4*>(wst + tid * 16);
-                        const uint4 w1 = *reinterpret_cast<const uint4*>(wst + 2048 + tid * 16);
+                        const uint8_t* wa = Wr + static_cast<size_t>(rp.slot()) * kTileBytes + tid * 16;
+                        const uint8_t* wb = Wr + static_cast<size_t>(r1.slot()) * kTileBytes + tid * 16;
+                        const uint4 a0 = *reinterpret_cast<const uint4*>(wa);
+                        const uint4 a1 = *reinterpret_cast<const uint4*>(wa + 2048);
+                        uint4 b0 = a0, b1 = a1;
+                        if (nb > 1) {
+                            b0 = *reinterpret_cast<const uint4*>(wb);
+                            b1 = *reinterpret_cast<const uint4*>(wb + 2048);
+                        }
                         uint32_t r[32];  // A columns 4w + s: word w (16 k), register s
-                        unpack_word_e4m3(w0.x, r + 0);
-                        unpack_word_e4m3(w0.y, r + 4);
-                        unpack_word_e4m3(w0.z, r + 8);
-                        unpack_word_e4m3(w0.w, r + 12);
-                        unpack_word_e4m3(w1.x, r + 16);
-                        unpack_word_e4m3(w1.y, r + 20);
-                        unpack_word_e4m3(w1.z, r + 24);
-                        unpack_word_e4m3(w1.w, r + 28);
-                        tmem_st32(tmem + lane_base + kACol + ab * kATileCols, r);
-                        // one wait for the batch's stores, then one arrival
-                        // announces the batch's A tiles
-                        if (e % kMmaBatch == kMmaBatch - 1 || e == len - 1) {
-                            tc_wait_st();
-                            tc_fence_before();
-                            __syncwarp();
-                            mbar_arrive_if(lane == 0, smem_u32(&c->a_full[(nbatch + e / kMmaBatch) % kBatchBars]));
+                        unpack_word_e4m3(a0.x, r + 0);
+                        unpack_word_e4m3(a0.y, r + 4);
+                        unpack_word_e4m3(a0.z, r + 8);
+                        unpack_word_e4m3(a0.w, r + 12);
+                        unpack_word_e4m3(a1.x, r + 16);
+                        unpack_word_e4m3(a1.y, r + 20);
+                        unpack_word_e4m3(a1.z, r + 24);
+                        unpack_word_e4m3(a1.w, r + 28);
+                        tmem_st32(tmem + lane_base + kACol + rp.ab * kATileCols, r);
+                        if (nb > 1) {
+                            unpack_word_e4m3(b0.x, r + 0);
+                            unpack_word_e4m3(b0.y, r + 4);
+                            unpack_word_e4m3(b0.z, r + 8);
+                            unpack_word_e4m3(b0.w, r + 12);
+                            unpack_word_e4m3(b1.x, r + 16);
+                            unpack_word_e4m3(b1.y, r + 20);
+                            unpack_word_e4m3(b1.z, r + 24);
+                            unpack_word_e4m3(b1.w, r + 28);
+                            tmem_st32(tmem + lane_base + kACol + r1.ab * kATileCols, r);
+                        }
+                        tc_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        mbar_arrive_if(lane == 0, smem_u32(&c->a_full[bn % kBatchBars]));
+                    }
+                    rp = r1;
+                    rp.next(R);
+                    e += nb;
+                }
+            } else {
+                for (int e = 0; e < len; ++e, rp.next(R)) {
+                    const int s = rp.slot();
+                    if (alive && rp.cp == 0) {
+                        alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[rp.q]), rp.qph, P.wait_ns));
+                        if (!alive && lane == 0) fail(c, P.err, kErrWaitW);
+                        if (alive) {
+                            alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->bfull[rp.q]), rp.qph, P.wait_ns));
+                            if (!alive && lane == 0) fail(c, P.err, kErrWaitB);
                         }
                     }
-                } else {
                     if (alive) {
+                        const uint8_t* wst = Wr + static_cast<size_t>(s) * kTileBytes;
                         const uint8_t* bst = Br + static_cast<size_t>(s) * BT;
                         const uint4 w0 = *reinterpret_cast<const uint4*>(wst + tid * 16);
                         const uint4 w1 = *reinterpret_cast<const uint4*>(wst + 2048 + tid * 16);

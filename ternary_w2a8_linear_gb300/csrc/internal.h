@@ -24,9 +24,9 @@ enum ComputePath : int {
 // add warps 5 and 6, which issue the MMAs of alternate batches.
 __host__ __device__ constexpr int gemm_threads(int path) { return path == kPathDP ? 192 : 224; }
 // Register cap of a GEMM thread (no spills at these caps): two GEMM CTAs take
-// 2 x 224 x 104 = 46,592 (tensor paths) or 2 x 192 x 120 = 46,080 (dp4a) of
+// 2 x 224 x 128 = 57,344 (tensor paths) or 2 x 192 x 120 = 46,080 (dp4a) of
 // an SM's 65,536 registers.
-__host__ __device__ constexpr int gemm_max_regs(int path) { return path == kPathDP ? 120 : 104; }
+__host__ __device__ constexpr int gemm_max_regs(int path) { return path == kPathDP ? 120 : 128; }
 
 struct GemmProblem {
     const uint8_t* pk;
