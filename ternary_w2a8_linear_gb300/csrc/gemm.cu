@@ -914,9 +914,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         ds.pi = ds.rt = ds.ka = ds.kb = 0;
         ds.t0 = 0;
         int d_seg = 0;
-        int d_rq[kOutRows];
-#pragma unroll
-        for (int m = 0; m < kOutRows; ++m) d_rq[m] = 0;
+        int d_rsl = 0;  // the deferred segment's prefix-sum lane value (code_sum)
         auto epilogue = [&](const Seg& es, int (&acc)[16]) {
             if (first_epi) {  // publish the dequant scales once
                 if (asc_mine) c->asc[tid / 16][tid % 16] = asc_reg;
@@ -952,7 +950,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
                     for (int m = 0; m < kRows; ++m) {
                         const float d = __fadd_rn(__fmul_rn(__uint_as_float(v[m]), 16.f), __uint_as_float(v[m + kRows]));
-                        acc[m] = __float2int_rn(__fmul_rn(d, 512.f)) - d_rq[m];
+                        acc[m] = __float2int_rn(__fmul_rn(d, 512.f)) - code_sum(d_rsl, m);
                     }
                 }
             }
@@ -1104,8 +1102,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 if (dv) finish_deferred();  // the previous segment, if this one was short
                 ds = sg;
                 d_seg = seg_idx;
-#pragma unroll
-                for (int m = 0; m < kOutRows; ++m) d_rq[m] = code_sum(rsl, m);
+                d_rsl = rsl;
                 dv = true;
             } else {
                 int acc[16];
