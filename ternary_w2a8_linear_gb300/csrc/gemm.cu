@@ -85,13 +85,12 @@ constexpr int kMaxRing = 6;          // chunks in the ring (upper bound)
 constexpr int kCtrlBytes = 2304;
 constexpr int kBarEpi = 1;           // named barrier: the four consumer warps
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kAccCol = 0;      // D: two accumulators (alternate segments) of 32 fp32 columns
-constexpr uint32_t kACol = 64;       // A: kATiles buffers of one k tile each
-constexpr uint32_t kATileCols = 32;  // 128 k, one e4m3 byte each
-constexpr int kATiles = 6;
+constexpr uint32_t kAccCol = 0;      // D: two accumulators (alternate segments), columns 0 .. 2 * d_cols
+constexpr uint32_t kATileCols = 32;  // A: one k tile (128 k, one e4m3 byte each) per buffer
+constexpr int kMaxATiles = 7;
 constexpr int kDeferTiles = 5;       // a segment's epilogue runs this many tiles into the next one
 constexpr int kMmaBatch = 2;         // k tiles per MMA-issuer wait
-constexpr int kBatchBars = 8;        // MMA batch completion barriers (> kATiles)
+constexpr int kBatchBars = 8;        // MMA batch completion barriers (> A buffers)
 constexpr int kSmemTarget = 102 * 1024;
 constexpr int kPrepThreads = 512;
 constexpr int kPrepUnits = 2;      // 16-element units of one row per thread and pass
@@ -135,6 +134,16 @@ __host__ __device__ constexpr int btile_brows(int path, int dp_rows) {
 // Bytes of one k tile of the activation operand: 8 units of 16 k, each
 // holding 16 bytes per operand row.
 __host__ __device__ constexpr int btile_bytes(int path, int dp_rows) { return btile_brows(path, dp_rows) * 128; }
+// Tensor-memory layout of the tensor paths: each accumulator is one fp32
+// column per B row (the MMA's N); the A buffers fill the rest of the 256
+// allocated columns (six at 16 rows, seven at 8).
+__host__ __device__ constexpr uint32_t tmem_d_cols(int path, int dp_rows) {
+    return static_cast<uint32_t>(btile_brows(path, dp_rows));
+}
+__host__ __device__ constexpr uint32_t tmem_a_col(int path, int dp_rows) { return 2 * tmem_d_cols(path, dp_rows); }
+__host__ __device__ constexpr int tmem_a_tiles(int path, int dp_rows) {
+    return path == kPathDP ? 1 : static_cast<int>((kTmemCols - tmem_a_col(path, dp_rows)) / kATileCols);
+}
 
 __device__ __forceinline__ void fail(Ctrl* c, int* err, int code) {
     *reinterpret_cast<volatile int*>(&c->failed) = 1;
@@ -218,17 +227,17 @@ struct ProcIter {
     }
 };
 
-// Position of local tile i (processing order) in the chunk ring and in the A
-// buffers, advanced one tile at a time (no division by the runtime ring size
+// Position of local tile i (processing order) in the chunk ring and in the kNA
+// A buffers, advanced one tile at a time (no division by the runtime ring size
 // on the way to an MMA issue or a barrier wait).
+template <int kNA>
 struct RingPos {
     int cp;          // i % kChunk
     int q;           // (i / kChunk) % R: ring slot of the chunk
     uint32_t qph;    // ((i / kChunk) / R) & 1: phase of that slot's barriers
-    int ab;          // i % kATiles: A buffer
-    uint32_t abph;   // (i / kATiles) & 1
+    int ab;          // i % kNA: A buffer
     int i;
-    __device__ void reset() { cp = q = ab = i = 0; qph = abph = 0u; }
+    __device__ void reset() { cp = q = ab = i = 0; qph = 0u; }
     __device__ void next(int R) {
         ++i;
         if (++cp == kChunk) {
@@ -238,10 +247,7 @@ struct RingPos {
                 qph ^= 1u;
             }
         }
-        if (++ab == kATiles) {
-            ab = 0;
-            abph ^= 1u;
-        }
+        if (++ab == kNA) ab = 0;
     }
     __device__ int slot() const { return q * kChunk + cp; }  // tile slot in the ring
 };
@@ -648,6 +654,12 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     constexpr bool kTC = PATH != kPathDP;
     constexpr int BT = btile_bytes(PATH, DPR);
     constexpr int kOutRows = btile_rows(PATH, DPR);  // M <= kOutRows (the host's path choice)
+    constexpr uint32_t kDCols = tmem_d_cols(PATH, DPR);
+    constexpr uint32_t kACol = tmem_a_col(PATH, DPR);
+    constexpr int kATiles = tmem_a_tiles(PATH, DPR);
+    static_assert(!kTC || (kATiles <= kMaxATiles && kATiles < kBatchBars && kDCols <= 32 &&
+                           kACol + kATiles * kATileCols <= kTmemCols), "tensor-memory layout");
+    using RP = RingPos<kATiles>;
     Ctrl* c = reinterpret_cast<Ctrl*>(smem);
     const int R = P.stages;                                  // chunks in the ring
     uint8_t* Wr = smem + kCtrlBytes;                         // [R][kChunk][4096]
@@ -798,7 +810,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(Br), kUnit, 128);
             constexpr uint64_t kStepDesc = (2 * kUnit) >> 4;      // 32 k further, in descriptor units
             constexpr uint64_t kTileDesc = static_cast<uint64_t>(BT) >> 4;
-            RingPos rp;
+            RP rp;
             rp.reset();
             int nbatch = 0, seg = 0, my_chunk = -1;
             bool ok = true;
@@ -808,10 +820,10 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 seg_ending_at(pp, np, t_begin, cur_end, sg);
                 cur_end = sg.t0;
                 const int len = sg.kb - sg.ka;
-                const uint32_t dcol = tmem + kAccCol + (seg & 1) * 32;
+                const uint32_t dcol = tmem + kAccCol + (seg & 1) * kDCols;
                 for (int e = 0; e < len && ok;) {
                     const int nb = min(kMmaBatch, len - e);
-                    RingPos r1 = rp;  // the batch's last tile
+                    RP r1 = rp;  // the batch's last tile
                     if (nb > 1) r1.next(R);
                     if ((nbatch & 1) == par) {
                         const int c0 = rp.i / kChunk, c1 = r1.i / kChunk;
@@ -895,7 +907,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         bool alive = true;
         int seg_idx = 0;
-        RingPos rp;
+        RP rp;
         rp.reset();
         // MMA batch of each of the last kATiles tiles (the batch that must
         // complete before an A buffer is written again); batches never span
@@ -940,7 +952,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 if (alive) {
                     // D column m: high parts of row m; column m + kRows: low parts
                     constexpr int kRows = btile_rows(PATH, DPR);
-                    const uint32_t dcol = tmem + lane_base + kAccCol + (d_seg & 1) * 32;
+                    const uint32_t dcol = tmem + lane_base + kAccCol + (d_seg & 1) * kDCols;
                     tc_fence_after();
                     uint32_t v[32];
                     tmem_ld16(dcol, *reinterpret_cast<uint32_t(*)[16]>(v));
@@ -979,7 +991,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 for (int e = 0; e < len;) {
                     const int nb = min(kMmaBatch, len - e);
                     if (dv && e <= kDeferTiles && kDeferTiles < e + nb) finish_deferred();
-                    RingPos r1 = rp;  // the batch's last tile
+                    RP r1 = rp;  // the batch's last tile
                     if (nb > 1) r1.next(R);
                     if (alive && rp.cp == 0) {
                         alive = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->wfull[rp.q]), rp.qph, P.wait_ns));
@@ -1021,7 +1033,11 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         // the segment's accumulator starts at zero (both MMA
                         // warps only add); its previous use was read out by
                         // the epilogue of the segment two back
-                        if (e == 0) tmem_st32_fill(tmem + lane_base + kAccCol + (seg_idx & 1) * 32, 0u);
+                        if (e == 0) {
+                            const uint32_t dz = tmem + lane_base + kAccCol + (seg_idx & 1) * kDCols;
+                            if constexpr (kDCols == 32) tmem_st32_fill(dz, 0u);
+                            else tmem_st16_fill(dz, 0u);
+                        }
                         const uint8_t* wa = Wr + static_cast<size_t>(rp.slot()) * kTileBytes + tid * 16;
                         const uint8_t* wb = Wr + static_cast<size_t>(r1.slot()) * kTileBytes + tid * 16;
                         const uint4 a0 = *reinterpret_cast<const uint4*>(wa);

@@ -165,6 +165,14 @@ __device__ __forceinline__ void tmem_st32_fill(uint32_t taddr, uint32_t v) {
         :: "r"(taddr), "r"(v) : "memory");
 }
 
+// Store the value v to 16 consecutive 32-bit columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st16_fill(uint32_t taddr, uint32_t v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"
+        :: "r"(taddr), "r"(v) : "memory");
+}
+
 // Load 16 consecutive 32-bit columns for this warp's 32 lanes.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
