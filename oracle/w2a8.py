@@ -35,6 +35,9 @@ The packed-weight format (``pack_tiles`` / ``unpack_tiles``) is this library's
 own internal layout, not the pages'; it is restated here from its written
 definition so that the device pack kernel can be checked byte for byte.
 
+The FP8 "fast" draft projection (``quant_act_fp8``, ``gemm_acc_fp8``,
+``fp8_linear``) follows the reading stated at its definition.
+
 Precision: the quantiser is fp32 (the specification fixes it); accumulation is
 exact int64; dequant is fp64 then rounded to fp32 (``dequant``), or, inside a
 layer chain, two fp32 roundings in a fixed order (``dequant_chain``).
@@ -215,6 +218,100 @@ def linear_chain(layers, x0: np.ndarray, out: str = "f32", x0_is_bf16: bool = Fa
         res.append(dict(y=y, acc=acc, q=q, a_scale=a_scale, amax=amax))
         x, is_bf16 = y, out == "bf16"
     return res
+
+
+# ---------------------------------------------------------------------------
+# "Fast" draft projections with FP8 activations.  The pages run cheaper "fast"
+# projections for drafting and more careful "critical" ones for generation
+# and verification, and on H20 "additionally" FP8 draft projections
+# ("Methodology in Plain English", M1).  They give no formula.  Reading taken:
+# the backbone weights stay ternary (packed 2-bit; -1, 0 and +1 are exact
+# FP8 values) and the draft rows' activations are quantised per row to FP8
+# E4M3 instead of int8, by absmax, with the same fp32 steps as ``quant_act``
+# and 448 (the largest finite E4M3 value) in place of 127:
+#   s = RN32(448 / amax);  e = E4M3(RN32(x * s));  a_scale = RN32(amax / 448);
+# E4M3 here is the OCP FP8 format without infinities: sign, 4 exponent bits
+# (bias 7), 3 mantissa bits; normal values 1.m * 2^E for E in -6..8 (largest
+# 1.75 * 2^8 = 448), subnormal values j * 2^-9; conversion rounds to nearest,
+# ties to even, and saturates at +-448.  The accumulation sum_k T * e is exact
+# here (every e is a multiple of 2^-9 below 2^9 in magnitude, so the sum is an
+# integer number of 2^-9 units below 2^33); the device accumulates in fp32,
+# so its results agree within a bound, not bit for bit.
+# ---------------------------------------------------------------------------
+FP8_MAX = 448.0
+FP8_MIN_EXP = -6        # smallest normal binade 2^-6
+FP8_MANT_BITS = 3
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Round fp32 (or exactly representable fp64) values to the E4M3 grid,
+    round-to-nearest-even, saturating at +-448.  Returns fp64 values.
+
+    The grid step in the binade [2^E, 2^(E+1)) is 2^(E-3) for E >= -6; below
+    2^-6 (the subnormals) it is 2^-9.  Dividing by a power of two is exact, so
+    rint (half to even) on the scaled value is the correctly rounded result."""
+    v = np.asarray(v, dtype=F64)
+    a = np.abs(v)
+    _, ex = np.frexp(a)                      # a = f * 2^ex, f in [0.5, 1)
+    binade = np.maximum(ex - 1, FP8_MIN_EXP)
+    step = np.ldexp(1.0, binade - FP8_MANT_BITS)
+    r = np.minimum(np.rint(a / step) * step, FP8_MAX)
+    return np.where(v < 0, -r, r)
+
+
+def quant_act_fp8(x: np.ndarray):
+    """Quantise each row of x (fp32 [M, K]) to E4M3 values by absmax.
+
+    Per row m, in fp32 round-to-nearest-even:
+      amax = max_k |x[m, k]|
+      amax == 0  ->  e = 0, a_scale = 0
+      otherwise  ->  s = 448 / amax;  e = E4M3(x * s);  a_scale = amax / 448
+    Returns (e fp64 [M, K] holding E4M3 values, a_scale fp32 [M])."""
+    x = np.asarray(x, dtype=F32)
+    if x.ndim != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    if not np.all(np.isfinite(x)):
+        raise ValueError("non-finite activation")
+    M, K = x.shape
+    e = np.zeros((M, K), dtype=F64)
+    a_scale = np.zeros(M, dtype=F32)
+    for m in range(M):
+        row = x[m]
+        amax = F32(np.max(np.abs(row))) if K else F32(0)
+        if amax == 0:
+            continue
+        s = F32(F32(FP8_MAX) / amax)
+        e[m] = e4m3_round((row * s).astype(F32))
+        a_scale[m] = F32(amax / F32(FP8_MAX))
+    return e, a_scale
+
+
+def quant_act_fp8_bf16(x_bits: np.ndarray):
+    """``quant_act_fp8`` on bf16 activations given as uint16 bit patterns."""
+    return quant_act_fp8(bf16_bits_to_f32(x_bits))
+
+
+def gemm_acc_fp8(T: np.ndarray, e: np.ndarray) -> np.ndarray:
+    """acc[m, n] = sum_k T[n, k] * e[m, k], exact: computed in int64 units of
+    2^-9 (every E4M3 value is an integer multiple of 2^-9) and returned as
+    fp64 (exact, below 2^33 units)."""
+    T = np.asarray(T)
+    e = np.asarray(e, dtype=F64)
+    if T.ndim != 2 or e.ndim != 2 or T.shape[1] != e.shape[1]:
+        raise ValueError("shape mismatch: T [N, K], e [M, K]")
+    units = e * 512.0
+    if units.size and not np.array_equal(units, np.rint(units)):
+        raise ValueError("e is not on the E4M3 grid")
+    acc_units = units.astype(np.int64) @ T.astype(np.int64).T
+    return acc_units.astype(F64) / 512.0
+
+
+def fp8_linear(T, w_scale, x, out: str = "f32", x_is_bf16: bool = False):
+    """quant_act_fp8 -> gemm_acc_fp8 -> dequant (fp64, rounded once).
+    Returns (y, acc, e, a_scale)."""
+    e, a_scale = quant_act_fp8_bf16(x) if x_is_bf16 else quant_act_fp8(x)
+    acc = gemm_acc_fp8(T, e)
+    return dequant(acc, a_scale, w_scale, out), acc, e, a_scale
 
 
 # ---------------------------------------------------------------------------

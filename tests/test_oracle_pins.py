@@ -429,3 +429,107 @@ def test_chain_negation_alternates_sign():
     res = oracle.linear_chain([(negI, np.float32(0.5))] * 5, x, out="f32")
     for l in range(1, 5):
         assert np.array_equal(res[l]["q"], -res[l - 1]["q"]), l
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) "fast" draft projection
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", list(_rows("e4m3_closed_forms.txt")))
+def test_e4m3_round_golden(case):
+    x, r, _ = case
+    got = oracle.e4m3_round(np.array([float(x)], dtype=np.float32))[0]
+    assert got == float(r)
+
+
+def test_e4m3_grid_has_127_nonnegative_values():
+    # exponent fields 0..15 x mantissas 0..7, minus the one NaN code (S.1111.111)
+    a = np.linspace(0.0, 500.0, 2_000_001, dtype=np.float32)
+    fine = np.ldexp(np.arange(0, 2 ** 14, dtype=np.float64), -14).astype(np.float32)  # dense near zero
+    vals = np.unique(oracle.e4m3_round(np.concatenate([a, fine])))
+    assert len(vals) == 127
+    assert vals[0] == 0.0 and vals[1] == 2.0 ** -9 and vals[-1] == 448.0
+    # every value is j * 2^(E-3) with 8 <= j <= 15 above 2^-6, j * 2^-9 below
+    for v in vals[1:]:
+        e = max(int(np.floor(np.log2(v))), -6)
+        j = v / 2.0 ** (e - 3)
+        assert j == int(j) and (j <= 15) and (j >= 8 or e == -6)
+
+
+def test_e4m3_round_matches_torch_float8_cast():
+    # library routine: torch's fp32 -> float8_e4m3fn conversion (round to
+    # nearest even) on values inside the finite range, including every midpoint
+    torch = pytest.importorskip("torch")
+    grid = np.unique(oracle.e4m3_round(np.linspace(0, 448, 400_001, dtype=np.float32)))
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+    rnd = np.random.default_rng(11).standard_normal(200_000).astype(np.float32) * np.float32(40)
+    x = np.concatenate([grid.astype(np.float32), mids, -mids, rnd, rnd * np.float32(1e-3)])
+    x = x[np.abs(x) <= 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float32).numpy().astype(np.float64)
+    assert np.array_equal(oracle.e4m3_round(x), ref)
+
+
+@pytest.mark.parametrize("case", list(_rows("quant_act_fp8_closed_forms.txt")))
+def test_quant_act_fp8_golden(case):
+    xs, es, amax = case
+    x = np.array([[float(v) for v in xs.split()]], dtype=np.float32)
+    e, a_scale = oracle.quant_act_fp8(x)
+    assert e[0].tolist() == [float(v) for v in es.split()]
+    expect = np.float32(float(amax)) / np.float32(448) if float(amax) else np.float32(0)
+    assert a_scale[0] == expect
+
+
+def test_quant_act_fp8_one_hot_and_power_of_two_scaling():
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        K = int(rng.integers(1, 300))
+        x = np.zeros((1, K), dtype=np.float32)
+        k0 = int(rng.integers(0, K))
+        x[0, k0] = np.float32(rng.standard_normal())
+        e, _ = oracle.quant_act_fp8(x)
+        assert e[0, k0] == np.sign(x[0, k0]) * 448.0
+        assert np.count_nonzero(e) == 1
+    x = rng.standard_normal((4, 777)).astype(np.float32)
+    e0, s0 = oracle.quant_act_fp8(x)
+    for j in (-7, -1, 3, 9):
+        ej, sj = oracle.quant_act_fp8((x * np.float32(2.0 ** j)).astype(np.float32))
+        assert np.array_equal(ej, e0)
+        assert np.array_equal(sj, (s0 * np.float32(2.0 ** j)).astype(np.float32))
+
+
+def test_gemm_acc_fp8_brute_force():
+    rng = np.random.default_rng(17)
+    for _ in range(30):
+        M, N, K = (int(v) for v in rng.integers(1, 5, size=3))
+        T = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+        x = rng.standard_normal((M, K)).astype(np.float32)
+        e, _ = oracle.quant_act_fp8(x)
+        acc = oracle.gemm_acc_fp8(T, e)
+        for m, n in itertools.product(range(M), range(N)):
+            exact = sum(Fraction(int(T[n, k])) * Fraction(float(e[m, k])) for k in range(K))
+            assert Fraction(float(acc[m, n])) == exact
+
+
+def test_fp8_linear_identity_and_negation():
+    rng = np.random.default_rng(23)
+    K = 96
+    x = rng.standard_normal((3, K)).astype(np.float32)
+    I = np.eye(K, dtype=np.int8)
+    _, acc, e, _ = oracle.fp8_linear(I, np.float32(1), x)
+    assert np.array_equal(acc, e)
+    _, acc_n, _, _ = oracle.fp8_linear(-I, np.float32(1), x)
+    assert np.array_equal(acc_n, -e)
+    _, acc_x, e_x, _ = oracle.fp8_linear(I, np.float32(1), -x)
+    assert np.array_equal(e_x, -e) and np.array_equal(acc_x, -acc)
+    assert np.array_equal(oracle.fp8_linear(np.zeros((5, K), np.int8), np.float32(0.5), x)[1], np.zeros((3, 5)))
+
+
+def test_fp8_linear_dequant_exact_rational():
+    rng = np.random.default_rng(29)
+    T = rng.integers(-1, 2, size=(7, 200)).astype(np.int8)
+    x = rng.standard_normal((2, 200)).astype(np.float32)
+    w = np.float32(0.0371)
+    y, acc, _, a_scale = oracle.fp8_linear(T, w, x)
+    for m in range(2):
+        for n in range(7):
+            exact = Fraction(float(acc[m, n])) * Fraction(float(a_scale[m])) * Fraction(float(w))
+            assert y[m, n] == np.float32(float(exact))  # one rounding of the exact product
