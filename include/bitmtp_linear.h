@@ -87,6 +87,28 @@ extern "C" {
  * activation tile for 5..8 and a 16-row tile for 9..16.  Forcing the tensor
  * path at widths 1..4 uses its 8-row tile; forcing dp4a is valid for widths
  * 1..4.) */
+/* "Fast" draft projection with FP8 activations.  The pages run cheaper "fast"
+ * projections for drafting, more careful "critical" ones for generation and
+ * verification, and on H20 FP8 draft projections ("BitMTP: When Multi-Token
+ * Prediction Meets Low-Bit Large Language Models", "Methodology in Plain
+ * English", M1); they give no formula.  With this flag every problem of the
+ * call keeps its ternary weights and quantises its activation rows per row to
+ * FP8 E4M3 instead of int8:
+ *   s = RN32(448 / amax);  e = E4M3(RN32(x * s));  a_scale = RN32(amax / 448)
+ * (E4M3: 3 mantissa bits, exponent bias 7, no infinities, largest finite 448;
+ * round to nearest even, saturating), then y = acc * a_scale * w_scale with
+ * acc = sum_k T * e accumulated in fp32 on the tensor cores, as
+ * sum_k (T + 1) * e - sum_k e.  That accumulation rounds only where a partial
+ * sum needs more than 24 significant bits: acc differs from the exact sum by
+ * at most (2 * ceil(K/32) + 2) * 2^-23 * sum_k (T + 2) * |e|, and is exact
+ * when every partial sum fits in 24 bits (for example all |e| in one binade
+ * and |acc| below 2^24 of its steps).  The order of the partial sums may vary
+ * from run to run, so rounded results may differ in their last bits.  Every
+ * width 1..16 runs on the tensor cores with a 16-row tile.  act.kind must be
+ * BITMTP_F32 or BITMTP_BF16 (act.amax may be given, as above); out.acc, if
+ * given, receives the fp32 accumulators' bit patterns instead of int32
+ * values.  Not combinable with BITMTP_FLAG_FORCE_DP. */
+#define BITMTP_FLAG_FP8        0x8u
 /* Test only, never for production calls: CTA 0 of the launch never requests
  * its first chunk of packed weights and every wait of the launch gives up
  * after 1 ms instead of 2 s, so the launch exercises its bounded-wait error

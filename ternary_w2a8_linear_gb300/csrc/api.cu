@@ -526,6 +526,10 @@ int check_problem(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M
 // tile up to 8 rows, 16 rows above.
 int choose_path(int max_m, unsigned flags, int* dp_rows) {
     const int r = max_m <= 1 ? 1 : (max_m <= 2 ? 2 : 4);
+    if (flags & BITMTP_FLAG_FP8) {  // every width on the FP8 tensor path
+        *dp_rows = 1;
+        return (flags & BITMTP_FLAG_FORCE_DP) ? -1 : kPathF8;
+    }
     if (flags & BITMTP_FLAG_FORCE_DP) {
         if (max_m > 4) return -1;
         *dp_rows = r;
@@ -539,6 +543,18 @@ int choose_path(int max_m, unsigned flags, int* dp_rows) {
 }
 
 
+
+// The flag combinations a call accepts: not both forced paths; FP8
+// activations only from raw rows, and not on the dp4a path.
+int check_flags(const GemmProblem* g, int n, unsigned flags) {
+    if ((flags & BITMTP_FLAG_FORCE_TC) && (flags & BITMTP_FLAG_FORCE_DP)) return BITMTP_ERR_INVALID;
+    if (flags & BITMTP_FLAG_FP8) {
+        if (flags & BITMTP_FLAG_FORCE_DP) return BITMTP_ERR_INVALID;
+        for (int i = 0; i < n; ++i)
+            if (g[i].M > 0 && g[i].act_kind == BITMTP_Q8) return BITMTP_ERR_INVALID;
+    }
+    return BITMTP_OK;
+}
 
 int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes, unsigned flags,
               cudaStream_t stream) {
@@ -793,7 +809,8 @@ int bitmtp_linear_gemm(const void* pk, float w_scale, int64_t N, int64_t K, int6
     std::memset(&g, 0, sizeof(g));
     int st = check_problem(pk, w_scale, N, K, M, act, out, &g);
     if (st != BITMTP_OK) return st;
-    if ((flags & BITMTP_FLAG_FORCE_TC) && (flags & BITMTP_FLAG_FORCE_DP)) return BITMTP_ERR_INVALID;
+    st = check_flags(&g, 1, flags);
+    if (st != BITMTP_OK) return st;
     if (g.M == 0) return BITMTP_OK;
     return run_gemms(&g, 1, workspace, workspace_bytes, flags, static_cast<cudaStream_t>(stream));
 }
@@ -809,6 +826,8 @@ int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc, void* work
         int st = check_problem(d[i].pk, d[i].w_scale, d[i].N, d[i].K, d[i].M, &d[i].act, &d[i].out, &g[i]);
         if (st != BITMTP_OK) return st;
     }
+    const int fst = check_flags(g, n_desc, flags);
+    if (fst != BITMTP_OK) return fst;
     if (n_desc == 0) return BITMTP_OK;
     return run_gemms(g, n_desc, workspace, workspace_bytes, flags, static_cast<cudaStream_t>(stream));
 }
@@ -819,7 +838,8 @@ int bitmtp_linear_gemm_noalloc(const void* pk, float w_scale, int64_t N, int64_t
     std::memset(&g, 0, sizeof(g));
     int st = check_problem(pk, w_scale, N, K, M, act, out, &g);
     if (st != BITMTP_OK) return st;
-    if ((flags & BITMTP_FLAG_FORCE_TC) && (flags & BITMTP_FLAG_FORCE_DP)) return BITMTP_ERR_INVALID;
+    st = check_flags(&g, 1, flags);
+    if (st != BITMTP_OK) return st;
     if (g.M == 0) return BITMTP_OK;
     const size_t need = bitmtp_linear_workspace_bytes(N, K, M);
     if (need == 0 || need > BITMTP_NOALLOC_SCRATCH_BYTES) return BITMTP_ERR_SHAPE;

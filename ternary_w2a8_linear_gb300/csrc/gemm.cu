@@ -125,24 +125,27 @@ static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
 // Activation rows an operand tile holds (rows from M on are zero).
 __host__ __device__ constexpr int btile_rows(int path, int dp_rows) {
-    return path == kPathTC16 ? 16 : path == kPathTC8 ? 8 : dp_rows;
+    return (path == kPathTC16 || path == kPathF8) ? 16 : path == kPathTC8 ? 8 : dp_rows;
 }
-// Operand rows: the tensor paths keep two (h and l) per activation row.
+// Operand rows: the int8 tensor paths keep two (h and l) per activation row.
 __host__ __device__ constexpr int btile_brows(int path, int dp_rows) {
-    return path == kPathDP ? dp_rows : 2 * btile_rows(path, dp_rows);
+    return (path == kPathDP || path == kPathF8) ? btile_rows(path, dp_rows) : 2 * btile_rows(path, dp_rows);
 }
 // Bytes of one k tile of the activation operand: 8 units of 16 k, each
 // holding 16 bytes per operand row.
 __host__ __device__ constexpr int btile_bytes(int path, int dp_rows) { return btile_brows(path, dp_rows) * 128; }
 // Tensor-memory layout of the tensor paths: each accumulator is one fp32
-// column per B row (the MMA's N); the A buffers fill the rest of the 256
-// allocated columns (six at 16 rows, seven at 8).
+// column per B row (the MMA's N); the FP8 path keeps 16 columns of the
+// constant A operand -2^-9 at the end; the A buffers fill the rest of the 256
+// allocated columns (six at 16 rows, seven at 8, six for FP8).
+constexpr uint32_t kNegCols = 16;
 __host__ __device__ constexpr uint32_t tmem_d_cols(int path, int dp_rows) {
     return static_cast<uint32_t>(btile_brows(path, dp_rows));
 }
 __host__ __device__ constexpr uint32_t tmem_a_col(int path, int dp_rows) { return 2 * tmem_d_cols(path, dp_rows); }
+__host__ __device__ constexpr uint32_t tmem_neg_col(int path) { return path == kPathF8 ? kTmemCols - kNegCols : kTmemCols; }
 __host__ __device__ constexpr int tmem_a_tiles(int path, int dp_rows) {
-    return path == kPathDP ? 1 : static_cast<int>((kTmemCols - tmem_a_col(path, dp_rows)) / kATileCols);
+    return path == kPathDP ? 1 : static_cast<int>((tmem_neg_col(path) - tmem_a_col(path, dp_rows)) / kATileCols);
 }
 
 __device__ __forceinline__ void fail(Ctrl* c, int* err, int code) {
@@ -159,9 +162,17 @@ __device__ __forceinline__ void unpack_word_e4m3(uint32_t w, uint32_t* r) {
     r[3] = (w >> 6) & 0x03030303u;
 }
 
-// Two integer-valued floats (|v| <= 15, exact in e4m3) -> their e4m3 bytes:
-// a in bits 0-7, b in bits 8-15 (hardware conversion; no rounding happens).
-__device__ __forceinline__ uint32_t e4m3x2_small(float a, float b) {
+// One tile row's 32 bytes (eight words) -> 32 registers of e4m3 bytes u * 2^-9.
+__device__ __forceinline__ void unpack_row_e4m3(const uint4& a0, const uint4& a1, uint32_t (&r)[32]) {
+    const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) unpack_word_e4m3(w[i], r + 4 * i);
+}
+
+// Two floats -> their E4M3 bytes, a in bits 0-7, b in bits 8-15 (hardware
+// conversion: round to nearest even, saturating at +-448).  The int8 paths
+// pass integer values |v| <= 15, which are exact in E4M3.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
     return r;
@@ -361,6 +372,7 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     constexpr int kBRows = btile_brows(PATH, DPR);
     constexpr int BT = btile_bytes(PATH, DPR);
     constexpr int kPass = kPrepThreads * kPrepUnits;  // 16-element units per pass
+    constexpr bool kF8 = PATH == kPathF8;             // E4M3 values instead of int8 codes
     __shared__ float red[kPrepThreads / 32];
     __shared__ int tsum[BITMTP_MAX_K / kTileK];
     pdl_launch_dependents();  // the GEMM may start streaming weights now
@@ -388,7 +400,7 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     float amax = 0.f, s = 0.f;
     if (have_amax) {
         amax = live ? __ldcg(pr.amax_in + m) : 0.f;
-        s = quant_scale(amax);
+        s = kF8 ? fp8_quant_scale(amax) : quant_scale(amax);
     }
     // Passes 0..npass-1 find the row's absmax; the quantisation then takes
     // the last pass first, from the values still in registers, and reads the
@@ -424,7 +436,7 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
                 amax = red[0];
 #pragma unroll
                 for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
-                s = quant_scale(amax);
+                s = kF8 ? fp8_quant_scale(amax) : quant_scale(amax);
             }
             continue;
         }
@@ -435,6 +447,21 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
             if (ps * kPass + j * kPrepThreads >= nunits) break;  // uniform over the block
             const int u = ps * kPass + j * kPrepThreads + tid;
             const bool uv = u < nunits;
+            if constexpr (kF8) {
+                // operand row m: E4M3(RN32(x * s)), rounded by the conversion
+                // (an all-zero row has s = 0); register si holds k = {2si,
+                // 2si+8, 2si+1, 2si+9} as below
+                uint8_t* unit = pr.actb + static_cast<size_t>(u >> 3) * BT + (u & 7) * (kBRows * 16);
+                uint32_t er[4];
+#pragma unroll
+                for (int si = 0; si < 4; ++si) {
+                    const int k0 = 2 * si, k1 = 2 * si + 8, k2 = 2 * si + 1, k3 = 2 * si + 9;
+                    er[si] = e4m3x2(__fmul_rn(v[j][k0], s), __fmul_rn(v[j][k1], s)) |
+                             (e4m3x2(__fmul_rn(v[j][k2], s), __fmul_rn(v[j][k3], s)) << 16);
+                }
+                if (uv) *reinterpret_cast<uint4*>(unit + m * 16) = make_uint4(er[0], er[1], er[2], er[3]);
+                continue;
+            }
             // codes as exact small floats: clamp(rint(RN(x * s))) gives the same
             // values as the integer quantiser (quant.cuh), without conversions
             float qf[16];
@@ -470,9 +497,9 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
 #pragma unroll
                 for (int si = 0; si < 4; ++si) {
                     const int k0 = 2 * si, k1 = 2 * si + 8, k2 = 2 * si + 1, k3 = 2 * si + 9;
-                    hr[si] = e4m3x2_small(h[k0], h[k1]) | (e4m3x2_small(h[k2], h[k3]) << 16);
-                    lr[si] = e4m3x2_small(fmaf(h[k0], -16.f, qf[k0]), fmaf(h[k1], -16.f, qf[k1])) |
-                             (e4m3x2_small(fmaf(h[k2], -16.f, qf[k2]), fmaf(h[k3], -16.f, qf[k3])) << 16);
+                    hr[si] = e4m3x2(h[k0], h[k1]) | (e4m3x2(h[k2], h[k3]) << 16);
+                    lr[si] = e4m3x2(fmaf(h[k0], -16.f, qf[k0]), fmaf(h[k1], -16.f, qf[k1])) |
+                             (e4m3x2(fmaf(h[k2], -16.f, qf[k2]), fmaf(h[k3], -16.f, qf[k3])) << 16);
                 }
                 if (uv) {
                     *reinterpret_cast<uint4*>(unit + m * 16) = make_uint4(hr[0], hr[1], hr[2], hr[3]);
@@ -486,8 +513,11 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     }
     __syncthreads();
 
-    // rsp[m][0] = 0, rsp[m][t + 1] = codes of k tiles 0..t summed
-    if (warp == 0) {
+    // rsp[m][0] = 0, rsp[m][t + 1] = codes of k tiles 0..t summed (int8
+    // paths; the FP8 path needs no code sums)
+    if (kF8) {
+        if (tid == 0) pr.asc[m] = fp8_dequant_scale(amax);
+    } else if (warp == 0) {
         const int KT = pr.kt;
         int* rsp = pr.rsp + m * (KT + 1);
         const int per = (KT + 31) / 32;
@@ -514,8 +544,12 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
 
 // ------------------------------------------------------------ epilogue --
 // Store y[m][n] (and acc); returns |y[m][n]| as stored.
+// kF: acc holds an fp32 accumulator's bit pattern (FP8 path), else an exact
+// integer sum.
+template <bool kF>
 __device__ __forceinline__ float store_out(const GemmProblem& pr, int m, int n, int acc, float a_scale) {
-    const float v = __fmul_rn(__fmul_rn(static_cast<float>(acc), a_scale), pr.w_scale);
+    const float a = kF ? __int_as_float(acc) : static_cast<float>(acc);
+    const float v = __fmul_rn(__fmul_rn(a, a_scale), pr.w_scale);
     const long long o = static_cast<long long>(m) * pr.ldy + n;
     float stored = v;
     if (pr.out_dtype == BITMTP_F32) {
@@ -555,13 +589,21 @@ __device__ __forceinline__ int seg_role(const Seg& s, const GemmProblem& pr) {
     return s.ka == 0 ? kWhole : kOwner;
 }
 
+// Partial sums of one output: integers, or fp32 bit patterns (kF).
+template <bool kF>
+__device__ __forceinline__ int acc_add(int a, int b) {
+    return kF ? __float_as_int(__fadd_rn(__int_as_float(a), __int_as_float(b))) : a + b;
+}
+
 // Finish one segment.  acc[m]: the exact sum_k T*q of the segment for the
-// thread's output column (row tile column tid) and block row m.  kRows: the
+// thread's output column (row tile column tid) and block row m (kF: the fp32
+// sum_k T*e of the FP8 path, as bit patterns; contributors' partial sums are
+// then added in CTA order).  kRows: the
 // compute path's rows per tile, a compile-time bound on M that keeps the
 // unrolled row loops (and the code) short.  owner_first: the first CTA of the
 // owner segment's row tile.  Every consumer thread calls it with the same
 // segment (the named barriers below need all four warps).
-template <int kRows>
+template <int kRows, bool kF>
 __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int p_lo, const Seg& s, int owner_first,
                                  int (&acc)[16], int tid, bool& alive) {
     const GemmProblem& pr = c->prob[s.pi];
@@ -601,10 +643,10 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int p_lo, const S
                 for (int g = 0; g < kGroups; ++g) {
                     if (4 * g < M) {
                         const int4 v = __ldcg(slot_ptr(P, cc, g, tid));
-                        acc[4 * g] += v.x;
-                        acc[4 * g + 1] += v.y;
-                        acc[4 * g + 2] += v.z;
-                        acc[4 * g + 3] += v.w;
+                        acc[4 * g] = acc_add<kF>(acc[4 * g], v.x);
+                        acc[4 * g + 1] = acc_add<kF>(acc[4 * g + 1], v.y);
+                        acc[4 * g + 2] = acc_add<kF>(acc[4 * g + 2], v.z);
+                        acc[4 * g + 3] = acc_add<kF>(acc[4 * g + 3], v.w);
                     }
                 }
             }
@@ -616,7 +658,7 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int p_lo, const S
     if (alive && n < pr.N) {
 #pragma unroll
         for (int m = 0; m < kRows; ++m)
-            if (m < M) am[m] = store_out(pr, m, n, acc[m], c->asc[s.pi - p_lo][m]);
+            if (m < M) am[m] = store_out<kF>(pr, m, n, acc[m], c->asc[s.pi - p_lo][m]);
     }
     if (pr.amax_out) {
         // first phase of the output rows' absmax: this warp's 32 columns, one
@@ -652,13 +694,15 @@ __global__ void __maxnreg__(gemm_max_regs(PATH))
 w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr bool kTC = PATH != kPathDP;
+    constexpr bool kF8 = PATH == kPathF8;  // fp32 accumulators (bit patterns in the int arrays)
     constexpr int BT = btile_bytes(PATH, DPR);
     constexpr int kOutRows = btile_rows(PATH, DPR);  // M <= kOutRows (the host's path choice)
     constexpr uint32_t kDCols = tmem_d_cols(PATH, DPR);
     constexpr uint32_t kACol = tmem_a_col(PATH, DPR);
     constexpr int kATiles = tmem_a_tiles(PATH, DPR);
+    constexpr uint32_t kNegCol = tmem_neg_col(PATH);
     static_assert(!kTC || (kATiles <= kMaxATiles && kATiles < kBatchBars && kDCols <= 32 &&
-                           kACol + kATiles * kATileCols <= kTmemCols), "tensor-memory layout");
+                           kACol + kATiles * kATileCols <= kNegCol), "tensor-memory layout");
     using RP = RingPos<kATiles>;
     Ctrl* c = reinterpret_cast<Ctrl*>(smem);
     const int R = P.stages;                                  // chunks in the ring
@@ -853,6 +897,14 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         mma_f8_ts_acc_if(leader, dcol, a0 + 8, b0 + kStepDesc, kIdesc);
                         mma_f8_ts_acc_if(leader, dcol, a0 + 16, b0 + 2 * kStepDesc, kIdesc);
                         mma_f8_ts_acc_if(leader, dcol, a0 + 24, b0 + 3 * kStepDesc, kIdesc);
+                        if constexpr (kF8) {
+                            // sum_k u*e*2^-9 - sum_k e*2^-9 = 2^-9 * sum_k T*e
+                            const uint32_t an = tmem + kNegCol;
+                            mma_f8_ts_acc_if(leader, dcol, an, b0, kIdesc);
+                            mma_f8_ts_acc_if(leader, dcol, an, b0 + kStepDesc, kIdesc);
+                            mma_f8_ts_acc_if(leader, dcol, an, b0 + 2 * kStepDesc, kIdesc);
+                            mma_f8_ts_acc_if(leader, dcol, an, b0 + 3 * kStepDesc, kIdesc);
+                        }
                         const uint32_t on1 = nb > 1 ? leader : 0u;
                         const uint64_t b1 = bdesc0 + static_cast<uint64_t>(r1.slot()) * kTileDesc;
                         const uint32_t a1 = tmem + kACol + r1.ab * kATileCols;
@@ -860,6 +912,13 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         mma_f8_ts_acc_if(on1, dcol, a1 + 8, b1 + kStepDesc, kIdesc);
                         mma_f8_ts_acc_if(on1, dcol, a1 + 16, b1 + 2 * kStepDesc, kIdesc);
                         mma_f8_ts_acc_if(on1, dcol, a1 + 24, b1 + 3 * kStepDesc, kIdesc);
+                        if constexpr (kF8) {
+                            const uint32_t an = tmem + kNegCol;
+                            mma_f8_ts_acc_if(on1, dcol, an, b1, kIdesc);
+                            mma_f8_ts_acc_if(on1, dcol, an, b1 + kStepDesc, kIdesc);
+                            mma_f8_ts_acc_if(on1, dcol, an, b1 + 2 * kStepDesc, kIdesc);
+                            mma_f8_ts_acc_if(on1, dcol, an, b1 + 3 * kStepDesc, kIdesc);
+                        }
                         mma_commit_if(leader, smem_u32(&c->mma_done[nbatch % kBatchBars]));
                     }
                     // chunk ends inside the batch: this warp's MMAs so far read them
@@ -905,6 +964,13 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             if (tid % 16 < pr.M) asc_reg = __ldcg(pr.asc + tid % 16);
         }
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        if constexpr (kF8) {
+            // the constant A operand -2^-9 (e4m3 0x81) of the FP8 path's
+            // correction MMAs; ordered before them by this warp's first
+            // A-tile arrival (wait::st, fence, mbarrier)
+            tmem_st16_fill(tmem + lane_base + kNegCol, 0x81818181u);
+            tc_wait_st();
+        }
         bool alive = true;
         int seg_idx = 0;
         RP rp;
@@ -933,7 +999,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 named_bar_sync(kBarEpi, 128);
                 first_epi = false;
             }
-            segment_epilogue<kOutRows>(P, c, p0, es, owner_first, acc, tid, alive);
+            segment_epilogue<kOutRows, kF8>(P, c, p0, es, owner_first, acc, tid, alive);
         };
         auto finish_deferred = [&]() {
             int acc[16];
@@ -956,13 +1022,20 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                     tc_fence_after();
                     uint32_t v[32];
                     tmem_ld16(dcol, *reinterpret_cast<uint32_t(*)[16]>(v));
-                    if constexpr (kRows == 16) tmem_ld16(dcol + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+                    if constexpr (kDCols == 32) tmem_ld16(dcol + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
                     tc_wait_ld();
                     tc_fence_before();
+                    if constexpr (kF8) {
+                        // FP8: D column m is row m's fp32 sum of T * e * 2^-9
 #pragma unroll
-                    for (int m = 0; m < kRows; ++m) {
-                        const float d = __fadd_rn(__fmul_rn(__uint_as_float(v[m]), 16.f), __uint_as_float(v[m + kRows]));
-                        acc[m] = __float2int_rn(__fmul_rn(d, 512.f)) - code_sum(d_rsl, m);
+                        for (int m = 0; m < kRows; ++m) acc[m] = __float_as_int(__fmul_rn(__uint_as_float(v[m]), 512.f));
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < kRows; ++m) {
+                            const float d = __fadd_rn(__fmul_rn(__uint_as_float(v[m]), 16.f),
+                                                      __uint_as_float(v[m + kRows]));
+                            acc[m] = __float2int_rn(__fmul_rn(d, 512.f)) - code_sum(d_rsl, m);
+                        }
                     }
                 }
             }
@@ -977,7 +1050,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             const GemmProblem& pr = pp[sg.pi];
             const int ka = sg.ka;
             const int len = sg.kb - sg.ka;
-            const int rsl = load_code_sum_lane(pr, ka, ka + len, lane);
+            const int rsl = kF8 ? 0 : load_code_sum_lane(pr, ka, ka + len, lane);
             int dacc[4][DPR];
 #pragma unroll
             for (int s4 = 0; s4 < 4; ++s4)
@@ -1048,24 +1121,10 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                             b1 = *reinterpret_cast<const uint4*>(wb + 2048);
                         }
                         uint32_t r[32];  // A columns 4w + s: word w (16 k), register s
-                        unpack_word_e4m3(a0.x, r + 0);
-                        unpack_word_e4m3(a0.y, r + 4);
-                        unpack_word_e4m3(a0.z, r + 8);
-                        unpack_word_e4m3(a0.w, r + 12);
-                        unpack_word_e4m3(a1.x, r + 16);
-                        unpack_word_e4m3(a1.y, r + 20);
-                        unpack_word_e4m3(a1.z, r + 24);
-                        unpack_word_e4m3(a1.w, r + 28);
+                        unpack_row_e4m3(a0, a1, r);
                         tmem_st32(tmem + lane_base + kACol + rp.ab * kATileCols, r);
                         if (nb > 1) {
-                            unpack_word_e4m3(b0.x, r + 0);
-                            unpack_word_e4m3(b0.y, r + 4);
-                            unpack_word_e4m3(b0.z, r + 8);
-                            unpack_word_e4m3(b0.w, r + 12);
-                            unpack_word_e4m3(b1.x, r + 16);
-                            unpack_word_e4m3(b1.y, r + 20);
-                            unpack_word_e4m3(b1.z, r + 24);
-                            unpack_word_e4m3(b1.w, r + 28);
+                            unpack_row_e4m3(b0, b1, r);
                             tmem_st32(tmem + lane_base + kACol + r1.ab * kATileCols, r);
                         }
                         tc_wait_st();
@@ -1220,6 +1279,7 @@ size_t gemm_smem_bytes(int path, int dp_rows, int stages) {
 cudaError_t launch_gemm(const GemmParams& prm, int path, int dp_rows, bool pdl, cudaStream_t stream) {
     if (path == kPathTC16) return launch_one<kPathTC16, 1>(prm, pdl, stream);
     if (path == kPathTC8) return launch_one<kPathTC8, 1>(prm, pdl, stream);
+    if (path == kPathF8) return launch_one<kPathF8, 1>(prm, pdl, stream);
     if (dp_rows <= 1) return launch_one<kPathDP, 1>(prm, pdl, stream);
     if (dp_rows <= 2) return launch_one<kPathDP, 2>(prm, pdl, stream);
     return launch_one<kPathDP, 4>(prm, pdl, stream);

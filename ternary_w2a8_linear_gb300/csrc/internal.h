@@ -18,6 +18,7 @@ enum ComputePath : int {
     kPathTC16 = 0,  // tcgen05, block width 9..16: B = 32 operand rows (h and l of 16 rows), 4096 B
     kPathTC8 = 1,   // tcgen05, block width 5..8:  B = 16 operand rows, 2048 B
     kPathDP = 2,    // dp4a, block width 1..4:     B = dp_rows rows of int8 codes, 128 B per row
+    kPathF8 = 3,    // tcgen05, FP8 activations (any width 1..16): B = 16 rows of E4M3 values, 2048 B
 };
 
 // GEMM block: warps 0-3 compute + epilogue, 4 bulk copies; the tensor paths

@@ -23,6 +23,14 @@ __device__ __forceinline__ float quant_scale(float amax) {
 __device__ __forceinline__ float dequant_scale(float amax) {
     return amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
 }
+// FP8 (E4M3) activations: the same steps with the largest finite E4M3 value,
+// 448, in place of 127.
+__device__ __forceinline__ float fp8_quant_scale(float amax) {
+    return amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+}
+__device__ __forceinline__ float fp8_dequant_scale(float amax) {
+    return amax > 0.f ? __fdiv_rn(amax, 448.f) : 0.f;
+}
 __device__ __forceinline__ int quantize(float v, float s) {
     int q = __float2int_rn(__fmul_rn(v, s));
     return max(-127, min(127, q));

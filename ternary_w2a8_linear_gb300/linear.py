@@ -26,6 +26,7 @@ ERR_INVALID, ERR_ALIGN, ERR_SHAPE, ERR_NOT_TERNARY, ERR_UNSUPPORTED, ERR_CUDA, E
     range(-1, -9, -1)
 F32, BF16, Q8 = 0, 1, 2
 FLAG_PDL, FLAG_FORCE_TC, FLAG_FORCE_DP, FLAG_TEST_WITHHOLD = 0x1, 0x2, 0x4, 0x100
+FLAG_FP8 = 0x8  # "fast" draft projection: FP8 (E4M3) activations; acc holds fp32 bit patterns
 MAX_M, MAX_K, MAX_N, MAX_GROUP = 16, 32768, 16777216, 8
 NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
@@ -337,7 +338,9 @@ def gemm(pk: torch.Tensor, w_scale: float, N: int, K: int, x: torch.Tensor,
          workspace_tensor: torch.Tensor | None = None):
     """y = W2A8 linear of x ([M, K] fp32 / bf16 raw, or int8 codes with a_scale).
 
-    Returns y, or (y, acc) when ``acc`` is True or a tensor."""
+    Returns y, or (y, acc) when ``acc`` is True or a tensor.  With FLAG_FP8
+    the int32 acc tensor holds the fp32 accumulators' bit patterns
+    (``acc.view(torch.float32)``)."""
     M = x.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=out_dtype, device=x.device)

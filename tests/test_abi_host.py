@@ -158,6 +158,11 @@ def test_gemm_validation(lib):
     assert gemm(out=_out(acc=FAKE, lda=3)) == L.ERR_INVALID
     assert gemm(w=float("nan")) == L.ERR_INVALID
     assert gemm(flags=L.FLAG_FORCE_TC | L.FLAG_FORCE_DP) == L.ERR_INVALID
+    # FP8 activations: raw rows only, never the dp4a path
+    assert gemm(act=_act(kind=L.Q8, a_scale=FAKE), flags=L.FLAG_FP8) == L.ERR_INVALID
+    assert gemm(flags=L.FLAG_FP8 | L.FLAG_FORCE_DP) == L.ERR_INVALID
+    assert gemm(M=0, act=_act(kind=L.Q8, a_scale=FAKE), flags=L.FLAG_FP8) == L.OK  # empty: a no-op
+    assert gemm(M=17, flags=L.FLAG_FP8) == L.ERR_SHAPE
     assert L.load().bitmtp_linear_gemm(FAKE, 0.02, 64, 64, 4, None, ctypes.byref(_out()), FAKE, WS, 0,
                                        None) == L.ERR_INVALID
     assert gemm(ws=None) == L.ERR_INVALID
@@ -180,6 +185,9 @@ def test_grouped_validation(lib):
     assert grp([good], None, 0, 0, None) == L.ERR_INVALID
     need = L.bitmtp_linear_workspace_bytes_grouped([good, good])
     assert grp([good, good], FAKE, need - 16, 0, None) == L.ERR_SHAPE
+    q8 = L.GemmDesc(FAKE, 0.02, 64, 64, 4, _act(kind=L.Q8, a_scale=FAKE), _out())
+    assert grp([good, q8], FAKE, WS, L.FLAG_FP8, None) == L.ERR_INVALID
+    assert grp([good], FAKE, WS, L.FLAG_FP8 | L.FLAG_FORCE_DP, None) == L.ERR_INVALID
 
 
 def test_workspace_bytes(lib):
@@ -206,6 +214,7 @@ def test_noalloc_validation(lib):
     assert na(FAKE, 0.02, 64, 64, 17, _act(), _out(), 0, None) == L.ERR_SHAPE
     assert na(FAKE, 0.02, 64, L.MAX_K + 1, 4, _act(), _out(), 0, None) == L.ERR_SHAPE
     assert na(FAKE, 0.02, 64, 64, 8, _act(), _out(), L.FLAG_FORCE_DP, None) == L.ERR_SHAPE
+    assert na(FAKE, 0.02, 64, 64, 8, _act(kind=L.Q8, a_scale=FAKE), _out(), L.FLAG_FP8, None) == L.ERR_INVALID
     assert na(None, 0.02, 64, 64, 4, _act(), _out(), 0, None) == L.ERR_INVALID
     assert na(FAKE, 0.02, 64, 64, 0, _act(), _out(), 0, None) == L.OK
     # the built-in array covers the workspace of every shape inside the limits
