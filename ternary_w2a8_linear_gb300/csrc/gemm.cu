@@ -135,15 +135,15 @@ __host__ __device__ constexpr int btile_brows(int path, int dp_rows) {
 // holding 16 bytes per operand row.
 __host__ __device__ constexpr int btile_bytes(int path, int dp_rows) { return btile_brows(path, dp_rows) * 128; }
 // Tensor-memory layout of the tensor paths: each accumulator is one fp32
-// column per B row (the MMA's N); the FP8 path keeps 16 columns of the
-// constant A operand -2^-9 at the end; the A buffers fill the rest of the 256
-// allocated columns (six at 16 rows, seven at 8, six for FP8).
-constexpr uint32_t kNegCols = 16;
+// column per B row (the MMA's N); the last 8 columns hold the constant A
+// operand -2^-9 (one MMA's 32 k); the A buffers fill the rest of the 256
+// allocated columns (five at 16 rows, six at 8 and for FP8).
+constexpr uint32_t kNegCols = 8;
 __host__ __device__ constexpr uint32_t tmem_d_cols(int path, int dp_rows) {
     return static_cast<uint32_t>(btile_brows(path, dp_rows));
 }
 __host__ __device__ constexpr uint32_t tmem_a_col(int path, int dp_rows) { return 2 * tmem_d_cols(path, dp_rows); }
-__host__ __device__ constexpr uint32_t tmem_neg_col(int path) { return path == kPathF8 ? kTmemCols - kNegCols : kTmemCols; }
+__host__ __device__ constexpr uint32_t tmem_neg_col(int path) { return path == kPathDP ? kTmemCols : kTmemCols - kNegCols; }
 __host__ __device__ constexpr int tmem_a_tiles(int path, int dp_rows) {
     return path == kPathDP ? 1 : static_cast<int>((tmem_neg_col(path) - tmem_a_col(path, dp_rows)) / kATileCols);
 }
@@ -360,8 +360,9 @@ __device__ __forceinline__ const char* act_row(const GemmProblem& pr, int m) {
 
 // ---------------------------------------------------- activation operand --
 // One CTA per (problem, row m < btile_rows).  Writes row m of every
-// activation tile of the problem (zeros for m >= M and beyond K), the prefix
-// sums rsp[m][0..kt] of the row's codes over k tiles, and asc[m].  Each
+// activation tile of the problem (zeros for m >= M and beyond K), on the
+// dp4a path the prefix sums rsp[m][0..kt] of the row's codes over k tiles,
+// and asc[m].  Each
 // thread owns whole 16-k units; rows of up to kPass units (K <= 16384) stay in
 // registers between the absmax and the quantisation (one pass over the row),
 // longer rows are read twice.  512 threads, at most 64 registers each.
@@ -441,7 +442,9 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
             continue;
         }
         // Eight consecutive threads cover one k tile; units per pass and units
-        // of the row are multiples of 8, so the 8-lane sums below see whole tiles.
+        // of the row are multiples of 8, so the 8-lane sums below see whole
+        // tiles (the dp4a path's code sums; the tensor paths correct for the
+        // weight offset with an MMA instead).
 #pragma unroll
         for (int j = 0; j < kPrepUnits; ++j) {
             if (ps * kPass + j * kPrepThreads >= nunits) break;  // uniform over the block
@@ -506,17 +509,21 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
                     *reinterpret_cast<uint4*>(unit + (m + kRows) * 16) = make_uint4(lr[0], lr[1], lr[2], lr[3]);
                 }
             }
+            if constexpr (PATH == kPathDP) {
 #pragma unroll
-            for (int o = 1; o < 8; o <<= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, o);
-            if (uv && (tid & 7) == 0) tsum[kt] = rsum;
+                for (int o = 1; o < 8; o <<= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, o);
+                if (uv && (tid & 7) == 0) tsum[kt] = rsum;
+            }
         }
     }
     __syncthreads();
 
-    // rsp[m][0] = 0, rsp[m][t + 1] = codes of k tiles 0..t summed (int8
-    // paths; the FP8 path needs no code sums)
-    if (kF8) {
-        if (tid == 0) pr.asc[m] = fp8_dequant_scale(amax);
+    // rsp[m][0] = 0, rsp[m][t + 1] = codes of k tiles 0..t summed (dp4a
+    // path only)
+    if (PATH != kPathDP) {
+        if (tid == 0)
+            pr.asc[m] = kF8 ? fp8_dequant_scale(amax)
+                            : (raw ? dequant_scale(amax) : (live ? pr.a_scale_in[m] : 0.f));
     } else if (warp == 0) {
         const int KT = pr.kt;
         int* rsp = pr.rsp + m * (KT + 1);
@@ -897,8 +904,9 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         mma_f8_ts_acc_if(leader, dcol, a0 + 8, b0 + kStepDesc, kIdesc);
                         mma_f8_ts_acc_if(leader, dcol, a0 + 16, b0 + 2 * kStepDesc, kIdesc);
                         mma_f8_ts_acc_if(leader, dcol, a0 + 24, b0 + 3 * kStepDesc, kIdesc);
-                        if constexpr (kF8) {
-                            // sum_k u*e*2^-9 - sum_k e*2^-9 = 2^-9 * sum_k T*e
+                        {
+                            // the correction: sum_k u*b*2^-9 - sum_k b*2^-9 =
+                            // 2^-9 * sum_k T*b for every operand row b
                             const uint32_t an = tmem + kNegCol;
                             mma_f8_ts_acc_if(leader, dcol, an, b0, kIdesc);
                             mma_f8_ts_acc_if(leader, dcol, an, b0 + kStepDesc, kIdesc);
@@ -912,7 +920,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                         mma_f8_ts_acc_if(on1, dcol, a1 + 8, b1 + kStepDesc, kIdesc);
                         mma_f8_ts_acc_if(on1, dcol, a1 + 16, b1 + 2 * kStepDesc, kIdesc);
                         mma_f8_ts_acc_if(on1, dcol, a1 + 24, b1 + 3 * kStepDesc, kIdesc);
-                        if constexpr (kF8) {
+                        {
                             const uint32_t an = tmem + kNegCol;
                             mma_f8_ts_acc_if(on1, dcol, an, b1, kIdesc);
                             mma_f8_ts_acc_if(on1, dcol, an, b1 + kStepDesc, kIdesc);
@@ -964,11 +972,11 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             if (tid % 16 < pr.M) asc_reg = __ldcg(pr.asc + tid % 16);
         }
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        if constexpr (kF8) {
-            // the constant A operand -2^-9 (e4m3 0x81) of the FP8 path's
-            // correction MMAs; ordered before them by this warp's first
-            // A-tile arrival (wait::st, fence, mbarrier)
-            tmem_st16_fill(tmem + lane_base + kNegCol, 0x81818181u);
+        if constexpr (kTC) {
+            // the constant A operand -2^-9 (e4m3 0x81) of the correction
+            // MMAs; ordered before them by this warp's first A-tile arrival
+            // (wait::st, fence, mbarrier)
+            tmem_st8_fill(tmem + lane_base + kNegCol, 0x81818181u);
             tc_wait_st();
         }
         bool alive = true;
@@ -992,7 +1000,6 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         ds.pi = ds.rt = ds.ka = ds.kb = 0;
         ds.t0 = 0;
         int d_seg = 0;
-        int d_rsl = 0;  // the deferred segment's prefix-sum lane value (code_sum)
         auto epilogue = [&](const Seg& es, int (&acc)[16]) {
             if (first_epi) {  // publish the dequant scales once
                 if (asc_mine) c->asc[tid / 16][tid % 16] = asc_reg;
@@ -1032,9 +1039,10 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                     } else {
 #pragma unroll
                         for (int m = 0; m < kRows; ++m) {
+                            // D holds 2^-9 * sum_k T*h and 2^-9 * sum_k T*l, exact
                             const float d = __fadd_rn(__fmul_rn(__uint_as_float(v[m]), 16.f),
                                                       __uint_as_float(v[m + kRows]));
-                            acc[m] = __float2int_rn(__fmul_rn(d, 512.f)) - code_sum(d_rsl, m);
+                            acc[m] = __float2int_rn(__fmul_rn(d, 512.f));
                         }
                     }
                 }
@@ -1050,7 +1058,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             const GemmProblem& pr = pp[sg.pi];
             const int ka = sg.ka;
             const int len = sg.kb - sg.ka;
-            const int rsl = kF8 ? 0 : load_code_sum_lane(pr, ka, ka + len, lane);
+            const int rsl = kTC ? 0 : load_code_sum_lane(pr, ka, ka + len, lane);
             int dacc[4][DPR];
 #pragma unroll
             for (int s4 = 0; s4 < 4; ++s4)
@@ -1177,7 +1185,6 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 if (dv) finish_deferred();  // the previous segment, if this one was short
                 ds = sg;
                 d_seg = seg_idx;
-                d_rsl = rsl;
                 dv = true;
             } else {
                 int acc[16];

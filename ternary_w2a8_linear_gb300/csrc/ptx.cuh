@@ -165,6 +165,13 @@ __device__ __forceinline__ void tmem_st32_fill(uint32_t taddr, uint32_t v) {
         :: "r"(taddr), "r"(v) : "memory");
 }
 
+// Store the value v to 8 consecutive 32-bit columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st8_fill(uint32_t taddr, uint32_t v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1};"
+        :: "r"(taddr), "r"(v) : "memory");
+}
+
 // Store the value v to 16 consecutive 32-bit columns of this warp's 32 lanes.
 __device__ __forceinline__ void tmem_st16_fill(uint32_t taddr, uint32_t v) {
     asm volatile(
