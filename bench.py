@@ -21,6 +21,10 @@ as a fraction of the measured copy bandwidth, and rows/s, at block widths
      2560 -> 32000 projection, rows 4-15 through a 2560 -> 2560 one, P(0)
      0.2 / 0.5 / 0.8, activations quantised to int8 first).
 
+Workloads 2 and 4 are also timed as "fast" draft projections (FP8 E4M3
+activations, BITMTP_FLAG_FP8); those figures are reported beside the W2A8
+ones and are not part of the headline value.
+
 A call is two launches: the activation preparation (absmax quantisation of
 the raw rows into the operand tiles) and the GEMM (2-bit weight stream, exact
 integer product, dequant), which starts streaming weights while the first
@@ -65,7 +69,7 @@ FALLBACK_HBM_GBS = 6800.0
 # the hash of the library sources it was taken with; reported only while the
 # sources are unchanged.  24beaa7b579ebcb9: the 216 launches of one step
 # (108 preparation + 108 GEMM), profiles/w2a8_streamk_large36_stack.md.
-CAPTURED_TRAFFIC: dict[str, int] = {"ae0eae0fa9056ac8": 4_996_088_064}
+CAPTURED_TRAFFIC: dict[str, int] = {"6b7aef6b87d75f89": 4_993_303_552}
 KERNEL_SOURCES = ("ternary_w2a8_linear_gb300/csrc/gemm.cu", "ternary_w2a8_linear_gb300/csrc/api.cu",
                   "ternary_w2a8_linear_gb300/csrc/internal.h", "ternary_w2a8_linear_gb300/csrc/ptx.cuh",
                   "ternary_w2a8_linear_gb300/csrc/quant.cuh", "include/bitmtp_linear.h")
@@ -352,6 +356,15 @@ def run_ours(args, rank, world):
         per_width[str(M)] = entry(inputs.LARGE_LAYERS * layer_set_bytes(inputs.LARGE_PROJ, M), t, M, peak)
         per_width[str(M)]["us_per_layer"] = round(t * 1e6 / inputs.LARGE_LAYERS, 2)
         del g
+    # the same stack as "fast" draft projections: FP8 (E4M3) activations
+    fp8_per_width = {}
+    for M in HEADLINE_WIDTHS:
+        g, _ = graph_of(torch, stream, lambda M=M: sum(large.grouped(l, M, cs, L.FLAG_PDL | L.FLAG_FP8)
+                                                       for l in range(inputs.LARGE_LAYERS)))
+        t = time_graph(torch, stream, g, 5)
+        fp8_per_width[str(M)] = entry(inputs.LARGE_LAYERS * layer_set_bytes(inputs.LARGE_PROJ, M), t, M, peak)
+        fp8_per_width[str(M)]["us_per_layer"] = round(t * 1e6 / inputs.LARGE_LAYERS, 2)
+        del g
 
     # the headline's layer 0 outputs at each width, for the oracle check
     check_outputs = {}
@@ -369,7 +382,8 @@ def run_ours(args, rank, world):
         raise RuntimeError(f"device error word set: {err:#x}")
     host_check = {"layer0": {p: large.host[p] for p in range(len(inputs.LARGE_PROJ))},
                   "outputs": {M: [bits_of(torch, y) for y in ys] for M, ys in check_outputs.items()}}
-    return dict(value=value, ms_per_step=ms_per_step, clocks=clocks, per_width=per_width, e2e=e2e,
+    return dict(value=value, ms_per_step=ms_per_step, clocks=clocks, per_width=per_width,
+                fp8_per_width=fp8_per_width, e2e=e2e,
                 per_config=per_config, tern=tern, gpu_launches=args.steps * launches_per_step,
                 launches_per_step=launches_per_step, host_check=host_check)
 
@@ -388,12 +402,13 @@ def run_configs(L, torch, dev, stream, peak):
     ls = Stack(L, torch, dev, inputs.BITNET2B_PROJ, copies,
                lambda p: (*inputs.bitnet2b_weights(p), inputs.bitnet2b_act(p, inputs.MAX_ROWS)),
                20_000, 0.5, True)
-    w2 = {"grouped": {}, "chained": {}}
+    w2 = {"grouped": {}, "chained": {}, "fp8_grouped": {}}
     G = 32
-    for mode in ("grouped", "chained"):
+    for mode in ("grouped", "chained", "fp8_grouped"):
+        fl = L.FLAG_PDL | (L.FLAG_FP8 if mode == "fp8_grouped" else 0)
         for M in range(1, inputs.MAX_ROWS + 1):
-            fn = ls.grouped if mode == "grouped" else ls.chained
-            g, _ = graph_of(torch, stream, lambda M=M, fn=fn: sum(fn(c % copies, M, cs, L.FLAG_PDL) for c in range(G)))
+            fn = ls.chained if mode == "chained" else ls.grouped
+            g, _ = graph_of(torch, stream, lambda M=M, fn=fn, fl=fl: sum(fn(c % copies, M, cs, fl) for c in range(G)))
             t = time_graph(torch, stream, g, 10) / G
             w2[mode][str(M)] = entry(layer_set_bytes(inputs.BITNET2B_PROJ, M), t, M, peak)
             del g
@@ -881,6 +896,8 @@ def main():
                      "kernel": "act_prep_kernel + w2a8_streamk_kernel (both launches of every grouped call; "
                                "108 calls per step); achieved = algorithmic bytes per step / mean step time"},
         "per_width": res["per_width"],
+        "fp8_per_width": dict(res["fp8_per_width"], what="the same stack with FP8 (E4M3) activations "
+                              "(\"fast\" draft projections), not part of value"),
         "per_config": res["per_config"],
         "e2e": res["e2e"],
         "ternarize_pack": res["tern"],
