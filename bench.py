@@ -560,7 +560,48 @@ def run_configs(L, torch, dev, stream, peak):
         del g, groups, arrs
     out["5_role_grouped_M16"] = {"unit": "per call (quant_act + grouped GEMM)", **w5}
     torch.cuda.synchronize()
+    out["block_step_D8"] = run_block_step(L, torch, dev)
     return out
+
+
+def run_block_step(L, torch, dev):
+    """NEXT #4: one hybrid-decoding block step on the role-dependent shapes
+    (8 drafts through a 2560 -> 2560 FP8 "fast" projection, 8 verifier rows
+    through a 2560 -> 32000 int8 "critical" projection), with the verifier
+    inputs prepared before the host's read of the confidence length (hoisted)
+    or after it, for a block that needs verification and one that does not.
+    Host wall clock per step, from the first enqueue to the end of the
+    step's last kernel (the host's round trip is what the hoisting hides)."""
+    import time
+    from ternary_w2a8_linear_gb300.blockstep import BlockStep
+    D, R, K, ND, NV = 8, 8, 2560, 2560, 32000
+    stream = torch.cuda.Stream()
+    pkd = L.pack(inputs.device_ternary(81000, (ND, K), 0.5, dev))
+    pkv = L.pack(inputs.device_ternary(81001, (NV, K), 0.5, dev))
+    draft = dict(pk=pkd, w_scale=0.02, N=ND, K=K, x=inputs.device_normal_bf16(81002, (D, K), dev, 0.01),
+                 y=torch.empty((D, ND), dtype=torch.bfloat16, device=dev),
+                 p=torch.zeros(D, dtype=torch.float32, device=dev))
+    verify = dict(pk=pkv, w_scale=0.03, N=NV, K=K, x=inputs.device_normal_bf16(81003, (R, K), dev, 0.01),
+                  y=torch.empty((R, NV), dtype=torch.bfloat16, device=dev))
+    bs = BlockStep(draft, verify, 0.9, 4, stream)
+    probs = {"verifies": [0.5, 0.3] + [0.99] * 6, "skips_verification": [0.5] + [0.99] * 7}
+    res = {"unit": "µs per block step (host wall clock)", "tau": 0.9, "m": 4}
+    for name, p in probs.items():
+        with torch.cuda.stream(stream):
+            draft["p"].copy_(torch.tensor(p, dtype=torch.float32))
+        stream.synchronize()
+        for hoist in (True, False):
+            for _ in range(20):
+                bs.run(hoist)
+                stream.synchronize()
+            ts = []
+            for _ in range(200):
+                t0 = time.perf_counter()
+                bs.run(hoist)
+                stream.synchronize()
+                ts.append(time.perf_counter() - t0)
+            res[f"{name}_{'hoisted' if hoist else 'not_hoisted'}"] = round(statistics.median(ts) * 1e6, 2)
+    return res
 
 
 def run_ternarize(L, torch, dev, stream):

@@ -2,6 +2,8 @@
 path through the C ABI binding, and compare with the oracle at the stated
 tolerances (bit-exact integers; fp32 within 1e-5 relative with exact zeros;
 bf16 within one bf16 ulp of the oracle's fp32 value rounded to bf16)."""
+import math
+
 import numpy as np
 import torch
 
@@ -59,3 +61,41 @@ def reference(T, w_scale, x, x_is_bf16):
     """Oracle result (y fp32, acc int64, q, a_scale)."""
     y, acc, q, a_scale, _ = oracle.w2a8_linear(T, w_scale, x, "f32", x_is_bf16=x_is_bf16)
     return y, acc, q, a_scale
+
+
+# ---------------------------------------------------------------------------
+# FP8 ("fast" draft projection) results: the fp32 accumulation adds
+# 2 * ceil(K/32) MMA results (sum_k (T+1)*e and -sum_k e per k step), so
+# |acc - sum_k T*e| <= (2 * ceil(K/32) + 2) * 2^-23 * sum_k (T+2)*|e|; y within
+# that times a_scale * w_scale plus two fp32 roundings (and the bf16 rounding).
+# ---------------------------------------------------------------------------
+def fp8_reference(T, w, x, is_bf16):
+    """Oracle (y fp32, exact acc, e, a_scale) and S = sum_k (T+2)*|e| per output."""
+    y, acc, e, a_scale = oracle.fp8_linear(T, w, x, "f32", x_is_bf16=is_bf16)
+    S = np.abs(e) @ (T.astype(np.float64) + 2).T
+    return y, acc, e, a_scale, S
+
+
+def fp8_acc_bound(K, S):
+    return (2 * math.ceil(K / 32) + 2) * 2.0 ** -23 * S
+
+
+def assert_fp8_within_bound(K, w, y, acc, ref, bf16_out):
+    """y: fp32 values or bf16 bit patterns; acc: the fp32 accumulators (or
+    None).  Returns the largest |acc error| / bound seen."""
+    y_ref, acc_ref, _, a_scale, S = ref
+    B = fp8_acc_bound(K, S)
+    ratio = 0.0
+    if acc is not None:
+        err = np.abs(acc.astype(np.float64) - acc_ref)
+        assert np.all(err <= B), f"acc beyond bound: max ratio {float(np.max(err / np.maximum(B, 1e-300))):.3g}"
+        ratio = float(np.max(err / np.maximum(B, 1e-300))) if err.size else 0.0
+    scale = a_scale.astype(np.float64)[:, None] * float(np.float32(w))
+    yr = np.abs(y_ref.astype(np.float64))
+    tol32 = B * scale * (1 + 2.0 ** -21) + 2.0 ** -21 * yr
+    yv = oracle.bf16_bits_to_f32(y).astype(np.float64) if bf16_out else np.asarray(y, dtype=np.float64)
+    tol = tol32 + (2.0 ** -8 * (yr + tol32) if bf16_out else 0.0)
+    yerr = np.abs(yv - y_ref.astype(np.float64))
+    assert np.all(yerr <= tol), f"y beyond bound at {tuple(np.argwhere(yerr > tol)[0])}"
+    assert np.all(yv[S == 0] == 0)  # every product and correction term zero: exact zero
+    return ratio

@@ -16,8 +16,6 @@ weights on the tensor cores, accumulating in fp32.  What is compared:
   |acc - sum_k T*e| <= (2 * ceil(K/32) + 2) * 2^-23 * sum_k (T+2)*|e|, and y
   within that bound times a_scale * w_scale plus the dequant roundings (two
   fp32 roundings, then the bf16 rounding for bf16 output)."""
-import math
-
 import numpy as np
 import pytest
 import torch
@@ -25,7 +23,7 @@ import torch
 import oracle
 from ternary_w2a8_linear_gb300 import build, inputs
 from ternary_w2a8_linear_gb300 import linear as L
-from gpu_util import bf16_bits, bf16_tensor, dev_tensor
+from gpu_util import assert_fp8_within_bound, bf16_bits, bf16_tensor, dev_tensor, fp8_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -64,29 +62,11 @@ def _run(T, w, x, is_bf16, out=torch.float32, flags=0, amax=None, ws=None):
 
 
 def _oracle(T, w, x, is_bf16):
-    y, acc, e, a_scale = oracle.fp8_linear(T, w, x, "f32", x_is_bf16=is_bf16)
-    S = np.abs(e) @ (T.astype(np.float64) + 2).T  # sum_k (T+2)*|e| per output (exact in fp64)
-    return y, acc, e, a_scale, S
-
-
-def _acc_bound(K, S):
-    return (2 * math.ceil(K / 32) + 2) * 2.0 ** -23 * S
+    return fp8_reference(T, w, x, is_bf16)
 
 
 def _check_within_bound(K, w, y, acc, ref, out):
-    y_ref, acc_ref, _, a_scale, S = ref
-    B = _acc_bound(K, S)
-    err = np.abs(acc.astype(np.float64) - acc_ref)
-    assert np.all(err <= B), f"acc beyond bound: max ratio {float(np.max(err / np.maximum(B, 1e-300))):.3g}"
-    scale = a_scale.astype(np.float64)[:, None] * float(np.float32(w))
-    tol32 = B * scale * (1 + 2.0 ** -21) + 2.0 ** -21 * np.abs(y_ref.astype(np.float64))
-    yv = oracle.bf16_bits_to_f32(y).astype(np.float64) if out == torch.bfloat16 else y.astype(np.float64)
-    tol = tol32 + (2.0 ** -8 * (np.abs(y_ref.astype(np.float64)) + tol32) if out == torch.bfloat16 else 0.0)
-    yerr = np.abs(yv - y_ref.astype(np.float64))
-    assert np.all(yerr <= tol), f"y beyond bound at {tuple(np.argwhere(yerr > tol)[0])}"
-    # exact zeros stay exact (S == 0: every product and correction term is zero)
-    assert np.all(yv[S == 0] == 0)
-    return float(np.max(err / np.maximum(B, 1e-300))) if err.size else 0.0
+    return assert_fp8_within_bound(K, w, y, acc, ref, out == torch.bfloat16)
 
 
 # ---------------------------------------------------------------------------
