@@ -811,7 +811,9 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         // refill ring slots as they are released
         for (int j = npre; j < nchunks; ++j) {
             const int q = j % R;
-            if (pending && mbar_test_wait(smem_u32(&c->slot_done), 0)) publish();
+            // one answer for the whole warp: the lanes must agree on `pending`
+            if (pending && __shfl_sync(0xffffffffu, mbar_test_wait(smem_u32(&c->slot_done), 0) ? 1u : 0u, 0))
+                publish();
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->empty[q]), ((j / R) - 1) & 1, P.wait_ns))) {
                 if (leader) fail(c, P.err, kErrWaitEmpty);
                 break;
