@@ -551,22 +551,44 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
 
 // ------------------------------------------------------------ epilogue --
 // Store y[m][n] (and acc); returns |y[m][n]| as stored.
-// kF: acc holds an fp32 accumulator's bit pattern (FP8 path), else an exact
-// integer sum.
+// The output fields of one problem, read once per segment into registers:
+// the problem record lives in shared memory behind a generic pointer, and
+// every generic store to y would otherwise force the compiler to read the
+// record again before the next one.
+struct OutRef {
+    void* y;
+    int32_t* acc;
+    long long ldy, lda;
+    float w_scale;
+    bool f32;
+};
+__device__ __forceinline__ OutRef out_ref(const GemmProblem& pr) {
+    OutRef o;
+    o.y = pr.y;
+    o.acc = pr.acc;
+    o.ldy = pr.ldy;
+    o.lda = pr.lda;
+    o.w_scale = pr.w_scale;
+    o.f32 = pr.out_dtype == BITMTP_F32;
+    return o;
+}
+
+// Store y[m][n] (and acc); returns |y[m][n]| as stored.  kF: acc holds an
+// fp32 accumulator's bit pattern (FP8 path), else an exact integer sum.
 template <bool kF>
-__device__ __forceinline__ float store_out(const GemmProblem& pr, int m, int n, int acc, float a_scale) {
+__device__ __forceinline__ float store_out(const OutRef& o, int m, int n, int acc, float a_scale) {
     const float a = kF ? __int_as_float(acc) : static_cast<float>(acc);
-    const float v = __fmul_rn(__fmul_rn(a, a_scale), pr.w_scale);
-    const long long o = static_cast<long long>(m) * pr.ldy + n;
+    const float v = __fmul_rn(__fmul_rn(a, a_scale), o.w_scale);
+    const long long off = static_cast<long long>(m) * o.ldy + n;
     float stored = v;
-    if (pr.out_dtype == BITMTP_F32) {
-        static_cast<float*>(pr.y)[o] = v;
+    if (o.f32) {
+        static_cast<float*>(o.y)[off] = v;
     } else {
         const __nv_bfloat16 h = __float2bfloat16_rn(v);
-        static_cast<__nv_bfloat16*>(pr.y)[o] = h;
+        static_cast<__nv_bfloat16*>(o.y)[off] = h;
         stored = __bfloat162float(h);
     }
-    if (pr.acc) pr.acc[static_cast<long long>(m) * pr.lda + n] = acc;
+    if (o.acc) o.acc[static_cast<long long>(m) * o.lda + n] = acc;
     return fabsf(stored);
 }
 
@@ -662,12 +684,18 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int p_lo, const S
     float am[kRows];
 #pragma unroll
     for (int m = 0; m < kRows; ++m) am[m] = 0.f;
+    const OutRef o = out_ref(pr);
+    float* const amax_out = pr.amax_out;
     if (alive && n < pr.N) {
+        // the rows' scales, all read before the first store
+        float asv[kRows];
+#pragma unroll
+        for (int m = 0; m < kRows; ++m) asv[m] = c->asc[s.pi - p_lo][m];
 #pragma unroll
         for (int m = 0; m < kRows; ++m)
-            if (m < M) am[m] = store_out<kF>(pr, m, n, acc[m], c->asc[s.pi - p_lo][m]);
+            if (m < M) am[m] = store_out<kF>(o, m, n, acc[m], asv[m]);
     }
-    if (pr.amax_out) {
+    if (amax_out) {
         // first phase of the output rows' absmax: this warp's 32 columns, one
         // atomic per row (non-negative floats order like their bit patterns)
 #pragma unroll
@@ -677,7 +705,7 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int p_lo, const S
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
                 if ((tid & 31) == 0 && v > 0.f)
-                    atomicMax(reinterpret_cast<unsigned*>(pr.amax_out + m), __float_as_uint(v));
+                    atomicMax(reinterpret_cast<unsigned*>(amax_out + m), __float_as_uint(v));
             }
         }
     }
