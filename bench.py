@@ -374,7 +374,7 @@ def run_ours(args, rank, world):
         stream.synchronize()
         check_outputs[M] = [large.y[0][p][:M].clone() for p in range(len(inputs.LARGE_PROJ))]
 
-    e2e = None if args.no_e2e else run_e2e(args, L, torch, dev, stream, large, world)
+    e2e = None if args.no_e2e else run_e2e(args, L, torch, dev, stream, large, world, check_outputs)
     per_config = None if args.no_per_config else run_configs(L, torch, dev, stream, peak)
     tern = None if args.no_ternarize else run_ternarize(L, torch, dev, stream)
     err = L.bitmtp_linear_device_error(stream)
@@ -659,11 +659,15 @@ def run_ternarize(L, torch, dev, stream):
                     "(one call, one sync)"}
 
 
-def run_e2e(args, L, torch, dev, stream, large, world):
+def run_e2e(args, L, torch, dev, stream, large, world, check_outputs=None):
     """The headline step through the library's C ABI with host buffers: every
     step copies the activations of every layer host->device from pinned
     memory (one copy), makes the 108 grouped calls and reads every output
-    back device->host (one copy), then synchronises."""
+    back device->host (one copy).  Steps are pipelined over two device buffer
+    sets: a side stream copies step k+1's activations in and step k-1's
+    outputs out while step k computes (events order each copy after the
+    compute it feeds or drains).  The timed region holds every step's copies
+    and ends when the last step's outputs are on the host."""
     nl, proj = inputs.LARGE_LAYERS, inputs.LARGE_PROJ
     kofs, off = {}, 0
     for layer in range(nl):
@@ -675,49 +679,85 @@ def run_e2e(args, L, torch, dev, stream, large, world):
         for p in range(len(proj)):
             o = kofs[(layer, p)]
             x_host[o:o + large.x[layer][p].numel()] = large.x[layer][p].reshape(-1).view(torch.int16).cpu()
-    x_dev = torch.empty_like(x_host, device=dev)
+    x_dev = [torch.empty_like(x_host, device=dev) for _ in range(2)]
     yofs, off = {}, 0
     for layer in range(nl):
         for p, (_, _, N) in enumerate(proj):
             yofs[(layer, p)] = off
             off += inputs.MAX_ROWS * N
-    y_dev = torch.empty(off, dtype=torch.int16, device=dev)
-    y_host = torch.empty(off, dtype=torch.int16).pin_memory()
+    y_dev = [torch.empty(off, dtype=torch.int16, device=dev) for _ in range(2)]
+    y_host = [torch.empty(off, dtype=torch.int16).pin_memory() for _ in range(2)]
     descs = {}
-    for layer in range(nl):
-        for M in HEADLINE_WIDTHS:
-            d = [L.GemmDesc(large.pk[layer][p].data_ptr(), large.w[layer][p], N, K, M,
-                            L.Act(L.BF16, x_dev.data_ptr() + 2 * kofs[(layer, p)], K, None),
-                            L.Out(L.BF16, y_dev.data_ptr() + 2 * yofs[(layer, p)], N, None, 0))
-                 for p, (_, K, N) in enumerate(proj)]
-            descs[(layer, M)] = ((L.GemmDesc * len(d))(*d), len(d))
+    for b in range(2):
+        for layer in range(nl):
+            for M in HEADLINE_WIDTHS:
+                d = [L.GemmDesc(large.pk[layer][p].data_ptr(), large.w[layer][p], N, K, M,
+                                L.Act(L.BF16, x_dev[b].data_ptr() + 2 * kofs[(layer, p)], K, None),
+                                L.Out(L.BF16, y_dev[b].data_ptr() + 2 * yofs[(layer, p)], N, None, 0))
+                     for p, (_, K, N) in enumerate(proj)]
+                descs[(b, layer, M)] = ((L.GemmDesc * len(d))(*d), len(d))
     lib = L.load()
     cs = L.ctypes.c_void_p(stream.cuda_stream)
     wsp = L.ctypes.c_void_p(large.ws.data_ptr())
     nb = large.ws.numel()
+    copy = torch.cuda.Stream()
+    x_in = [torch.cuda.Event() for _ in range(2)]      # activations of buffer b on the device
+    done = [torch.cuda.Event() for _ in range(2)]      # compute of buffer b finished
+    drained = [torch.cuda.Event() for _ in range(2)]   # outputs of buffer b on the host
 
-    def one():
-        x_dev.copy_(x_host, non_blocking=True)
-        for M in HEADLINE_WIDTHS:
-            for layer in range(nl):
-                arr, n = descs[(layer, M)]
-                st = lib.bitmtp_linear_gemm_grouped(arr, n, wsp, nb, L.FLAG_PDL, cs)
-                if st != L.OK:
-                    raise L.BitmtpError(st, "gemm_grouped")
-        y_host.copy_(y_dev, non_blocking=True)
+    def copy_in(b):
+        with torch.cuda.stream(copy):
+            copy.wait_event(done[b])       # the step that last read x_dev[b] has finished
+            x_dev[b].copy_(x_host, non_blocking=True)
+            x_in[b].record(copy)
+
+    def run(steps):
+        copy.wait_stream(stream)
+        for b in range(2):                 # the events start signalled
+            done[b].record(stream)
+        copy_in(0)
+        for k in range(steps):
+            b = k % 2
+            if k + 1 < steps:
+                copy_in(b ^ 1)             # next step's activations, behind this step's compute only
+            stream.wait_event(x_in[b])
+            stream.wait_event(drained[b]) if k >= 2 else None   # y_dev[b] read out by step k-2
+            for M in HEADLINE_WIDTHS:
+                for layer in range(nl):
+                    arr, n = descs[(b, layer, M)]
+                    st = lib.bitmtp_linear_gemm_grouped(arr, n, wsp, nb, L.FLAG_PDL, cs)
+                    if st != L.OK:
+                        raise L.BitmtpError(st, "gemm_grouped")
+            done[b].record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(done[b])
+                y_host[b].copy_(y_dev[b], non_blocking=True)
+                drained[b].record(copy)
+        copy.synchronize()
         stream.synchronize()
 
     with torch.cuda.stream(stream):
-        for _ in range(2):
-            one()
+        run(2)
         dist_barrier(world)
         t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            one()
+        run(args.e2e_steps)
         t1 = time.perf_counter()
     sec = dist_max(t1 - t0, world)
+    # the last step's outputs, as read back to the host, against the headline
+    # graph's layer 0 at the last width (the int8 path is deterministic)
+    checked = None
+    if check_outputs is not None:
+        M = HEADLINE_WIDTHS[-1]
+        yl = y_host[(args.e2e_steps - 1) % 2]
+        for p, (_, _, N) in enumerate(proj):
+            got = yl[yofs[(0, p)]:yofs[(0, p)] + M * N].numpy().view(np.uint16).reshape(M, N)
+            if not np.array_equal(got, bits_of(torch, check_outputs[M][p])):
+                raise RuntimeError(f"e2e outputs differ from the headline graph's (layer 0, projection {p})")
+        checked = f"layer 0 at width {M}: every output of the last step equal to the headline graph's"
     return {"value": round(headline_step_bytes() * args.e2e_steps * world / sec / 1e9, 2), "unit": "GB/s",
-            "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
+            "checked": checked,
+            "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host[0].numel() * 2,
+            "pipelined": "two buffer sets; copies of steps k+1 (in) and k-1 (out) overlap step k",
             "steps": args.e2e_steps, "ms_per_step": round(sec * 1e3 / args.e2e_steps, 4)}
 
 
