@@ -158,16 +158,15 @@ struct TernParams {
 constexpr int kHistBins = 512;
 constexpr int kBinOff = 128;
 constexpr int kNonFiniteBin = 511;
-constexpr int kHistBlocksPerSm = 8;  // 8 x 256 threads: a full SM
 
 // Blocks of the absmean pass for a matrix of N x K entries out of `total`
-// entries in the group: the larger of its share of one full wave
-// (kHistBlocksPerSm blocks on every SM) and one block per 64 K entries up to
+// entries in the group: the larger of its share of one full wave (per_sm
+// resident blocks on every SM) and one block per 64 K entries up to
 // a full wave; at least one, at most one per row on the row walk, and never
 // fewer than keep a thread at or below 2^22 entries (the accumulator bound
 // above).
-int hist_blocks(int64_t N, int64_t K, int64_t total, bool flat, int sms) {
-    const int64_t full = static_cast<int64_t>(kHistBlocksPerSm) * std::max(sms, 1);
+int hist_blocks(int64_t N, int64_t K, int64_t total, bool flat, int sms, int per_sm) {
+    const int64_t full = static_cast<int64_t>(std::max(per_sm, 1)) * std::max(sms, 1);
     const int64_t per_thread_max = static_cast<int64_t>(256) << 22;
     const int64_t min_blocks = (N * K + per_thread_max - 1) / per_thread_max;
     const int64_t share = (full * N * K + total - 1) / total;
@@ -233,22 +232,50 @@ absmean_hist_kernel(const __grid_constant__ TernParams P) {
         const long long stride = static_cast<long long>(nblk) * blockDim.x;
         const long long first = static_cast<long long>(blk) * blockDim.x + threadIdx.x;
         const float4* W4 = reinterpret_cast<const float4*>(W);
-#pragma unroll 4
-        for (long long i = first; i < n4; i += stride) {
+        // four loads in flight before any of their entries is added (the
+        // shared-memory atomics of the slow path would otherwise keep the
+        // compiler from hoisting the next load above them)
+        long long i = first;
+        for (; i + 3 * stride < n4; i += 4 * stride) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = ld_f4_hint(W4 + i + u * stride, pol);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                add(v[u].x);
+                add(v[u].y);
+                add(v[u].z);
+                add(v[u].w);
+            }
+        }
+        for (; i < n4; i += stride) {
             const float4 v = ld_f4_hint(W4 + i, pol);
             add(v.x);
             add(v.y);
             add(v.z);
             add(v.w);
         }
-        for (long long i = 4 * n4 + first; i < total; i += stride) add(W[i]);
+        for (long long i1 = 4 * n4 + first; i1 < total; i1 += stride) add(W[i1]);
     } else {
         const int K4 = vec ? K / 4 : 0;
         for (int n = blk; n < N; n += nblk) {
             const float* row = W + static_cast<long long>(n) * ldw;
             const float4* row4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 4
-            for (int k4 = threadIdx.x; k4 < K4; k4 += blockDim.x) {
+            const int bd = static_cast<int>(blockDim.x);
+            int k4 = threadIdx.x;
+            for (; k4 + 3 * bd < K4; k4 += 4 * bd) {  // four loads in flight, as above
+                float4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = ld_f4_hint(row4 + k4 + u * bd, pol);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    add(v[u].x);
+                    add(v[u].y);
+                    add(v[u].z);
+                    add(v[u].w);
+                }
+            }
+            for (; k4 < K4; k4 += bd) {
                 const float4 v = ld_f4_hint(row4 + k4, pol);
                 add(v.x);
                 add(v.y);
@@ -425,6 +452,7 @@ quant_act_kernel(const void* __restrict__ x, int kind, int K, long long ldx, int
 struct DevInfo {
     std::atomic<int> state{0};   // 0 unknown, 1 ok, -1 unsupported
     int sms = 0;
+    int hist_per_sm = 1;         // resident absmean-pass blocks per SM (its register use decides)
     int* err = nullptr;
     std::atomic<int> dirty{0};   // the no-alloc scratch may hold flags of a launch that gave up
 };
@@ -455,8 +483,14 @@ int current_device(DevInfo** info) {
                 cudaGetLastError();
                 return BITMTP_ERR_CUDA;
             }
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, absmean_hist_kernel, 256, 0) != cudaSuccess) {
+                cudaGetLastError();
+                return BITMTP_ERR_CUDA;
+            }
             d.err = static_cast<int*>(p);
             d.sms = sms;
+            d.hist_per_sm = std::max(per_sm, 1);
             st = 1;
         }
         d.state.store(st, std::memory_order_release);
@@ -730,7 +764,7 @@ int bitmtp_linear_ternarize_pack_grouped(const bitmtp_ternarize_desc* d, int n_d
         m.vec = aligned16(g.W) && (g.ldw % 4) == 0;
         m.flat = aligned16(g.W) && g.ldw == g.K;
         m.blk_begin = static_cast<int>(blocks);
-        m.blocks = hist_blocks(g.N, g.K, total, m.flat != 0, dev->sms);
+        m.blocks = hist_blocks(g.N, g.K, total, m.flat != 0, dev->sms, dev->hist_per_sm);
         m.tile_begin = static_cast<int>(tiles);
         m.pk = static_cast<uint32_t*>(g.pk);
         m.trailer = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(g.pk) + need - 16);
