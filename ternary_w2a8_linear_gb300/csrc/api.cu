@@ -322,6 +322,20 @@ __device__ __forceinline__ void wide_add_shifted(unsigned long long (&L)[kLimbs]
     }
 }
 
+// L += R (two 512-bit integers; the sum fits, as every total here does).
+__device__ __forceinline__ void wide_add(unsigned long long (&L)[kLimbs], const unsigned long long (&R)[kLimbs]) {
+    unsigned long long carry = 0ull;
+#pragma unroll
+    for (int j = 0; j < kLimbs; ++j) {
+        const unsigned long long s1 = L[j] + R[j];
+        const unsigned long long c1 = s1 < R[j] ? 1ull : 0ull;
+        const unsigned long long s2 = s1 + carry;
+        const unsigned long long c2 = s2 < carry ? 1ull : 0ull;
+        L[j] = s2;
+        carry = c1 | c2;
+    }
+}
+
 // 64 bits of L from bit pos (bits past the top read as 0).
 __device__ __forceinline__ unsigned long long wide_bits(const unsigned long long (&L)[kLimbs], int pos) {
     const int i = pos >> 6, o = pos & 63;
@@ -367,7 +381,9 @@ __device__ __forceinline__ double wide_to_double(const unsigned long long (&L)[k
                                                        (mant & ((1ull << 52) - 1ull))));
 }
 
-// One block of kHistBins threads: the exact sum from the global bins,
+// One block of kHistBins threads: the exact sum from the global bins (warp 0:
+// each lane adds every 32nd bin into its own 512-bit integer, then a shuffle
+// tree adds the 32 partial sums; integer additions, so the order is free),
 // gamma = max(RN32(RN64(sum) / count), 1e-5) into *w_scale, the non-finite
 // flag, and the packed buffer's trailer {magic, N, K, 0}.
 __global__ void __launch_bounds__(kHistBins)
@@ -380,10 +396,18 @@ absmean_finish_kernel(const __grid_constant__ TernParams P) {
     const int e = threadIdx.x;
     H[e] = P.bins[static_cast<size_t>(mi) * kHistBins + e];
     __syncthreads();
+    if (e >= 32) return;
+    unsigned long long L[kLimbs] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+    for (int j = 65 + e; j < kNonFiniteBin; j += 32)
+        if (H[j]) wide_add_shifted(L, H[j], j - 65);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        unsigned long long R[kLimbs];
+#pragma unroll
+        for (int k = 0; k < kLimbs; ++k) R[k] = __shfl_down_sync(0xffffffffu, L[k], off);
+        if (e < off) wide_add(L, R);
+    }
     if (e == 0) {
-        unsigned long long L[kLimbs] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
-        for (int j = 65; j < kNonFiniteBin; ++j)
-            if (H[j]) wide_add_shifted(L, H[j], j - 65);
         const long long count = static_cast<long long>(N) * K;
         const double mean = __ddiv_rn(wide_to_double(L), static_cast<double>(count));
         *mt.w_scale = fmaxf(__double2float_rn(mean), 1e-5f);
