@@ -190,18 +190,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr) : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]; kind::f8f6f4 (8-bit float inputs, fp32
-// accumulate, K = 32 per instruction), one CTA, issued only where `on` is
-// non-zero (a guard predicate, no branch).
-__device__ __forceinline__ void mma_f8_ts_if(uint32_t on, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p, g;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "setp.ne.b32 g, %5, 0;\n\t"
-                 "@g tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
-                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(on) : "memory");
-}
-// The same, always accumulating into D (the caller zeroed it).
+// D[tmem] += A[tmem] * B[smem]; kind::f8f6f4 (8-bit float inputs, fp32
+// accumulate, K = 32 per instruction), one CTA, always accumulating (the
+// caller zeroed D), issued only where `on` is non-zero (a guard predicate,
+// no branch).
 __device__ __forceinline__ void mma_f8_ts_acc_if(uint32_t on, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                  uint32_t idesc) {
     asm volatile("{\n\t.reg .pred g;\n\t"
