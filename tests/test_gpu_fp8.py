@@ -203,3 +203,22 @@ def test_fp8_withheld_chunk_times_out_then_next_call_is_exact():
     _, acc = _run(T, np.float32(0.5), x, False, ws=ws)
     _, acc_ref, _, _, _ = _oracle(T, np.float32(0.5), x, False)
     assert np.array_equal(acc.astype(np.float64), acc_ref)
+
+
+def test_fp8_through_the_noalloc_entry():
+    """The FP8 flag through the entry point that allocates nothing: identity
+    weights, so the accumulators are the E4M3 values exactly."""
+    M, K = 6, 1000
+    rng = np.random.default_rng(515)
+    x = rng.standard_normal((M, K), dtype=np.float32)
+    T = np.eye(K, dtype=np.int8)
+    pk = L.pack(dev_tensor(T))
+    xd = dev_tensor(x)
+    y = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    acc = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    st = L.bitmtp_linear_gemm_noalloc(L._ptr(pk), 1.0, K, K, M, L.make_act(xd), L.make_out(y, acc),
+                                      L.FLAG_FP8, L._stream(None))
+    assert st == L.OK, L.status_string(st)
+    torch.cuda.synchronize()
+    _, _, e, _, _ = fp8_reference(T, np.float32(1), x, False)
+    assert np.array_equal(acc.view(torch.float32).cpu().numpy().astype(np.float64), e)
