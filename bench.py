@@ -452,7 +452,8 @@ def run_configs(L, torch, dev, stream, peak):
                 if r != L.OK:
                     raise L.BitmtpError(r, "gemm")
                 x, xa = y, am
-        return 2 * inputs.BITNET2B_LAYERS * len(chain)
+        calls = inputs.BITNET2B_LAYERS * len(chain)
+        return calls + 1 if handoff else 2 * calls  # a call with the absmax handed over is one launch
 
     chain_bytes = inputs.BITNET2B_LAYERS * sum(L.packed_bytes(N, K) + M3 * K * 2
                                                for _, K, N in (inputs.BITNET2B_PROJ[p] for p in chain))
@@ -466,7 +467,9 @@ def run_configs(L, torch, dev, stream, peak):
         del g
     w3["layer_chain_what"] = ("per layer q -> o -> up -> down, each output (bf16) the next call's input, "
                               "30 layers, width 4, one CUDA graph with PDL; amax_handoff: each call's "
-                              "epilogues reduce its output rows' absmax for the next call")
+                              "epilogues reduce its output rows' absmax for the next call, which then "
+                              "runs as one launch (the GEMM quantises its own activation tiles); "
+                              "own_absmax: a preparation launch before every GEMM")
     out["3_bitnet2b_30_layers_M4"] = w3
     del st
 

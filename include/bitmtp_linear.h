@@ -220,8 +220,12 @@ typedef struct bitmtp_act {
     const float* amax;     /* optional, BITMTP_F32/BF16 only (NULL otherwise): device
                               [M] = max_k |x[m][k]| of exactly these rows, e.g. the
                               amax output of the GEMM that wrote x (a layer chain);
-                              the preparation then skips its own absmax pass.  Any
-                              other value gives wrong codes.                        */
+                              the call then skips its own absmax pass, and when
+                              every problem of a call at block width 1..4 brings
+                              it (the dp4a path, not BITMTP_FLAG_FP8) the call is
+                              one launch: the GEMM quantises the rows itself, with
+                              the same steps and codes, and no preparation kernel
+                              runs.  Any other value gives wrong codes.            */
 } bitmtp_act;
 
 /* Output of a GEMM. */
@@ -233,18 +237,19 @@ typedef struct bitmtp_out {
     int64_t lda;           /* >= N when acc != NULL                                  */
     float* amax;           /* optional device [M]: receives max_n |y[m][n]| of the
                               values stored (after the bf16 rounding for BITMTP_BF16),
-                              ready to be the next call's act.amax; the call's first
-                              launch zeroes it, its epilogues combine per-CTA maxima
-                              with atomics (the first phase of a two-phase row
-                              absmax, the next call's preparation the second).  Must
-                              not overlap y, acc or this call's act.amax.           */
+                              ready to be the next call's act.amax; the call zeroes
+                              it before its epilogues combine per-CTA maxima with
+                              atomics (the first phase of a two-phase row absmax,
+                              the next call's quantisation the second).  Must not
+                              overlap y, acc or this call's act.amax.              */
 } bitmtp_out;
 
 /* Workspace of a GEMM call: a device buffer the caller allocates once,
  * 16-byte aligned, of at least the size these queries return, and
  * zero-fills before its first use (e.g. cudaMemset).  It holds a fixed part
  * of about 2.5 MiB -- one slot of partial sums per CTA for row tiles split
- * between CTAs, and a ready flag per slot -- and each problem's quantised
+ * between CTAs, a ready flag per slot and two synchronisation words of the
+ * one-launch layer-chain calls -- and each problem's quantised
  * activation operand (about 4 KiB per 128 in-features).  Every call leaves
  * the flags at zero, so one workspace serves calls of any shapes that fit.
  * Calls that may execute concurrently on the GPU need distinct workspaces;
@@ -263,7 +268,9 @@ size_t bitmtp_linear_workspace_bytes(int64_t N, int64_t K, int64_t M);
  * Two kernel launches: the first quantises the activation rows
  * (BITMTP_F32/BF16, with the quantiser above; BITMTP_Q8 rows are taken as
  * they are) into the workspace, the second streams the packed weights and
- * writes y (and acc); it starts streaming while the first one runs.
+ * writes y (and acc); it starts streaming while the first one runs.  One
+ * launch for a layer-chain call at block width 1..4 (see act.amax): the GEMM
+ * quantises the rows while its first weights stream in.
  * The compute path is chosen from M (width specialisation); results do not
  * depend on the choice. */
 int bitmtp_linear_gemm(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M,
@@ -318,16 +325,16 @@ int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc,
  *     load the library's device code).  Make that first call before any
  *     stream capture begins.
  *   - Sharing: all calls on a device share the one array and it keeps what
- *     the previous call left.  The part that must start at zero (the ready
- *     flags, 1.25 KiB) starts zeroed and every call leaves it at zero; only a
+ *     the previous call left.  The part that must start at zero (sync
+ *     words and ready flags, 1.5 KiB) starts zeroed and every call leaves it at zero; only a
  *     call that gave up a bounded wait can leave it dirty, and once
  *     bitmtp_linear_device_error has reported that, the next call clears it
  *     first (one memset on `stream`).  Calls whose work can overlap on the GPU
  *     (different streams without ordering between them, or different host
  *     threads) race on the array and give wrong results; order them on one
  *     stream or use bitmtp_linear_gemm with distinct workspaces.
- * Enqueues the two kernels of bitmtp_linear_gemm on `stream` (preceded by
- * that memset only after a reported error). */
+ * Enqueues the kernels of bitmtp_linear_gemm on `stream` (preceded by that
+ * memset only after a reported error). */
 int bitmtp_linear_gemm_noalloc(const void* pk, float w_scale, int64_t N, int64_t K, int64_t M,
                                const bitmtp_act* act, const bitmtp_out* out,
                                unsigned flags, void* stream);

@@ -662,6 +662,16 @@ int run_gemms(const GemmProblem* probs, int n, void* workspace, size_t ws_bytes,
     prm.flags = reinterpret_cast<unsigned*>(w + kWsFlags);
     prm.slots = reinterpret_cast<int*>(w + kWsSlots);
     prm.err = dev->err;
+    // a layer chain on the dp4a path: every live problem brings its rows'
+    // absmax, so the GEMM quantises its own activation tiles (no preparation
+    // launch); the workspace's first two words order the out.amax zeroing
+    bool fused = path == kPathDP, any_amax_out = false;
+    for (int i = 0; i < np; ++i) {
+        fused = fused && prm.p[i].act_kind != BITMTP_Q8 && prm.p[i].amax_in != nullptr;
+        any_amax_out = any_amax_out || prm.p[i].amax_out != nullptr;
+    }
+    prm.fused = fused ? 1 : 0;
+    prm.sync_words = (fused && any_amax_out) ? reinterpret_cast<unsigned*>(w) : nullptr;
     const bool test_withhold = (flags & BITMTP_FLAG_TEST_WITHHOLD) != 0;
     prm.withhold = test_withhold ? 0 : -1;
     prm.wait_ns = test_withhold ? kTestWaitNs : kWaitNs;
@@ -910,11 +920,12 @@ int bitmtp_linear_gemm_noalloc(const void* pk, float w_scale, int64_t N, int64_t
     st = noalloc_scratch(&scratch);
     if (st != BITMTP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The flags must start at zero.  The array starts zeroed and every launch
-    // leaves them at zero, except one that gave up a bounded wait: once
-    // bitmtp_linear_device_error has reported that, the next call clears them.
+    // The sync words and flags must start at zero.  The array starts zeroed
+    // and every launch leaves them at zero, except one that gave up a bounded
+    // wait: once bitmtp_linear_device_error has reported that, the next call
+    // clears them.
     if (dev->dirty.exchange(0, std::memory_order_acq_rel) != 0) {
-        st = cuda_status(cudaMemsetAsync(static_cast<uint8_t*>(scratch) + kWsFlags, 0, kWsSlots - kWsFlags, s));
+        st = cuda_status(cudaMemsetAsync(scratch, 0, kWsSlots, s));
         if (st != BITMTP_OK) {
             dev->dirty.store(1, std::memory_order_release);
             return st;

@@ -1,7 +1,8 @@
 // gemm.cu -- the W2A8 ternary linear on sm_103a: an activation-operand
 // preparation kernel followed by a persistent, warp-specialised stream-K GEMM.
 //
-// Two launches per call, chained by programmatic dependent launch (PDL):
+// Two launches per call, chained by programmatic dependent launch (PDL)
+// (one in the layer-chain mode of the dp4a path, below):
 //
 //   act_prep_kernel   one CTA per (problem, activation row): the row's absmax
 //                     and int8 codes (the quantiser of the standalone kernel,
@@ -56,7 +57,14 @@
 //   dp4a (kPathDP): four byte masks per code word, four int32 accumulators
 //     per row (scales 4^s, recombined with exact shifts).
 // With u = T + 1, sum_k T*q = sum_k u*q - sum_k q; the second sum comes from
-// the preparation kernel's prefix sums.  Both paths store the activation
+// the preparation kernel's prefix sums.
+//
+// Layer-chain mode (dp4a path, every problem's row absmax handed over by the
+// call that wrote the rows): no preparation kernel.  The consumer warps
+// quantise the first ring chunk's activation tiles themselves and warp 5 the
+// later ones, with per-tile code sums in shared memory; CTA 0 zeroes the
+// output absmax and releases every CTA's epilogues through a workspace word,
+// which the last CTA to finish resets.  A kernel instantiation of its own.  Both paths store the activation
 // operand in units of 16 k: per operand row 16 bytes, byte 4s + b holding
 // k = {2s, 2s+8, 2s+1, 2s+9}[b] of the unit -- the order in which one shift
 // and mask per register lays out the code word.
@@ -104,6 +112,7 @@ enum : int {
     kErrWaitEmpty = 0x106,
     kErrWaitFlag = 0x107,
     kErrWaitSlot = 0x108,
+    kErrWaitZero = 0x109,
 };
 
 struct Ctrl {
@@ -115,6 +124,7 @@ struct Ctrl {
     uint64_t dfull[2][4];         // MMA warp 5 + i finished segment s: dfull[i][s & 3]
     uint64_t slot_done;           // contributor partial sums stored (four consumer warps)
     uint64_t drained[2];          // after a failed wait: every MMA MMA warp 5 + i issued is complete
+    uint64_t zero_ready;          // fused dp4a mode: the output absmax is zeroed for this launch
     uint32_t tmem_base;
     int failed;
     int owner_ok;
@@ -549,6 +559,219 @@ act_prep_kernel(const __grid_constant__ GemmParams P) {
     fence_proxy_async_global();
 }
 
+// ------------------------------------------------ fused activation tiles --
+// Layer-chain mode of the dp4a path (every problem brings its rows' absmax):
+// the GEMM writes the activation tiles of its ring itself, from the raw rows,
+// with the quantiser and byte order of the preparation kernel, instead of the
+// producer copying a preparation kernel's output.  Chunk j holds the tiles
+// whose weights the producer's chunk j brings (processing order).  Unit g of
+// a chunk (0 <= g < 32 * DPR) is 16-k unit g % 8 of operand row (g / 8) % DPR
+// of chunk tile g / (8 * DPR); the eight consecutive units of one (tile, row)
+// sum its codes into Rs[tile slot][row] for the consumers' u = T + 1
+// correction.  The consumer warps quantise chunk 0 (one unit per thread:
+// they would only wait for it), warp 5 the later chunks, one unit per lane
+// and pass, ahead of the consumers.
+
+// Codes of one unit into `dst` (16 bytes; register si holds k = {2si, 2si+8,
+// 2si+1, 2si+9}); returns their sum.  q = clamp(rint(RN(x * s)), -127, 127)
+// in integers, the same values as the preparation kernel's float steps.
+__device__ __forceinline__ int quant_unit(const float (&v)[16], float sc, uint8_t* dst, bool store) {
+    int q[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) q[e] = max(-127, min(127, __float2int_rn(__fmul_rn(v[e], sc))));
+    uint32_t reg[4];
+    int sum = 0;
+#pragma unroll
+    for (int si = 0; si < 4; ++si) {
+        reg[si] = (static_cast<uint32_t>(q[2 * si]) & 0xFFu) | ((static_cast<uint32_t>(q[2 * si + 8]) & 0xFFu) << 8) |
+                  ((static_cast<uint32_t>(q[2 * si + 1]) & 0xFFu) << 16) | (static_cast<uint32_t>(q[2 * si + 9]) << 24);
+        sum = __dp4a(static_cast<int>(reg[si]), 0x01010101, sum);
+    }
+    if (store) *reinterpret_cast<uint4*>(dst) = make_uint4(reg[0], reg[1], reg[2], reg[3]);
+    return sum;
+}
+
+// Chunk 0 by the consumer warps: thread tid < 32 * DPR quantises unit tid.
+template <int DPR>
+__device__ __noinline__ void fused_chunk0(const GemmProblem* pp, int np, long long t_begin, long long t_end,
+                                             uint8_t* tiles, int* rs, int tid) {
+    constexpr int BT = btile_bytes(kPathDP, DPR);
+    const int nloc = static_cast<int>(t_end - t_begin);
+    const int cnt = min(kChunk, nloc);
+    const int ti = tid / (8 * DPR), m = (tid >> 3) % DPR;
+    ProcIter it;
+    it.init(pp, np, t_begin, t_end);
+    for (int z = 0; z < ti && z + 1 < cnt; ++z) it.next(pp, np, t_begin);
+    const GemmProblem& pr = pp[it.s.pi];
+    const bool live = ti < cnt && m < pr.M;
+    float v[16];
+    float amax = 0.f;
+    if (live) {
+        amax = __ldcg(pr.amax_in + m);
+        load16(pr, act_row(pr, m), pr.vec_ok != 0, it.k * kTileK + (tid & 7) * 16, v);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = 0.f;
+    }
+    int rsum = quant_unit(v, quant_scale(amax), tiles + static_cast<size_t>(ti) * BT + (tid & 7) * (DPR * 16) + m * 16,
+                          ti < cnt);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, o);
+    if (ti < cnt && (tid & 7) == 0) rs[ti * 4 + m] = rsum;
+}
+
+// Chunks 1.. by warp 5.  Per chunk all of a lane's loads are issued first,
+// unconditionally (one round trip to L2 per chunk): units that are not whole
+// aligned vectors read a harmless aligned dummy and are reloaded element by
+// element afterwards (the rare tail).  The quantisation then runs as a rolled
+// loop (the unit's registers shifted down each pass): this code runs once
+// per chunk and warp, and its size, not its arithmetic, sets its speed.
+// kWide: some problem of the launch has fp32 rows (four 16-byte loads per
+// unit instead of two).  One call covers the kPer units i0 .. i0 + kPer - 1
+// of the lane.
+template <int DPR, bool kWide, int kPer>
+__device__ __forceinline__ void fused_chunk(const GemmProblem* pp, const int (&tp)[kChunk], const int (&tk)[kChunk],
+                                            int cnt, int m, int lane, int i0, const uint4* dummy, uint8_t* tiles,
+                                            int* rs) {
+    constexpr int BT = btile_bytes(kPathDP, DPR);
+    constexpr int kLd = kWide ? 4 : 2;
+    uint4 raw[kPer][kLd];
+    int pis[kPer], k0s[kPer];
+    bool vec[kPer], live[kPer];
+    // the row's absmax for the chunk's first problem (every CTA reads the same
+    // few words: one load per chunk, not per unit)
+    const GemmProblem& p0 = pp[tp[0]];
+    const float am0 = __ldcg(m < p0.M ? p0.amax_in + m : reinterpret_cast<const float*>(dummy));
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int ti = ((i0 + i) * 32 + lane) / (8 * DPR);
+        int pi = 0, kk = 0;
+#pragma unroll
+        for (int z = 0; z < kChunk; ++z)
+            if (z == ti) {
+                pi = tp[z];
+                kk = tk[z];
+            }
+        const GemmProblem& pr = pp[pi];
+        pis[i] = pi;
+        k0s[i] = kk * kTileK + (lane & 7) * 16;
+        live[i] = ti < cnt && m < pr.M;
+        vec[i] = live[i] && pr.vec_ok != 0 && k0s[i] + 16 <= pr.K;
+        const bool f32 = pr.act_kind == BITMTP_F32;
+        const uint4* src = vec[i] ? reinterpret_cast<const uint4*>(act_row(pr, m) + (f32 ? 4ll : 2ll) * k0s[i])
+                                  : dummy;
+        raw[i][0] = __ldcg(src);
+        raw[i][1] = __ldcg(src + 1);
+        if constexpr (kWide) {
+            const uint4* src2 = (vec[i] && f32) ? src + 2 : src;
+            raw[i][2] = __ldcg(src2);
+            raw[i][3] = __ldcg(src2 + 1);
+        }
+    }
+#pragma unroll 1
+    for (int i = 0; i < kPer; ++i) {
+        const int ti = ((i0 + i) * 32 + lane) / (8 * DPR);
+        const GemmProblem& pr = pp[pis[0]];
+        const bool f32 = pr.act_kind == BITMTP_F32;
+        float v[16];
+        if constexpr (kWide) {
+            if (f32) {
+                const uint32_t w[16] = {raw[0][0].x, raw[0][0].y, raw[0][0].z, raw[0][0].w,
+                                        raw[0][1].x, raw[0][1].y, raw[0][1].z, raw[0][1].w,
+                                        raw[0][2].x, raw[0][2].y, raw[0][2].z, raw[0][2].w,
+                                        raw[0][3].x, raw[0][3].y, raw[0][3].z, raw[0][3].w};
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(w[e]);
+            }
+        }
+        if (!f32) {
+            const uint32_t w[8] = {raw[0][0].x, raw[0][0].y, raw[0][0].z, raw[0][0].w,
+                                   raw[0][1].x, raw[0][1].y, raw[0][1].z, raw[0][1].w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                v[2 * e] = __uint_as_float(w[e] << 16);
+                v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            }
+        }
+        if (!vec[0]) {
+            float t[16];
+            if (live[0]) {
+                load16_tail(pr.act_kind, act_row(pr, m), pr.K, k0s[0], t);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) t[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = t[e];
+        }
+        float amax = am0;
+        if (pis[0] != tp[0]) amax = __ldcg(pr.amax_in + m);  // a problem boundary inside the chunk
+        if (!live[0]) amax = 0.f;
+        int rsum = quant_unit(v, quant_scale(amax),
+                              tiles + static_cast<size_t>(ti) * BT + (lane & 7) * (DPR * 16) + m * 16, ti < cnt);
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, o);
+        if (ti < cnt && (lane & 7) == 0) rs[ti * 4 + m] = rsum;
+        // the next unit into position 0
+#pragma unroll
+        for (int k = 0; k + 1 < kPer; ++k) {
+#pragma unroll
+            for (int l = 0; l < kLd; ++l) raw[k][l] = raw[k + 1][l];
+            pis[k] = pis[k + 1];
+            k0s[k] = k0s[k + 1];
+            vec[k] = vec[k + 1];
+            live[k] = live[k + 1];
+        }
+    }
+}
+
+template <int DPR>
+__device__ void fused_act_tiles(const GemmParams& P, Ctrl* c, const GemmProblem* pp, int np, long long t_begin,
+                                long long t_end, int R, uint8_t* Br, int* Rs, int lane) {
+    constexpr int BT = btile_bytes(kPathDP, DPR);
+    const int nloc = static_cast<int>(t_end - t_begin);
+    const int nchunks = (nloc + kChunk - 1) / kChunk;
+    if (nchunks < 2) return;  // chunk 0 is the consumer warps'
+    const int m = (lane >> 3) % DPR;  // the lane's operand row, the same for all its units
+    bool wide = false;
+    for (int i = 0; i < np; ++i) wide = wide || pp[i].act_kind == BITMTP_F32;
+    // an aligned address that is always valid to read (this CTA's own
+    // partial-sum slot): the target of loads whose results are not used
+    const uint4* dummy = reinterpret_cast<const uint4*>(P.slots) + static_cast<size_t>(blockIdx.x) * 4 * kTileN;
+    ProcIter it;
+    it.init(pp, np, t_begin, t_end);
+    for (int z = 0; z < kChunk; ++z) it.next(pp, np, t_begin);  // past chunk 0 (whole: nchunks >= 2)
+    pdl_wait();  // the rows and their absmax come from the kernel before this one
+    for (int j = 1; j < nchunks; ++j) {
+        const int q = j % R;
+        if (j >= R &&
+            !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->empty[q]), ((j / R) - 1) & 1, P.wait_ns))) {
+            if (lane == 0) fail(c, P.err, kErrWaitEmpty);
+            return;
+        }
+        const int cnt = min(kChunk, nloc - j * kChunk);
+        int tp[kChunk], tk[kChunk];  // problem and k tile of each chunk tile
+#pragma unroll
+        for (int z = 0; z < kChunk; ++z) {
+            tp[z] = it.s.pi;
+            tk[z] = it.k;
+            if (z < cnt) it.next(pp, np, t_begin);
+        }
+        uint8_t* tiles = Br + static_cast<size_t>(q) * kChunk * BT;
+        int* rs = Rs + q * kChunk * 4;
+        constexpr int kPer = DPR;  // units per lane and chunk (32 * DPR / 32)
+        if (wide) {  // fp32 rows: half of the units per batch of loads (registers)
+            constexpr int kHalf = kPer > 1 ? kPer / 2 : 1;
+            for (int i0 = 0; i0 < kPer; i0 += kHalf)
+                fused_chunk<DPR, true, kHalf>(pp, tp, tk, cnt, m, lane, i0, dummy, tiles, rs);
+        } else {
+            fused_chunk<DPR, false, kPer>(pp, tp, tk, cnt, m, lane, 0, dummy, tiles, rs);
+        }
+        __syncwarp();
+        mbar_arrive_if(lane == 0, smem_u32(&c->bfull[q]));  // release: the tiles and sums above
+    }
+}
+
 // ------------------------------------------------------------ epilogue --
 // Store y[m][n] (and acc); returns |y[m][n]| as stored.
 // The output fields of one problem, read once per segment into registers:
@@ -604,6 +827,19 @@ __device__ __forceinline__ bool wait_flag(const unsigned* f, unsigned long long 
     if (ld_acquire_gpu(f) != 0u) return true;
     const uint64_t t0 = global_ns();
     for (;;) {
+        if (ld_acquire_gpu(f) != 0u) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// The same wait with a pause between polls, for a word that every CTA of
+// the launch polls at once: back-to-back polls from every SM would queue at
+// the word's L2 slice ahead of the loads the other warps need.
+__device__ __forceinline__ bool wait_flag_backoff(const unsigned* f, unsigned long long limit_ns) {
+    if (ld_acquire_gpu(f) != 0u) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        __nanosleep(100);
         if (ld_acquire_gpu(f) != 0u) return true;
         if (global_ns() - t0 > limit_ns) return false;
     }
@@ -667,7 +903,30 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int p_lo, const S
         named_bar_sync(kBarEpi, 128);
         alive = alive && c->owner_ok;
         if (alive) {
-            for (int cc = owner_first; cc < b; ++cc) {
+            // a long row tile split over many short CTA ranges has many
+            // contributors: on the dp4a path (one group of rows) their slots
+            // are read kBatch at a time, all loads in flight together, and
+            // added in CTA order
+            constexpr int kBatch = 8;
+            int cc = owner_first;
+            for (; kGroups == 1 && cc + kBatch <= b; cc += kBatch) {
+                int4 v[kBatch][kGroups];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+                    for (int g = 0; g < kGroups; ++g)
+                        v[u][g] = (4 * g < M) ? __ldcg(slot_ptr(P, cc + u, g, tid)) : make_int4(0, 0, 0, 0);
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+                    for (int g = 0; g < kGroups; ++g) {
+                        acc[4 * g] = acc_add<kF>(acc[4 * g], v[u][g].x);
+                        acc[4 * g + 1] = acc_add<kF>(acc[4 * g + 1], v[u][g].y);
+                        acc[4 * g + 2] = acc_add<kF>(acc[4 * g + 2], v[u][g].z);
+                        acc[4 * g + 3] = acc_add<kF>(acc[4 * g + 3], v[u][g].w);
+                    }
+            }
+            for (; cc < b; ++cc) {
 #pragma unroll
                 for (int g = 0; g < kGroups; ++g) {
                     if (4 * g < M) {
@@ -724,12 +983,17 @@ __device__ __forceinline__ int code_sum(int v, int m) {
     return __shfl_sync(0xffffffffu, v, 16 + m) - __shfl_sync(0xffffffffu, v, m);
 }
 
-template <int PATH, int DPR>
+template <int PATH, int DPR, bool kFused>
 __global__ void __maxnreg__(gemm_max_regs(PATH))
 w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr bool kTC = PATH != kPathDP;
     constexpr bool kF8 = PATH == kPathF8;  // fp32 accumulators (bit patterns in the int arrays)
+    // fused activation tiles (the dp4a path only): a kernel of its own, so
+    // the other kernels carry none of its code
+    static_assert(!kFused || PATH == kPathDP, "fused mode is a dp4a-path mode");
+    constexpr bool fused = kFused;
+    unsigned* const sync_words = kFused ? P.sync_words : nullptr;
     constexpr int BT = btile_bytes(PATH, DPR);
     constexpr int kOutRows = btile_rows(PATH, DPR);  // M <= kOutRows (the host's path choice)
     constexpr uint32_t kDCols = tmem_d_cols(PATH, DPR);
@@ -743,6 +1007,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     const int R = P.stages;                                  // chunks in the ring
     uint8_t* Wr = smem + kCtrlBytes;                         // [R][kChunk][4096]
     uint8_t* Br = Wr + static_cast<size_t>(R) * kChunk * kTileBytes;  // [R][kChunk][BT]
+    int* Rs = reinterpret_cast<int*>(Br + static_cast<size_t>(R) * kChunk * BT);  // dp4a fused: [R * kChunk][4]
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -768,8 +1033,9 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
     static_assert(offsetof(Ctrl, slot_done) == offsetof(Ctrl, wfull) + 8 * (3 * kMaxRing + kBatchBars + kBatchBars + 8),
                   "mbarriers not consecutive");
     static_assert(offsetof(Ctrl, drained) == offsetof(Ctrl, slot_done) + 8, "mbarriers not consecutive");
-    if (tid < 3 * kMaxRing + kBatchBars + kBatchBars + 11) {
-        uint32_t count = 1;                                                          // wfull, bfull, mma_done, dfull, drained
+    static_assert(offsetof(Ctrl, zero_ready) == offsetof(Ctrl, drained) + 16, "mbarriers not consecutive");
+    if (tid < 3 * kMaxRing + kBatchBars + kBatchBars + 12) {
+        uint32_t count = 1;                                            // wfull, bfull, mma_done, dfull, drained, zero_ready
         if (tid >= 2 * kMaxRing && tid < 3 * kMaxRing) count = kTC ? 2 : 4;          // empty
         else if (tid >= 3 * kMaxRing && tid < 3 * kMaxRing + kBatchBars) count = 4;  // a_full
         else if (tid == 3 * kMaxRing + kBatchBars + kBatchBars + 8) count = 4;          // slot_done
@@ -830,11 +1096,33 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             if (!withheld) w_issued[j] = j + 1;
         }
         pdl_wait();  // the activation tiles are written by the preparation kernel
+        const bool copy_acts = !fused;  // fused: the consumer warps and warp 5 write them
         const uint64_t pol_b = policy_evict_last();
-        for (int j = 0; j < npre; ++j) {
-            issue_acts(pp, np, t_begin, ita, min(kChunk, nloc - j * kChunk), BT,
-                       Br + static_cast<size_t>(j) * kChunk * BT, smem_u32(&c->bfull[j]), pol_b, leader);
-            b_issued[j] = j + 1;
+        if (copy_acts) {
+            for (int j = 0; j < npre; ++j) {
+                issue_acts(pp, np, t_begin, ita, min(kChunk, nloc - j * kChunk), BT,
+                           Br + static_cast<size_t>(j) * kChunk * BT, smem_u32(&c->bfull[j]), pol_b, leader);
+                b_issued[j] = j + 1;
+            }
+        } else if (sync_words != nullptr) {
+            // this launch's epilogues combine the output rows' absmax into
+            // amax_out: CTA 0 zeroes it and sets sync word 0; every CTA waits
+            // for the word here, long before its first epilogue, and passes
+            // it on to its consumer warps by zero_ready
+            if (b == 0) {
+                for (int i = 0; i < np; ++i)
+                    if (pp[i].amax_out != nullptr && lane < pp[i].M) pp[i].amax_out[lane] = 0.f;
+                __syncwarp();
+                if (leader) {
+                    __threadfence();
+                    *reinterpret_cast<volatile unsigned*>(sync_words) = 1u;
+                }
+            }
+            if (leader) {
+                if (!wait_flag_backoff(sync_words, P.wait_ns)) fail(c, P.err, kErrWaitZero);
+                mbar_arrive(smem_u32(&c->zero_ready));
+            }
+            __syncwarp();
         }
         // refill ring slots as they are released
         for (int j = npre; j < nchunks; ++j) {
@@ -850,9 +1138,11 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             issue_weights(pp, np, t_begin, itw, cnt, Wr + static_cast<size_t>(q) * kChunk * kTileBytes,
                           smem_u32(&c->wfull[q]), pol, leader);
             w_issued[q] = j + 1;
-            issue_acts(pp, np, t_begin, ita, cnt, BT, Br + static_cast<size_t>(q) * kChunk * BT,
-                       smem_u32(&c->bfull[q]), pol_b, leader);
-            b_issued[q] = j + 1;
+            if (copy_acts) {
+                issue_acts(pp, np, t_begin, ita, cnt, BT, Br + static_cast<size_t>(q) * kChunk * BT,
+                           smem_u32(&c->bfull[q]), pol_b, leader);
+                b_issued[q] = j + 1;
+            }
         }
         if (pending) {
             if (__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c->slot_done), 0, P.wait_ns))) {
@@ -977,6 +1267,8 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 mma_commit_if(leader, smem_u32(&c->drained[par]));
                 (void)mbar_wait_bounded(smem_u32(&c->drained[par]), 0, 100000000ull);
             }
+        } else {
+            if (fused) fused_act_tiles<DPR>(P, c, pp, np, t_begin, t_end, R, Br, Rs, lane);
         }
         __syncwarp();
     } else {
@@ -999,7 +1291,18 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         const bool asc_mine = tid < (p1 - p0 + 1) * 16;
         if (asc_mine) {
             const GemmProblem& pr = pp[p0 + tid / 16];
-            if (tid % 16 < pr.M) asc_reg = __ldcg(pr.asc + tid % 16);
+            if (tid % 16 < pr.M)
+                asc_reg = __ldcg(fused ? pr.amax_in + tid % 16 : pr.asc + tid % 16);  // fused: the absmax
+        }
+        if constexpr (!kTC) {
+            if (fused) {
+                // chunk 0 of the ring, quantised here (warp 5 takes the later
+                // ones); its bfull phase is then completed by hand, so the
+                // loop below waits for it like for any other chunk
+                if (tid < 32 * DPR) fused_chunk0<DPR>(pp, np, t_begin, t_end, Br, Rs, tid);
+                named_bar_sync(kBarEpi, 128);
+                if (tid == 0) mbar_arrive(smem_u32(&c->bfull[0]));
+            }
         }
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         if constexpr (kTC) {
@@ -1032,8 +1335,13 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         int d_seg = 0;
         auto epilogue = [&](const Seg& es, int (&acc)[16]) {
             if (first_epi) {  // publish the dequant scales once
-                if (asc_mine) c->asc[tid / 16][tid % 16] = asc_reg;
+                if (asc_mine) c->asc[tid / 16][tid % 16] = fused ? dequant_scale(asc_reg) : asc_reg;
+                // fused: no atomic on amax_out before CTA 0 has zeroed it
+                if (sync_words != nullptr && tid == 0 && alive &&
+                    !mbar_wait_bounded(smem_u32(&c->zero_ready), 0, P.wait_ns))
+                    fail(c, P.err, kErrWaitZero);
                 named_bar_sync(kBarEpi, 128);
+                if (sync_words != nullptr) alive = alive && !*reinterpret_cast<volatile int*>(&c->failed);
                 first_epi = false;
             }
             segment_epilogue<kOutRows, kF8>(P, c, p0, es, owner_first, acc, tid, alive);
@@ -1088,7 +1396,10 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
             const GemmProblem& pr = pp[sg.pi];
             const int ka = sg.ka;
             const int len = sg.kb - sg.ka;
-            const int rsl = kTC ? 0 : load_code_sum_lane(pr, ka, ka + len, lane);
+            const int rsl = (kTC || fused) ? 0 : load_code_sum_lane(pr, ka, ka + len, lane);
+            int rs[DPR];  // fused: the segment's code sums, from Rs
+#pragma unroll
+            for (int m = 0; m < DPR; ++m) rs[m] = 0;
             int dacc[4][DPR];
 #pragma unroll
             for (int s4 = 0; s4 < 4; ++s4)
@@ -1188,6 +1499,12 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                     if (alive) {
                         const uint8_t* wst = Wr + static_cast<size_t>(s) * kTileBytes;
                         const uint8_t* bst = Br + static_cast<size_t>(s) * BT;
+                        if (fused) {
+                            const int4 rv = *reinterpret_cast<const int4*>(Rs + s * 4);
+                            const int rva[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                            for (int m = 0; m < DPR; ++m) rs[m] += rva[m];
+                        }
                         const uint4 w0 = *reinterpret_cast<const uint4*>(wst + tid * 16);
                         const uint4 w1 = *reinterpret_cast<const uint4*>(wst + 2048 + tid * 16);
                         const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -1222,7 +1539,8 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
                 for (int m = 0; m < 16; ++m) acc[m] = 0;
 #pragma unroll
                 for (int m = 0; m < DPR; ++m)
-                    acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) - code_sum(rsl, m);
+                    acc[m] = dacc[0][m] + (dacc[1][m] >> 2) + (dacc[2][m] >> 4) + (dacc[3][m] >> 6) -
+                             (fused ? rs[m] : code_sum(rsl, m));
                 epilogue(sg, acc);
             }
             ++seg_idx;
@@ -1233,6 +1551,14 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
 
     // ------------------------------------------------------- tear-down --
     __syncthreads();
+    if (sync_words != nullptr && tid == 0) {
+        // every epilogue of this CTA has passed its wait on sync word 0: the
+        // last CTA to get here resets both words for the next launch
+        if (atomicAdd(sync_words + 1, 1u) == static_cast<unsigned>(P.nctas) - 1u) {
+            atomicExch(sync_words, 0u);
+            atomicExch(sync_words + 1, 0u);
+        }
+    }
     if (warp == 4 && lane == 0 && c->failed) {
         // never release shared memory with a bulk copy still in flight: wait
         // (bounded) for the last requested phase of every slot
@@ -1260,9 +1586,9 @@ cudaLaunchAttribute pdl_attr() {
     return a;
 }
 
-template <int PATH, int DPR>
+template <int PATH, int DPR, bool kFused>
 cudaError_t launch_one(const GemmParams& prm, bool pdl, cudaStream_t stream) {
-    auto kern = &w2a8_streamk_kernel<PATH, DPR>;
+    auto kern = &w2a8_streamk_kernel<PATH, DPR, kFused>;
     // the opt-in shared-memory size, once per device (first-use races only
     // repeat the same call)
     static std::atomic<unsigned long long> configured{0ull};
@@ -1285,8 +1611,10 @@ cudaError_t launch_one(const GemmParams& prm, bool pdl, cudaStream_t stream) {
     pc.stream = stream;
     pc.attrs = attr;
     pc.numAttrs = pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&pc, &act_prep_kernel<PATH, DPR>, prm);
-    if (e != cudaSuccess) return e;
+    if (!kFused) {
+        e = cudaLaunchKernelEx(&pc, &act_prep_kernel<PATH, DPR>, prm);
+        if (e != cudaSuccess) return e;
+    }
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(prm.nctas), 1, 1);
@@ -1294,7 +1622,10 @@ cudaError_t launch_one(const GemmParams& prm, bool pdl, cudaStream_t stream) {
     cfg.dynamicSmemBytes = gemm_smem_bytes(PATH, DPR, prm.stages);
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;  // overlaps the preparation kernel: only weights are read before its wait
+    // overlaps the kernel before it (the preparation kernel, or in fused mode
+    // the caller's previous kernel when the caller allows it): only weights
+    // are read before its wait
+    cfg.numAttrs = (kFused && !pdl) ? 0 : 1;
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
@@ -1310,16 +1641,18 @@ int gemm_stages(int path, int dp_rows) {
 
 size_t gemm_smem_bytes(int path, int dp_rows, int stages) {
     return static_cast<size_t>(kCtrlBytes) +
-           static_cast<size_t>(stages) * kChunk * (kTileBytes + btile_bytes(path, dp_rows));
+           static_cast<size_t>(stages) * kChunk * (kTileBytes + btile_bytes(path, dp_rows)) +
+           (path == kPathDP ? static_cast<size_t>(stages) * kChunk * 16 : 0);  // fused mode's code sums
 }
 
 cudaError_t launch_gemm(const GemmParams& prm, int path, int dp_rows, bool pdl, cudaStream_t stream) {
-    if (path == kPathTC16) return launch_one<kPathTC16, 1>(prm, pdl, stream);
-    if (path == kPathTC8) return launch_one<kPathTC8, 1>(prm, pdl, stream);
-    if (path == kPathF8) return launch_one<kPathF8, 1>(prm, pdl, stream);
-    if (dp_rows <= 1) return launch_one<kPathDP, 1>(prm, pdl, stream);
-    if (dp_rows <= 2) return launch_one<kPathDP, 2>(prm, pdl, stream);
-    return launch_one<kPathDP, 4>(prm, pdl, stream);
+    if (path == kPathTC16) return launch_one<kPathTC16, 1, false>(prm, pdl, stream);
+    if (path == kPathTC8) return launch_one<kPathTC8, 1, false>(prm, pdl, stream);
+    if (path == kPathF8) return launch_one<kPathF8, 1, false>(prm, pdl, stream);
+    const bool f = prm.fused != 0;
+    if (dp_rows <= 1) return f ? launch_one<kPathDP, 1, true>(prm, pdl, stream) : launch_one<kPathDP, 1, false>(prm, pdl, stream);
+    if (dp_rows <= 2) return f ? launch_one<kPathDP, 2, true>(prm, pdl, stream) : launch_one<kPathDP, 2, false>(prm, pdl, stream);
+    return f ? launch_one<kPathDP, 4, true>(prm, pdl, stream) : launch_one<kPathDP, 4, false>(prm, pdl, stream);
 }
 
 }  // namespace bitmtp

@@ -57,6 +57,10 @@ struct GemmParams {
     int stages;               // chunks in the shared-memory ring
     int nctas;
     int withhold;             // test only: ring chunk CTA 0 never requests (-1: none)
+    int fused;                // dp4a path, every row's absmax handed over: no preparation
+                              // kernel; warp 5 quantises the activation tiles into the ring
+    unsigned* sync_words;     // fused with an out.amax: [0] out.amax zeroed for this launch,
+                              // [1] CTAs finished (both left at zero); else null
     int tiles_q, tiles_r;     // stream-K split: CTA b gets tiles_q tiles, plus one if b < tiles_r
     long long total_tiles;
     unsigned long long wait_ns;  // bound on every wait of the launch
@@ -68,7 +72,8 @@ struct GemmParams {
 constexpr int kMaxCtas = 320;         // persistent CTAs per launch (>= 2 per SM on GB300)
 constexpr int kMinTilesPerCta = 4;    // fewer CTAs on small problems: fewer split row tiles
 
-// Workspace: partial-sum-ready flags (must be zero when a launch starts; every
+// Workspace: two sync words of the fused dp4a mode (bytes 0-7) and the
+// partial-sum-ready flags (both must be zero when a launch starts; every
 // launch leaves them at zero), one partial-sum slot per CTA, then one
 // activation region per problem (sized by its k tiles).
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -86,9 +91,10 @@ size_t gemm_smem_bytes(int path, int dp_rows, int stages);
 int gemm_stages(int path, int dp_rows);
 
 // Launch the activation preparation kernel, then the stream-K GEMM kernel
-// (params validated and filled).  `pdl` lets the preparation kernel overlap
-// the kernel before it on the stream; the GEMM always overlaps the
-// preparation kernel (it only streams weights before waiting for it).
+// (params validated and filled); in fused mode the GEMM kernel alone.  `pdl`
+// lets the first of them overlap the kernel before it on the stream; the GEMM
+// always overlaps the preparation kernel (it only streams weights before
+// waiting for it).
 cudaError_t launch_gemm(const GemmParams& prm, int path, int dp_rows, bool pdl, cudaStream_t stream);
 
 }  // namespace bitmtp

@@ -358,12 +358,14 @@ def gemm(pk: torch.Tensor, w_scale: float, N: int, K: int, x: torch.Tensor,
 
 def gemm_grouped(problems, flags: int = 0, stream=None, workspace_tensor: torch.Tensor | None = None):
     """One launch over several problems.  Each problem is a dict with keys
-    pk, w_scale, N, K, x, (a_scale), y, (acc)."""
+    pk, w_scale, N, K, x, (a_scale), (amax: the rows' absmax handed over),
+    y, (acc), (amax_out: receives the output rows' absmax)."""
     descs = []
     for p in problems:
         x = p["x"]
         descs.append(GemmDesc(p["pk"].data_ptr(), float(p["w_scale"]), p["N"], p["K"], x.shape[0],
-                              make_act(x, p.get("a_scale")), make_out(p["y"], p.get("acc"))))
+                              make_act(x, p.get("a_scale"), p.get("amax")),
+                              make_out(p["y"], p.get("acc"), p.get("amax_out"))))
     if not descs:
         return
     nb = bitmtp_linear_workspace_bytes_grouped(descs)
