@@ -7,11 +7,12 @@ dequant in the kernel's fixed order) bit for bit, and the same chain without
 the handed-over absmax gives the same bits.
 
 At widths 1-4 (the dp4a path) a call whose every problem brings its rows'
-absmax runs fused: no preparation launch, the GEMM quantises its own
+absmax runs as one launch: no preparation kernel, the GEMM quantises its own
 activation tiles.  Its single calls, grouped calls over mixed K, unaligned
 and ragged rows, calls without an output absmax, and a chain replayed from a
 CUDA graph (the workspace's sync words back at zero after every launch) are
-compared with the oracle bit for bit."""
+compared with the oracle bit for bit; so are the same handed-over-absmax
+calls at widths 5-16 (the tensor paths, with the preparation kernel)."""
 import numpy as np
 import pytest
 import torch
@@ -156,6 +157,14 @@ def _check(got_y, got_acc, got_amax, exp, out_dtype):
     (1, 32000, 6912, False, 1, "f32", True),
     (3, 20000, 1000, False, 0, "bf16", True),
     (2, 16000, 2560, True, 5, "f32", False),
+    # the tensor paths (the preparation kernel takes the handed-over absmax)
+    (5, 2560, 2560, True, 0, "bf16", True),
+    (8, 1000, 300, False, 1, "f32", True),
+    (9, 130, 1000, True, 3, "bf16", True),
+    (16, 2560, 6912, True, 0, "f32", True),
+    (16, 384, 2560, False, 0, "bf16", False),
+    (8, 32000, 2560, True, 0, "bf16", True),
+    (16, 11008, 4096, False, 1, "f32", True),
 ])
 def test_fused_call_matches_oracle(M, N, K, is_bf16, offset, out_dtype, with_amax_out):
     rng = np.random.default_rng(9400 + M * 13 + K)
@@ -183,10 +192,13 @@ def test_fused_call_matches_oracle(M, N, K, is_bf16, offset, out_dtype, with_ama
         assert int(ws[:1536].abs().sum()) == 0  # sync words and flags left at zero
 
 
-@pytest.mark.parametrize("M", [1, 3, 4])
+@pytest.mark.parametrize("M", [1, 3, 4, 8, 12, 16])
 def test_fused_grouped_mixed_k(M):
     rng = np.random.default_rng(9500 + M)
-    shapes = [(2560, 2560), (6912, 2560), (300, 1000), (2560, 6912)]  # (K, N)
+    if M <= 4:
+        shapes = [(2560, 2560), (6912, 2560), (300, 1000), (2560, 6912)]  # (K, N)
+    else:  # the tensor paths
+        shapes = [(1024, 1024), (300, 1000), (2048, 512), (1000, 130)]
     probs, exps = [], []
     for i, (K, N) in enumerate(shapes):
         T = inputs.ternary(rng, (N, K), 0.5)
