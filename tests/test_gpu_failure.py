@@ -11,20 +11,24 @@ bitmtp_linear_device_error (and that reading clears it), and that the next
 normal call on the same device and workspace -- zero-filled again, as the
 header asks after an error -- matches the oracle.  Both compute paths run it:
 the dp4a path (no tensor memory) and the tensor path (its tensor memory must
-be freed for the next launch to allocate)."""
+be freed for the next launch to allocate), and so does the dp4a path's
+one-launch layer-chain mode (quantising warps, the output-absmax zeroing word
+and its reset)."""
 import numpy as np
 import pytest
 import torch
 
 from ternary_w2a8_linear_gb300 import build, inputs
 from ternary_w2a8_linear_gb300 import linear as L
-from gpu_util import assert_f32_close, dev_tensor, reference
+import oracle
+from gpu_util import assert_f32_close, bf16_tensor, dev_tensor, reference
 
 pytestmark = pytest.mark.gpu
 
 # the kernel's wait codes (weights, activation tiles, A full, A empty, D,
-# ring slot, contributor flag, contributor slot)
-WAIT_CODES = set(range(0x101, 0x109))
+# ring slot, contributor flag, contributor slot, the one-launch mode's zeroed
+# output absmax)
+WAIT_CODES = set(range(0x101, 0x10A))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -83,4 +87,43 @@ def test_noalloc_recovers_after_reported_error():
         assert st == L.OK
         _, acc_ref, _, _ = reference(T, w, x, False)
         assert np.array_equal(acc.cpu().numpy(), acc_ref)
+    assert L.bitmtp_linear_device_error() == 0
+
+
+def test_one_launch_chain_call_times_out_then_next_call_is_exact():
+    """The one-launch mode (rows' absmax handed over, width 4) on a call with
+    eleven ring chunks per CTA, so warp 5 quantises too, and an output absmax,
+    so the zeroing word is in play: the withheld chunk ends the launch with a
+    wait code, and after the workspace is zero-filled again the same call is
+    exact, twice (the second time on the word the first one reset)."""
+    M, N, K = 4, 32000, 6912
+    rng = np.random.default_rng(2468)
+    T = inputs.ternary(rng, (N, K), 0.5)
+    x = inputs.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    amax_in = dev_tensor(np.max(np.abs(oracle.bf16_bits_to_f32(x)), axis=1).astype(np.float32))
+    pk = L.pack(dev_tensor(T))
+    xd = bf16_tensor(x)
+    nb = L.bitmtp_linear_workspace_bytes(N, K, M)
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    amax_out = torch.empty(M, dtype=torch.float32, device="cuda")
+    act, out = L.make_act(xd, amax=amax_in), L.make_out(y, acc, amax=amax_out)
+    st = L.bitmtp_linear_gemm(L._ptr(pk), 0.03, N, K, M, act, out, L._ptr(ws), nb,
+                              L.FLAG_PDL | L.FLAG_TEST_WITHHOLD, L._stream(None))
+    assert st == L.OK, L.status_string(st)
+    code = L.bitmtp_linear_device_error()
+    assert code in WAIT_CODES, hex(code)
+    assert L.bitmtp_linear_device_error() == 0
+
+    ws.zero_()
+    q, _, _ = oracle.quant_act_bf16(x)
+    acc_ref = oracle.gemm_acc(T, q)
+    for _ in range(2):
+        st = L.bitmtp_linear_gemm(L._ptr(pk), 0.03, N, K, M, act, out, L._ptr(ws), nb, L.FLAG_PDL,
+                                  L._stream(None))
+        assert st == L.OK
+        torch.cuda.synchronize()
+        assert np.array_equal(acc.cpu().numpy(), acc_ref.astype(np.int32))
+        assert int(ws[:1536].abs().sum()) == 0
     assert L.bitmtp_linear_device_error() == 0
