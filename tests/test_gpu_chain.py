@@ -216,6 +216,31 @@ def test_fused_grouped_mixed_k(M):
         _check(pr["y"], pr["acc"], pr["amax_out"], exp, "bf16")
 
 
+@pytest.mark.parametrize("M", [2, 4])
+def test_fused_grouped_mixed_kinds_several_chunks(M):
+    """One-launch grouped call over bf16 and fp32 rows (aligned and not), with
+    about 13 tiles per CTA: warp 5 quantises chunks that hold tiles of two
+    problems of different kinds."""
+    rng = np.random.default_rng(9700 + M)
+    specs = [(2560, 16000, True, 0), (6912, 2560, False, 0), (1000, 8000, False, 1), (300, 6000, True, 3)]
+    probs, exps = [], []
+    for i, (K, N, is_bf16, offset) in enumerate(specs):
+        T = inputs.ternary(rng, (N, K), 0.45)
+        w = np.float32(0.015 + 0.005 * i)
+        xf = rng.standard_normal((M, K)).astype(np.float32)
+        x = inputs.to_bf16_bits(xf) if is_bf16 else xf
+        probs.append(dict(pk=L.pack(dev_tensor(T)), w_scale=float(w), N=N, K=K, x=_act_on_device(x, is_bf16, offset),
+                          amax=dev_tensor(_row_amax(x, is_bf16)),
+                          y=torch.empty((M, N), dtype=torch.float32, device="cuda"),
+                          acc=torch.empty((M, N), dtype=torch.int32, device="cuda"),
+                          amax_out=torch.full((M,), -1.0, dtype=torch.float32, device="cuda")))
+        exps.append(_expect(T, w, x, is_bf16, "f32"))
+    L.gemm_grouped(probs, flags=L.FLAG_PDL)
+    torch.cuda.synchronize()
+    for pr, exp in zip(probs, exps):
+        _check(pr["y"], pr["acc"], pr["amax_out"], exp, "f32")
+
+
 def test_fused_chain_replayed_from_a_graph():
     """The 4-layer chain at width 2, captured once with PDL and replayed three
     times on one workspace: every replay gives the oracle's chain and leaves
