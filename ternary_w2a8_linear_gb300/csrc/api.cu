@@ -152,7 +152,12 @@ struct TernParams {
 //   sum at scale 2^(j - kBinOff - 150), entry (m, e) into bin e + kBinOff;
 // * at the end each thread adds its accumulator, in four 32-bit pieces, to
 //   bins b + 32 i + kBinOff (i = 0..3), and each block adds its non-zero bins
-//   into one global set of bins (zeroed by the host before the launch).
+//   into one global set of bins (zeroed by the host before the launch);
+// * the common entries, |w| in [2^-14, 8), never reach the integer road: as
+//   integers at the fixed scale 2^-37 they are summed exactly in fp32 pieces
+//   (absmean_hist_kernel's add_fast) and added as two 32-bit pieces to bins
+//   113 + kBinOff and 145 + kBinOff; the pass then runs on the
+//   floating-point pipe instead of saturating the integer one.
 // Bins 89..438 are the only ones used; bin 511 counts non-finite entries.  A
 // bin stays below 2^39 * 2^24 + 2^17 * 2^32 < 2^64.
 constexpr int kHistBins = 512;
@@ -225,6 +230,34 @@ absmean_hist_kernel(const __grid_constant__ TernParams P) {
             atomicAdd(&h[e + kBinOff], m);
         }
     };
+    // The common entries, |w| in [2^-14, 8), on the floating-point pipe:
+    // |w| * 2^37 = a * 2^20 + b exactly, with p = |w| * 2^17 (exact, below
+    // 2^20), a = RN(p) (an integer, by adding and subtracting 1.5 * 2^23) and
+    // b = (p - a) * 2^20 (p - a is exact by Sterbenz, as p >= 8, and a
+    // multiple of 2^-20 in [-1/2, 1/2], so b is an integer of at most 2^19).
+    // a and b are summed in fp32 over at most 16 entries (sums below 2^24 stay
+    // exact), then flushed into 64-bit integers; sa * 2^20 + sb is the sum of
+    // |w| * 2^37 over the thread's common entries.
+    float fa = 0.f, fb = 0.f;
+    unsigned long long sa = 0ull;
+    long long sb = 0ll;
+    auto add_fast = [&](float w) {
+        const uint32_t bits = __float_as_uint(w) & 0x7FFFFFFFu;
+        if (bits - 0x38800000u < 0x41000000u - 0x38800000u) {  // 2^-14 <= |w| < 8
+            const float p = __fmul_rn(__uint_as_float(bits), 131072.f);
+            const float a = __fadd_rn(__fadd_rn(p, 12582912.f), -12582912.f);
+            fa = __fadd_rn(fa, a);
+            fb = __fadd_rn(fb, __fmul_rn(__fadd_rn(p, -a), 1048576.f));
+        } else if (bits != 0u) {  // zeros add nothing; the rest (NaN and inf too) as above
+            add(w);
+        }
+    };
+    auto flush = [&]() {  // at most 16 add_fast calls since the last flush
+        sa += static_cast<unsigned long long>(__float2uint_rn(fa));
+        sb += static_cast<long long>(__float2int_rn(fb));
+        fa = 0.f;
+        fb = 0.f;
+    };
     const uint64_t pol = policy_evict_last();
     if (flat) {
         const long long total = static_cast<long long>(N) * K;
@@ -242,18 +275,20 @@ absmean_hist_kernel(const __grid_constant__ TernParams P) {
             for (int u = 0; u < 4; ++u) v[u] = ld_f4_hint(W4 + i + u * stride, pol);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                add(v[u].x);
-                add(v[u].y);
-                add(v[u].z);
-                add(v[u].w);
+                add_fast(v[u].x);
+                add_fast(v[u].y);
+                add_fast(v[u].z);
+                add_fast(v[u].w);
             }
+            flush();
         }
         for (; i < n4; i += stride) {
             const float4 v = ld_f4_hint(W4 + i, pol);
-            add(v.x);
-            add(v.y);
-            add(v.z);
-            add(v.w);
+            add_fast(v.x);
+            add_fast(v.y);
+            add_fast(v.z);
+            add_fast(v.w);
+            flush();
         }
         for (long long i1 = 4 * n4 + first; i1 < total; i1 += stride) add(W[i1]);
     } else {
@@ -269,21 +304,30 @@ absmean_hist_kernel(const __grid_constant__ TernParams P) {
                 for (int u = 0; u < 4; ++u) v[u] = ld_f4_hint(row4 + k4 + u * bd, pol);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    add(v[u].x);
-                    add(v[u].y);
-                    add(v[u].z);
-                    add(v[u].w);
+                    add_fast(v[u].x);
+                    add_fast(v[u].y);
+                    add_fast(v[u].z);
+                    add_fast(v[u].w);
                 }
+                flush();
             }
             for (; k4 < K4; k4 += bd) {
                 const float4 v = ld_f4_hint(row4 + k4, pol);
-                add(v.x);
-                add(v.y);
-                add(v.z);
-                add(v.w);
+                add_fast(v.x);
+                add_fast(v.y);
+                add_fast(v.z);
+                add_fast(v.w);
+                flush();
             }
             for (int k = 4 * K4 + threadIdx.x; k < K; k += blockDim.x) add(row[k]);
         }
+    }
+    {
+        // the common entries' sum at the fixed scale 2^-37 (exponent 113),
+        // non-negative and below 2^63, in two 32-bit pieces
+        const unsigned long long fix = static_cast<unsigned long long>(static_cast<long long>(sa << 20) + sb);
+        if (fix & 0xFFFFFFFFull) atomicAdd(&h[113 + kBinOff], fix & 0xFFFFFFFFull);
+        if (fix >> 32) atomicAdd(&h[145 + kBinOff], fix >> 32);
     }
     if (have_base) {
         const unsigned long long piece[4] = {acc_lo & 0xFFFFFFFFull, acc_lo >> 32, acc_hi & 0xFFFFFFFFull, acc_hi >> 32};

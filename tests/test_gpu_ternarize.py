@@ -55,6 +55,23 @@ def test_wide_magnitude_range_subnormals_and_zeros():
     _check(W)
 
 
+def test_fixed_scale_window_boundaries():
+    """Entries at and next to the edges of the window [2^-14, 8) that the
+    absmean pass sums at a fixed scale, mixed with entries outside it (tiny,
+    subnormal, zero, large) and with ordinary weights, in a matrix large enough
+    for many blocks and threads: the scale bit for bit."""
+    rng = np.random.default_rng(77)
+    N, K = 513, 1031
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    edges = np.array([2.0 ** -14, np.nextafter(np.float32(2.0 ** -14), np.float32(0)),
+                      np.nextafter(np.float32(2.0 ** -14), np.float32(1)), np.nextafter(np.float32(8), np.float32(0)),
+                      8.0, np.nextafter(np.float32(8), np.float32(9)), 7.99999, 1e-30, 1e-44, 0.0, 1e6, 3.0e38,
+                      2.0 ** -14 + 2.0 ** -37, 0.5 + 2.0 ** -24], dtype=np.float32)
+    idx = rng.integers(0, N * K, size=4000)
+    W.reshape(-1)[idx] = edges[rng.integers(0, len(edges), size=idx.size)] * np.where(rng.random(idx.size) < 0.5, -1, 1)
+    _check(W)
+
+
 def test_summation_order_case():
     W = np.array([[2.0 ** 30, 64.0, 2.0 ** -23, 2.0 ** -23]], dtype=np.float32)
     pk, g, T = _check(W)
