@@ -250,7 +250,7 @@ typedef struct bitmtp_out {
  * of about 2.5 MiB -- one slot of partial sums per CTA for row tiles split
  * between CTAs, a ready flag per slot and two synchronisation words of the
  * one-launch layer-chain calls -- and each problem's quantised
- * activation operand (about 4 KiB per 128 in-features).  Every call leaves
+ * activation operand (about 4.5 KiB per 128 in-features).  Every call leaves
  * the flags at zero, so one workspace serves calls of any shapes that fit.
  * Calls that may execute concurrently on the GPU need distinct workspaces;
  * calls ordered on one stream may share one.  After a call that ends in

@@ -196,9 +196,9 @@ def test_workspace_bytes(lib):
     a256 = lambda x: -(-x // 256) * 256
     # a 256-byte header, one ready flag and one partial-sum slot (16 rows x 128
     # columns of int32) per CTA of the largest grid, then one activation region
-    # per problem: 4 KiB per k tile, prefix sums of 16 rows, 16 scales
+    # per problem: 4.5 KiB per k tile, prefix sums of 16 rows, 16 scales
     fixed = 256 + a256(320 * 4) + 320 * 16 * 128 * 4
-    region = lambda kt: a256(kt * 4096) + a256(16 * (kt + 1) * 4) + 256
+    region = lambda kt: a256(kt * 4608) + a256(16 * (kt + 1) * 4) + 256
     assert wb(128, 128, 1) == fixed + region(1)
     assert wb(32000, 2560, 16) == fixed + region(20)
     assert wb(32000, 2560, 1) == wb(5, 2560, 16)   # depends on K only
