@@ -326,7 +326,7 @@ int bitmtp_linear_gemm_grouped(const bitmtp_gemm_desc* d, int n_desc,
  *     stream capture begins.
  *   - Sharing: all calls on a device share the one array and it keeps what
  *     the previous call left.  The part that must start at zero (sync
- *     words and ready flags, 1.5 KiB) starts zeroed and every call leaves it at zero; only a
+ *     words and ready flags, 40.25 KiB) starts zeroed and every call leaves it at zero; only a
  *     call that gave up a bounded wait can leave it dirty, and once
  *     bitmtp_linear_device_error has reported that, the next call clears it
  *     first (one memset on `stream`).  Calls whose work can overlap on the GPU

@@ -892,9 +892,9 @@ __device__ void segment_epilogue(const GemmParams& P, Ctrl* c, int p_lo, const S
         if (tid == 0) c->owner_ok = 1;
         named_bar_sync(kBarEpi, 128);
         for (int cc = owner_first + tid; cc < b; cc += 128) {
-            const bool ok = alive && wait_flag(P.flags + cc, P.wait_ns);
+            const bool ok = alive && wait_flag(P.flags + static_cast<size_t>(cc) * kFlagStride, P.wait_ns);
             if (ok) {
-                P.flags[cc] = 0u;  // consumed (no CTA of this launch sets it again)
+                P.flags[static_cast<size_t>(cc) * kFlagStride] = 0u;  // consumed (no CTA of this launch sets it again)
             } else {
                 c->owner_ok = 0;
                 if (alive) fail(c, P.err, kErrWaitFlag);
@@ -1091,7 +1091,7 @@ w2a8_streamk_kernel(const __grid_constant__ GemmParams P) {
         auto publish = [&]() {
             if (leader && !c->failed) {
                 __threadfence();  // the slot's stores before the flag
-                *reinterpret_cast<volatile unsigned*>(P.flags + b) = 1u;
+                *reinterpret_cast<volatile unsigned*>(P.flags + static_cast<size_t>(b) * kFlagStride) = 1u;
             }
             pending = false;
         };

@@ -64,7 +64,7 @@ struct GemmParams {
     int tiles_q, tiles_r;     // stream-K split: CTA b gets tiles_q tiles, plus one if b < tiles_r
     long long total_tiles;
     unsigned long long wait_ns;  // bound on every wait of the launch
-    unsigned* flags;          // [kMaxCtas] partial-sum-ready flags (left at zero)
+    unsigned* flags;          // [kMaxCtas][kFlagStride] partial-sum-ready flags, word 0 of each (left at zero)
     int* slots;               // [kMaxCtas][4][128][4] int32 partial sums of split row tiles
     int* err;                 // device error word
 };
@@ -78,7 +78,12 @@ constexpr int kMinTilesPerCta = 4;    // fewer CTAs on small problems: fewer spl
 // activation region per problem (sized by its k tiles).
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 constexpr size_t kWsFlags = 256;
-constexpr size_t kWsSlots = kWsFlags + align256(static_cast<size_t>(kMaxCtas) * 4);
+// One ready flag per 128-byte line: packed 32 to a line, every CTA's polls
+// and stores went to a handful of L2 lines, and spreading them out made the
+// 16-row calls 0.67 µs and the width-4 layer-chain calls 0.76 µs faster
+// (measured).
+constexpr int kFlagStride = 32;  // words
+constexpr size_t kWsSlots = kWsFlags + static_cast<size_t>(kMaxCtas) * kFlagStride * 4;
 constexpr size_t kWsAct = kWsSlots + static_cast<size_t>(kMaxCtas) * 16 * kTileN * 4;
 // 4.5 KiB per k tile, not the 4 KiB the largest operand tile needs: with
 // regions of exactly 4 KiB per tile a grouped call's problems started at

@@ -194,10 +194,11 @@ def test_workspace_bytes(lib):
     wb = L.bitmtp_linear_workspace_bytes
     assert wb(0, 64, 4) == 0 and wb(64, 0, 4) == 0 and wb(64, 64, 0) == 0 and wb(64, 64, 17) == 0
     a256 = lambda x: -(-x // 256) * 256
-    # a 256-byte header, one ready flag and one partial-sum slot (16 rows x 128
-    # columns of int32) per CTA of the largest grid, then one activation region
-    # per problem: 4.5 KiB per k tile, prefix sums of 16 rows, 16 scales
-    fixed = 256 + a256(320 * 4) + 320 * 16 * 128 * 4
+    # a 256-byte header, one ready flag (on its own 128-byte line) and one
+    # partial-sum slot (16 rows x 128 columns of int32) per CTA of the largest
+    # grid, then one activation region per problem: 4.5 KiB per k tile, prefix
+    # sums of 16 rows, 16 scales
+    fixed = 256 + 320 * 128 + 320 * 16 * 128 * 4
     region = lambda kt: a256(kt * 4608) + a256(16 * (kt + 1) * 4) + 256
     assert wb(128, 128, 1) == fixed + region(1)
     assert wb(32000, 2560, 16) == fixed + region(20)
