@@ -69,7 +69,7 @@ FALLBACK_HBM_GBS = 6800.0
 # the hash of the library sources it was taken with; reported only while the
 # sources are unchanged: the 216 launches of one step (108 preparation + 108
 # GEMM), dram__bytes_read.sum + dram__bytes_write.sum.
-CAPTURED_TRAFFIC: dict[str, int] = {"3a808f4b6074dcdf": 4_992_816_384}
+CAPTURED_TRAFFIC: dict[str, int] = {"1f518e9a6c0a032d": 4_996_310_016}
 KERNEL_SOURCES = ("ternary_w2a8_linear_gb300/csrc/gemm.cu", "ternary_w2a8_linear_gb300/csrc/api.cu",
                   "ternary_w2a8_linear_gb300/csrc/internal.h", "ternary_w2a8_linear_gb300/csrc/ptx.cuh",
                   "ternary_w2a8_linear_gb300/csrc/quant.cuh", "include/bitmtp_linear.h")
